@@ -1,0 +1,174 @@
+"""fp64 CPU oracle for the Inkling attention hot path (test infrastructure).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package.  The CUDA
+product path never calls it.
+
+The arithmetic lives in ``oracle.c`` (plain C, fp64, OpenMP over independent
+rows); this module only compiles it with gcc and marshals numpy arrays.
+bf16 tensors cross this boundary as their raw uint16 bit patterns.
+
+What each function computes, with the passages it follows, is stated in the
+header comment of ``oracle.c``.  Every function here is pinned by tests in
+``tests/test_oracle_pins.py`` against library routines (torch SDPA, numpy
+correlate, torch rms_norm), closed forms and hand-derived fixtures in
+``tests/golden/``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (gcc, -O2, OpenMP)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            D = ctypes.c_double
+            lib.oracle_f64_to_bf16.argtypes = [D]
+            lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
+            lib.oracle_log_scale.argtypes = [D, D]
+            lib.oracle_log_scale.restype = D
+            lib.oracle_prologue.argtypes = (
+                [I, P, I, I, I, P, P, P, P, P, P, P, D, P, I, P, P, P, I, I, P, P, P, P, P, P, P])
+            lib.oracle_prologue.restype = I
+            lib.oracle_attention.argtypes = (
+                [I, P, P, I, I, I, I, I, I, D, D, P, P, P, P, P, P, I, I, I, P, I, P, P, I])
+            lib.oracle_attention.restype = I
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def f64_to_bf16_bits(x: float) -> int:
+    """Round one double to bf16 (ties to even) and return its bit pattern."""
+    return int(_load().oracle_f64_to_bf16(float(x)))
+
+
+def log_scale(T: float, base: float) -> float:
+    """lambda = max(1, ln T / ln base) (1 when base <= 1)."""
+    return float(_load().oracle_log_scale(float(T), float(base)))
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to float64."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def prologue(*, cu_seqlens_q, Hq, Hkv, d, q, k, v, conv_w_k, conv_w_v, q_norm_w, k_norm_w,
+             eps, state_slot, conv_state_k, conv_state_v, slot_mapping, block_size,
+             k_cache, v_cache, want_f64=False):
+    """Run the prologue oracle.
+
+    Inputs are numpy arrays (bf16 as uint16 bits).  conv_state_k/v and
+    k_cache/v_cache are copied, updated and returned; the caller's arrays are
+    not modified.  Returns a dict with q_out, k_cache, v_cache, conv_state_k,
+    conv_state_v, kc (bf16 bits of the conv output), vc and, when want_f64,
+    kc_f64 / vc_f64 (the conv sums before rounding).
+    """
+    lib = _load()
+    cu = _c(cu_seqlens_q, np.int32)
+    B = cu.shape[0] - 1
+    N = int(cu[-1])
+    C = Hkv * d
+    q = _c(q, np.uint16); k = _c(k, np.uint16); v = _c(v, np.uint16)
+    wk = _c(conv_w_k, np.float32); wv = _c(conv_w_v, np.float32)
+    gq = _c(q_norm_w, np.float32); gk = _c(k_norm_w, np.float32)
+    ss = _c(state_slot, np.int32)
+    sk = np.array(conv_state_k, dtype=np.uint16, copy=True, order="C")
+    sv = np.array(conv_state_v, dtype=np.uint16, copy=True, order="C")
+    sm = _c(slot_mapping, np.int32)
+    kc_cache = np.array(k_cache, dtype=np.uint16, copy=True, order="C")
+    vc_cache = np.array(v_cache, dtype=np.uint16, copy=True, order="C")
+    q_out = np.zeros((N, Hq, d), dtype=np.uint16)
+    kc = np.zeros((N, C), dtype=np.uint16)
+    vc = np.zeros((N, C), dtype=np.uint16)
+    kc64 = np.zeros((N, C), dtype=np.float64) if want_f64 else None
+    vc64 = np.zeros((N, C), dtype=np.float64) if want_f64 else None
+    num_state_slots = sk.shape[0]
+    num_blocks = kc_cache.shape[0]
+    rc = lib.oracle_prologue(B, _ptr(cu), Hq, Hkv, d, _ptr(q), _ptr(k), _ptr(v), _ptr(wk), _ptr(wv),
+                             _ptr(gq), _ptr(gk), float(eps), _ptr(ss), num_state_slots,
+                             _ptr(sk), _ptr(sv), _ptr(sm), block_size, num_blocks,
+                             _ptr(q_out), _ptr(kc_cache), _ptr(vc_cache),
+                             _ptr(kc64), _ptr(vc64), _ptr(kc), _ptr(vc))
+    if rc != 0:
+        raise ValueError(f"oracle_prologue failed with code {rc}")
+    out = dict(q_out=q_out, k_cache=kc_cache, v_cache=vc_cache, conv_state_k=sk,
+               conv_state_v=sv, kc=kc, vc=vc)
+    if want_f64:
+        out["kc_f64"] = kc64
+        out["vc_f64"] = vc64
+    return out
+
+
+def attention(*, cu_seqlens_q, seqlen_k, Hq, Hkv, d, d_r, rel_extent, window,
+              softmax_scale, log_scale_base, q, r, P, k_cache, v_cache, block_table,
+              block_size, rows=None, n_threads=0):
+    """Run the attention oracle; returns (out float64, lse float64).
+
+    With rows=None every token row is computed and out has shape [N][Hq][d];
+    otherwise out is [len(rows)][Hq][d] for the listed token indices.
+    """
+    lib = _load()
+    cu = _c(cu_seqlens_q, np.int32)
+    sk = _c(seqlen_k, np.int32)
+    B = cu.shape[0] - 1
+    N = int(cu[-1])
+    q = _c(q, np.uint16)
+    r = _c(r, np.uint16) if r is not None else None
+    P = _c(P, np.float32) if P is not None else None
+    kcache = _c(k_cache, np.uint16)
+    vcache = _c(v_cache, np.uint16)
+    bt = _c(block_table, np.int32)
+    max_blocks = bt.shape[1]
+    num_blocks = kcache.shape[0]
+    rws = None if rows is None else _c(rows, np.int32)
+    nr = N if rows is None else int(rws.shape[0])
+    out = np.zeros((nr, Hq, d), dtype=np.float64)
+    lse = np.zeros((nr, Hq), dtype=np.float64)
+    rc = lib.oracle_attention(B, _ptr(cu), _ptr(sk), Hq, Hkv, d, d_r, rel_extent, window,
+                              float(softmax_scale), float(log_scale_base), _ptr(q), _ptr(r),
+                              _ptr(P), _ptr(kcache), _ptr(vcache), _ptr(bt), max_blocks,
+                              block_size, num_blocks, _ptr(rws), nr, _ptr(out), _ptr(lse),
+                              int(n_threads))
+    if rc != 0:
+        raise ValueError(f"oracle_attention failed with code {rc}")
+    return out, lse
