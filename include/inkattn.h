@@ -1,0 +1,197 @@
+/*
+ * inkattn.h -- C ABI of libinkattn.so, the GB300 (sm_103a) attention hot path of
+ * one Inkling decoder layer.
+ *
+ * Sources, cited by page title and section heading:
+ *   [SG] "SGLang と Miles が Inkling を初日からサポート：975Bのマルチモーダル最先端モデルが公開"
+ *        (winzheng.jp review page)
+ *   [VJ] "vLLM TML Inkling サポート" (agentlenshq.com, Japanese)
+ *   [VV] "vLLM hỗ trợ TML Inkling ngay khi ra mắt với hiệu năng tối ưu" (gpuhub.net)
+ *
+ * General conventions
+ *   - Every pointer inside a params struct is a DEVICE pointer owned by the caller.
+ *     The library allocates no device memory; the only scratch memory (the split-KV
+ *     partials of inkattn_decode) is a caller-provided workspace.
+ *   - bf16 tensors are IEEE bfloat16 (inkattn_bf16 holds the raw 16-bit pattern);
+ *     all arrays are dense and row-major in the layouts stated per field.
+ *   - Every call is asynchronous on the caller's CUDA stream (passed as void*, a
+ *     cudaStream_t; NULL = the legacy default stream), keeps no state between calls
+ *     and is safe to call from several host threads.
+ *   - Host-side validation runs before any launch; on failure the call returns
+ *     INKATTN_ERR_INVALID_ARG or INKATTN_ERR_UNSUPPORTED and launches nothing.
+ *   - Index arrays are read only on the device.  Kernels bounds-check every index
+ *     they read (cu_seqlens_q, seqlen_k, state_slot, slot_mapping, block_table);
+ *     an out-of-range value skips the access and, when dev_status is non-NULL,
+ *     writes INKATTN_ERR_DEVICE_BOUNDS there.  Bounded device waits that run out
+ *     write INKATTN_ERR_DEVICE_TIMEOUT.  The first error written wins; the caller
+ *     zeroes *dev_status before the call and reads it after synchronising.
+ *   - head_dim must be 128 and block_size 64, else INKATTN_ERR_UNSUPPORTED.
+ */
+#ifndef INKATTN_H
+#define INKATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define INKATTN_ABI_VERSION 1
+
+/* The library is built with hidden visibility; only these entry points are exported. */
+#if defined(__GNUC__)
+#define INKATTN_API __attribute__((visibility("default")))
+#else
+#define INKATTN_API
+#endif
+
+typedef uint16_t inkattn_bf16;
+
+typedef enum inkattn_status {
+    INKATTN_OK = 0,
+    INKATTN_ERR_INVALID_ARG = 1,     /* bad pointer, size, or combination of sizes     */
+    INKATTN_ERR_UNSUPPORTED = 2,     /* valid but not implemented (head_dim, block ...) */
+    INKATTN_ERR_CUDA = 3,            /* a CUDA runtime call or launch failed            */
+    INKATTN_ERR_DEVICE_TIMEOUT = 4,  /* written to *dev_status by a bounded device wait */
+    INKATTN_ERR_DEVICE_BOUNDS = 5    /* written to *dev_status by a device bounds check */
+} inkattn_status;
+
+/* Short English text for a status code (static storage, never NULL). */
+INKATTN_API const char *inkattn_status_string(inkattn_status s);
+
+/* INKATTN_ABI_VERSION of the built library. */
+INKATTN_API int inkattn_abi_version(void);
+
+/* ------------------------------------------------------------------------------
+ * The attention prologue [SG §ShortConv 最適化：融合、グラフキャプチャ、シャーディング]:
+ * K/V ShortConv + conv-state carry + Q/K RMSNorm + paged KV write, one kernel.
+ *
+ * Let C = Hkv*128, g = Hq/Hkv.  Sequence b owns new tokens
+ * [cu_seqlens_q[b], cu_seqlens_q[b+1]).  For each sequence and channel c, with xs =
+ * the 3 carried rows (oldest first) followed by the new rows of k (resp. v):
+ *   kc[t][c] = bf16( sum_{k=0..3} conv_w_k[c][k] * xs[t+k][c] )     (fp32 accumulate,
+ *   vc[t][c] = bf16( same with v and conv_w_v )                      taps in order 0..3)
+ * [SG §ShortConv：4カ所に現れる短距離因果畳み込み: W = 4, current token plus the 3 previous
+ * positions of the same channel; conv_w[c][3] weighs the current token].
+ * The state slot then holds the last 3 rows of xs [VV §Quản lý bộ nhớ đệm sconv].
+ * Per (token, head) over the 128 values, in fp32, rounded to bf16:
+ *   q_out = q  / sqrt(mean(q^2)  + eps) * q_norm_w
+ *   kn    = kc / sqrt(mean(kc^2) + eps) * k_norm_w
+ * [SG §Inkling のモデルアーキテクチャ: ShortConv on K and V before the Q/K normalisation].
+ * Then, with slot = slot_mapping[t]: k_cache[slot/64][hk][slot%64][:] = kn,
+ * v_cache[...] = vc.  V is not normalised and Q is not convolved.
+ * ------------------------------------------------------------------------------ */
+typedef struct inkattn_prologue_params {
+    size_t struct_size;        /* = sizeof(inkattn_prologue_params)                      */
+    int32_t B;                 /* sequences in the batch, >= 1                           */
+    int32_t N_tok;             /* new tokens = cu_seqlens_q[B], >= 0                     */
+    int32_t max_seqlen_q;      /* >= every q_len[b]; sizes the grid                      */
+    int32_t Hq, Hkv;           /* query / KV heads, Hq % Hkv == 0                        */
+    int32_t head_dim;          /* 128                                                    */
+    int32_t block_size;        /* paged-cache block, 64                                  */
+    int32_t num_blocks;        /* cache capacity in blocks (bounds check)                */
+    int32_t num_state_slots;   /* conv-state capacity in slots (bounds check)            */
+    float eps;                 /* RMSNorm epsilon, >= 0                                  */
+    const inkattn_bf16 *q;     /* [N_tok][Hq][128]                                       */
+    const inkattn_bf16 *k;     /* [N_tok][C]  (K projection output, before the conv)     */
+    const inkattn_bf16 *v;     /* [N_tok][C]                                             */
+    const float *conv_w_k;     /* [C][4]                                                 */
+    const float *conv_w_v;     /* [C][4]                                                 */
+    const float *q_norm_w;     /* [128], shared by all query heads                       */
+    const float *k_norm_w;     /* [128], shared by all KV heads                          */
+    const int32_t *cu_seqlens_q;   /* [B+1], non-decreasing, cu[0] = 0                   */
+    const int32_t *state_slot;     /* [B], distinct values in [0, num_state_slots)       */
+    const int32_t *slot_mapping;   /* [N_tok], distinct values in [0, num_blocks*64)     */
+    inkattn_bf16 *conv_state_k;    /* [num_state_slots][3][C], read then overwritten     */
+    inkattn_bf16 *conv_state_v;    /* [num_state_slots][3][C]                            */
+    inkattn_bf16 *q_out;           /* [N_tok][Hq][128]                                   */
+    inkattn_bf16 *k_cache;         /* [num_blocks][Hkv][64][128]                         */
+    inkattn_bf16 *v_cache;         /* [num_blocks][Hkv][64][128]                         */
+    int32_t *dev_status;           /* nullable, see the conventions above                */
+} inkattn_prologue_params;
+
+/* Runs the prologue.  Buffers may not alias except as stated (conv_state_* in/out). */
+INKATTN_API inkattn_status inkattn_prologue(const inkattn_prologue_params *p, void *stream);
+
+/* ------------------------------------------------------------------------------
+ * Relative-position-bias GQA attention over the paged cache
+ * [SG §相対位置バイアス付き Attention; VJ §TML Inkling モデルアーキテクチャ
+ *  "Hybrid Attention", "Relative Attention"; VV §FA4 với sheared bias].
+ *
+ * Sequence b has q_len = cu_seqlens_q[b+1]-cu_seqlens_q[b] new tokens at positions
+ * i = seqlen_k[b]-q_len+t; key j (0 <= j < seqlen_k[b]) sits at position j in block
+ * block_table[b][j/64], offset j%64, head kv = h / (Hq/Hkv).  For query head h:
+ *   s_ij = lambda_b * ( softmax_scale * q_i.k_j + bias_hij ),
+ *   bias_hij = sum_{e<d_r} r[i][h][e] * P[h][e][i-j]  if 0 <= i-j < rel_extent, else 0,
+ * visible keys: j <= i, and i-j < window when window > 0 (sliding-window layer),
+ *   lambda_b = max(1, ln(seqlen_k[b]) / ln(log_scale_base)) when log_scale_base > 1
+ *             (full layers' length-dependent logit scaling), else 1,
+ *   out_i = sum_j softmax_j(s_ij) v_j,  lse_i = ln sum_j exp(s_ij)  (natural log).
+ * softmax_scale <= 0 selects 1/sqrt(128).
+ * ------------------------------------------------------------------------------ */
+typedef struct inkattn_attn_params {
+    size_t struct_size;        /* = sizeof(inkattn_attn_params)                          */
+    int32_t B;                 /* sequences, >= 1                                        */
+    int32_t N_tok;             /* query rows = cu_seqlens_q[B]                           */
+    int32_t max_seqlen_q;      /* >= every q_len[b]                                      */
+    int32_t max_seqlen_k;      /* >= every seqlen_k[b]                                   */
+    int32_t Hq, Hkv;           /* Hq % Hkv == 0                                          */
+    int32_t head_dim;          /* 128                                                    */
+    int32_t block_size;        /* 64                                                     */
+    int32_t num_blocks;        /* cache capacity in blocks (bounds check)                */
+    int32_t max_blocks_per_seq;/* row length of block_table                              */
+    int32_t d_r;               /* relative feature size: 16, 32, 48 or 64                */
+    int32_t rel_extent;        /* >= 0; 0 disables the bias                              */
+    int32_t window;            /* 0 = full attention, else the sliding window (keys)     */
+    float softmax_scale;       /* <= 0 -> 1/sqrt(128)                                    */
+    float log_scale_base;      /* <= 1 -> no length-dependent scaling (8192 on full layers) */
+    const inkattn_bf16 *q;     /* [N_tok][Hq][128], the normalised queries               */
+    const inkattn_bf16 *r;     /* [N_tok][Hq][d_r]  (nullable iff rel_extent == 0)      */
+    const float *P;            /* [Hq][d_r][rel_extent] (nullable iff rel_extent == 0)   */
+    const inkattn_bf16 *k_cache;   /* [num_blocks][Hkv][64][128]                         */
+    const inkattn_bf16 *v_cache;   /* [num_blocks][Hkv][64][128]                         */
+    const int32_t *cu_seqlens_q;   /* [B+1]                                              */
+    const int32_t *seqlen_k;       /* [B], q_len[b] <= seqlen_k[b] <= max_seqlen_k       */
+    const int32_t *block_table;    /* [B][max_blocks_per_seq]                            */
+    inkattn_bf16 *out;             /* [N_tok][Hq][128]                                   */
+    float *lse;                    /* nullable, [N_tok][Hq]                              */
+    int32_t *dev_status;           /* nullable                                           */
+} inkattn_attn_params;
+
+/* Prefill (any q_len): writes out (and lse). */
+INKATTN_API inkattn_status inkattn_prefill(const inkattn_attn_params *p, void *stream);
+
+/* ------------------------------------------------------------------------------
+ * Split-KV decode [VJ §低レイテンシコレクティブとカーネル "FA4 Kernel"; VV §FA4 với
+ * sheared bias: num_splits is picked per configuration from batch size, TP size and
+ * KV length].  Decode shapes: max_seqlen_q <= 16 and max_seqlen_q*(Hq/Hkv) <= 128
+ * (e.g. 9 MTP-verify tokens x 8 query heads per KV head).  Same math as prefill.
+ * ------------------------------------------------------------------------------ */
+
+/* The split count the library would pick for these params on a GPU with num_sms
+ * SMs (tensor-parallel size 1).  Host only; returns >= 1, or 0 for invalid params. */
+INKATTN_API int inkattn_decode_num_splits(const inkattn_attn_params *p, int num_sms);
+
+/* Bytes of workspace inkattn_decode needs for num_splits (0 = the heuristic on the
+ * current device): N_tok*Hq*S*(128+1)*4 rounded up to 256, or 0 when S resolves to 1. */
+INKATTN_API size_t inkattn_decode_workspace_bytes(const inkattn_attn_params *p, int num_splits);
+
+/* Decode pass.  num_splits: 0 = heuristic, else 1..64.  With one split the result
+ * goes straight to out/lse; otherwise each split's own softmax-normalised partial
+ * output and its lse go to the workspace, and inkattn_combine must follow on the
+ * same stream with the same num_splits.
+ * workspace: device memory of at least inkattn_decode_workspace_bytes bytes,
+ * 256-byte aligned, owned by the caller, not read by the host. */
+INKATTN_API inkattn_status inkattn_decode(const inkattn_attn_params *p, int num_splits,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/* Merges the per-split partials: lse = ln sum_s exp(lse_s), out = sum_s
+ * exp(lse_s - lse) out_s.  A no-op when num_splits resolves to 1. */
+INKATTN_API inkattn_status inkattn_combine(const inkattn_attn_params *p, int num_splits,
+                               const void *workspace, size_t workspace_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* INKATTN_H */

@@ -172,3 +172,38 @@ def attention(*, cu_seqlens_q, seqlen_k, Hq, Hkv, d, d_r, rel_extent, window,
     if rc != 0:
         raise ValueError(f"oracle_attention failed with code {rc}")
     return out, lse
+
+
+# ------------------------------------------------------------------ workload adapters
+
+def _bits(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.detach().contiguous().cpu().numpy()
+
+
+def prologue_for_inputs(x, workload):
+    """The prologue oracle on a dict of workload tensors (any device, as produced by
+    relative_bias_hybrid_gb300.inputs.make_inputs).  Returns numpy arrays."""
+    d = workload.head_dim
+    return prologue(cu_seqlens_q=_bits(x["cu_seqlens_q"]), Hq=workload.Hq, Hkv=workload.Hkv, d=d,
+                    q=_bits(x["q"]), k=_bits(x["k"]), v=_bits(x["v"]),
+                    conv_w_k=_bits(x["conv_w_k"]), conv_w_v=_bits(x["conv_w_v"]),
+                    q_norm_w=_bits(x["q_norm_w"]), k_norm_w=_bits(x["k_norm_w"]), eps=workload.eps,
+                    state_slot=_bits(x["state_slot"]), conv_state_k=_bits(x["conv_state_k"]),
+                    conv_state_v=_bits(x["conv_state_v"]), slot_mapping=_bits(x["slot_mapping"]),
+                    block_size=workload.block_size, k_cache=_bits(x["k_cache"]),
+                    v_cache=_bits(x["v_cache"]))
+
+
+def attention_for_inputs(x, workload, q_bits, k_cache_bits, v_cache_bits, rows=None, n_threads=0):
+    """The attention oracle for a workload, on the given normalised queries and caches
+    (bf16 bit arrays) and the workload's r, P, lengths and block table."""
+    return attention(cu_seqlens_q=_bits(x["cu_seqlens_q"]), seqlen_k=_bits(x["seqlen_k"]),
+                     Hq=workload.Hq, Hkv=workload.Hkv, d=workload.head_dim, d_r=workload.d_r,
+                     rel_extent=workload.rel_extent, window=workload.window, softmax_scale=0.0,
+                     log_scale_base=workload.log_scale_base, q=q_bits, r=_bits(x["r"]),
+                     P=_bits(x["P"]), k_cache=k_cache_bits, v_cache=v_cache_bits,
+                     block_table=_bits(x["block_table"]), block_size=workload.block_size,
+                     rows=rows, n_threads=n_threads)

@@ -1,0 +1,311 @@
+// api.cu -- the extern "C" entry points of libinkattn.so: host-side validation, TMA
+// descriptor setup, the decode split heuristic, and the launches.
+//
+// Nothing here computes on the host: every step of the path runs in the kernels of
+// prologue.cu, prefill_mma.cu and decode.cu.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/inkattn.h"
+#include "internal.h"
+
+namespace inkattn {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// ---------------------------------------------------------------- device checks
+
+std::atomic<int> g_dev_ok[kMaxDevices];       // 0 unknown, 1 sm_103, 2 other
+std::atomic<int> g_dev_sms[kMaxDevices];
+
+inkattn_status check_device(int *sms_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return INKATTN_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return INKATTN_ERR_UNSUPPORTED;
+    int ok = g_dev_ok[dev].load(std::memory_order_acquire);
+    if (ok == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return INKATTN_ERR_CUDA;
+        g_dev_sms[dev].store(sms, std::memory_order_relaxed);
+        ok = (major == 10 && minor == 3) ? 1 : 2;
+        g_dev_ok[dev].store(ok, std::memory_order_release);
+    }
+    if (sms_out) *sms_out = g_dev_sms[dev].load(std::memory_order_relaxed);
+    return ok == 1 ? INKATTN_OK : INKATTN_ERR_UNSUPPORTED;
+}
+
+// ---------------------------------------------------------------- TMA encode
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+bool aligned(const void *ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; }
+
+// ---------------------------------------------------------------- validation
+
+inkattn_status validate_prologue(const inkattn_prologue_params *p) {
+    if (!p || p->struct_size != sizeof(inkattn_prologue_params)) return INKATTN_ERR_INVALID_ARG;
+    if (p->B < 1 || p->N_tok < 0 || p->max_seqlen_q < 0 || p->Hq < 1 || p->Hkv < 1 ||
+        p->Hq % p->Hkv != 0 || p->num_blocks < 1 || p->num_state_slots < 1 || !(p->eps >= 0.f))
+        return INKATTN_ERR_INVALID_ARG;
+    if (p->N_tok > 0 && p->max_seqlen_q < 1) return INKATTN_ERR_INVALID_ARG;
+    if (p->B > 65535 || p->Hkv > 65535) return INKATTN_ERR_INVALID_ARG;
+    if ((long long)p->num_blocks * 64 > INT_MAX) return INKATTN_ERR_INVALID_ARG;
+    if (p->head_dim != kHeadDim || p->block_size != kBlock) return INKATTN_ERR_UNSUPPORTED;
+    const void *ptrs16[] = {p->q, p->k, p->v, p->conv_state_k, p->conv_state_v, p->q_out,
+                            p->k_cache, p->v_cache};
+    for (const void *ptr : ptrs16)
+        if (!ptr || !aligned(ptr, 16)) return INKATTN_ERR_INVALID_ARG;
+    const void *ptrs4[] = {p->conv_w_k, p->conv_w_v, p->q_norm_w, p->k_norm_w, p->cu_seqlens_q,
+                           p->state_slot, p->slot_mapping};
+    for (const void *ptr : ptrs4)
+        if (!ptr || !aligned(ptr, 4)) return INKATTN_ERR_INVALID_ARG;
+    if (p->dev_status && !aligned(p->dev_status, 4)) return INKATTN_ERR_INVALID_ARG;
+    return INKATTN_OK;
+}
+
+inkattn_status validate_attn(const inkattn_attn_params *p) {
+    if (!p || p->struct_size != sizeof(inkattn_attn_params)) return INKATTN_ERR_INVALID_ARG;
+    if (p->B < 1 || p->B > 65535 || p->N_tok < 0 || p->max_seqlen_q < 0 || p->max_seqlen_k < 0 ||
+        p->Hq < 1 || p->Hkv < 1 || p->Hq % p->Hkv != 0 || p->Hq > 65535 || p->num_blocks < 1 ||
+        p->max_blocks_per_seq < 1 || p->rel_extent < 0 || p->window < 0)
+        return INKATTN_ERR_INVALID_ARG;
+    if (p->N_tok > 0 && (p->max_seqlen_q < 1 || p->max_seqlen_k < p->max_seqlen_q))
+        return INKATTN_ERR_INVALID_ARG;
+    if ((long long)p->max_blocks_per_seq * kBlock < p->max_seqlen_k) return INKATTN_ERR_INVALID_ARG;
+    if ((long long)p->num_blocks * p->Hkv * kBlock >= (1ll << 31)) return INKATTN_ERR_INVALID_ARG;
+    if (p->head_dim != kHeadDim || p->block_size != kBlock) return INKATTN_ERR_UNSUPPORTED;
+    if (!(p->softmax_scale == p->softmax_scale) || !(p->log_scale_base == p->log_scale_base))
+        return INKATTN_ERR_INVALID_ARG;
+    const void *ptrs16[] = {p->q, p->k_cache, p->v_cache, p->out};
+    for (const void *ptr : ptrs16)
+        if (!ptr || !aligned(ptr, 16)) return INKATTN_ERR_INVALID_ARG;
+    const void *ptrs4[] = {p->cu_seqlens_q, p->seqlen_k, p->block_table};
+    for (const void *ptr : ptrs4)
+        if (!ptr || !aligned(ptr, 4)) return INKATTN_ERR_INVALID_ARG;
+    if (p->lse && !aligned(p->lse, 4)) return INKATTN_ERR_INVALID_ARG;
+    if (p->dev_status && !aligned(p->dev_status, 4)) return INKATTN_ERR_INVALID_ARG;
+    if (p->rel_extent > 0) {
+        if (p->d_r < 16 || p->d_r > 64 || p->d_r % 16 != 0) return INKATTN_ERR_UNSUPPORTED;
+        if (!p->r || !p->P || !aligned(p->r, 4) || !aligned(p->P, 4)) return INKATTN_ERR_INVALID_ARG;
+    }
+    return INKATTN_OK;
+}
+
+AttnScalars scalars(const inkattn_attn_params &p) {
+    AttnScalars s;
+    s.scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)kHeadDim);
+    s.group = p.Hq / p.Hkv;
+    return s;
+}
+
+inkattn_status launch_status(cudaError_t e) { return e == cudaSuccess ? INKATTN_OK : INKATTN_ERR_CUDA; }
+
+// Decode split heuristic.  Cost model, in units of "one 64-key K+V block streamed by one
+// CTA slot": the KV stream takes waves(S) * ceil(nblk / S); the split partials add their
+// write + read traffic spread over all slots, plus a fixed cost for the combine launch.
+int pick_splits(const inkattn_attn_params &p, int num_sms) {
+    const int g = p.Hq / p.Hkv;
+    long long nblk = (p.max_seqlen_k + kBlock - 1) / kBlock;
+    if (p.window > 0) {
+        const long long span = ((long long)p.window + p.max_seqlen_q + kBlock - 1) / kBlock + 1;
+        if (span < nblk) nblk = span;
+    }
+    if (nblk < 1) nblk = 1;
+    const long long units = (long long)p.B * p.Hkv;
+    const long long slots = (long long)(num_sms > 0 ? num_sms : 1) * kDecodeCtasPerSm;
+    if (units >= 2 * slots) return 1;
+    const long long rows_per_unit = (long long)p.max_seqlen_q * g;
+    const double block_bytes = 2.0 * kBlock * kHeadDim * 2;   // K + V of one block
+    int best = 1;
+    double best_cost = 1e300;
+    for (int S = 1; S <= kDecodeMaxSplits; ++S) {
+        const long long per = (nblk + S - 1) / S;
+        if (S > 1 && per < kDecodeMinSplitBlocks) break;
+        const long long waves = (units * S + slots - 1) / slots;
+        double cost = (double)waves * (double)per;
+        if (S > 1) {
+            const double ws_bytes = 2.0 * units * rows_per_unit * S * (kHeadDim + 1) * 4.0;
+            cost += ws_bytes / block_bytes / (double)slots + kCombineCostBlocks;
+        }
+        if (cost < best_cost * (1.0 - 1e-9)) {
+            best_cost = cost;
+            best = S;
+        }
+    }
+    return best;
+}
+
+size_t ws_o_bytes(const inkattn_attn_params &p, int S) {
+    const size_t b = (size_t)p.N_tok * p.Hq * S * kHeadDim * 4;
+    return (b + 255) & ~(size_t)255;
+}
+size_t ws_lse_bytes(const inkattn_attn_params &p, int S) {
+    const size_t b = (size_t)p.N_tok * p.Hq * S * 4;
+    return (b + 255) & ~(size_t)255;
+}
+
+inkattn_status validate_decode_shape(const inkattn_attn_params &p) {
+    const int g = p.Hq / p.Hkv;
+    if (p.max_seqlen_q > 16 || (long long)p.max_seqlen_q * g > kDecodeMaxRows) return INKATTN_ERR_UNSUPPORTED;
+    return INKATTN_OK;
+}
+
+inkattn_status resolve_splits(const inkattn_attn_params &p, int requested, int *S_out) {
+    if (requested < 0 || requested > kDecodeMaxSplits) return INKATTN_ERR_INVALID_ARG;
+    if (requested > 0) {
+        *S_out = requested;
+        return INKATTN_OK;
+    }
+    int sms = 0;
+    inkattn_status st = check_device(&sms);
+    if (st != INKATTN_OK) return st;
+    *S_out = pick_splits(p, sms);
+    return INKATTN_OK;
+}
+
+}  // namespace
+
+bool make_cache_map(CUtensorMap *map, const void *base, long long rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+    cuuint32_t box[2] = {64, 64};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_q_map(CUtensorMap *map, const void *base, int n_tok, int hq, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hq, (cuuint64_t)(n_tok > 0 ? n_tok : 1)};
+    cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)hq * kHeadDim * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace inkattn
+
+using namespace inkattn;
+
+extern "C" {
+
+const char *inkattn_status_string(inkattn_status s) {
+    switch (s) {
+        case INKATTN_OK: return "ok";
+        case INKATTN_ERR_INVALID_ARG: return "invalid argument";
+        case INKATTN_ERR_UNSUPPORTED: return "unsupported configuration or device";
+        case INKATTN_ERR_CUDA: return "CUDA runtime error";
+        case INKATTN_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+        case INKATTN_ERR_DEVICE_BOUNDS: return "device index out of bounds";
+    }
+    return "unknown status";
+}
+
+int inkattn_abi_version(void) { return INKATTN_ABI_VERSION; }
+
+inkattn_status inkattn_prologue(const inkattn_prologue_params *p, void *stream) {
+    inkattn_status st = validate_prologue(p);
+    if (st != INKATTN_OK) return st;
+    if ((st = check_device(nullptr)) != INKATTN_OK) return st;
+    if (p->N_tok == 0) return INKATTN_OK;
+    return launch_status(launch_prologue(*p, static_cast<cudaStream_t>(stream)));
+}
+
+inkattn_status inkattn_prefill(const inkattn_attn_params *p, void *stream) {
+    inkattn_status st = validate_attn(p);
+    if (st != INKATTN_OK) return st;
+    if ((st = check_device(nullptr)) != INKATTN_OK) return st;
+    if (p->N_tok == 0) return INKATTN_OK;
+    CUtensorMap qmap, kmap, vmap;
+    const long long rows = (long long)p->num_blocks * p->Hkv * kBlock;
+    if (!make_q_map(&qmap, p->q, p->N_tok, p->Hq, kPrefillMmaRows) ||
+        !make_cache_map(&kmap, p->k_cache, rows) || !make_cache_map(&vmap, p->v_cache, rows))
+        return INKATTN_ERR_CUDA;
+    return launch_status(launch_prefill_mma(*p, scalars(*p), qmap, kmap, vmap,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+int inkattn_decode_num_splits(const inkattn_attn_params *p, int num_sms) {
+    if (validate_attn(p) != INKATTN_OK || validate_decode_shape(*p) != INKATTN_OK || num_sms < 1) return 0;
+    return pick_splits(*p, num_sms);
+}
+
+size_t inkattn_decode_workspace_bytes(const inkattn_attn_params *p, int num_splits) {
+    if (validate_attn(p) != INKATTN_OK) return 0;
+    int S = 0;
+    if (resolve_splits(*p, num_splits, &S) != INKATTN_OK || S <= 1) return 0;
+    return ws_o_bytes(*p, S) + ws_lse_bytes(*p, S);
+}
+
+inkattn_status inkattn_decode(const inkattn_attn_params *p, int num_splits, void *workspace,
+                              size_t workspace_bytes, void *stream) {
+    inkattn_status st = validate_attn(p);
+    if (st != INKATTN_OK) return st;
+    if ((st = validate_decode_shape(*p)) != INKATTN_OK) return st;
+    if (num_splits < 0 || num_splits > kDecodeMaxSplits) return INKATTN_ERR_INVALID_ARG;
+    if ((st = check_device(nullptr)) != INKATTN_OK) return st;
+    int S = 0;
+    if ((st = resolve_splits(*p, num_splits, &S)) != INKATTN_OK) return st;
+    float *ws_o = nullptr, *ws_lse = nullptr;
+    if (S > 1) {
+        const size_t need = ws_o_bytes(*p, S) + ws_lse_bytes(*p, S);
+        if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return INKATTN_ERR_INVALID_ARG;
+        ws_o = static_cast<float *>(workspace);
+        ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + ws_o_bytes(*p, S));
+    }
+    if (p->N_tok == 0) return INKATTN_OK;
+    CUtensorMap kmap, vmap;
+    const long long rows = (long long)p->num_blocks * p->Hkv * kBlock;
+    if (!make_cache_map(&kmap, p->k_cache, rows) || !make_cache_map(&vmap, p->v_cache, rows))
+        return INKATTN_ERR_CUDA;
+    return launch_status(launch_decode(*p, scalars(*p), S, ws_o, ws_lse, kmap, vmap,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+inkattn_status inkattn_combine(const inkattn_attn_params *p, int num_splits, const void *workspace,
+                               size_t workspace_bytes, void *stream) {
+    inkattn_status st = validate_attn(p);
+    if (st != INKATTN_OK) return st;
+    if ((st = validate_decode_shape(*p)) != INKATTN_OK) return st;
+    if (num_splits < 0 || num_splits > kDecodeMaxSplits) return INKATTN_ERR_INVALID_ARG;
+    if ((st = check_device(nullptr)) != INKATTN_OK) return st;
+    int S = 0;
+    if ((st = resolve_splits(*p, num_splits, &S)) != INKATTN_OK) return st;
+    if (S <= 1 || p->N_tok == 0) return INKATTN_OK;
+    const size_t need = ws_o_bytes(*p, S) + ws_lse_bytes(*p, S);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return INKATTN_ERR_INVALID_ARG;
+    const float *ws_o = static_cast<const float *>(workspace);
+    const float *ws_lse = reinterpret_cast<const float *>(static_cast<const char *>(workspace) + ws_o_bytes(*p, S));
+    return launch_status(launch_combine(*p, S, ws_o, ws_lse, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

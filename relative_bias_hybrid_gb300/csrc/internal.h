@@ -1,0 +1,47 @@
+// internal.h -- launchers shared between the entry points (api.cu) and the kernel files.
+// Each launcher assumes its params were validated by api.cu and returns the CUDA
+// error of the launch.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/inkattn.h"
+
+namespace inkattn {
+
+constexpr int kHeadDim = 128;
+constexpr int kBlock = 64;          // paged-cache block (tokens)
+
+// Resolved per-call scalars of an attention call (host-computed).
+struct AttnScalars {
+    float scale;          // softmax scale (1/sqrt(128) by default)
+    int group;            // Hq / Hkv
+};
+
+cudaError_t launch_prologue(const inkattn_prologue_params &p, cudaStream_t stream);
+
+// Decode: S = num_splits (>= 1).  ws_o / ws_lse are unused when S == 1.
+constexpr int kDecodeMaxRows = 128;     // max_seqlen_q * group
+constexpr int kDecodeMaxSplits = 64;
+constexpr int kDecodeCtasPerSm = 1;     // design occupancy used by the split heuristic
+constexpr int kDecodeMinSplitBlocks = 8; // a split streams at least 8 cache blocks (512 keys)
+constexpr double kCombineCostBlocks = 2.0; // fixed cost of the combine launch, in block loads
+cudaError_t launch_decode(const inkattn_attn_params &p, const AttnScalars &s, int num_splits,
+                          float *ws_o, float *ws_lse, const CUtensorMap &kmap,
+                          const CUtensorMap &vmap, cudaStream_t stream);
+cudaError_t launch_combine(const inkattn_attn_params &p, int num_splits, const float *ws_o,
+                           const float *ws_lse, cudaStream_t stream);
+
+constexpr int kPrefillMmaRows = 128;   // query rows per CTA of the mma.sync prefill
+cudaError_t launch_prefill_mma(const inkattn_attn_params &p, const AttnScalars &s,
+                               const CUtensorMap &qmap, const CUtensorMap &kmap,
+                               const CUtensorMap &vmap, cudaStream_t stream);
+
+// TMA descriptor for a paged cache viewed as [num_blocks*Hkv*64 rows][128] bf16,
+// box 64 rows x 64 columns, 128-byte swizzle.  Returns false on failure.
+bool make_cache_map(CUtensorMap *map, const void *base, long long rows);
+// TMA descriptor for q viewed as [N_tok][Hq][128] bf16, box {64, 1, box_rows}, 128-byte swizzle.
+bool make_q_map(CUtensorMap *map, const void *base, int n_tok, int hq, int box_rows);
+
+}  // namespace inkattn

@@ -1,0 +1,206 @@
+// prologue.cu -- the fused attention prologue: K/V ShortConv (W = 4) with conv-state
+// carry, Q/K RMSNorm and the paged KV-cache write, in one kernel.
+//
+// [SGLang と Miles が Inkling を初日からサポート, §ShortConv 最適化：融合、グラフキャプチャ、
+//  シャーディング]: K/V convolution, Q/K RMSNorm and the KV-cache write fused into one
+//  attention-prologue kernel with no intermediate write-back.
+// [same page, §ShortConv：4カ所に現れる短距離因果畳み込み]: per-channel causal conv along the
+//  tokens over the current token and the W-1 = 3 previous positions.
+// [vLLM hỗ trợ TML Inkling ..., §Quản lý bộ nhớ đệm sconv]: the state keeps the hidden
+//  states of the last W-1 tokens.
+//
+// Work split: one CTA per (16-token tile of one sequence, KV head hk).  It handles, for
+// its tokens, the g = Hq/Hkv query heads of that KV head (RMSNorm only), the K stream
+// of head hk (conv, round to bf16, RMSNorm, cache write) and the V stream (conv,
+// round, cache write).  Each 128-value row is owned by a half-warp: 16 lanes x 16 bytes,
+// so every global access is a full 256-byte row, coalesced.
+//
+// Conv-state carry without races: tiles are aligned to sequence starts, so every read of
+// the carried rows (tokens 0..2) happens in tile 0 of the sequence; that same CTA, after
+// a block barrier, writes the new state for its own 128 channels.  No other CTA touches
+// those channels of that state slot.
+#include "common.cuh"
+#include "internal.h"
+
+namespace inkattn {
+
+constexpr int kPrologueTokens = 16;
+constexpr int kPrologueThreads = 256;
+constexpr int kRowsInFlight = 2;   // rows a half-warp loads before it computes
+
+__device__ __forceinline__ void unpack8(const uint4 &u, float (&x)[8]) {
+    x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x);
+    x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
+    x[4] = bf16_lo(u.z); x[5] = bf16_hi(u.z);
+    x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
+    uint4 u;
+    u.x = pack_bf16(x[0], x[1]); u.y = pack_bf16(x[2], x[3]);
+    u.z = pack_bf16(x[4], x[5]); u.w = pack_bf16(x[6], x[7]);
+    return u;
+}
+
+__global__ void __launch_bounds__(kPrologueThreads)
+k_prologue(const inkattn_prologue_params p) {
+    __shared__ float s_wk[kHeadDim * 4], s_wv[kHeadDim * 4];
+    __shared__ float s_gq[kHeadDim], s_gk[kHeadDim];
+
+    const int tile = blockIdx.x, b = blockIdx.y, hk = blockIdx.z;
+    const int tid = threadIdx.x;
+    const int C = p.Hkv * kHeadDim;
+    const int g = p.Hq / p.Hkv;
+
+    for (int i = tid; i < kHeadDim * 4; i += kPrologueThreads) {
+        s_wk[i] = p.conv_w_k[(size_t)hk * kHeadDim * 4 + i];
+        s_wv[i] = p.conv_w_v[(size_t)hk * kHeadDim * 4 + i];
+    }
+    if (tid < kHeadDim) {
+        s_gq[tid] = p.q_norm_w[tid];
+        s_gk[tid] = p.k_norm_w[tid];
+    }
+
+    const int start = p.cu_seqlens_q[b];
+    const int end = p.cu_seqlens_q[b + 1];
+    const int slot = p.state_slot[b];
+    if (start < 0 || end < start || end > p.N_tok || end - start > p.max_seqlen_q ||
+        slot < 0 || slot >= p.num_state_slots) {
+        if (tid == 0) set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
+        return;   // uniform over the CTA
+    }
+    const int q_len = end - start;
+    const int t0 = tile * kPrologueTokens;
+    if (t0 >= q_len) return;   // (an empty sequence keeps its state unchanged)
+    const int nt = min(kPrologueTokens, q_len - t0);
+    __syncthreads();
+
+    const int kinds = g + 2;                  // g query rows, the K row, the V row
+    const int rows = nt * kinds;
+    const int half = tid >> 4;                // 16 half-warps per CTA
+    const int c0 = (tid & 15) * 8;            // 8 channels per lane within the head
+    const size_t head_off = (size_t)hk * kHeadDim + c0;
+    const long long slot_limit = (long long)p.num_blocks * kBlock;
+
+    for (int base = 0; base < rows; base += 16 * kRowsInFlight) {
+        float x[kRowsInFlight][8];
+        int kind_of[kRowsInFlight], tok_of[kRowsInFlight];
+        // phase 1: loads (and the conv, which only needs loads)
+#pragma unroll
+        for (int u = 0; u < kRowsInFlight; ++u) {
+            const int row = base + u * 16 + half;
+            kind_of[u] = -1;
+            tok_of[u] = 0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[u][e] = 0.f;
+            if (row >= rows) continue;
+            const int tt = row / kinds, kind = row - tt * kinds;
+            const int t = t0 + tt;
+            const long long tok = (long long)start + t;
+            kind_of[u] = kind;
+            tok_of[u] = (int)tok;
+            if (kind < g) {
+                const int h = hk * g + kind;
+                const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
+                    p.q + ((size_t)tok * p.Hq + h) * kHeadDim + c0));
+                unpack8(raw, x[u]);
+            } else {
+                const bool isk = (kind == g);
+                const inkattn_bf16 *src = isk ? p.k : p.v;
+                const inkattn_bf16 *st = isk ? p.conv_state_k : p.conv_state_v;
+                const float *w = isk ? s_wk : s_wv;
+                float acc[8];
+#pragma unroll
+                for (int tap = 0; tap < 4; ++tap) {
+                    const int idx = t + tap;      // index into [3 carried rows ; new rows]
+                    uint4 raw;
+                    if (idx < 3) {
+                        raw = *reinterpret_cast<const uint4 *>(
+                            st + ((size_t)slot * 3 + idx) * C + head_off);
+                    } else {
+                        raw = __ldg(reinterpret_cast<const uint4 *>(
+                            src + ((size_t)start + idx - 3) * C + head_off));
+                    }
+                    float xv[8];
+                    unpack8(raw, xv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float we = w[(c0 + e) * 4 + tap];
+                        acc[e] = tap == 0 ? we * xv[e] : fmaf(we, xv[e], acc[e]);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e)   // the conv output is rounded to bf16
+                    x[u][e] = __bfloat162float(__float2bfloat16_rn(acc[e]));
+            }
+        }
+        // phase 2: RMSNorm (all lanes take part in the shuffles) and stores
+#pragma unroll
+        for (int u = 0; u < kRowsInFlight; ++u) {
+            float ss = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss = fmaf(x[u][e], x[u][e], ss);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            const int kind = kind_of[u];
+            if (kind < 0) continue;
+            const int tok = tok_of[u];
+            const float inv = __frsqrt_rn(ss * (1.0f / kHeadDim) + p.eps);
+            if (kind < g) {
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[e] = x[u][e] * inv * s_gq[c0 + e];
+                const int h = hk * g + kind;
+                *reinterpret_cast<uint4 *>(p.q_out + ((size_t)tok * p.Hq + h) * kHeadDim + c0) =
+                    pack8(y);
+            } else {
+                const int sm = p.slot_mapping[tok];
+                if (sm < 0 || (long long)sm >= slot_limit) {
+                    set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
+                    continue;
+                }
+                const size_t dst = (((size_t)(sm / kBlock) * p.Hkv + hk) * kBlock + (sm % kBlock)) *
+                                   kHeadDim + c0;
+                if (kind == g) {
+                    float y[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) y[e] = x[u][e] * inv * s_gk[c0 + e];
+                    *reinterpret_cast<uint4 *>(p.k_cache + dst) = pack8(y);
+                } else {
+                    *reinterpret_cast<uint4 *>(p.v_cache + dst) = pack8(x[u]);
+                }
+            }
+        }
+    }
+
+    // new conv state = the last 3 rows of [carried rows ; new rows], for this head's channels
+    if (tile != 0) return;
+    uint4 nv = make_uint4(0, 0, 0, 0);
+    int task = tid;                              // 2 streams x 3 rows x 16 chunks
+    const bool active = task < 2 * 3 * 16;
+    const int stream = task / 48, r = (task / 16) % 3, chunk = task % 16;
+    const size_t ch = (size_t)hk * kHeadDim + chunk * 8;
+    inkattn_bf16 *st = stream == 0 ? p.conv_state_k : p.conv_state_v;
+    if (active) {
+        const int idx = q_len + r;
+        if (idx < 3) {
+            nv = *reinterpret_cast<const uint4 *>(st + ((size_t)slot * 3 + idx) * C + ch);
+        } else {
+            const inkattn_bf16 *src = stream == 0 ? p.k : p.v;
+            nv = __ldg(reinterpret_cast<const uint4 *>(src + ((size_t)start + idx - 3) * C + ch));
+        }
+    }
+    __syncthreads();   // every read of the old state (conv taps and the rows above) is done
+    if (active) *reinterpret_cast<uint4 *>(st + ((size_t)slot * 3 + r) * C + ch) = nv;
+}
+
+cudaError_t launch_prologue(const inkattn_prologue_params &p, cudaStream_t stream) {
+    const int tiles = p.max_seqlen_q > 0 ? (p.max_seqlen_q + kPrologueTokens - 1) / kPrologueTokens : 1;
+    dim3 grid(tiles, p.B, p.Hkv);
+    k_prologue<<<grid, kPrologueThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace inkattn

@@ -1,0 +1,84 @@
+"""One pass of the hot path for a workload: prologue, then prefill or decode + combine.
+
+Plumbing only: this module allocates the output buffers with torch, fills the params
+structs through the binding and issues the C-ABI calls in order on one stream.
+"""
+from __future__ import annotations
+
+from typing import Dict, Optional
+
+import torch
+
+from . import inkattn as ia
+from .inputs import Workload
+
+
+class AttentionStep:
+    """Buffers + calls of one attention-layer pass over device-resident inputs.
+
+    mode "prefill": inkattn_prologue then inkattn_prefill.
+    mode "decode":  inkattn_prologue then inkattn_decode (+ inkattn_combine when the
+                    split count is above one).
+    The conv state and the KV cache in `inputs` are updated in place by every run.
+    """
+
+    def __init__(self, w: Workload, inputs: Dict[str, torch.Tensor], mode: str = "prefill",
+                 num_splits: int = 0, with_lse: bool = True):
+        if mode not in ("prefill", "decode"):
+            raise ValueError(mode)
+        self.w, self.x, self.mode = w, inputs, mode
+        dev = inputs["q"].device
+        N, Hq, d = inputs["q"].shape
+        self.q_out = torch.empty_like(inputs["q"])
+        self.out = torch.empty((N, Hq, d), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((N, Hq), dtype=torch.float32, device=dev) if with_lse else None
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        max_q = max(w.q_lens) if w.q_lens else 0
+        max_k = max(w.seqlen_k) if w.seqlen_k else 0
+        self.pro = ia.prologue_params(
+            q=inputs["q"], k=inputs["k"], v=inputs["v"], conv_w_k=inputs["conv_w_k"],
+            conv_w_v=inputs["conv_w_v"], q_norm_w=inputs["q_norm_w"], k_norm_w=inputs["k_norm_w"],
+            cu_seqlens_q=inputs["cu_seqlens_q"], state_slot=inputs["state_slot"],
+            slot_mapping=inputs["slot_mapping"], conv_state_k=inputs["conv_state_k"],
+            conv_state_v=inputs["conv_state_v"], q_out=self.q_out, k_cache=inputs["k_cache"],
+            v_cache=inputs["v_cache"], max_seqlen_q=max_q, eps=w.eps, dev_status=self.status)
+        self.attn = ia.attn_params(
+            q=self.q_out, k_cache=inputs["k_cache"], v_cache=inputs["v_cache"],
+            cu_seqlens_q=inputs["cu_seqlens_q"], seqlen_k=inputs["seqlen_k"],
+            block_table=inputs["block_table"], out=self.out, max_seqlen_q=max_q, max_seqlen_k=max_k,
+            r=inputs["r"], P=inputs["P"], rel_extent=w.rel_extent, window=w.window,
+            log_scale_base=w.log_scale_base, lse=self.lse, dev_status=self.status)
+        self.num_splits = 0
+        self.workspace: Optional[torch.Tensor] = None
+        if mode == "decode":
+            self.num_splits = num_splits if num_splits > 0 else self.heuristic_splits()
+            nbytes = ia.inkattn_decode_workspace_bytes(self.attn, self.num_splits)
+            if nbytes:
+                self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+    def heuristic_splits(self) -> int:
+        sms = torch.cuda.get_device_properties(self.x["q"].device).multi_processor_count
+        return ia.inkattn_decode_num_splits(self.attn, sms)
+
+    def run_prologue(self, stream=None):
+        ia.inkattn_prologue(self.pro, stream)
+
+    def run_attention(self, stream=None):
+        if self.mode == "prefill":
+            ia.inkattn_prefill(self.attn, stream)
+        else:
+            ia.inkattn_decode(self.attn, self.num_splits, self.workspace, stream)
+            ia.inkattn_combine(self.attn, self.num_splits, self.workspace, stream)
+
+    def run(self, stream=None):
+        self.run_prologue(stream)
+        self.run_attention(stream)
+
+    def launches_per_run(self) -> int:
+        n = 2
+        if self.mode == "decode" and self.num_splits > 1:
+            n += 1
+        return n
+
+    def device_status(self) -> int:
+        return int(self.status.item())

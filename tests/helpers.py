@@ -43,3 +43,27 @@ def paged_cache(k_dense, v_dense, block_size, Hkv, d, perm_seed=None, spare=0):
             kc[blk, :, off, :] = k_dense[b][j]
             vc[blk, :, off, :] = v_dense[b][j]
     return kc, vc, table
+
+
+def bf16_ulp_diff(a_bits, b_bits) -> np.ndarray:
+    """|a - b| in units of the bf16 spacing at max(|a|, |b|), element-wise."""
+    a, b = from_bits(a_bits), from_bits(b_bits)
+    m = np.maximum(np.abs(a), np.abs(b))
+    ulp = np.exp2(np.floor(np.log2(np.maximum(m, 2.0 ** -126))) - 7)
+    return np.abs(a - b) / ulp
+
+
+def compact_cache(k_cache_bits, v_cache_bits, block_table, seqlen_k, seqs, block_size=64):
+    """The blocks of the listed sequences only, with a block table renumbered to match
+    (so the oracle can run on a few sequences of a large paged cache)."""
+    rows, blocks = [], []
+    for b in seqs:
+        n = (int(seqlen_k[b]) + block_size - 1) // block_size
+        ids = np.asarray(block_table[b, :n])
+        rows.append(np.arange(len(blocks), len(blocks) + n))
+        blocks.extend(ids.tolist())
+    idx = np.asarray(blocks)
+    table = np.full((len(seqs), max(len(r) for r in rows)), -1, np.int32)
+    for i, r in enumerate(rows):
+        table[i, :len(r)] = r
+    return k_cache_bits[idx], v_cache_bits[idx], table

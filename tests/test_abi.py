@@ -1,0 +1,136 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point the header
+declares, its ctypes mirror matches the C struct layout, and host-side validation and
+the split heuristic work without touching the device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "inkattn.h")
+
+
+@pytest.fixture(scope="module")
+def ia():
+    from relative_bias_hybrid_gb300 import build
+    build.build()
+    import relative_bias_hybrid_gb300.inkattn as ia
+    ia.lib()
+    return ia
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"INKATTN_API\s+[\w\s\*]+?\b(inkattn_\w+)\s*\(", text)
+
+
+def test_header_declares_the_entry_points():
+    names = set(_declared_functions())
+    assert {"inkattn_prologue", "inkattn_prefill", "inkattn_decode", "inkattn_combine",
+            "inkattn_decode_num_splits", "inkattn_decode_workspace_bytes",
+            "inkattn_status_string", "inkattn_abi_version"} <= names
+
+
+def test_library_exports_every_declared_symbol(ia):
+    out = subprocess.run(["nm", "-D", "--defined-only", ia.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in _declared_functions():
+        assert name in exported, name
+        assert hasattr(ia.lib(), name)
+    # hidden visibility: nothing else named inkattn_* leaks out
+    assert {n for n in exported if n.startswith("inkattn_")} == set(_declared_functions())
+
+
+def test_ctypes_structs_match_c_layout(ia, tmp_path):
+    structs = {"inkattn_prologue_params": ia.PrologueParams, "inkattn_attn_params": ia.AttnParams}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", f'#include "{HEADER}"', "int main(void){"]
+    for cname, py in structs.items():
+        lines.append(f'printf("{cname} sizeof %zu\\n", sizeof({cname}));')
+        for fname, _ in py._fields_:
+            lines.append(f'printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines.append("return 0;}")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", str(src), "-o", str(exe)], check=True)
+    got = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    for line in filter(None, got):
+        cname, field, value = line.split()
+        py = structs[cname]
+        if field == "sizeof":
+            assert ctypes.sizeof(py) == int(value), cname
+        else:
+            assert getattr(py, field).offset == int(value), (cname, field)
+
+
+def test_status_strings(ia):
+    assert ia.status_string(0) == "ok"
+    assert "invalid" in ia.status_string(1)
+    assert "timed out" in ia.status_string(4)
+    assert "bounds" in ia.status_string(5)
+    assert ia.abi_version() == 1
+
+
+def _attn(ia, **kw):
+    p = ia.AttnParams()
+    p.struct_size = ctypes.sizeof(ia.AttnParams)
+    p.B, p.N_tok, p.max_seqlen_q, p.max_seqlen_k = 32, 32 * 9, 9, 32768
+    p.Hq, p.Hkv, p.head_dim, p.block_size = 64, 8, 128, 64
+    p.num_blocks, p.max_blocks_per_seq = 32 * 512, 512
+    p.d_r, p.rel_extent, p.window = 32, 1024, 0
+    p.log_scale_base = 8192.0
+    fake = 1 << 20   # any 256-aligned non-null value: these calls never dereference it
+    for f in ("q", "r", "P", "k_cache", "v_cache", "cu_seqlens_q", "seqlen_k", "block_table", "out"):
+        setattr(p, f, fake)
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_host_validation_rejects_before_any_launch(ia):
+    L = ia.lib()
+    assert L.inkattn_prefill(None, None) == ia.INKATTN_ERR_INVALID_ARG
+    assert L.inkattn_prologue(None, None) == ia.INKATTN_ERR_INVALID_ARG
+    assert ia.inkattn_prefill(_attn(ia, struct_size=8), raise_on_error=False, stream=0) == \
+        ia.INKATTN_ERR_INVALID_ARG
+    assert ia.inkattn_prefill(_attn(ia, head_dim=64), raise_on_error=False, stream=0) == \
+        ia.INKATTN_ERR_UNSUPPORTED
+    assert ia.inkattn_prefill(_attn(ia, block_size=32), raise_on_error=False, stream=0) == \
+        ia.INKATTN_ERR_UNSUPPORTED
+    assert ia.inkattn_prefill(_attn(ia, Hq=63), raise_on_error=False, stream=0) == \
+        ia.INKATTN_ERR_INVALID_ARG
+    assert ia.inkattn_prefill(_attn(ia, q=None), raise_on_error=False, stream=0) == \
+        ia.INKATTN_ERR_INVALID_ARG
+    assert ia.inkattn_prefill(_attn(ia, q=(1 << 20) + 2), raise_on_error=False, stream=0) == \
+        ia.INKATTN_ERR_INVALID_ARG      # not 16-byte aligned
+    assert ia.inkattn_prefill(_attn(ia, d_r=24), raise_on_error=False, stream=0) == \
+        ia.INKATTN_ERR_UNSUPPORTED
+    assert ia.inkattn_prefill(_attn(ia, max_blocks_per_seq=10), raise_on_error=False, stream=0) == \
+        ia.INKATTN_ERR_INVALID_ARG      # table too short for max_seqlen_k
+    # decode-only shape limits
+    assert ia.inkattn_decode(_attn(ia, max_seqlen_q=17), 4, None, raise_on_error=False, stream=0) == \
+        ia.INKATTN_ERR_UNSUPPORTED
+    assert ia.inkattn_decode(_attn(ia), 65, None, raise_on_error=False, stream=0) == \
+        ia.INKATTN_ERR_INVALID_ARG
+
+
+def test_split_heuristic_and_workspace_size(ia):
+    p = _attn(ia)
+    S = ia.inkattn_decode_num_splits(p, 152)
+    assert 1 < S <= 64
+    nblk = 32768 // 64
+    assert -(-nblk // S) >= 8                      # each split streams >= 8 blocks
+    # enough (sequence, KV head) units to fill two waves: no split
+    assert ia.inkattn_decode_num_splits(_attn(ia, B=64, N_tok=64 * 9), 152) == 1
+    # short KV: few blocks, few splits
+    short = _attn(ia, B=1, N_tok=9, max_seqlen_k=1024, max_blocks_per_seq=16)
+    assert ia.inkattn_decode_num_splits(short, 152) <= 2
+    # explicit split counts need no device
+    per = 32 * 9 * 64 * 5
+    expect = ((per * 128 * 4 + 255) // 256) * 256 + ((per * 4 + 255) // 256) * 256
+    assert ia.inkattn_decode_workspace_bytes(p, 5) == expect
+    assert ia.inkattn_decode_workspace_bytes(p, 1) == 0
+    assert ia.inkattn_decode_num_splits(_attn(ia, max_seqlen_q=17), 152) == 0

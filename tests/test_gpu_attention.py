@@ -1,0 +1,230 @@
+"""GPU parity of inkattn_prefill / inkattn_decode + inkattn_combine against the fp64
+oracle, on the same bf16 queries and caches the GPU prologue produced (so the attention
+error is isolated).  Bar: max-abs <= 1e-2 and mean-abs <= 1e-3 on the outputs, and
+|lse - lse_ref| <= 2e-3.  Full-size workloads are checked on sampled rows (all heads),
+chosen to include tile edges, window and rel_extent edges and sequence ends."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import compact_cache
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS, LSE_ABS = 1e-2, 1e-3, 2e-3
+
+
+@pytest.fixture(scope="module")
+def env(oracle_mod):
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from relative_bias_hybrid_gb300 import build
+    build.build()
+    from relative_bias_hybrid_gb300 import inputs as gen
+    from relative_bias_hybrid_gb300.step import AttentionStep
+    return gen, AttentionStep, oracle_mod
+
+
+def _run(env, w, mode="prefill", seed=0, device_inputs=False, num_splits=0):
+    gen, AttentionStep, _ = env
+    if device_inputs:
+        x = gen.make_inputs(w, seed=seed, device="cuda")
+        x_cpu = None
+    else:
+        x_cpu = gen.make_inputs(w, seed=seed, device="cpu")
+        x = {k: v.cuda() for k, v in x_cpu.items()}
+    step = AttentionStep(w, x, mode=mode, num_splits=num_splits)
+    step.run()
+    torch.cuda.synchronize()
+    assert step.device_status() == 0
+    return x_cpu, x, step
+
+
+def _compare(out, lse, o_ref, lse_ref, what):
+    err = np.abs(out - o_ref)
+    assert np.isfinite(out).all(), what
+    assert err.max() <= MAX_ABS, (what, err.max())
+    assert err.mean() <= MEAN_ABS, (what, err.mean())
+    if lse is not None:
+        assert np.abs(lse - lse_ref).max() <= LSE_ABS, (what, np.abs(lse - lse_ref).max())
+
+
+def _check_all_rows(env, w, x_cpu, x, step):
+    gen, _, oracle = env
+    o_ref, lse_ref = oracle.attention_for_inputs(x_cpu, w, gen.bits(step.q_out), gen.bits(x["k_cache"]),
+                                                 gen.bits(x["v_cache"]))
+    _compare(step.out.float().cpu().numpy(), step.lse.cpu().numpy(), o_ref, lse_ref, w.name)
+
+
+def _sample_rows(w, extra=()):
+    rows = set(extra)
+    start = 0
+    for b, n in enumerate(w.q_lens):
+        pre = w.prefix_lens[b]
+        for t in (0, 1, 63, 64, 127, 128, 129, n // 2, n - 129, n - 128, n - 2, n - 1):
+            if 0 <= t < n:
+                rows.add(start + t)
+        for edge in (w.window, w.rel_extent):         # positions where a window / extent edge lands
+            for dt in (-1, 0, 1):
+                t = edge + dt - pre
+                if edge and 0 <= t < n:
+                    rows.add(start + t)
+        start += n
+    return np.array(sorted(rows), np.int32)
+
+
+def _check_rows(env, w, x, step, rows):
+    """Oracle on sampled rows; only the tensors the oracle needs are copied to the host."""
+    gen, _, oracle = env
+    x_cpu = {k: x[k].cpu() for k in ("cu_seqlens_q", "seqlen_k", "r", "P", "block_table")}
+    o_ref, lse_ref = oracle.attention_for_inputs(x_cpu, w, gen.bits(step.q_out), gen.bits(x["k_cache"]),
+                                                 gen.bits(x["v_cache"]), rows=rows)
+    idx = torch.as_tensor(rows.astype(np.int64), device="cuda")
+    out = step.out.index_select(0, idx).float().cpu().numpy()
+    lse = step.lse.index_select(0, idx).cpu().numpy()
+    _compare(out, lse, o_ref, lse_ref, w.name)
+
+
+# ---------------------------------------------------------------- prefill
+
+def test_prefill_tiny_all_rows(env):
+    gen = env[0]
+    w = gen.workload("tiny")
+    _check_all_rows(env, w, *_run(env, w))
+
+
+@pytest.mark.parametrize("case", ["swa_ragged", "full_logscale", "no_bias", "extent_past_T", "gqa4"])
+def test_prefill_small_mixed(env, case):
+    gen = env[0]
+    kw = dict(Hq=8, Hkv=2, q_lens=[200, 77, 300, 1], prefix_lens=[0, 150, 37, 9])
+    if case == "swa_ragged":
+        w = gen.custom(case, window=100, rel_extent=70, **kw)
+    elif case == "full_logscale":
+        w = gen.custom(case, window=0, rel_extent=130, log_scale_base=64.0, **kw)
+    elif case == "no_bias":
+        w = gen.custom(case, window=0, rel_extent=0, **kw)
+    elif case == "extent_past_T":
+        w = gen.custom(case, window=0, rel_extent=600, **kw)
+    else:
+        w = gen.custom(case, Hq=16, Hkv=4, q_lens=[257, 129], prefix_lens=[64, 0], window=192,
+                       rel_extent=96, d_r=64)
+    _check_all_rows(env, w, *_run(env, w, seed=11))
+
+
+@pytest.mark.parametrize("name", ["swa", "full", "ragged"])
+def test_prefill_full_size_sampled(env, name):
+    gen = env[0]
+    w = gen.workload(name)
+    _, x, step = _run(env, w, device_inputs=True, seed=1)
+    rows = _sample_rows(w)
+    if name == "full":
+        rows = rows[:: max(1, len(rows) // 24)]
+    _check_rows(env, w, x, step, rows)
+
+
+# ---------------------------------------------------------------- decode
+
+@pytest.mark.parametrize("splits", [1, 0, 3, 7])
+def test_decode_small(env, splits):
+    gen = env[0]
+    w = gen.custom("dec", Hq=16, Hkv=2, q_lens=[9, 9, 4, 1], prefix_lens=[700, 40, 1500, 3000],
+                   rel_extent=200, log_scale_base=256.0)
+    _check_all_rows(env, w, *_run(env, w, mode="decode", seed=4, num_splits=splits))
+
+
+def test_decode_sliding_window(env):
+    gen = env[0]
+    w = gen.custom("dec-swa", Hq=64, Hkv=8, q_lens=[9, 9], prefix_lens=[5000, 300], rel_extent=512,
+                   window=1024)
+    _check_all_rows(env, w, *_run(env, w, mode="decode", seed=6, num_splits=4))
+
+
+def test_decode_full_size_sampled(env):
+    """The MTP-verify workload (32 x 9 queries, KV 32768): three sequences against the
+    oracle; all sequences agree between one split and the heuristic's split count."""
+    gen, AttentionStep, oracle = env
+    w = gen.workload("decode")
+    x = gen.make_inputs(w, seed=2, device="cuda")
+    snap = {k: x[k].clone() for k in ("k_cache", "v_cache", "conv_state_k", "conv_state_v")}
+    step = AttentionStep(w, x, mode="decode")
+    assert step.num_splits > 1
+    step.run()
+    torch.cuda.synchronize()
+    assert step.device_status() == 0
+    seqs = [0, 17, 31]
+    bt = x["block_table"].cpu().numpy()
+    sk = x["seqlen_k"].cpu().numpy()
+    blocks = np.concatenate([bt[b, :(sk[b] + 63) // 64] for b in seqs])
+    idx = torch.as_tensor(blocks.astype(np.int64), device="cuda")
+    kc = gen.bits(x["k_cache"].index_select(0, idx))
+    vc = gen.bits(x["v_cache"].index_select(0, idx))
+    table = np.full((3, bt.shape[1]), -1, np.int32)
+    pos = 0
+    for i, b in enumerate(seqs):
+        n = (sk[b] + 63) // 64
+        table[i, :n] = np.arange(pos, pos + n)
+        pos += n
+    rows = np.concatenate([np.arange(b * 9, b * 9 + 9) for b in seqs])
+    q = gen.bits(step.q_out)[rows]
+    sub = gen.custom("dec3", Hq=64, Hkv=8, q_lens=[9] * 3, prefix_lens=[32759] * 3, rel_extent=1024,
+                     log_scale_base=8192.0)
+    xs = {"cu_seqlens_q": torch.tensor([0, 9, 18, 27], dtype=torch.int32),
+          "seqlen_k": torch.tensor([32768] * 3, dtype=torch.int32),
+          "r": x["r"][torch.as_tensor(rows.astype(np.int64), device="cuda")].cpu(),
+          "P": x["P"].cpu(), "block_table": torch.from_numpy(table)}
+    o_ref, lse_ref = oracle.attention_for_inputs(xs, sub, q, kc, vc)
+    ridx = torch.as_tensor(rows.astype(np.int64), device="cuda")
+    _compare(step.out.index_select(0, ridx).float().cpu().numpy(),
+             step.lse.index_select(0, ridx).cpu().numpy(), o_ref, lse_ref, "decode")
+    # same caches and conv state, one split: every sequence agrees
+    out_h = step.out.float().clone()
+    for k, v in snap.items():
+        x[k].copy_(v)
+    one = AttentionStep(w, x, mode="decode", num_splits=1)
+    one.run()
+    torch.cuda.synchronize()
+    assert (one.out.float() - out_h).abs().max().item() <= 2e-2
+
+
+def test_decode_equals_prefill_tail(env):
+    """Decoding the last 9 tokens against the cache equals the last 9 rows of a prefill."""
+    gen, AttentionStep, _ = env
+    T = 1000
+    wp = gen.custom("pre", Hq=16, Hkv=2, q_lens=[T], prefix_lens=[0], rel_extent=300,
+                    log_scale_base=128.0)
+    x_cpu = gen.make_inputs(wp, seed=12, device="cpu")
+    x = {k: v.cuda() for k, v in x_cpu.items()}
+    pre = AttentionStep(wp, x, mode="prefill")
+    pre.run()
+    wd = gen.custom("dec", Hq=16, Hkv=2, q_lens=[9], prefix_lens=[T - 9], rel_extent=300,
+                    log_scale_base=128.0)
+    xd = dict(x)
+    xd["r"] = x["r"][T - 9:].contiguous()
+    xd["cu_seqlens_q"] = torch.tensor([0, 9], dtype=torch.int32, device="cuda")
+    dec_q = pre.q_out[T - 9:].contiguous()
+    import relative_bias_hybrid_gb300.inkattn as ia
+    out = torch.empty_like(dec_q)
+    lse = torch.empty(dec_q.shape[:2], dtype=torch.float32, device="cuda")
+    p = ia.attn_params(q=dec_q, k_cache=x["k_cache"], v_cache=x["v_cache"], cu_seqlens_q=xd["cu_seqlens_q"],
+                       seqlen_k=x["seqlen_k"], block_table=x["block_table"], out=out, max_seqlen_q=9,
+                       max_seqlen_k=T, r=xd["r"], P=x["P"], rel_extent=300, log_scale_base=128.0, lse=lse)
+    for S in (1, 4):
+        nb = ia.inkattn_decode_workspace_bytes(p, S)
+        ws = torch.empty(max(nb, 1), dtype=torch.uint8, device="cuda")
+        ia.inkattn_decode(p, S, ws)
+        ia.inkattn_combine(p, S, ws)
+        torch.cuda.synchronize()
+        assert (out.float() - pre.out[T - 9:].float()).abs().max().item() <= 1e-2
+        assert (lse - pre.lse[T - 9:]).abs().max().item() <= 2e-3
+
+
+def test_bad_block_id_is_flagged(env):
+    gen, AttentionStep, _ = env
+    w = gen.custom("badblk", Hq=8, Hkv=2, q_lens=[100], prefix_lens=[50], rel_extent=20)
+    x_cpu = gen.make_inputs(w, seed=13, device="cpu")
+    x_cpu["block_table"][0, 1] = 10 ** 6
+    x = {k: v.cuda() for k, v in x_cpu.items()}
+    step = AttentionStep(w, x, mode="prefill")
+    step.run()
+    torch.cuda.synchronize()
+    assert step.device_status() == 5
