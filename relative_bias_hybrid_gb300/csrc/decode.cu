@@ -95,6 +95,10 @@ k_decode(const DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
     const int my_hi = min(blk_end, my_lo + per);
     const int my_n = max(0, my_hi - my_lo);
 
+    if ((s_base & 1023u) != 0u) {      // the 128-byte-swizzled TMA boxes need 1024-byte alignment
+        if (threadIdx.x == 0) set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
+        return;
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < kDecStages; ++s) {
             mbar_init(bar_full + 8 * s, 1);

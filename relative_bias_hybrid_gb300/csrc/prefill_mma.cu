@@ -75,6 +75,10 @@ k_prefill_mma(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
     const uint32_t bar_empty = bar_full + kPmStages * 8;
     const uint32_t bar_q = bar_empty + kPmStages * 8;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kPmBarOff + (2 * kPmStages + 1) * 8);
+    if ((s_base & 1023u) != 0u) {      // the 128-byte-swizzled TMA boxes need 1024-byte alignment
+        if (threadIdx.x == 0) set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
+        return;
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < kPmStages; ++s) {
             mbar_init(bar_full + 8 * s, 1);
