@@ -9,6 +9,9 @@
 // [vLLM hỗ trợ TML Inkling ..., §Quản lý bộ nhớ đệm sconv]: the state keeps the hidden
 //  states of the last W-1 tokens.
 //
+// The conv sum of each channel is formed exactly (error-free products and sums in fp32)
+// and rounded once to bf16, which is the correctly rounded value of the definition.
+//
 // Work split: one CTA per (16-token tile of one sequence, KV head hk).  It handles, for
 // its tokens, the g = Hq/Hkv query heads of that KV head (RMSNorm only), the K stream
 // of head hk (conv, round to bf16, RMSNorm, cache write) and the V stream (conv,
@@ -42,9 +45,52 @@ __device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
     return u;
 }
 
+// Exact-sum helpers for the conv: a*b = p + e exactly (fma), a + b = s + e exactly.
+__device__ __forceinline__ void two_prod(float a, float b, float &p, float &e) {
+    p = a * b;
+    e = fmaf(a, b, -p);
+}
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+    s = a + b;
+    const float bb = s - a;
+    e = (a - (s - bb)) + (b - bb);
+}
+
+// bf16 of the value hi + lo (|lo| <= half an fp32 ulp of hi), rounded to nearest even:
+// rounding hi alone is right unless hi sits exactly on a bf16 tie, where lo decides.
+__device__ __forceinline__ float round_pair_bf16(float hi, float lo) {
+    const uint32_t u = __float_as_uint(hi);
+    if ((u & 0xFFFFu) == 0x8000u && lo != 0.f) {
+        const bool away = (lo > 0.f) == (hi > 0.f);
+        return __uint_as_float(((u >> 16) + (away ? 1u : 0u)) << 16);
+    }
+    return __bfloat162float(__float2bfloat16_rn(hi));
+}
+
+// Correctly rounded bf16 of sum_{k=0..3} w[k]*x[k]: the products are split exactly and
+// the running sum is carried as an unevaluated pair, so hi + lo equals the exact sum up
+// to ~2^-47 of the largest term (fp32 accumulation alone can lose every bit of a
+// strongly cancelling sum).
+__device__ __forceinline__ float conv4_bf16(const float (&w)[4], const float (&x)[4]) {
+    float s, c;
+    two_prod(w[0], x[0], s, c);
+#pragma unroll
+    for (int k = 1; k < 4; ++k) {
+        float p, pe, t, te;
+        two_prod(w[k], x[k], p, pe);
+        two_sum(s, p, t, te);
+        s = t;
+        c += te + pe;
+    }
+    float hi, lo;
+    two_sum(s, c, hi, lo);
+    return round_pair_bf16(hi, lo);
+}
+
 __global__ void __launch_bounds__(kPrologueThreads)
 k_prologue(const inkattn_prologue_params p) {
-    __shared__ float s_wk[kHeadDim * 4], s_wv[kHeadDim * 4];
+    __shared__ __align__(16) float s_wk[kHeadDim * 4];
+    __shared__ __align__(16) float s_wv[kHeadDim * 4];
     __shared__ float s_gq[kHeadDim], s_gk[kHeadDim];
 
     const int tile = blockIdx.x, b = blockIdx.y, hk = blockIdx.z;
@@ -109,7 +155,7 @@ k_prologue(const inkattn_prologue_params p) {
                 const inkattn_bf16 *src = isk ? p.k : p.v;
                 const inkattn_bf16 *st = isk ? p.conv_state_k : p.conv_state_v;
                 const float *w = isk ? s_wk : s_wv;
-                float acc[8];
+                float xt[4][8];
 #pragma unroll
                 for (int tap = 0; tap < 4; ++tap) {
                     const int idx = t + tap;      // index into [3 carried rows ; new rows]
@@ -121,17 +167,15 @@ k_prologue(const inkattn_prologue_params p) {
                         raw = __ldg(reinterpret_cast<const uint4 *>(
                             src + ((size_t)start + idx - 3) * C + head_off));
                     }
-                    float xv[8];
-                    unpack8(raw, xv);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float we = w[(c0 + e) * 4 + tap];
-                        acc[e] = tap == 0 ? we * xv[e] : fmaf(we, xv[e], acc[e]);
-                    }
+                    unpack8(raw, xt[tap]);
                 }
 #pragma unroll
-                for (int e = 0; e < 8; ++e)   // the conv output is rounded to bf16
-                    x[u][e] = __bfloat162float(__float2bfloat16_rn(acc[e]));
+                for (int e = 0; e < 8; ++e) {   // the conv output is rounded to bf16
+                    const float4 w4 = *reinterpret_cast<const float4 *>(w + (c0 + e) * 4);
+                    const float we[4] = {w4.x, w4.y, w4.z, w4.w};
+                    const float xe[4] = {xt[0][e], xt[1][e], xt[2][e], xt[3][e]};
+                    x[u][e] = conv4_bf16(we, xe);
+                }
             }
         }
         // phase 2: RMSNorm (all lanes take part in the shuffles) and stores
