@@ -48,6 +48,10 @@ extern "C" {
 
 typedef uint16_t inkattn_bf16;
 
+/* Element type of the attention output. */
+#define INKATTN_DTYPE_BF16 0
+#define INKATTN_DTYPE_F32 1
+
 typedef enum inkattn_status {
     INKATTN_OK = 0,
     INKATTN_ERR_INVALID_ARG = 1,     /* bad pointer, size, or combination of sizes     */
@@ -144,6 +148,7 @@ typedef struct inkattn_attn_params {
     int32_t d_r;               /* relative feature size: 16, 32, 48 or 64                */
     int32_t rel_extent;        /* >= 0; 0 disables the bias                              */
     int32_t window;            /* 0 = full attention, else the sliding window (keys)     */
+    int32_t out_dtype;         /* INKATTN_DTYPE_BF16 (0) or INKATTN_DTYPE_F32 (1) for out */
     float softmax_scale;       /* <= 0 -> 1/sqrt(128)                                    */
     float log_scale_base;      /* <= 1 -> no length-dependent scaling (8192 on full layers) */
     const inkattn_bf16 *q;     /* [N_tok][Hq][128], the normalised queries               */
@@ -154,7 +159,8 @@ typedef struct inkattn_attn_params {
     const int32_t *cu_seqlens_q;   /* [B+1]                                              */
     const int32_t *seqlen_k;       /* [B], q_len[b] <= seqlen_k[b] <= max_seqlen_k       */
     const int32_t *block_table;    /* [B][max_blocks_per_seq]                            */
-    inkattn_bf16 *out;             /* [N_tok][Hq][128]                                   */
+    void *out;                     /* [N_tok][Hq][128], bf16 or fp32 per out_dtype; the   */
+                                   /* bf16 form is the fp32 result rounded once (RNE)     */
     float *lse;                    /* nullable, [N_tok][Hq]                              */
     int32_t *dev_status;           /* nullable                                           */
 } inkattn_attn_params;

@@ -97,6 +97,7 @@ inkattn_status validate_attn(const inkattn_attn_params *p) {
     if ((long long)p->max_blocks_per_seq * kBlock < p->max_seqlen_k) return INKATTN_ERR_INVALID_ARG;
     if ((long long)p->num_blocks * p->Hkv * kBlock >= (1ll << 31)) return INKATTN_ERR_INVALID_ARG;
     if (p->head_dim != kHeadDim || p->block_size != kBlock) return INKATTN_ERR_UNSUPPORTED;
+    if (p->out_dtype != INKATTN_DTYPE_BF16 && p->out_dtype != INKATTN_DTYPE_F32) return INKATTN_ERR_INVALID_ARG;
     if (!(p->softmax_scale == p->softmax_scale) || !(p->log_scale_base == p->log_scale_base))
         return INKATTN_ERR_INVALID_ARG;
     const void *ptrs16[] = {p->q, p->k_cache, p->v_cache, p->out};

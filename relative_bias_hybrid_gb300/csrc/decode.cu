@@ -410,14 +410,18 @@ k_decode(const DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
                 const size_t qrow = (size_t)(start + t) * p.Hq + hk * g + hh;
                 const float lse_nat = l > 0.f ? (ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
                 if (a.S == 1) {
-                    inkattn_bf16 *dst = p.out + qrow * kHeadDim;
 #pragma unroll
                     for (int n = 0; n < 16; ++n) {
                         const int c = n * 8 + 2 * tq;
                         const float *src = mb + (gq + 8 * hr) * kHeadDim + c;
                         const float v0 = (o[n][2 * hr] * w0 + src[0] * w1) * inv;
                         const float v1 = (o[n][2 * hr + 1] * w0 + src[1] * w1) * inv;
-                        *reinterpret_cast<uint32_t *>(dst + c) = pack_bf16(v0, v1);
+                        if (p.out_dtype == INKATTN_DTYPE_F32)
+                            *reinterpret_cast<float2 *>(static_cast<float *>(p.out) + qrow * kHeadDim + c) =
+                                make_float2(v0, v1);
+                        else
+                            *reinterpret_cast<uint32_t *>(static_cast<inkattn_bf16 *>(p.out) + qrow * kHeadDim + c) =
+                                pack_bf16(v0, v1);
                     }
                     if (p.lse && tq == 0) p.lse[qrow] = lse_nat;
                 } else {
@@ -463,10 +467,15 @@ k_combine(const inkattn_attn_params p, int S, const float *__restrict__ ws_o,
         }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    uint2 pk;
-    pk.x = pack_bf16(acc.x * inv, acc.y * inv);
-    pk.y = pack_bf16(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2 *>(p.out + row * kHeadDim + lane * 4) = pk;
+    if (p.out_dtype == INKATTN_DTYPE_F32) {
+        *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + row * kHeadDim + lane * 4) =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    } else {
+        uint2 pk;
+        pk.x = pack_bf16(acc.x * inv, acc.y * inv);
+        pk.y = pack_bf16(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2 *>(static_cast<inkattn_bf16 *>(p.out) + row * kHeadDim + lane * 4) = pk;
+    }
     if (p.lse && lane == 0) p.lse[row] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
 }
 

@@ -320,11 +320,18 @@ k_prefill_mma(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
         if (rr >= q_len) continue;
         const size_t qrow = (size_t)(start + rr) * p.Hq + h;
         const float inv = l_run[hr] > 0.f ? 1.f / l_run[hr] : 0.f;
-        inkattn_bf16 *dst = p.out + qrow * kHeadDim;
+        if (p.out_dtype == INKATTN_DTYPE_F32) {
+            float *dst = static_cast<float *>(p.out) + qrow * kHeadDim;
 #pragma unroll
-        for (int n = 0; n < 16; ++n) {
-            const int c = n * 8 + 2 * tq;
-            *reinterpret_cast<uint32_t *>(dst + c) = pack_bf16(o[n][2 * hr] * inv, o[n][2 * hr + 1] * inv);
+            for (int n = 0; n < 16; ++n)
+                *reinterpret_cast<float2 *>(dst + n * 8 + 2 * tq) =
+                    make_float2(o[n][2 * hr] * inv, o[n][2 * hr + 1] * inv);
+        } else {
+            inkattn_bf16 *dst = static_cast<inkattn_bf16 *>(p.out) + qrow * kHeadDim;
+#pragma unroll
+            for (int n = 0; n < 16; ++n)
+                *reinterpret_cast<uint32_t *>(dst + n * 8 + 2 * tq) =
+                    pack_bf16(o[n][2 * hr] * inv, o[n][2 * hr + 1] * inv);
         }
         if (p.lse && tq == 0) {
             const float ref = m_run[hr] == -INFINITY ? 0.f : m_run[hr];

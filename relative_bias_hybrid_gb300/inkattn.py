@@ -24,6 +24,8 @@ INKATTN_ERR_UNSUPPORTED = 2
 INKATTN_ERR_CUDA = 3
 INKATTN_ERR_DEVICE_TIMEOUT = 4
 INKATTN_ERR_DEVICE_BOUNDS = 5
+INKATTN_DTYPE_BF16 = 0
+INKATTN_DTYPE_F32 = 1
 
 _c_i32 = ctypes.c_int32
 _c_ptr = ctypes.c_void_p
@@ -51,7 +53,7 @@ class AttnParams(ctypes.Structure):
         ("B", _c_i32), ("N_tok", _c_i32), ("max_seqlen_q", _c_i32), ("max_seqlen_k", _c_i32),
         ("Hq", _c_i32), ("Hkv", _c_i32), ("head_dim", _c_i32), ("block_size", _c_i32),
         ("num_blocks", _c_i32), ("max_blocks_per_seq", _c_i32), ("d_r", _c_i32),
-        ("rel_extent", _c_i32), ("window", _c_i32),
+        ("rel_extent", _c_i32), ("window", _c_i32), ("out_dtype", _c_i32),
         ("softmax_scale", ctypes.c_float), ("log_scale_base", ctypes.c_float),
         ("q", _c_ptr), ("r", _c_ptr), ("P", _c_ptr), ("k_cache", _c_ptr), ("v_cache", _c_ptr),
         ("cu_seqlens_q", _c_ptr), ("seqlen_k", _c_ptr), ("block_table", _c_ptr),
@@ -230,7 +232,13 @@ def attn_params(*, q, k_cache, v_cache, cu_seqlens_q, seqlen_k, block_table, out
     p.cu_seqlens_q = _ptr(cu_seqlens_q, i32, "cu_seqlens_q")
     p.seqlen_k = _ptr(seqlen_k, i32, "seqlen_k")
     p.block_table = _ptr(block_table, i32, "block_table")
-    p.out = _ptr(out, bf, "out")
+    if out.dtype == torch.float32:
+        p.out_dtype = INKATTN_DTYPE_F32
+    elif out.dtype == bf:
+        p.out_dtype = INKATTN_DTYPE_BF16
+    else:
+        raise TypeError(f"out: expected bfloat16 or float32, got {out.dtype}")
+    p.out = _ptr(out, None, "out")
     p.lse = _ptr(lse, f32, "lse")
     p.dev_status = _ptr(dev_status, i32, "dev_status")
     return p

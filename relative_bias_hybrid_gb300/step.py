@@ -23,14 +23,14 @@ class AttentionStep:
     """
 
     def __init__(self, w: Workload, inputs: Dict[str, torch.Tensor], mode: str = "prefill",
-                 num_splits: int = 0, with_lse: bool = True):
+                 num_splits: int = 0, with_lse: bool = True, out_dtype=torch.bfloat16):
         if mode not in ("prefill", "decode"):
             raise ValueError(mode)
         self.w, self.x, self.mode = w, inputs, mode
         dev = inputs["q"].device
         N, Hq, d = inputs["q"].shape
         self.q_out = torch.empty_like(inputs["q"])
-        self.out = torch.empty((N, Hq, d), dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty((N, Hq, d), dtype=out_dtype, device=dev)
         self.lse = torch.empty((N, Hq), dtype=torch.float32, device=dev) if with_lse else None
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         max_q = max(w.q_lens) if w.q_lens else 0

@@ -2,7 +2,11 @@
 oracle, on the same bf16 queries and caches the GPU prologue produced (so the attention
 error is isolated).  Bar: max-abs <= 1e-2 and mean-abs <= 1e-3 on the outputs, and
 |lse - lse_ref| <= 2e-3.  Full-size workloads are checked on sampled rows (all heads),
-chosen to include tile edges, window and rel_extent edges and sequence ends."""
+chosen to include tile edges, window and rel_extent edges and sequence ends.
+
+The bar is checked on fp32 outputs (out_dtype = f32): a bf16 output adds its own
+rounding, up to half a bf16 ulp (0.0078 for |o| in [2, 4), 0.0156 above 4), which alone
+can exceed 1e-2.  A separate test pins the bf16 output to the fp32 one rounded once."""
 import numpy as np
 import pytest
 import torch
@@ -25,7 +29,7 @@ def env(oracle_mod):
     return gen, AttentionStep, oracle_mod
 
 
-def _run(env, w, mode="prefill", seed=0, device_inputs=False, num_splits=0):
+def _run(env, w, mode="prefill", seed=0, device_inputs=False, num_splits=0, out_dtype=torch.float32):
     gen, AttentionStep, _ = env
     if device_inputs:
         x = gen.make_inputs(w, seed=seed, device="cuda")
@@ -33,7 +37,7 @@ def _run(env, w, mode="prefill", seed=0, device_inputs=False, num_splits=0):
     else:
         x_cpu = gen.make_inputs(w, seed=seed, device="cpu")
         x = {k: v.cuda() for k, v in x_cpu.items()}
-    step = AttentionStep(w, x, mode=mode, num_splits=num_splits)
+    step = AttentionStep(w, x, mode=mode, num_splits=num_splits, out_dtype=out_dtype)
     step.run()
     torch.cuda.synchronize()
     assert step.device_status() == 0
@@ -43,7 +47,8 @@ def _run(env, w, mode="prefill", seed=0, device_inputs=False, num_splits=0):
 def _compare(out, lse, o_ref, lse_ref, what):
     err = np.abs(out - o_ref)
     assert np.isfinite(out).all(), what
-    assert err.max() <= MAX_ABS, (what, err.max())
+    where = np.unravel_index(int(np.argmax(err)), err.shape)
+    assert err.max() <= MAX_ABS, (what, err.max(), "at", where, "ref", o_ref[where], "mean", err.mean())
     assert err.mean() <= MEAN_ABS, (what, err.mean())
     if lse is not None:
         assert np.abs(lse - lse_ref).max() <= LSE_ABS, (what, np.abs(lse - lse_ref).max())
@@ -146,7 +151,7 @@ def test_decode_full_size_sampled(env):
     w = gen.workload("decode")
     x = gen.make_inputs(w, seed=2, device="cuda")
     snap = {k: x[k].clone() for k in ("k_cache", "v_cache", "conv_state_k", "conv_state_v")}
-    step = AttentionStep(w, x, mode="decode")
+    step = AttentionStep(w, x, mode="decode", out_dtype=torch.float32)
     assert step.num_splits > 1
     step.run()
     torch.cuda.synchronize()
@@ -180,7 +185,7 @@ def test_decode_full_size_sampled(env):
     out_h = step.out.float().clone()
     for k, v in snap.items():
         x[k].copy_(v)
-    one = AttentionStep(w, x, mode="decode", num_splits=1)
+    one = AttentionStep(w, x, mode="decode", num_splits=1, out_dtype=torch.float32)
     one.run()
     torch.cuda.synchronize()
     assert (one.out.float() - out_h).abs().max().item() <= 2e-2
@@ -194,7 +199,7 @@ def test_decode_equals_prefill_tail(env):
                     log_scale_base=128.0)
     x_cpu = gen.make_inputs(wp, seed=12, device="cpu")
     x = {k: v.cuda() for k, v in x_cpu.items()}
-    pre = AttentionStep(wp, x, mode="prefill")
+    pre = AttentionStep(wp, x, mode="prefill", out_dtype=torch.float32)
     pre.run()
     wd = gen.custom("dec", Hq=16, Hkv=2, q_lens=[9], prefix_lens=[T - 9], rel_extent=300,
                     log_scale_base=128.0)
@@ -203,7 +208,7 @@ def test_decode_equals_prefill_tail(env):
     xd["cu_seqlens_q"] = torch.tensor([0, 9], dtype=torch.int32, device="cuda")
     dec_q = pre.q_out[T - 9:].contiguous()
     import relative_bias_hybrid_gb300.inkattn as ia
-    out = torch.empty_like(dec_q)
+    out = torch.empty(dec_q.shape, dtype=torch.float32, device="cuda")
     lse = torch.empty(dec_q.shape[:2], dtype=torch.float32, device="cuda")
     p = ia.attn_params(q=dec_q, k_cache=x["k_cache"], v_cache=x["v_cache"], cu_seqlens_q=xd["cu_seqlens_q"],
                        seqlen_k=x["seqlen_k"], block_table=x["block_table"], out=out, max_seqlen_q=9,
@@ -228,3 +233,32 @@ def test_bad_block_id_is_flagged(env):
     step.run()
     torch.cuda.synchronize()
     assert step.device_status() == 5
+
+
+@pytest.mark.parametrize("mode,splits", [("prefill", 0), ("decode", 1), ("decode", 4)])
+def test_bf16_output_is_the_fp32_output_rounded_once(env, mode, splits):
+    gen, AttentionStep, _ = env
+    import relative_bias_hybrid_gb300.inkattn as ia
+    if mode == "prefill":
+        w = gen.custom("rnd", Hq=8, Hkv=2, q_lens=[300, 129], prefix_lens=[0, 40], rel_extent=90,
+                       window=200)
+    else:
+        w = gen.custom("rnd", Hq=16, Hkv=2, q_lens=[9, 7], prefix_lens=[900, 2000], rel_extent=300,
+                       log_scale_base=512.0)
+    x = gen.make_inputs(w, seed=14, device="cuda")
+    step = AttentionStep(w, x, mode=mode, num_splits=splits, out_dtype=torch.float32)
+    step.run_prologue()
+    step.run_attention()
+    out_bf = torch.empty(step.out.shape, dtype=torch.bfloat16, device="cuda")
+    p = ia.attn_params(q=step.q_out, k_cache=x["k_cache"], v_cache=x["v_cache"],
+                       cu_seqlens_q=x["cu_seqlens_q"], seqlen_k=x["seqlen_k"],
+                       block_table=x["block_table"], out=out_bf, max_seqlen_q=max(w.q_lens),
+                       max_seqlen_k=max(w.seqlen_k), r=x["r"], P=x["P"], rel_extent=w.rel_extent,
+                       window=w.window, log_scale_base=w.log_scale_base)
+    if mode == "prefill":
+        ia.inkattn_prefill(p)
+    else:
+        ia.inkattn_decode(p, step.num_splits, step.workspace)
+        ia.inkattn_combine(p, step.num_splits, step.workspace)
+    torch.cuda.synchronize()
+    assert torch.equal(out_bf.view(torch.int16), step.out.to(torch.bfloat16).view(torch.int16))
