@@ -197,6 +197,37 @@ INKATTN_API inkattn_status inkattn_decode(const inkattn_attn_params *p, int num_
 INKATTN_API inkattn_status inkattn_combine(const inkattn_attn_params *p, int num_splits,
                                const void *workspace, size_t workspace_bytes, void *stream);
 
+/* ------------------------------------------------------------------------------
+ * Decode without a caller-provided workspace.  The pages have no counterpart: this
+ * is a library convenience.
+ *
+ * For callers that cannot allocate device memory where they decode: code running in a
+ * host function enqueued on a stream (no CUDA API calls are allowed there), plugin
+ * hosts that own all device memory and pass only inputs and outputs, and serving loops
+ * that must not allocate on the hot path (an allocation can synchronise the device).
+ *
+ * Same computation and result as inkattn_decode followed by inkattn_combine with the
+ * same num_splits (0 = the heuristic), writing out/lse.  The split partials go to a
+ * static device buffer of INKATTN_DECODE_NOALLOC_MAX_BYTES inside the library instead
+ * of a workspace; the call allocates nothing (no cudaMalloc, cudaFree or allocating
+ * library routine).
+ *   - Returns INKATTN_ERR_INVALID_ARG when the partials for the resolved split count
+ *     need more than INKATTN_DECODE_NOALLOC_MAX_BYTES, i.e. when
+ *     inkattn_decode_workspace_bytes(p, S) exceeds it; pass a smaller num_splits.
+ *   - The buffer's device address is looked up once per device, by the first call made
+ *     with that device current; make that first call before any stream capture.
+ *   - Every call on a device shares the one buffer and it keeps the last call's
+ *     contents.  Each call writes every partial it reads, so nothing needs clearing,
+ *     but calls whose GPU work overlaps (on different streams, or from several host
+ *     threads without ordering) race on the buffer: serialise them.
+ *   - Each GPU on which this part of the library is loaded holds the buffer until the
+ *     process exits.
+ * ------------------------------------------------------------------------------ */
+#define INKATTN_DECODE_NOALLOC_MAX_BYTES (64u << 20)
+
+INKATTN_API inkattn_status inkattn_decode_noalloc(const inkattn_attn_params *p, int num_splits,
+                                                  void *stream);
+
 #ifdef __cplusplus
 }
 #endif

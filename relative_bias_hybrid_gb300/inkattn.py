@@ -98,6 +98,8 @@ def lib():
             L.inkattn_decode.restype = ctypes.c_int
             L.inkattn_combine.argtypes = [P(AttnParams), ctypes.c_int, _c_ptr, ctypes.c_size_t, _c_ptr]
             L.inkattn_combine.restype = ctypes.c_int
+            L.inkattn_decode_noalloc.argtypes = [P(AttnParams), ctypes.c_int, _c_ptr]
+            L.inkattn_decode_noalloc.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -158,6 +160,17 @@ def inkattn_combine(p: AttnParams, num_splits: int, workspace: Optional[torch.Te
     nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     return _check(lib().inkattn_combine(ctypes.byref(p), int(num_splits), ptr, nbytes, _stream(stream)),
                   "inkattn_combine", raise_on_error)
+
+
+DECODE_NOALLOC_MAX_BYTES = 64 << 20
+
+
+def inkattn_decode_noalloc(p: AttnParams, num_splits: int, stream=None, raise_on_error=True) -> int:
+    """Decode + combine with the split partials in the library's static device buffer
+    (no workspace argument, no allocation): for callers that cannot allocate device
+    memory where they decode."""
+    return _check(lib().inkattn_decode_noalloc(ctypes.byref(p), int(num_splits), _stream(stream)),
+                  "inkattn_decode_noalloc", raise_on_error)
 
 
 # ------------------------------------------------------------------ marshalling helpers
