@@ -38,7 +38,8 @@ import torch  # noqa: E402
 METRIC = "rel-bias attn prefill TFLOP/s & decode KV GB/s (1 GB300, % of roofline)"
 L2_FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = {
-    "k_prefill_mma": ["relative_bias_hybrid_gb300/csrc/prefill_mma.cu", "relative_bias_hybrid_gb300/csrc/common.cuh"],
+    "k_prefill_tc": ["relative_bias_hybrid_gb300/csrc/prefill_tc.cu", "relative_bias_hybrid_gb300/csrc/tcgen05.cuh",
+                     "relative_bias_hybrid_gb300/csrc/common.cuh"],
     "k_decode": ["relative_bias_hybrid_gb300/csrc/decode.cu", "relative_bias_hybrid_gb300/csrc/common.cuh"],
     "k_prologue": ["relative_bias_hybrid_gb300/csrc/prologue.cu", "relative_bias_hybrid_gb300/csrc/common.cuh"],
 }
@@ -415,8 +416,8 @@ def run_gpu(args, world, rank, local):
     prefill_tf = fl / (att_ms * 1e-3) / 1e12
     pro_gbs = prologue_bytes(w) / (pro_ms * 1e-3) / 1e9
     dec_gbs = dbytes / (dec_ms * 1e-3) / 1e9
-    traffic = ncu_traffic("k_prefill_mma", "swa")
-    roof = {"bound": "tensor", "kernel": "k_prefill_mma", "achieved": prefill_tf, "peak": peaks["bf16"],
+    traffic = ncu_traffic("k_prefill_tc", "swa")
+    roof = {"bound": "tensor", "kernel": "k_prefill_tc", "achieved": prefill_tf, "peak": peaks["bf16"],
             "unit": "TFLOP/s", "frac": prefill_tf / peaks["bf16"], "peak_src": peaks["src"] + " (burst bf16)",
             "traffic": traffic, "algorithmic_flop_per_launch": fl}
     line = {

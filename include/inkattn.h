@@ -145,14 +145,14 @@ typedef struct inkattn_attn_params {
     int32_t block_size;        /* 64                                                     */
     int32_t num_blocks;        /* cache capacity in blocks (bounds check)                */
     int32_t max_blocks_per_seq;/* row length of block_table                              */
-    int32_t d_r;               /* relative feature size: 16, 32, 48 or 64                */
+    int32_t d_r;               /* relative feature size: 16 or 32                        */
     int32_t rel_extent;        /* >= 0; 0 disables the bias                              */
     int32_t window;            /* 0 = full attention, else the sliding window (keys)     */
     int32_t out_dtype;         /* INKATTN_DTYPE_BF16 (0) or INKATTN_DTYPE_F32 (1) for out */
     float softmax_scale;       /* <= 0 -> 1/sqrt(128)                                    */
     float log_scale_base;      /* <= 1 -> no length-dependent scaling (8192 on full layers) */
     const inkattn_bf16 *q;     /* [N_tok][Hq][128], the normalised queries               */
-    const inkattn_bf16 *r;     /* [N_tok][Hq][d_r]  (nullable iff rel_extent == 0)      */
+    const inkattn_bf16 *r;     /* [N_tok][Hq][d_r], 16-byte aligned (nullable iff rel_extent == 0) */
     const float *P;            /* [Hq][d_r][rel_extent] (nullable iff rel_extent == 0)   */
     const inkattn_bf16 *k_cache;   /* [num_blocks][Hkv][64][128]                         */
     const inkattn_bf16 *v_cache;   /* [num_blocks][Hkv][64][128]                         */

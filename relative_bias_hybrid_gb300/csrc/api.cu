@@ -2,7 +2,7 @@
 // descriptor setup, the decode split heuristic, and the launches.
 //
 // Nothing here computes on the host: every step of the path runs in the kernels of
-// prologue.cu, prefill_mma.cu and decode.cu.
+// prologue.cu, prefill_tc.cu and decode.cu.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -109,8 +109,8 @@ inkattn_status validate_attn(const inkattn_attn_params *p) {
     if (p->lse && !aligned(p->lse, 4)) return INKATTN_ERR_INVALID_ARG;
     if (p->dev_status && !aligned(p->dev_status, 4)) return INKATTN_ERR_INVALID_ARG;
     if (p->rel_extent > 0) {
-        if (p->d_r < 16 || p->d_r > 64 || p->d_r % 16 != 0) return INKATTN_ERR_UNSUPPORTED;
-        if (!p->r || !p->P || !aligned(p->r, 4) || !aligned(p->P, 4)) return INKATTN_ERR_INVALID_ARG;
+        if (p->d_r != 16 && p->d_r != 32) return INKATTN_ERR_UNSUPPORTED;
+        if (!p->r || !p->P || !aligned(p->r, 16) || !aligned(p->P, 4)) return INKATTN_ERR_INVALID_ARG;
     }
     return INKATTN_OK;
 }
@@ -248,11 +248,11 @@ inkattn_status inkattn_prefill(const inkattn_attn_params *p, void *stream) {
     if (p->N_tok == 0) return INKATTN_OK;
     CUtensorMap qmap, kmap, vmap;
     const long long rows = (long long)p->num_blocks * p->Hkv * kBlock;
-    if (!make_q_map(&qmap, p->q, p->N_tok, p->Hq, kPrefillMmaRows) ||
+    if (!make_q_map(&qmap, p->q, p->N_tok, p->Hq, kPrefillTcRows) ||
         !make_cache_map(&kmap, p->k_cache, rows) || !make_cache_map(&vmap, p->v_cache, rows))
         return INKATTN_ERR_CUDA;
-    return launch_status(launch_prefill_mma(*p, scalars(*p), qmap, kmap, vmap,
-                                            static_cast<cudaStream_t>(stream)));
+    return launch_status(launch_prefill_tc(*p, scalars(*p), qmap, kmap, vmap,
+                                           static_cast<cudaStream_t>(stream)));
 }
 
 int inkattn_decode_num_splits(const inkattn_attn_params *p, int num_sms) {

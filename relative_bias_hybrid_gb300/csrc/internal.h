@@ -33,10 +33,10 @@ cudaError_t launch_decode(const inkattn_attn_params &p, const AttnScalars &s, in
 cudaError_t launch_combine(const inkattn_attn_params &p, int num_splits, const float *ws_o,
                            const float *ws_lse, cudaStream_t stream);
 
-constexpr int kPrefillMmaRows = 128;   // query rows per CTA of the mma.sync prefill
-cudaError_t launch_prefill_mma(const inkattn_attn_params &p, const AttnScalars &s,
-                               const CUtensorMap &qmap, const CUtensorMap &kmap,
-                               const CUtensorMap &vmap, cudaStream_t stream);
+// tcgen05 prefill: 128 query rows per CTA, d_r <= 32.
+constexpr int kPrefillTcRows = 128;
+cudaError_t launch_prefill_tc(const inkattn_attn_params &p, const AttnScalars &s, const CUtensorMap &qmap,
+                              const CUtensorMap &kmap, const CUtensorMap &vmap, cudaStream_t stream);
 
 // TMA descriptor for a paged cache viewed as [num_blocks*Hkv*64 rows][128] bf16,
 // box 64 rows x 64 columns, 128-byte swizzle.  Returns false on failure.

@@ -1,0 +1,565 @@
+// prefill_tc.cu -- relative-position-bias GQA prefill on the 5th-generation tensor cores
+// (tcgen05 + TMEM + TMA), sm_103a.
+//
+// [SGLang と Miles が Inkling を初日からサポート, §相対位置バイアス付き Attention]: every logit
+// gets the learned, query-conditioned bias r_i . P_h[:, i-j] for 0 <= i-j < rel_extent and
+// nothing beyond; future keys are masked; sliding-window and full layers are mixed; full
+// layers scale the logits by a length-dependent factor.
+// [same page, §Relative Attention と FA4 経路] and [vLLM hỗ trợ TML Inkling ..., §FA4 với
+// sheared bias]: a warp-specialized attention kernel that applies the relative term as a
+// sheared bias band.
+//
+// One CTA per (128-query tile of one sequence, query head).  Roles:
+//   warp 0      producer: TMA loads of the Q tile and of 128-key K/V tiles (two 64-key
+//               cache blocks, two 64-column boxes each, 128-byte swizzle) into a 3-slot
+//               ring; the relative-projection windows P_h[:, chunk] for the bias band
+//               (plain loads: rel_extent need not keep rows 16-byte aligned).
+//   warp 1      MMA issuer (one lane): S = Q K^T (operands in shared memory), O += P V
+//               (P read from TMEM), R = r P_h (tf32, both operands K-major) for the band.
+//   warps 2-5   softmax: thread i owns query row i (TMEM lane i).
+// TMEM (512 columns): O [0,128) | S0 [128,256) | S1 [256,384) | R [384,512).  P (bf16)
+// overwrites the first 64 columns of its S buffer.  S is double-buffered so Q K^T of the
+// next tile runs while the softmax works on this one.
+//
+// Key tiles are walked nearest-first (from the diagonal outwards).  With D_n the offset
+// i0 - j0 of tile n (i0 = the tile's first query position, j0 = the key tile's first key),
+// row a of tile n needs distances D_n + a - b for its 128 keys b: a window that shifts with
+// the row (the shear).  The windows of consecutive tiles abut, so the band is covered by
+// chunks C_n = [D_n + 1, D_n + 128] of 128 distances, one new chunk per tile (plus
+// C_{-1} = [D_0 - 127, D_0] before the first).  For each chunk the MMA warp computes
+// R[a][x] = r_a . P_h[:, D_n + 1 + x] (M=128, N=128, K=d_r) into TMEM.  Row a owns one
+// row of a 128-entry fp16 buffer indexed by key column; it resolves the shear as it moves
+// its values there: value x is the bias of column a - 1 - x in tile n when x < a (moved
+// before tile n reads its bias) and of column a + 127 - x in tile n + 1 when x >= a (moved
+// after).  Each tile then reads its bias row with sequential 16-byte loads.  Tiles farther
+// than rel_extent skip all of this.
+//
+// The softmax runs in the log2 domain and keeps a stale row maximum unless the new one
+// exceeds it by more than 8 (P stays below 2^8); only then is O rescaled in TMEM.
+#include "common.cuh"
+#include "internal.h"
+#include "tcgen05.cuh"
+
+namespace inkattn {
+
+namespace {
+
+constexpr int kRows = 128;                 // query rows per CTA (MMA M)
+constexpr int kKeys = 128;                 // keys per tile (MMA N of Q K^T, K of P V)
+constexpr int kSlots = 3;                  // K/V ring slots
+constexpr int kSlotBytes = 32768;          // one K or V tile: [d half][128 keys][128 B]
+constexpr int kThreads = 192;
+constexpr int kStageStride = 136;          // halves per row of the bias buffer
+constexpr int kMaxDr = 32;
+constexpr int kPwinBytes = 128 * 128;      // [128 distances][32 fp32] (K-major)
+
+constexpr int kOffQ = 0;
+constexpr int kOffKV = 32768;
+constexpr int kOffPwin = kOffKV + kSlots * kSlotBytes;
+constexpr int kOffRfeat = kOffPwin + 2 * kPwinBytes;
+constexpr int kOffStage = kOffRfeat + 16384;
+constexpr int kOffBar = kOffStage + kRows * kStageStride * 2;
+
+enum Bar {
+    B_Q = 0, B_KV_FULL = 1, B_KV_EMPTY = 4, B_S_FULL = 7, B_P_FULL = 9, B_PV_DONE = 11,
+    B_R_FULL = 12, B_R_EMPTY = 13, B_PW_FULL = 14, B_PW_EMPTY = 16, B_RFEAT = 18, B_DRAIN = 19,
+    B_COUNT = 20
+};
+constexpr int kSmem = kOffBar + B_COUNT * 8 + 16;
+
+constexpr uint32_t kTmemO = 0, kTmemS0 = 128, kTmemR = 384;
+
+struct TcArgs {
+    inkattn_attn_params p;
+    float scale;            // softmax scale
+    int n_qtiles_max;       // gridDim.y
+    long long kv_rows;      // rows of the cache tensor maps (OOB row = this)
+};
+
+__device__ __forceinline__ uint32_t sw128_chunk(int row, int chunk) {
+    return (uint32_t)(row * 128 + (((chunk ^ row) & 7) << 4));
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
+             const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const inkattn_attn_params &p = A.p;
+    const int h = blockIdx.x, b = blockIdx.z;
+    const int qt = A.n_qtiles_max - 1 - (int)blockIdx.y;     // longest tiles first
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = p.Hq / p.Hkv, hk = h / g;
+
+    // ---- sequence and tile geometry (uniform over the CTA)
+    const int start = p.cu_seqlens_q[b], end = p.cu_seqlens_q[b + 1];
+    const int T = p.seqlen_k[b];
+    const int q_len = end - start;
+    if (start < 0 || end < start || end > p.N_tok || q_len > p.max_seqlen_q || T < q_len ||
+        T > p.max_seqlen_k) {
+        if (threadIdx.x == 0 && qt == 0 && h == 0) set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
+        return;
+    }
+    const int row0 = qt * kRows;
+    if (row0 >= q_len) return;
+    const int pos0 = T - q_len;
+    const int p_lo = pos0 + row0;                                  // position of row 0
+    const int p_hi = pos0 + min(q_len, row0 + kRows) - 1;          // last valid row
+    const int k_lo = p.window > 0 ? max(0, p_lo - p.window + 1) : 0;
+    const int t_hi = p_hi / kKeys, t_lo = k_lo / kKeys;
+    const int N = t_hi - t_lo + 1;                                 // key tiles
+    const bool has_bias = p.rel_extent > 0;
+    int n_band = 0;
+    if (has_bias) {
+        // tile n is in the band iff its smallest distance D_n - 127 is below rel_extent
+        const long long lim = (long long)p.rel_extent + 127 - (p_lo - (long long)kKeys * t_hi);
+        const long long nb = (lim + kKeys - 1) / kKeys;
+        n_band = lim <= 0 ? 0 : (nb < N ? (int)nb : N);
+    }
+    const int d_r = p.d_r;
+
+    const uint32_t s_base = smem_u32(smem);
+    if ((s_base & 1023u) != 0u) {
+        if (threadIdx.x == 0) set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
+        return;
+    }
+    auto bar = [&](int i) { return s_base + kOffBar + 8u * (uint32_t)i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffBar + B_COUNT * 8);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffBar + B_COUNT * 8 + 4);
+    // every lane waits; the outcome is made uniform over the warp, because the warps that
+    // act on it next issue warp-collective (.sync.aligned) tcgen05 instructions
+    auto wwait = [&](uint32_t addr, uint32_t parity) -> bool {
+        const bool r = mbar_wait(addr, parity, p.dev_status, abort_flag);
+        return __all_sync(0xffffffffu, r);
+    };
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(B_Q), 1);
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(bar(B_KV_FULL + s), 1);
+            mbar_init(bar(B_KV_EMPTY + s), 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(B_S_FULL + s), 1);
+            mbar_init(bar(B_P_FULL + s), 128);
+            mbar_init(bar(B_PW_FULL + s), 1);
+            mbar_init(bar(B_PW_EMPTY + s), 1);
+        }
+        mbar_init(bar(B_PV_DONE), 1);
+        mbar_init(bar(B_R_FULL), 1);
+        mbar_init(bar(B_R_EMPTY), 128);
+        mbar_init(bar(B_RFEAT), 128);
+        mbar_init(bar(B_DRAIN), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(smem_u32(tmem_slot), 512);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const float lam = (p.log_scale_base > 1.f) ? fmaxf(1.f, logf((float)T) / logf(p.log_scale_base)) : 1.f;
+    const float c_qk = lam * A.scale * kLog2e;       // S (with the bias folded in) -> log2 logit
+    const float inv_scale = 1.f / A.scale;           // bias in S units
+
+    if (warp == 0) {
+        // ================================ producer ================================
+        bool ok = true;
+        const uint32_t q_dst = s_base + kOffQ;
+        if (lane == 0) {
+            tma_prefetch_desc(&qmap);
+            tma_prefetch_desc(&kmap);
+            tma_prefetch_desc(&vmap);
+            mbar_arrive_expect_tx(bar(B_Q), 2 * 16384);
+            tma_load_3d(q_dst, &qmap, 0, h, start + row0, bar(B_Q));
+            tma_load_3d(q_dst + 16384, &qmap, 64, h, start + row0, bar(B_Q));
+        }
+        // relative-projection window of chunk rho-1 (rho = 0 is C_{-1}): 128 distances from
+        // D_{rho-1} + 1, stored K-major for the tf32 MMA ([distance][d_r] fp32, 128-byte rows,
+        // 128-byte swizzle).  Lane l fills distances l, l+32, l+64, l+96 (coalesced loads).
+        auto load_pwin = [&](int rho) -> bool {
+            const int slot = rho & 1;
+            if (rho >= 2 && !wwait(bar(B_PW_EMPTY + slot), ((rho >> 1) - 1) & 1))
+                return false;
+            const int x0 = p_lo - kKeys * (t_hi - (rho - 1)) + 1;
+            unsigned char *win = smem + kOffPwin + slot * kPwinBytes;
+            const float *Ph = p.P + (size_t)h * d_r * p.rel_extent;
+            float v[4][kMaxDr];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int dl = x0 + lane + 32 * j;
+                const bool in = dl >= 0 && dl < p.rel_extent;
+#pragma unroll
+                for (int k = 0; k < kMaxDr; ++k)
+                    v[j][k] = (in && k < d_r) ? __ldg(Ph + (size_t)k * p.rel_extent + dl) : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int x = lane + 32 * j;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<float4 *>(win + sw128_chunk(x, c)) =
+                        make_float4(v[j][4 * c], v[j][4 * c + 1], v[j][4 * c + 2], v[j][4 * c + 3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_PW_FULL + slot));
+            return true;
+        };
+        auto load_kv = [&](int n, int isv) -> bool {
+            const int L = 2 * n + isv, slot = L % kSlots;
+            if (L >= kSlots && !wwait(bar(B_KV_EMPTY + slot), ((L / kSlots) - 1) & 1))
+                return false;
+            if (lane == 0) {
+                const int t = t_hi - n;
+                const uint32_t dst = s_base + kOffKV + slot * kSlotBytes;
+                const uint32_t fb = bar(B_KV_FULL + slot);
+                mbar_arrive_expect_tx(fb, kSlotBytes);
+                const void *map = isv ? static_cast<const void *>(&vmap) : static_cast<const void *>(&kmap);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int lb = 2 * t + half;                 // logical cache block
+                    long long row = A.kv_rows;                   // past the tensor: TMA fills zeros
+                    if ((long long)lb * kBlock < T) {
+                        const int blk = lb < p.max_blocks_per_seq
+                            ? p.block_table[(size_t)b * p.max_blocks_per_seq + lb] : -1;
+                        if (blk >= 0 && blk < p.num_blocks) row = ((long long)blk * p.Hkv + hk) * kBlock;
+                        else set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
+                    }
+                    tma_load_2d(dst + half * 8192, map, 0, (int)row, fb);
+                    tma_load_2d(dst + 16384 + half * 8192, map, 64, (int)row, fb);
+                }
+            }
+            __syncwarp();
+            return true;
+        };
+        if (n_band > 0) ok = load_pwin(0);
+        for (int n = 0; n < N && ok; ++n) {
+            ok = load_kv(n, 0) && load_kv(n, 1);
+            if (ok && n < n_band) ok = load_pwin(n + 1);
+        }
+        // nothing may still be landing in shared memory when the CTA tears down
+        if (lane == 0) {
+            mbar_wait(bar(B_Q), 0, p.dev_status, abort_flag);
+            const int loads = 2 * N;
+            for (int L = max(0, loads - kSlots); L < loads; ++L)
+                mbar_wait(bar(B_KV_FULL + L % kSlots), (L / kSlots) & 1, p.dev_status, abort_flag);
+        }
+    } else if (warp == 1) {
+        // ================================ MMA issuer ================================
+        const uint32_t id_qk = tc::idesc(128, 128, tc::kFmtBF16, 0, 0);
+        const uint32_t id_pv = tc::idesc(128, 128, tc::kFmtBF16, 0, 1);
+        const uint32_t id_r = tc::idesc(128, 128, tc::kFmtTF32, 0, 0);
+        const uint32_t q_smem = s_base + kOffQ;
+        bool ok = wwait(bar(B_Q), 0);
+        if (ok && n_band > 0) ok = wwait(bar(B_RFEAT), 0);
+
+        auto issue_r = [&](int rho) -> bool {
+            if (rho >= 1 && !wwait(bar(B_R_EMPTY), (rho - 1) & 1)) return false;
+            const int slot = rho & 1;
+            if (!wwait(bar(B_PW_FULL + slot), (rho >> 1) & 1)) return false;
+            tc::fence_after();
+            if (lane == 0) {
+                const uint32_t win = s_base + kOffPwin + slot * kPwinBytes;
+                for (int kk = 0; kk < d_r / 8; ++kk) {
+                    const uint64_t da = tc::sdesc_sw128(s_base + kOffRfeat + kk * 32, 16, 1024);
+                    const uint64_t db = tc::sdesc_sw128(win + kk * 32, 16, 1024);
+                    tc::mma_tf32_ss(tmem + kTmemR, da, db, id_r, kk > 0);
+                }
+                tc::commit(bar(B_R_FULL));
+                tc::commit(bar(B_PW_EMPTY + slot));
+            }
+            __syncwarp();
+            return true;
+        };
+        auto issue_pv = [&](int m) -> bool {
+            if (!wwait(bar(B_P_FULL + (m & 1)), (m >> 1) & 1)) return false;
+            const int L = 2 * m + 1, slot = L % kSlots;
+            if (!wwait(bar(B_KV_FULL + slot), (L / kSlots) & 1)) return false;
+            const uint32_t vs = s_base + kOffKV + slot * kSlotBytes;
+            // keys at or past the sequence end inside a loaded block: zero their V rows so
+            // that P = 0 there contributes exact zeros whatever the cache slots hold
+            const int j0 = (t_hi - m) * kKeys;
+            const int nvalid = min(kKeys, T - j0);
+            const int nload = min(kKeys, (int)(((long long)((T + kBlock - 1) / kBlock)) * kBlock - j0));
+            if (nvalid < nload) {
+                unsigned char *vp = smem + kOffKV + slot * kSlotBytes;
+                const int rows = nload - nvalid;
+                for (int idx = lane; idx < rows * 16; idx += 32) {
+                    const int key = nvalid + idx / 16, dh = (idx >> 3) & 1, ch = idx & 7;
+                    *reinterpret_cast<uint4 *>(vp + dh * 16384 + (key >> 6) * 8192 + (key & 63) * 128 + ch * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            tc::fence_after();
+            if (lane == 0) {
+                const uint32_t ps = tmem + kTmemS0 + (uint32_t)(m & 1) * 128;
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t db = tc::sdesc_sw128(vs + kk * 2048, 16384, 1024);
+                    tc::mma_bf16_ts(tmem + kTmemO, ps + kk * 8, db, id_pv, (m > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc::commit(bar(B_PV_DONE));
+                tc::commit(bar(B_KV_EMPTY + slot));
+            }
+            __syncwarp();
+            return true;
+        };
+
+        if (ok && n_band > 0) ok = issue_r(0);
+        for (int n = 0; n < N && ok; ++n) {
+            const int L = 2 * n, slot = L % kSlots;
+            ok = wwait(bar(B_KV_FULL + slot), (L / kSlots) & 1);
+            if (!ok) break;
+            tc::fence_after();
+            if (lane == 0) {
+                const uint32_t ks = s_base + kOffKV + slot * kSlotBytes;
+                const uint32_t sd = tmem + kTmemS0 + (uint32_t)(n & 1) * 128;
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    tc::mma_bf16_ss(sd, tc::sdesc_sw128(q_smem + off, 16, 1024),
+                                    tc::sdesc_sw128(ks + off, 16, 1024), id_qk, kk > 0);
+                }
+                tc::commit(bar(B_S_FULL + (n & 1)));
+                tc::commit(bar(B_KV_EMPTY + slot));
+            }
+            __syncwarp();
+            if (n < n_band) ok = issue_r(n + 1);
+            if (ok && n >= 1) ok = issue_pv(n - 1);
+        }
+        if (ok) ok = issue_pv(N - 1);
+        // every MMA of this CTA has completed before TMEM is released
+        if (lane == 0) tc::commit(bar(B_DRAIN));
+        __syncwarp();
+        (void)wwait(bar(B_DRAIN), 0);
+    } else {
+        // ================================ softmax ================================
+        const int quad = warp & 3;
+        const int a = quad * 32 + lane;                       // query row = TMEM lane
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        const int row = row0 + a;                             // row within the sequence
+        const int i_pos = p_lo + a;
+        __half *stage = reinterpret_cast<__half *>(smem + kOffStage) + a * kStageStride;
+        bool ok = true;
+
+        if (n_band > 0) {
+            // this row's relative features as fp32, K-major with the 128-byte swizzle
+            float4 f[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) f[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (row < q_len) {
+                const inkattn_bf16 *src = p.r + ((size_t)(start + row) * p.Hq + h) * d_r;
+#pragma unroll
+                for (int c = 0; c < kMaxDr / 8; ++c) {
+                    if (c * 8 < d_r) {
+                        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(src + c * 8));
+                        f[2 * c] = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+                        f[2 * c + 1] = make_float4(bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w));
+                    }
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<float4 *>(smem + kOffRfeat + sw128_chunk(a, c)) = f[c];
+            fence_proxy_async_smem();
+            mbar_arrive(bar(B_RFEAT));
+        }
+
+        // Move this row's values of the chunk in TMEM R (x inv_scale) into the bias buffer,
+        // indexed by key column: value x of chunk C_n is the bias of key column a - 1 - x in
+        // tile n (x < a, first part) and of key column a + 127 - x in tile n + 1 (x >= a).
+        auto drain = [&](bool first_part) {
+            __half *base = stage + (first_part ? a - 1 : a + 127);
+            uint32_t r[32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                tc::ld32(tmem + kTmemR + lane_off + c * 32, r);
+                tc::wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int x = c * 32 + e;
+                    if ((x < a) == first_part) base[-x] = __float2half_rn(__uint_as_float(r[e]) * inv_scale);
+                }
+            }
+        };
+
+        float m_run = -INFINITY, l_run = 0.f;
+        int r_round = 0;
+        // PV_DONE completes one phase per P V product, in order.  A parity wait is only
+        // unambiguous while the barrier is at most one phase past the last phase this thread
+        // observed, so every phase is waited for: tile n waits for P V of tile n - 1 (before
+        // its O rescale, which needs it anyway), and the epilogue for the last one.
+        auto wait_pv = [&](int m) -> bool { return wwait(bar(B_PV_DONE), m & 1); };
+        for (int n = 0; n < N; ++n) {
+            if (!(ok = wwait(bar(B_S_FULL + (n & 1)), (n >> 1) & 1))) break;
+            tc::fence_after();
+            const uint32_t sbuf = tmem + kTmemS0 + (uint32_t)(n & 1) * 128 + lane_off;
+            float s[128];
+            {
+                uint32_t r[32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    tc::ld32(sbuf + c * 32, r);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]);
+                }
+            }
+            if (n < n_band) {
+                if (n == 0) {
+                    if (!(ok = wwait(bar(B_R_FULL), r_round & 1))) break;
+                    tc::fence_after();
+                    drain(false);                                 // C_{-1}: positions >= a
+                    tc::fence_before();
+                    mbar_arrive(bar(B_R_EMPTY));
+                    ++r_round;
+                }
+                if (!(ok = wwait(bar(B_R_FULL), r_round & 1))) break;
+                tc::fence_after();
+                drain(true);                                      // C_n: positions < a
+#pragma unroll
+                for (int c8 = 0; c8 < 16; ++c8) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(stage + 8 * c8);
+                    const __half2 *hp = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __half22float2(hp[e]);
+                        s[8 * c8 + 2 * e] += f.x;
+                        s[8 * c8 + 2 * e + 1] += f.y;
+                    }
+                }
+                drain(false);                                     // C_n: positions >= a (tile n+1)
+                tc::fence_before();
+                mbar_arrive(bar(B_R_EMPTY));
+                ++r_round;
+            }
+            // scale, mask, row maximum
+            const int j0 = (t_hi - n) * kKeys;
+            const bool need_mask = (j0 + kKeys - 1 > p_lo) || (j0 + kKeys - 1 >= T) ||
+                                   (p.window > 0 && p_lo + kRows - 1 - j0 >= p.window);
+            float mx = -INFINITY;
+            if (need_mask) {
+#pragma unroll
+                for (int bb = 0; bb < 128; ++bb) {
+                    const int j = j0 + bb;
+                    const bool vis = j <= i_pos && j < T && (p.window == 0 || i_pos - j < p.window);
+                    s[bb] = vis ? s[bb] * c_qk : -INFINITY;
+                    mx = fmaxf(mx, s[bb]);
+                }
+            } else {
+#pragma unroll
+                for (int bb = 0; bb < 128; ++bb) {
+                    s[bb] *= c_qk;
+                    mx = fmaxf(mx, s[bb]);
+                }
+            }
+            if (n > 0) {
+                if (!(ok = wait_pv(n - 1))) break;
+                tc::fence_after();
+            }
+            // lazy rescale: keep the running maximum unless it is exceeded by more than 8
+            const bool need = mx > m_run + 8.f;
+            if (__any_sync(0xffffffffu, need)) {
+                const float m_new = need ? fmaxf(m_run, mx) : m_run;
+                // 0 when only m_run is -inf; 1 when the row has seen no visible key at all
+                const float corr = m_new == -INFINITY ? 1.f : fast_exp2(m_run - m_new);
+                if (n > 0) {
+                    uint32_t o[32];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        tc::ld32(tmem + kTmemO + lane_off + c * 32, o);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+                        tc::st32(tmem + kTmemO + lane_off + c * 32, o);
+                    }
+                    tc::wait_st();
+                }
+                l_run *= corr;
+                m_run = m_new;
+            }
+            const float ref = m_run == -INFINITY ? 0.f : m_run;
+            float ls = 0.f;
+#pragma unroll
+            for (int hp = 0; hp < 2; ++hp) {                  // P for keys [64 hp, 64 hp + 64)
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float e0 = fast_exp2(s[64 * hp + 2 * e] - ref);
+                    const float e1 = fast_exp2(s[64 * hp + 2 * e + 1] - ref);
+                    ls += e0 + e1;
+                    pk[e] = pack_bf16(e0, e1);
+                }
+                tc::st32(sbuf + hp * 32, pk);
+            }
+            l_run += ls;
+            tc::wait_st();
+            tc::fence_before();
+            mbar_arrive(bar(B_P_FULL + (n & 1)));
+        }
+        // epilogue: O / l for the valid rows, and lse
+        if (ok) ok = wait_pv(N - 1);
+        if (ok) {
+            tc::fence_after();
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            const bool valid = row < q_len;
+            const size_t qrow = (size_t)(start + row) * p.Hq + h;
+            uint32_t o[32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                tc::ld32(tmem + kTmemO + lane_off + c * 32, o);
+                tc::wait_ld();
+                if (!valid) continue;
+                if (p.out_dtype == INKATTN_DTYPE_F32) {
+                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + qrow * kHeadDim + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv, __uint_as_float(o[4 * e + 1]) * inv,
+                                             __uint_as_float(o[4 * e + 2]) * inv, __uint_as_float(o[4 * e + 3]) * inv);
+                } else {
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<inkattn_bf16 *>(p.out) + qrow * kHeadDim + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        dst[e] = make_uint4(
+                            pack_bf16(__uint_as_float(o[8 * e]) * inv, __uint_as_float(o[8 * e + 1]) * inv),
+                            pack_bf16(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv),
+                            pack_bf16(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv),
+                            pack_bf16(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv));
+                }
+            }
+            if (valid && p.lse) {
+                const float ref = m_run == -INFINITY ? 0.f : m_run;
+                p.lse[qrow] = l_run > 0.f ? (ref + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+            }
+        }
+    }
+
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+cudaError_t launch_prefill_tc(const inkattn_attn_params &p, const AttnScalars &s, const CUtensorMap &qmap,
+                              const CUtensorMap &kmap, const CUtensorMap &vmap, cudaStream_t stream) {
+    TcArgs a;
+    a.p = p;
+    a.scale = s.scale;
+    a.n_qtiles_max = (p.max_seqlen_q + kRows - 1) / kRows;
+    a.kv_rows = (long long)p.num_blocks * p.Hkv * kBlock;
+    cudaError_t err = cudaFuncSetAttribute(k_prefill_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (err != cudaSuccess) return err;
+    dim3 grid(p.Hq, a.n_qtiles_max, p.B);
+    k_prefill_tc<<<grid, kThreads, kSmem, stream>>>(a, qmap, kmap, vmap);
+    return cudaGetLastError();
+}
+
+}  // namespace inkattn
