@@ -155,6 +155,20 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// exp2 on the FMA/ALU pipes, to share the load of the special-function unit.
+// x = n + f with n = round(x) (adding 1.5 * 2^23 leaves n in the low mantissa bits) and
+// f in [-1/2, 1/2]; 2^f by a degree-3 polynomial with minimax relative error 7.5e-5 on
+// that interval (coefficients fitted by csrc/fit_exp2_poly.py); 2^n is added to the
+// exponent field.  Inputs below -125 are clamped (the result is then ~2^-125, not 0).
+__device__ __forceinline__ float soft_exp2(float x) {
+    x = fmaxf(x, -125.f);
+    const float t = x + 12582912.f;
+    const float f = x - (t - 12582912.f);
+    const float p = fmaf(fmaf(fmaf(0.0551716685295105f, f, 0.2426111251115799f), f, 0.6932609677314758f), f,
+                         0.9999280571937561f);
+    return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
 }

@@ -16,7 +16,8 @@
 //               (plain loads: rel_extent need not keep rows 16-byte aligned).
 //   warp 1      MMA issuer (one lane): S = Q K^T (operands in shared memory), O += P V
 //               (P read from TMEM), R = r P_h (tf32, both operands K-major) for the band.
-//   warps 2-5   softmax: thread i owns query row i (TMEM lane i).
+//   warps 2-9   softmax: two warpgroups; row i (TMEM lane i) is shared by one thread of
+//               each, which own its key columns [0, 64) and [64, 128).
 // TMEM (512 columns): O [0,128) | S0 [128,256) | S1 [256,384) | R [384,512).  P (bf16)
 // overwrites the first 64 columns of its S buffer.  S is double-buffered so Q K^T of the
 // next tile runs while the softmax works on this one.
@@ -35,7 +36,9 @@
 // than rel_extent skip all of this.
 //
 // The softmax runs in the log2 domain and keeps a stale row maximum unless the new one
-// exceeds it by more than 8 (P stays below 2^8); only then is O rescaled in TMEM.
+// exceeds it by more than 8 (P stays below 2^8); only then is O rescaled in TMEM.  Half of
+// the exponentials go to the special-function unit and half to a polynomial on the FMA
+// pipe, since 16 exp2 per clock per SM would alone take as long as the MMAs of a tile.
 #include "common.cuh"
 #include "internal.h"
 #include "tcgen05.cuh"
@@ -48,7 +51,7 @@ constexpr int kRows = 128;                 // query rows per CTA (MMA M)
 constexpr int kKeys = 128;                 // keys per tile (MMA N of Q K^T, K of P V)
 constexpr int kSlots = 3;                  // K/V ring slots
 constexpr int kSlotBytes = 32768;          // one K or V tile: [d half][128 keys][128 B]
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;            // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
 constexpr int kStageStride = 136;          // halves per row of the bias buffer
 constexpr int kMaxDr = 32;
 constexpr int kPwinBytes = 128 * 128;      // [128 distances][32 fp32] (K-major)
@@ -58,12 +61,13 @@ constexpr int kOffKV = 32768;
 constexpr int kOffPwin = kOffKV + kSlots * kSlotBytes;
 constexpr int kOffRfeat = kOffPwin + 2 * kPwinBytes;
 constexpr int kOffStage = kOffRfeat + 16384;
-constexpr int kOffBar = kOffStage + kRows * kStageStride * 2;
+constexpr int kOffXchg = kOffStage + kRows * kStageStride * 2;   // row maxima / sums of the two halves
+constexpr int kOffBar = kOffXchg + 3 * 2 * kRows * 4;
 
 enum Bar {
     B_Q = 0, B_KV_FULL = 1, B_KV_EMPTY = 4, B_S_FULL = 7, B_P_FULL = 9, B_PV_DONE = 11,
     B_R_FULL = 12, B_R_EMPTY = 13, B_PW_FULL = 14, B_PW_EMPTY = 16, B_RFEAT = 18, B_DRAIN = 19,
-    B_COUNT = 20
+    B_PAIR = 20, B_COUNT = 24
 };
 constexpr int kSmem = kOffBar + B_COUNT * 8 + 16;
 
@@ -142,15 +146,16 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(B_S_FULL + s), 1);
-            mbar_init(bar(B_P_FULL + s), 128);
+            mbar_init(bar(B_P_FULL + s), 256);
             mbar_init(bar(B_PW_FULL + s), 1);
             mbar_init(bar(B_PW_EMPTY + s), 1);
         }
         mbar_init(bar(B_PV_DONE), 1);
         mbar_init(bar(B_R_FULL), 1);
-        mbar_init(bar(B_R_EMPTY), 128);
-        mbar_init(bar(B_RFEAT), 128);
+        mbar_init(bar(B_R_EMPTY), 256);
+        mbar_init(bar(B_RFEAT), 256);
         mbar_init(bar(B_DRAIN), 1);
+        for (int q = 0; q < 4; ++q) mbar_init(bar(B_PAIR + q), 64);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -211,8 +216,9 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             if (lane == 0) mbar_arrive(bar(B_PW_FULL + slot));
             return true;
         };
+        int kv_loads = 0;                       // K/V tiles issued, in the MMA warp's order
         auto load_kv = [&](int n, int isv) -> bool {
-            const int L = 2 * n + isv, slot = L % kSlots;
+            const int L = kv_loads++, slot = L % kSlots;
             if (L >= kSlots && !wwait(bar(B_KV_EMPTY + slot), ((L / kSlots) - 1) & 1))
                 return false;
             if (lane == 0) {
@@ -238,16 +244,22 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             __syncwarp();
             return true;
         };
+        // the MMA warp consumes K_0, [W_1], then per tile n >= 1: K_n, [W_{n+1}], V_{n-1},
+        // and finally V_{N-1} (W = relative-projection window); loading in that order lets
+        // K_{n+1} reuse the slot of V_{n-2} instead of waiting for V_{n-1} to be consumed
         if (n_band > 0) ok = load_pwin(0);
-        for (int n = 0; n < N && ok; ++n) {
-            ok = load_kv(n, 0) && load_kv(n, 1);
+        if (ok) ok = load_kv(0, 0);
+        if (ok && 0 < n_band) ok = load_pwin(1);
+        for (int n = 1; n < N && ok; ++n) {
+            ok = load_kv(n, 0);
             if (ok && n < n_band) ok = load_pwin(n + 1);
+            if (ok) ok = load_kv(n - 1, 1);
         }
+        if (ok) ok = load_kv(N - 1, 1);
         // nothing may still be landing in shared memory when the CTA tears down
         if (lane == 0) {
             mbar_wait(bar(B_Q), 0, p.dev_status, abort_flag);
-            const int loads = 2 * N;
-            for (int L = max(0, loads - kSlots); L < loads; ++L)
+            for (int L = max(0, kv_loads - kSlots); L < kv_loads; ++L)
                 mbar_wait(bar(B_KV_FULL + L % kSlots), (L / kSlots) & 1, p.dev_status, abort_flag);
         }
     } else if (warp == 1) {
@@ -277,9 +289,10 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             __syncwarp();
             return true;
         };
+        int kv_used = 0;                         // K/V tiles consumed, same order as loaded
         auto issue_pv = [&](int m) -> bool {
             if (!wwait(bar(B_P_FULL + (m & 1)), (m >> 1) & 1)) return false;
-            const int L = 2 * m + 1, slot = L % kSlots;
+            const int L = kv_used++, slot = L % kSlots;
             if (!wwait(bar(B_KV_FULL + slot), (L / kSlots) & 1)) return false;
             const uint32_t vs = s_base + kOffKV + slot * kSlotBytes;
             // keys at or past the sequence end inside a loaded block: zero their V rows so
@@ -314,7 +327,7 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
 
         if (ok && n_band > 0) ok = issue_r(0);
         for (int n = 0; n < N && ok; ++n) {
-            const int L = 2 * n, slot = L % kSlots;
+            const int L = kv_used++, slot = L % kSlots;
             ok = wwait(bar(B_KV_FULL + slot), (L / kSlots) & 1);
             if (!ok) break;
             tc::fence_after();
@@ -340,52 +353,70 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         (void)wwait(bar(B_DRAIN), 0);
     } else {
         // ================================ softmax ================================
+        // Two warpgroups share the 128 rows: warps 2-5 (half 0) and 6-9 (half 1) read the
+        // same TMEM lane quarters; thread (half w, row a) owns key columns [64 w, 64 w + 64)
+        // of row a.  The two threads of a row exchange row maxima (and, at the end, row
+        // sums) through shared memory with a 64-thread named barrier per lane quarter.
         const int quad = warp & 3;
+        const int hw = (warp - 2) >> 2;                       // column half
         const int a = quad * 32 + lane;                       // query row = TMEM lane
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const int row = row0 + a;                             // row within the sequence
         const int i_pos = p_lo + a;
+        const int cb = 64 * hw;                               // first key column of this thread
         __half *stage = reinterpret_cast<__half *>(smem + kOffStage) + a * kStageStride;
+        float *xchg = reinterpret_cast<float *>(smem + kOffXchg);   // [2 tiles][2 halves][128 rows]
+        // the two threads of each row meet on an mbarrier (a bounded wait, unlike bar.sync)
+        int pair_phase = 0;
+        auto pair_sync = [&]() -> bool {
+            mbar_arrive(bar(B_PAIR + quad));
+            return wwait(bar(B_PAIR + quad), (pair_phase++) & 1);
+        };
         bool ok = true;
 
         if (n_band > 0) {
-            // this row's relative features as fp32, K-major with the 128-byte swizzle
-            float4 f[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) f[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+            // this row's relative features as fp32, K-major with the 128-byte swizzle; each
+            // half writes 4 of the 8 16-byte chunks
             if (row < q_len) {
                 const inkattn_bf16 *src = p.r + ((size_t)(start + row) * p.Hq + h) * d_r;
 #pragma unroll
-                for (int c = 0; c < kMaxDr / 8; ++c) {
-                    if (c * 8 < d_r) {
-                        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(src + c * 8));
-                        f[2 * c] = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
-                        f[2 * c + 1] = make_float4(bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w));
+                for (int c = 0; c < 2; ++c) {
+                    const int cc = 2 * hw + c;                // 8-element group of the features
+                    float4 f0 = make_float4(0.f, 0.f, 0.f, 0.f), f1 = f0;
+                    if (cc * 8 < d_r) {
+                        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(src + cc * 8));
+                        f0 = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+                        f1 = make_float4(bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w));
                     }
+                    *reinterpret_cast<float4 *>(smem + kOffRfeat + sw128_chunk(a, 2 * cc)) = f0;
+                    *reinterpret_cast<float4 *>(smem + kOffRfeat + sw128_chunk(a, 2 * cc + 1)) = f1;
                 }
-            }
+            } else {
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<float4 *>(smem + kOffRfeat + sw128_chunk(a, c)) = f[c];
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<float4 *>(smem + kOffRfeat + sw128_chunk(a, 4 * hw + c)) =
+                        make_float4(0.f, 0.f, 0.f, 0.f);
+            }
             fence_proxy_async_smem();
             mbar_arrive(bar(B_RFEAT));
         }
 
-        // Move this row's values of the chunk in TMEM R (x inv_scale) into the bias buffer,
-        // indexed by key column: value x of chunk C_n is the bias of key column a - 1 - x in
-        // tile n (x < a, first part) and of key column a + 127 - x in tile n + 1 (x >= a).
+        // Move this thread's half (positions [cb, cb + 64)) of the chunk in TMEM R (times
+        // inv_scale) into the row's bias buffer, indexed by key column: value x of chunk C_n
+        // is the bias of key column a - 1 - x in tile n (x < a, first part) and of key
+        // column a + 127 - x in tile n + 1 (x >= a).
         auto drain = [&](bool first_part) {
-            __half *base = stage + (first_part ? a - 1 : a + 127);
+            __half *base = stage + (first_part ? a - 1 : a + 127) - cb;
             uint32_t r[32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                tc::ld32(tmem + kTmemR + lane_off + c * 32, r);
+            for (int c = 0; c < 2; ++c) {
+                tc::ld32(tmem + kTmemR + lane_off + cb + c * 32, r);
                 tc::wait_ld();
+                const int lim = a - cb - 32 * c;              // e < lim  <=>  x < a
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int x = c * 32 + e;
-                    if ((x < a) == first_part) base[-x] = __float2half_rn(__uint_as_float(r[e]) * inv_scale);
-                }
+                for (int e = 0; e < 32; ++e)
+                    if ((e < lim) == first_part)
+                        base[-(32 * c + e)] = __float2half_rn(__uint_as_float(r[e]) * inv_scale);
             }
         };
 
@@ -400,16 +431,12 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             if (!(ok = wwait(bar(B_S_FULL + (n & 1)), (n >> 1) & 1))) break;
             tc::fence_after();
             const uint32_t sbuf = tmem + kTmemS0 + (uint32_t)(n & 1) * 128 + lane_off;
-            float s[128];
+            float s[64];
             {
-                uint32_t r[32];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    tc::ld32(sbuf + c * 32, r);
-                    tc::wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]);
-                }
+                uint32_t *su = reinterpret_cast<uint32_t *>(s);
+                tc::ld32(sbuf + cb, *reinterpret_cast<uint32_t(*)[32]>(su));
+                tc::ld32(sbuf + cb + 32, *reinterpret_cast<uint32_t(*)[32]>(su + 32));
+                tc::wait_ld();
             }
             if (n < n_band) {
                 if (n == 0) {
@@ -423,9 +450,10 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                 if (!(ok = wwait(bar(B_R_FULL), r_round & 1))) break;
                 tc::fence_after();
                 drain(true);                                      // C_n: positions < a
+                if (!(ok = pair_sync())) break;                   // both halves moved
 #pragma unroll
-                for (int c8 = 0; c8 < 16; ++c8) {
-                    const uint4 u = *reinterpret_cast<const uint4 *>(stage + 8 * c8);
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(stage + cb + 8 * c8);
                     const __half2 *hp = reinterpret_cast<const __half2 *>(&u);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -434,31 +462,40 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                         s[8 * c8 + 2 * e + 1] += f.y;
                     }
                 }
+                if (!(ok = pair_sync())) break;                   // both halves read tile n
                 drain(false);                                     // C_n: positions >= a (tile n+1)
                 tc::fence_before();
                 mbar_arrive(bar(B_R_EMPTY));
                 ++r_round;
             }
-            // scale, mask, row maximum
+            // mask and row maximum over this thread's 64 columns (unscaled; the scale is > 0)
             const int j0 = (t_hi - n) * kKeys;
+            int b_lo, span;                                       // visible: (unsigned)(b - b_lo) <= span
+            {
+                const int jv_lo = p.window > 0 ? i_pos - p.window + 1 : 0;
+                const int jv_hi = min(i_pos, T - 1);
+                b_lo = jv_hi >= jv_lo ? jv_lo - j0 - cb : (1 << 20);
+                span = jv_hi >= jv_lo ? jv_hi - jv_lo : 0;
+            }
             const bool need_mask = (j0 + kKeys - 1 > p_lo) || (j0 + kKeys - 1 >= T) ||
                                    (p.window > 0 && p_lo + kRows - 1 - j0 >= p.window);
-            float mx = -INFINITY;
             if (need_mask) {
 #pragma unroll
-                for (int bb = 0; bb < 128; ++bb) {
-                    const int j = j0 + bb;
-                    const bool vis = j <= i_pos && j < T && (p.window == 0 || i_pos - j < p.window);
-                    s[bb] = vis ? s[bb] * c_qk : -INFINITY;
-                    mx = fmaxf(mx, s[bb]);
-                }
-            } else {
-#pragma unroll
-                for (int bb = 0; bb < 128; ++bb) {
-                    s[bb] *= c_qk;
-                    mx = fmaxf(mx, s[bb]);
-                }
+                for (int bb = 0; bb < 64; ++bb)
+                    s[bb] = ((unsigned)(bb - b_lo) <= (unsigned)span) ? s[bb] : -INFINITY;
             }
+            float m8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) m8[e] = s[e];
+#pragma unroll
+            for (int bb = 8; bb < 64; ++bb) m8[bb & 7] = fmaxf(m8[bb & 7], s[bb]);
+            float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            float *xc = xchg + (n & 1) * 256;
+            xc[hw * 128 + a] = mx;
+            if (!(ok = pair_sync())) break;                       // also: both halves hold S
+            mx = fmaxf(mx, xc[(1 - hw) * 128 + a]);
+            mx = mx == -INFINITY ? -INFINITY : mx * c_qk;        // log2 units
             if (n > 0) {
                 if (!(ok = wait_pv(n - 1))) break;
                 tc::fence_after();
@@ -472,12 +509,12 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                 if (n > 0) {
                     uint32_t o[32];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        tc::ld32(tmem + kTmemO + lane_off + c * 32, o);
+                    for (int c = 0; c < 2; ++c) {
+                        tc::ld32(tmem + kTmemO + lane_off + cb + c * 32, o);
                         tc::wait_ld();
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-                        tc::st32(tmem + kTmemO + lane_off + c * 32, o);
+                        tc::st32(tmem + kTmemO + lane_off + cb + c * 32, o);
                     }
                     tc::wait_st();
                 }
@@ -485,45 +522,48 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                 m_run = m_new;
             }
             const float ref = m_run == -INFINITY ? 0.f : m_run;
-            float ls = 0.f;
+            float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            uint32_t pk[32];
 #pragma unroll
-            for (int hp = 0; hp < 2; ++hp) {                  // P for keys [64 hp, 64 hp + 64)
-                uint32_t pk[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float e0 = fast_exp2(s[64 * hp + 2 * e] - ref);
-                    const float e1 = fast_exp2(s[64 * hp + 2 * e + 1] - ref);
-                    ls += e0 + e1;
-                    pk[e] = pack_bf16(e0, e1);
-                }
-                tc::st32(sbuf + hp * 32, pk);
+            for (int e = 0; e < 32; ++e) {
+                const float e0 = fast_exp2(fmaf(s[2 * e], c_qk, -ref));
+                const float e1 = soft_exp2(fmaf(s[2 * e + 1], c_qk, -ref));
+                l8[e & 7] += e0 + e1;
+                pk[e] = pack_bf16(e0, e1);
             }
-            l_run += ls;
+            // P for keys [64 w, 64 w + 64) -> packed columns [32 w, 32 w + 32) of the buffer
+            tc::st32(sbuf + 32 * hw, pk);
+            l_run += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
             tc::wait_st();
             tc::fence_before();
             mbar_arrive(bar(B_P_FULL + (n & 1)));
         }
-        // epilogue: O / l for the valid rows, and lse
+        // epilogue: the row sum of both halves, then O / l for this thread's 64 columns
+        float *xl = xchg + 512;
+        xl[hw * 128 + a] = l_run;
+        if (ok) ok = pair_sync();
+        const float l_tot = l_run + xl[(1 - hw) * 128 + a];
         if (ok) ok = wait_pv(N - 1);
         if (ok) {
             tc::fence_after();
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
             const bool valid = row < q_len;
             const size_t qrow = (size_t)(start + row) * p.Hq + h;
             uint32_t o[32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                tc::ld32(tmem + kTmemO + lane_off + c * 32, o);
+            for (int c = 0; c < 2; ++c) {
+                tc::ld32(tmem + kTmemO + lane_off + cb + c * 32, o);
                 tc::wait_ld();
                 if (!valid) continue;
+                const int col = cb + c * 32;
                 if (p.out_dtype == INKATTN_DTYPE_F32) {
-                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + qrow * kHeadDim + c * 32);
+                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + qrow * kHeadDim + col);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv, __uint_as_float(o[4 * e + 1]) * inv,
                                              __uint_as_float(o[4 * e + 2]) * inv, __uint_as_float(o[4 * e + 3]) * inv);
                 } else {
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<inkattn_bf16 *>(p.out) + qrow * kHeadDim + c * 32);
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<inkattn_bf16 *>(p.out) + qrow * kHeadDim + col);
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
                         dst[e] = make_uint4(
@@ -533,9 +573,9 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                             pack_bf16(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv));
                 }
             }
-            if (valid && p.lse) {
+            if (valid && p.lse && hw == 0) {
                 const float ref = m_run == -INFINITY ? 0.f : m_run;
-                p.lse[qrow] = l_run > 0.f ? (ref + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+                p.lse[qrow] = l_tot > 0.f ? (ref + log2f(l_tot)) * 0.6931471805599453f : -INFINITY;
             }
         }
     }
