@@ -127,7 +127,7 @@ INKATTN_API inkattn_status inkattn_prologue(const inkattn_prologue_params *p, vo
  * i = seqlen_k[b]-q_len+t; key j (0 <= j < seqlen_k[b]) sits at position j in block
  * block_table[b][j/64], offset j%64, head kv = h / (Hq/Hkv).  For query head h:
  *   s_ij = lambda_b * ( softmax_scale * q_i.k_j + bias_hij ),
- *   bias_hij = sum_{e<d_r} r[i][h][e] * P[h][e][i-j]  if 0 <= i-j < rel_extent, else 0,
+ *   bias_hij = sum_{e<d_r} r[i][h][e] * P[h][i-j][e]  if 0 <= i-j < rel_extent, else 0,
  * visible keys: j <= i, and i-j < window when window > 0 (sliding-window layer),
  *   lambda_b = max(1, ln(seqlen_k[b]) / ln(log_scale_base)) when log_scale_base > 1
  *             (full layers' length-dependent logit scaling), else 1,
@@ -145,7 +145,7 @@ typedef struct inkattn_attn_params {
     int32_t block_size;        /* 64                                                     */
     int32_t num_blocks;        /* cache capacity in blocks (bounds check)                */
     int32_t max_blocks_per_seq;/* row length of block_table                              */
-    int32_t d_r;               /* relative feature size: 16 or 32                        */
+    int32_t d_r;               /* relative feature size: 32                              */
     int32_t rel_extent;        /* >= 0; 0 disables the bias                              */
     int32_t window;            /* 0 = full attention, else the sliding window (keys)     */
     int32_t out_dtype;         /* INKATTN_DTYPE_BF16 (0) or INKATTN_DTYPE_F32 (1) for out */
@@ -153,7 +153,9 @@ typedef struct inkattn_attn_params {
     float log_scale_base;      /* <= 1 -> no length-dependent scaling (8192 on full layers) */
     const inkattn_bf16 *q;     /* [N_tok][Hq][128], the normalised queries               */
     const inkattn_bf16 *r;     /* [N_tok][Hq][d_r], 16-byte aligned (nullable iff rel_extent == 0) */
-    const float *P;            /* [Hq][d_r][rel_extent] (nullable iff rel_extent == 0)   */
+    const float *P;            /* [Hq][rel_extent][d_r]: per query head, per distance,   */
+                               /* the d_r projection weights; 16-byte aligned (nullable  */
+                               /* iff rel_extent == 0)                                   */
     const inkattn_bf16 *k_cache;   /* [num_blocks][Hkv][64][128]                         */
     const inkattn_bf16 *v_cache;   /* [num_blocks][Hkv][64][128]                         */
     const int32_t *cu_seqlens_q;   /* [B+1]                                              */

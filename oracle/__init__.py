@@ -144,6 +144,9 @@ def attention(*, cu_seqlens_q, seqlen_k, Hq, Hkv, d, d_r, rel_extent, window,
               block_size, rows=None, n_threads=0):
     """Run the attention oracle; returns (out float64, lse float64).
 
+    P is [Hq][rel_extent][d_r]: P[h][delta] holds the d_r weights that project r onto
+    the relative logit of distance delta (the matrix P_h of the method, distance-major).
+
     With rows=None every token row is computed and out has shape [N][Hq][d];
     otherwise out is [len(rows)][Hq][d] for the listed token indices.
     """

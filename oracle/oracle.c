@@ -32,7 +32,7 @@
  *      with blk = slot / block_size, off = slot % block_size.
  *   5. Attention with relative-position bias [SG §相対位置バイアス付き Attention;
  *      VJ §TML Inkling モデルアーキテクチャ "Relative Attention", "Hybrid Attention"]:
- *      s_j = lambda * ( scale * q.k_j + [0 <= i-j < rel_extent] * sum_k r[i][h][k] P[h][k][i-j] )
+ *      s_j = lambda * ( scale * q.k_j + [0 <= i-j < rel_extent] * sum_k r[i][h][k] P_h[k][i-j] )
  *      over keys j <= i (and i-j < window for sliding-window layers),
  *      o = softmax(s) . V, lse = log sum_j exp(s_j).
  *      lambda = max(1, ln T / ln base) on full layers that enable it (T = the
@@ -193,7 +193,8 @@ int oracle_prologue(int B, const int32_t *cu_seqlens_q, int Hq, int Hkv, int d,
 /*
  * Attention with the relative-position bias: step 5 above.
  *
- *   q [N][Hq][d] (the normalised queries), r [N][Hq][d_r], P [Hq][d_r][rel_extent] fp32,
+ *   q [N][Hq][d] (the normalised queries), r [N][Hq][d_r], P [Hq][rel_extent][d_r] fp32
+ *   (P_h[k][delta] stored at P[h][delta][k]: the d_r weights of one distance are contiguous),
  *   k_cache, v_cache [num_blocks][Hkv][block_size][d], block_table [B][max_blocks].
  * Sequence b has q_len = cu_seqlens_q[b+1]-cu_seqlens_q[b] new tokens, which
  * sit at positions seqlen_k[b]-q_len+t; key j sits at position j and lives in
@@ -280,7 +281,7 @@ int oracle_attention(int B, const int32_t *cu_seqlens_q, const int32_t *seqlen_k
                 if (delta < rel_extent && rv) {
                     for (int e = 0; e < d_r; ++e)
                         bias += bf16_bits_to_f64(rv[e]) *
-                                (double)P[((size_t)h * d_r + e) * rel_extent + delta];
+                                (double)P[((size_t)h * rel_extent + delta) * d_r + e];
                 }
                 const double sj = lam * (scale * dot + bias);
                 s[j - j_lo] = sj;

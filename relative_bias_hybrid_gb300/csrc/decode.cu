@@ -234,7 +234,7 @@ k_decode(const DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
                 named_bar_sync(1, n_compute * 32);      // previous block's table reads done
                 for (int hh = warp; hh < g; hh += n_compute) {
                     const int h = hk * g + hh;
-                    const float *Ph = p.P + (size_t)h * p.d_r * p.rel_extent;
+                    const float *Ph = p.P + (size_t)h * p.rel_extent * p.d_r;
                     const inkattn_bf16 *rh = p.r + ((size_t)start * p.Hq + h) * p.d_r;
                     uint32_t rf[4][4];
 #pragma unroll
@@ -258,10 +258,9 @@ k_decode(const DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
                             const int e0 = kk * 16 + 2 * tq;
                             float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
                             if (dv) {
-                                p0 = __ldg(Ph + (size_t)e0 * p.rel_extent + dl);
-                                p1 = __ldg(Ph + (size_t)(e0 + 1) * p.rel_extent + dl);
-                                p2 = __ldg(Ph + (size_t)(e0 + 8) * p.rel_extent + dl);
-                                p3 = __ldg(Ph + (size_t)(e0 + 9) * p.rel_extent + dl);
+                                const float2 lo = __ldg(reinterpret_cast<const float2 *>(Ph + (size_t)dl * p.d_r + e0));
+                                const float2 hi = __ldg(reinterpret_cast<const float2 *>(Ph + (size_t)dl * p.d_r + e0 + 8));
+                                p0 = lo.x; p1 = lo.y; p2 = hi.x; p3 = hi.y;
                             }
                             mma_16816(acc, rf[kk], pack_bf16(p0, p1), pack_bf16(p2, p3));
                         }

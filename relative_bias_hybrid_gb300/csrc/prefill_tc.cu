@@ -12,8 +12,7 @@
 // One CTA per (128-query tile of one sequence, query head).  Roles:
 //   warp 0      producer: TMA loads of the Q tile and of 128-key K/V tiles (two 64-key
 //               cache blocks, two 64-column boxes each, 128-byte swizzle) into a 3-slot
-//               ring; the relative-projection windows P_h[:, chunk] for the bias band
-//               (plain loads: rel_extent need not keep rows 16-byte aligned).
+//               ring; the relative-projection windows (128 distances of P_h) for the band.
 //   warp 1      MMA issuer (one lane): S = Q K^T (operands in shared memory), O += P V
 //               (P read from TMEM), R = r P_h (tf32, both operands K-major) for the band.
 //   warps 2-9   softmax: two warpgroups; row i (TMEM lane i) is shared by one thread of
@@ -36,9 +35,10 @@
 // than rel_extent skip all of this.
 //
 // The softmax runs in the log2 domain and keeps a stale row maximum unless the new one
-// exceeds it by more than 8 (P stays below 2^8); only then is O rescaled in TMEM.  Half of
-// the exponentials go to the special-function unit and half to a polynomial on the FMA
-// pipe, since 16 exp2 per clock per SM would alone take as long as the MMAs of a tile.
+// exceeds it by more than 8 (P stays below 2^8); only then is O rescaled in TMEM.  A quarter
+// of the exponentials go to a polynomial on the FMA pipe and the rest to the special-function
+// unit: 16 exp2 per clock per SM would alone take as long as the MMAs of a tile, while the
+// polynomial costs issue slots the softmax warps share.
 #include "common.cuh"
 #include "internal.h"
 #include "tcgen05.cuh"
@@ -53,7 +53,7 @@ constexpr int kSlots = 3;                  // K/V ring slots
 constexpr int kSlotBytes = 32768;          // one K or V tile: [d half][128 keys][128 B]
 constexpr int kThreads = 320;            // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
 constexpr int kStageStride = 136;          // halves per row of the bias buffer
-constexpr int kMaxDr = 32;
+constexpr int kMaxDr = 32;                 // d_r (the relative features fill one 128-byte row)
 constexpr int kPwinBytes = 128 * 128;      // [128 distances][32 fp32] (K-major)
 
 constexpr int kOffQ = 0;
@@ -66,8 +66,8 @@ constexpr int kOffBar = kOffXchg + 3 * 2 * kRows * 4;
 
 enum Bar {
     B_Q = 0, B_KV_FULL = 1, B_KV_EMPTY = 4, B_S_FULL = 7, B_P_FULL = 9, B_PV_DONE = 11,
-    B_R_FULL = 12, B_R_EMPTY = 13, B_PW_FULL = 14, B_PW_EMPTY = 16, B_RFEAT = 18, B_DRAIN = 19,
-    B_PAIR = 20, B_COUNT = 24
+    B_R_FULL = 13, B_R_EMPTY = 14, B_PW_FULL = 15, B_PW_EMPTY = 17, B_RFEAT = 19, B_DRAIN = 20,
+    B_PAIR = 21, B_COUNT = 25
 };
 constexpr int kSmem = kOffBar + B_COUNT * 8 + 16;
 
@@ -88,7 +88,8 @@ __device__ __forceinline__ uint32_t sw128_chunk(int row, int chunk) {
 
 __global__ void __launch_bounds__(kThreads, 1)
 k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
-             const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
+             const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+             const __grid_constant__ CUtensorMap pmap) {
     extern __shared__ __align__(1024) unsigned char smem[];
     const inkattn_attn_params &p = A.p;
     const int h = blockIdx.x, b = blockIdx.z;
@@ -149,8 +150,8 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             mbar_init(bar(B_P_FULL + s), 256);
             mbar_init(bar(B_PW_FULL + s), 1);
             mbar_init(bar(B_PW_EMPTY + s), 1);
+            mbar_init(bar(B_PV_DONE + s), 1);
         }
-        mbar_init(bar(B_PV_DONE), 1);
         mbar_init(bar(B_R_FULL), 1);
         mbar_init(bar(B_R_EMPTY), 256);
         mbar_init(bar(B_RFEAT), 256);
@@ -180,40 +181,25 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             tma_prefetch_desc(&qmap);
             tma_prefetch_desc(&kmap);
             tma_prefetch_desc(&vmap);
+            if (n_band > 0) tma_prefetch_desc(&pmap);
             mbar_arrive_expect_tx(bar(B_Q), 2 * 16384);
             tma_load_3d(q_dst, &qmap, 0, h, start + row0, bar(B_Q));
             tma_load_3d(q_dst + 16384, &qmap, 64, h, start + row0, bar(B_Q));
         }
-        // relative-projection window of chunk rho-1 (rho = 0 is C_{-1}): 128 distances from
-        // D_{rho-1} + 1, stored K-major for the tf32 MMA ([distance][d_r] fp32, 128-byte rows,
-        // 128-byte swizzle).  Lane l fills distances l, l+32, l+64, l+96 (coalesced loads).
+        // relative-projection window of chunk rho-1 (rho = 0 is C_{-1}): P_h rows of the 128
+        // distances from D_{rho-1} + 1, one TMA box [128][d_r] fp32 that lands K-major with
+        // the 128-byte swizzle, as the tf32 MMA reads it; distances outside [0, rel_extent)
+        // are out of the tensor and arrive as zeros
         auto load_pwin = [&](int rho) -> bool {
             const int slot = rho & 1;
             if (rho >= 2 && !wwait(bar(B_PW_EMPTY + slot), ((rho >> 1) - 1) & 1))
                 return false;
-            const int x0 = p_lo - kKeys * (t_hi - (rho - 1)) + 1;
-            unsigned char *win = smem + kOffPwin + slot * kPwinBytes;
-            const float *Ph = p.P + (size_t)h * d_r * p.rel_extent;
-            float v[4][kMaxDr];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int dl = x0 + lane + 32 * j;
-                const bool in = dl >= 0 && dl < p.rel_extent;
-#pragma unroll
-                for (int k = 0; k < kMaxDr; ++k)
-                    v[j][k] = (in && k < d_r) ? __ldg(Ph + (size_t)k * p.rel_extent + dl) : 0.f;
+            if (lane == 0) {
+                const int x0 = p_lo - kKeys * (t_hi - (rho - 1)) + 1;
+                mbar_arrive_expect_tx(bar(B_PW_FULL + slot), kPwinBytes);
+                tma_load_3d(s_base + kOffPwin + slot * kPwinBytes, &pmap, 0, x0, h, bar(B_PW_FULL + slot));
             }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int x = lane + 32 * j;
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<float4 *>(win + sw128_chunk(x, c)) =
-                        make_float4(v[j][4 * c], v[j][4 * c + 1], v[j][4 * c + 2], v[j][4 * c + 3]);
-            }
-            fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_PW_FULL + slot));
             return true;
         };
         int kv_loads = 0;                       // K/V tiles issued, in the MMA warp's order
@@ -267,7 +253,18 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         const uint32_t id_qk = tc::idesc(128, 128, tc::kFmtBF16, 0, 0);
         const uint32_t id_pv = tc::idesc(128, 128, tc::kFmtBF16, 0, 1);
         const uint32_t id_r = tc::idesc(128, 128, tc::kFmtTF32, 0, 0);
-        const uint32_t q_smem = s_base + kOffQ;
+        // Base descriptors, built once; the per-k-step ones differ only in the start
+        // address field (bits 0-13, 16-byte units), which never carries out of its 14 bits
+        // since shared-memory addresses stay below 256 KB.
+        const uint64_t dq = tc::sdesc_sw128(s_base + kOffQ, 16, 1024);
+        uint64_t dk[kSlots], dv[kSlots];
+#pragma unroll
+        for (int sl = 0; sl < kSlots; ++sl) {
+            dk[sl] = tc::sdesc_sw128(s_base + kOffKV + sl * kSlotBytes, 16, 1024);
+            dv[sl] = tc::sdesc_sw128(s_base + kOffKV + sl * kSlotBytes, 16384, 1024);
+        }
+        const uint64_t dr = tc::sdesc_sw128(s_base + kOffRfeat, 16, 1024);
+        const uint64_t dw0 = tc::sdesc_sw128(s_base + kOffPwin, 16, 1024);
         bool ok = wwait(bar(B_Q), 0);
         if (ok && n_band > 0) ok = wwait(bar(B_RFEAT), 0);
 
@@ -277,12 +274,9 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             if (!wwait(bar(B_PW_FULL + slot), (rho >> 1) & 1)) return false;
             tc::fence_after();
             if (lane == 0) {
-                const uint32_t win = s_base + kOffPwin + slot * kPwinBytes;
-                for (int kk = 0; kk < d_r / 8; ++kk) {
-                    const uint64_t da = tc::sdesc_sw128(s_base + kOffRfeat + kk * 32, 16, 1024);
-                    const uint64_t db = tc::sdesc_sw128(win + kk * 32, 16, 1024);
-                    tc::mma_tf32_ss(tmem + kTmemR, da, db, id_r, kk > 0);
-                }
+                const uint64_t dw = dw0 + (uint64_t)(slot * kPwinBytes >> 4);
+                for (int kk = 0; kk < d_r / 8; ++kk)
+                    tc::mma_tf32_ss(tmem + kTmemR, dr + (uint64_t)(kk * 2), dw + (uint64_t)(kk * 2), id_r, kk > 0);
                 tc::commit(bar(B_R_FULL));
                 tc::commit(bar(B_PW_EMPTY + slot));
             }
@@ -294,7 +288,6 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             if (!wwait(bar(B_P_FULL + (m & 1)), (m >> 1) & 1)) return false;
             const int L = kv_used++, slot = L % kSlots;
             if (!wwait(bar(B_KV_FULL + slot), (L / kSlots) & 1)) return false;
-            const uint32_t vs = s_base + kOffKV + slot * kSlotBytes;
             // keys at or past the sequence end inside a loaded block: zero their V rows so
             // that P = 0 there contributes exact zeros whatever the cache slots hold
             const int j0 = (t_hi - m) * kKeys;
@@ -314,11 +307,12 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             tc::fence_after();
             if (lane == 0) {
                 const uint32_t ps = tmem + kTmemS0 + (uint32_t)(m & 1) * 128;
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t db = tc::sdesc_sw128(vs + kk * 2048, 16384, 1024);
-                    tc::mma_bf16_ts(tmem + kTmemO, ps + kk * 8, db, id_pv, (m > 0 || kk > 0) ? 1u : 0u);
-                }
-                tc::commit(bar(B_PV_DONE));
+                const uint64_t db = dv[slot];
+                tc::mma_bf16_ts(tmem + kTmemO, ps, db, id_pv, m > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 1; kk < 8; ++kk)
+                    tc::mma_bf16_ts(tmem + kTmemO, ps + kk * 8, db + (uint64_t)(kk * 128), id_pv, 1u);
+                tc::commit(bar(B_PV_DONE + (m & 1)));
                 tc::commit(bar(B_KV_EMPTY + slot));
             }
             __syncwarp();
@@ -332,12 +326,12 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             if (!ok) break;
             tc::fence_after();
             if (lane == 0) {
-                const uint32_t ks = s_base + kOffKV + slot * kSlotBytes;
                 const uint32_t sd = tmem + kTmemS0 + (uint32_t)(n & 1) * 128;
+                const uint64_t db = dk[slot];
+#pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    tc::mma_bf16_ss(sd, tc::sdesc_sw128(q_smem + off, 16, 1024),
-                                    tc::sdesc_sw128(ks + off, 16, 1024), id_qk, kk > 0);
+                    const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                    tc::mma_bf16_ss(sd, dq + off, db + off, id_qk, kk > 0 ? 1u : 0u);
                 }
                 tc::commit(bar(B_S_FULL + (n & 1)));
                 tc::commit(bar(B_KV_EMPTY + slot));
@@ -422,11 +416,11 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
 
         float m_run = -INFINITY, l_run = 0.f;
         int r_round = 0;
-        // PV_DONE completes one phase per P V product, in order.  A parity wait is only
-        // unambiguous while the barrier is at most one phase past the last phase this thread
-        // observed, so every phase is waited for: tile n waits for P V of tile n - 1 (before
-        // its O rescale, which needs it anyway), and the epilogue for the last one.
-        auto wait_pv = [&](int m) -> bool { return wwait(bar(B_PV_DONE), m & 1); };
+        // P V of tile m signals PV_DONE[m & 1], phase m >> 1.  The MMA warp issues Q K^T of
+        // tile m + 2 after P V of tile m, so once this thread has seen S of tile m + 2 the
+        // phase before tile m's (tile m - 2) is complete: a parity wait is then unambiguous
+        // without observing every phase, and the softmax waits only when it rescales O.
+        auto wait_pv = [&](int m) -> bool { return wwait(bar(B_PV_DONE + (m & 1)), (m >> 1) & 1); };
         for (int n = 0; n < N; ++n) {
             if (!(ok = wwait(bar(B_S_FULL + (n & 1)), (n >> 1) & 1))) break;
             tc::fence_after();
@@ -496,10 +490,6 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             if (!(ok = pair_sync())) break;                       // also: both halves hold S
             mx = fmaxf(mx, xc[(1 - hw) * 128 + a]);
             mx = mx == -INFINITY ? -INFINITY : mx * c_qk;        // log2 units
-            if (n > 0) {
-                if (!(ok = wait_pv(n - 1))) break;
-                tc::fence_after();
-            }
             // lazy rescale: keep the running maximum unless it is exceeded by more than 8
             const bool need = mx > m_run + 8.f;
             if (__any_sync(0xffffffffu, need)) {
@@ -507,6 +497,8 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                 // 0 when only m_run is -inf; 1 when the row has seen no visible key at all
                 const float corr = m_new == -INFINITY ? 1.f : fast_exp2(m_run - m_new);
                 if (n > 0) {
+                    if (!(ok = wait_pv(n - 1))) break;            // O holds P V of tiles < n
+                    tc::fence_after();
                     uint32_t o[32];
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
@@ -527,7 +519,8 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
                 const float e0 = fast_exp2(fmaf(s[2 * e], c_qk, -ref));
-                const float e1 = soft_exp2(fmaf(s[2 * e + 1], c_qk, -ref));
+                const float x1 = fmaf(s[2 * e + 1], c_qk, -ref);
+                const float e1 = (e & 1) ? soft_exp2(x1) : fast_exp2(x1);
                 l8[e & 7] += e0 + e1;
                 pk[e] = pack_bf16(e0, e1);
             }
@@ -589,7 +582,8 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
 }
 
 cudaError_t launch_prefill_tc(const inkattn_attn_params &p, const AttnScalars &s, const CUtensorMap &qmap,
-                              const CUtensorMap &kmap, const CUtensorMap &vmap, cudaStream_t stream) {
+                              const CUtensorMap &kmap, const CUtensorMap &vmap, const CUtensorMap &pmap,
+                              cudaStream_t stream) {
     TcArgs a;
     a.p = p;
     a.scale = s.scale;
@@ -598,7 +592,7 @@ cudaError_t launch_prefill_tc(const inkattn_attn_params &p, const AttnScalars &s
     cudaError_t err = cudaFuncSetAttribute(k_prefill_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (err != cudaSuccess) return err;
     dim3 grid(p.Hq, a.n_qtiles_max, p.B);
-    k_prefill_tc<<<grid, kThreads, kSmem, stream>>>(a, qmap, kmap, vmap);
+    k_prefill_tc<<<grid, kThreads, kSmem, stream>>>(a, qmap, kmap, vmap, pmap);
     return cudaGetLastError();
 }
 

@@ -131,7 +131,7 @@ def _normal(shape, std, device, seed, tensor, dtype):
 def make_inputs(w: Workload, seed: int = 0, device="cpu") -> Dict[str, torch.Tensor]:
     """All inputs of one prologue + attention pass, as torch tensors on `device`.
 
-    Keys: q, k, v [N,Hq,d]/[N,C]/[N,C] bf16; r [N,Hq,d_r] bf16; P [Hq,d_r,rel_extent]
+    Keys: q, k, v [N,Hq,d]/[N,C]/[N,C] bf16; r [N,Hq,d_r] bf16; P [Hq,rel_extent,d_r]
     fp32; conv_w_k, conv_w_v [C,4] fp32; q_norm_w, k_norm_w [d] fp32;
     conv_state_k, conv_state_v [B,3,C] bf16; state_slot [B]; cu_seqlens_q [B+1];
     seqlen_k [B]; block_table [B,max_blocks] (-1 past each sequence's blocks);
@@ -145,7 +145,7 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu") -> Dict[str, torch.Ten
     out["k"] = _normal((N, C), 1.0, device, seed, "k", bf)
     out["v"] = _normal((N, C), 1.0, device, seed, "v", bf)
     out["r"] = _normal((N, w.Hq, w.d_r), 1.0, device, seed, "r", bf)
-    out["P"] = _normal((w.Hq, w.d_r, max(w.rel_extent, 1)), 0.02, device, seed, "P", torch.float32)
+    out["P"] = _normal((w.Hq, max(w.rel_extent, 1), w.d_r), 0.02, device, seed, "P", torch.float32)
     out["conv_w_k"] = _normal((C, 4), 0.5, device, seed, "conv_w_k", torch.float32)
     out["conv_w_v"] = _normal((C, 4), 0.5, device, seed, "conv_w_v", torch.float32)
     out["q_norm_w"] = 1.0 + _normal((d,), 0.1, device, seed, "q_norm_w", torch.float32)

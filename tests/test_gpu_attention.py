@@ -112,7 +112,7 @@ def test_prefill_small_mixed(env, case):
         w = gen.custom(case, window=0, rel_extent=600, **kw)
     else:
         w = gen.custom(case, Hq=16, Hkv=4, q_lens=[257, 129], prefix_lens=[64, 0], window=192,
-                       rel_extent=96, d_r=16)
+                       rel_extent=96, d_r=32)
     _check_all_rows(env, w, *_run(env, w, seed=11))
 
 

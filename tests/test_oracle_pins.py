@@ -256,9 +256,15 @@ def _attn_case(rng, q_lens, prefix, Hq=4, Hkv=2, d=16, d_r=4, rel_extent=0, P=No
     if P is None:
         P = (0.3 * rng.standard_normal((Hq, d_r, max(rel_extent, 1)))).astype(np.float32)
     cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    # P is given as the matrices P_h [d_r][distance]; the oracle stores it distance-major
     return dict(cu_seqlens_q=cu, seqlen_k=np.array(T, np.int32), Hq=Hq, Hkv=Hkv, d=d, d_r=d_r,
                 rel_extent=rel_extent, window=0, softmax_scale=0.0, log_scale_base=0.0, q=q, r=r,
-                P=P, k_cache=kc, v_cache=vc, block_table=table, block_size=block_size), kd, vd
+                P=_stored(P), k_cache=kc, v_cache=vc, block_table=table, block_size=block_size), kd, vd
+
+
+def _stored(P_math):
+    """[Hq][d_r][rel_extent] (the matrices P_h) -> the [Hq][rel_extent][d_r] storage."""
+    return np.ascontiguousarray(np.asarray(P_math, np.float32).transpose(0, 2, 1))
 
 
 def _sdpa_rows(args, kd, vd, bias_fn=None, window=0, lam=1.0):
@@ -295,7 +301,7 @@ def test_attention_hand_golden(oracle_mod):
     zero = np.zeros((3, 1, 1))
     kc, vc, table = paged_cache([to_bits(zero)], [to_bits(np.array([1.0, 2, 4]).reshape(3, 1, 1))],
                                 4, 1, 1)
-    P = np.array([[[0.0, math.log(2.0)]]], np.float32)
+    P = _stored(np.array([[[0.0, math.log(2.0)]]], np.float32))    # P_0 = [[0, ln 2]]
     for case in "ABC":
         sel = [r for r in rows if r[0] == case]
         window, base = int(sel[0][1]), float(sel[0][2])
@@ -317,7 +323,7 @@ def test_zero_bias_is_causal_sdpa_with_gqa_and_prefix(oracle_mod):
     ref = _sdpa_rows(args, kd, vd)
     assert np.abs(out - ref).max() < 1e-12
     # P = 0 with a non-zero extent gives the same result
-    args2 = dict(args, rel_extent=5, P=np.zeros((4, 4, 5), np.float32))
+    args2 = dict(args, rel_extent=5, P=np.zeros((4, 5, 4), np.float32))
     out2, _ = oracle_mod.attention(**args2)
     assert np.abs(out2 - ref).max() < 1e-12
 
@@ -387,7 +393,7 @@ def test_bias_depends_only_on_distance(oracle_mod):
     kc_b, vc_b, tab_b = paged_cache([np.concatenate([junk_k, kd])], [np.concatenate([junk_v, vd])],
                                     4, Hkv, d, perm_seed=1)
     common = dict(Hq=Hq, Hkv=Hkv, d=d, d_r=d_r, rel_extent=E, window=W, softmax_scale=0.0,
-                  log_scale_base=0.0, P=P, block_size=4)
+                  log_scale_base=0.0, P=_stored(P), block_size=4)
     oa, la = oracle_mod.attention(cu_seqlens_q=np.array([0, n], np.int32),
                                   seqlen_k=np.array([n], np.int32), q=q, r=r, k_cache=kc_a,
                                   v_cache=vc_a, block_table=tab_a, **common)
@@ -421,7 +427,7 @@ def test_rel_extent_one_biases_only_the_diagonal(oracle_mod):
     rng = np.random.default_rng(17)
     args, kd, vd = _attn_case(rng, [9], [2], rel_extent=1)
     r = from_bits(args["r"])
-    P = args["P"]
+    P = args["P"].transpose(0, 2, 1)          # back to P_h [d_r][distance]
 
     def bias(b, h, i, j):
         diag = r[:, h, :] @ P[h, :, 0].astype(np.float64)       # [n]
