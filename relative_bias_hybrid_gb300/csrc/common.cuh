@@ -19,6 +19,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // A device wait that has not completed after this many nanoseconds gives up,
 // records INKATTN_ERR_DEVICE_TIMEOUT and lets the kernel wind down.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s
+constexpr uint32_t kWaitSleepNs = 100000u;         // longest single suspension of a waiting thread
 
 __device__ __forceinline__ void set_status(int32_t *st, int code) {
     if (st) atomicCAS(st, 0, code);
@@ -67,22 +68,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended (instead of returning at once) until
+// the phase completes or about `ns` nanoseconds have passed, so a waiting warp takes no
+// issue slots from the warps that share its scheduler.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity), "r"(ns) : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Returns false (and
-// records a timeout) if it has not completed within kWaitLimitNs, or at once
-// when *abort is already set by another role of the same CTA.
+// records a timeout) if it has not completed within kWaitLimitNs, or soon after
+// *abort is set by another role of the same CTA.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t *status,
                                           volatile int *abort) {
     if (mbar_try_wait(bar, parity)) return true;
-    uint64_t t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63) == 0) {
-            if (abort && *abort) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
-                set_status(status, INKATTN_ERR_DEVICE_TIMEOUT);
-                if (abort) *abort = 1;
-                return false;
-            }
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+        if (abort && *abort) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            set_status(status, INKATTN_ERR_DEVICE_TIMEOUT);
+            if (abort) *abort = 1;
+            return false;
         }
     }
 }
@@ -167,6 +178,59 @@ __device__ __forceinline__ float soft_exp2(float x) {
     const float p = fmaf(fmaf(fmaf(0.0551716685295105f, f, 0.2426111251115799f), f, 0.6932609677314758f), f,
                          0.9999280571937561f);
     return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+}
+
+// ---------------------------------------------------------------- paired fp32 (sm_100 family)
+// Two fp32 lanes per instruction (fma/add/mul .f32x2), each lane rounded to nearest even
+// exactly like its scalar form.
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+// max of three (one instruction on the sm_100 family)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// soft_exp2 on two lanes at once: the same range reduction and polynomial, with the
+// additions and multiply-adds paired; 2^n enters the exponent field by an integer
+// shift-add (n << 23 plus the bits of p, modulo 2^32).
+__device__ __forceinline__ float2 soft_exp2x2(float2 x) {
+    x.x = fmaxf(x.x, -125.f);
+    x.y = fmaxf(x.y, -125.f);
+    const float2 magic = make_float2(12582912.f, 12582912.f);
+    const float2 t = fadd2(x, magic);
+    const float2 r = fadd2(t, make_float2(-12582912.f, -12582912.f));
+    const float2 f = ffma2(r, make_float2(-1.f, -1.f), x);
+    float2 p = ffma2(make_float2(0.0551716685295105f, 0.0551716685295105f), f,
+                     make_float2(0.2426111251115799f, 0.2426111251115799f));
+    p = ffma2(p, f, make_float2(0.6932609677314758f, 0.6932609677314758f));
+    p = ffma2(p, f, make_float2(0.9999280571937561f, 0.9999280571937561f));
+    return make_float2(__uint_as_float((__float_as_uint(t.x) << 23) + __float_as_uint(p.x)),
+                       __uint_as_float((__float_as_uint(t.y) << 23) + __float_as_uint(p.y)));
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {

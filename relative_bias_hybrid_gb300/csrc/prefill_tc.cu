@@ -35,10 +35,11 @@
 // than rel_extent skip all of this.
 //
 // The softmax runs in the log2 domain and keeps a stale row maximum unless the new one
-// exceeds it by more than 8 (P stays below 2^8); only then is O rescaled in TMEM.  A quarter
-// of the exponentials go to a polynomial on the FMA pipe and the rest to the special-function
-// unit: 16 exp2 per clock per SM would alone take as long as the MMAs of a tile, while the
-// polynomial costs issue slots the softmax warps share.
+// exceeds it by more than 8 (P stays below 2^8); only then is O rescaled in TMEM.  Column
+// pairs go through paired fp32 instructions (fma/add .f32x2); three pairs in eight take a
+// polynomial exp2 on the FMA pipe and the rest the special-function unit: 16 exp2 per clock
+// per SM would alone take about as long as the MMAs of a tile, while the polynomial costs
+// issue slots the softmax warps share.
 #include "common.cuh"
 #include "internal.h"
 #include "tcgen05.cuh"
@@ -284,10 +285,15 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             return true;
         };
         int kv_used = 0;                         // K/V tiles consumed, same order as loaded
+        auto next_tile = [&](int &slot) -> bool {
+            const int L = kv_used++;
+            slot = L % kSlots;
+            return wwait(bar(B_KV_FULL + slot), (L / kSlots) & 1);
+        };
         auto issue_pv = [&](int m) -> bool {
             if (!wwait(bar(B_P_FULL + (m & 1)), (m >> 1) & 1)) return false;
-            const int L = kv_used++, slot = L % kSlots;
-            if (!wwait(bar(B_KV_FULL + slot), (L / kSlots) & 1)) return false;
+            int slot;
+            if (!next_tile(slot)) return false;
             // keys at or past the sequence end inside a loaded block: zero their V rows so
             // that P = 0 there contributes exact zeros whatever the cache slots hold
             const int j0 = (t_hi - m) * kKeys;
@@ -321,8 +327,8 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
 
         if (ok && n_band > 0) ok = issue_r(0);
         for (int n = 0; n < N && ok; ++n) {
-            const int L = kv_used++, slot = L % kSlots;
-            ok = wwait(bar(B_KV_FULL + slot), (L / kSlots) & 1);
+            int slot;
+            ok = next_tile(slot);
             if (!ok) break;
             tc::fence_after();
             if (lane == 0) {
@@ -451,9 +457,10 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                     const __half2 *hp = reinterpret_cast<const __half2 *>(&u);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float2 f = __half22float2(hp[e]);
-                        s[8 * c8 + 2 * e] += f.x;
-                        s[8 * c8 + 2 * e + 1] += f.y;
+                        const float2 f = fadd2(make_float2(s[8 * c8 + 2 * e], s[8 * c8 + 2 * e + 1]),
+                                               __half22float2(hp[e]));
+                        s[8 * c8 + 2 * e] = f.x;
+                        s[8 * c8 + 2 * e + 1] = f.y;
                     }
                 }
                 if (!(ok = pair_sync())) break;                   // both halves read tile n
@@ -478,13 +485,16 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                 for (int bb = 0; bb < 64; ++bb)
                     s[bb] = ((unsigned)(bb - b_lo) <= (unsigned)span) ? s[bb] : -INFINITY;
             }
-            float m8[8];
+            // four chains of three-input maxima over 16 columns each
+            float m4[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) m8[e] = s[e];
+            for (int c = 0; c < 4; ++c) {
+                float m = fmax3(s[16 * c], s[16 * c + 1], s[16 * c + 2]);
 #pragma unroll
-            for (int bb = 8; bb < 64; ++bb) m8[bb & 7] = fmaxf(m8[bb & 7], s[bb]);
-            float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                for (int e = 3; e < 15; e += 2) m = fmax3(m, s[16 * c + e], s[16 * c + e + 1]);
+                m4[c] = fmaxf(m, s[16 * c + 15]);
+            }
+            float mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
             float *xc = xchg + (n & 1) * 256;
             xc[hw * 128 + a] = mx;
             if (!(ok = pair_sync())) break;                       // also: both halves hold S
@@ -514,19 +524,25 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                 m_run = m_new;
             }
             const float ref = m_run == -INFINITY ? 0.f : m_run;
-            float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            const float2 cq = make_float2(c_qk, c_qk), nref = make_float2(-ref, -ref);
+            float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                            make_float2(0.f, 0.f)};
             uint32_t pk[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-                const float e0 = fast_exp2(fmaf(s[2 * e], c_qk, -ref));
-                const float x1 = fmaf(s[2 * e + 1], c_qk, -ref);
-                const float e1 = (e & 1) ? soft_exp2(x1) : fast_exp2(x1);
-                l8[e & 7] += e0 + e1;
-                pk[e] = pack_bf16(e0, e1);
+                // column pairs, logits to log2 units relative to the running maximum; three
+                // pairs in eight take the polynomial exp2, the rest the special-function unit
+                const float2 x = ffma2(make_float2(s[2 * e], s[2 * e + 1]), cq, nref);
+                const int k8 = e & 7;
+                const float2 y = (k8 == 1 || k8 == 4 || k8 == 6)
+                    ? soft_exp2x2(x) : make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                l4[e & 3] = fadd2(l4[e & 3], y);
+                pk[e] = pack_bf16(y.x, y.y);
             }
             // P for keys [64 w, 64 w + 64) -> packed columns [32 w, 32 w + 32) of the buffer
             tc::st32(sbuf + 32 * hw, pk);
-            l_run += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+            const float2 l2 = fadd2(fadd2(l4[0], l4[1]), fadd2(l4[2], l4[3]));
+            l_run += l2.x + l2.y;
             tc::wait_st();
             tc::fence_before();
             mbar_arrive(bar(B_P_FULL + (n & 1)));

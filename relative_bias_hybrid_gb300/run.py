@@ -1,0 +1,58 @@
+"""Runs one named workload's hot path a few times on the current GPU and prints the
+per-pass device time of each call.  Meant as the target of a profiler command, e.g.
+
+    ncu --set full --clock-control none -k regex:k_prefill_tc -s 2 -c 1 \\
+        python -m relative_bias_hybrid_gb300.run swa --iters 3
+
+Every pass is the whole path (prologue, then prefill or decode + combine) on seeded
+synthetic inputs already resident on the device.  ``--seqs N`` keeps only the first N
+sequences of a batched workload (a smaller case of the same kernel, for captures that
+must hold less memory).
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+
+import torch
+
+from . import inputs as gen
+from .step import AttentionStep
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("workload", choices=["tiny", "swa", "full", "decode", "ragged"])
+    ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--seqs", type=int, default=0, help="keep only the first N sequences")
+    ap.add_argument("--seed", type=int, default=0)
+    args = ap.parse_args(argv)
+
+    w = gen.workload(args.workload)
+    if args.seqs > 0 and args.seqs < w.B:
+        w = dataclasses.replace(w, name=f"{w.name}[:{args.seqs}]", q_lens=w.q_lens[:args.seqs],
+                                prefix_lens=w.prefix_lens[:args.seqs])
+    dev = torch.device("cuda", torch.cuda.current_device())
+    x = gen.make_inputs(w, seed=args.seed, device=dev)
+    step = AttentionStep(w, x, mode="decode" if args.workload == "decode" else "prefill")
+    stream = torch.cuda.Stream(device=dev)
+    print(w.describe(), f"num_splits={step.num_splits}" if step.mode == "decode" else "")
+    with torch.cuda.stream(stream):
+        for it in range(args.iters):
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e[0].record(stream)
+            step.run_prologue(stream)
+            e[1].record(stream)
+            step.run_attention(stream)
+            e[2].record(stream)
+            stream.synchronize()
+            print(f"pass {it}: prologue {e[0].elapsed_time(e[1]):.4f} ms, "
+                  f"attention {e[1].elapsed_time(e[2]):.4f} ms")
+    status = step.device_status()
+    print(f"device status {status}")
+    if status != 0:
+        raise SystemExit(1)
+
+
+if __name__ == "__main__":
+    main()
