@@ -122,6 +122,32 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, int c
         : "memory");
 }
 
+// As tma_load_2d, multicast: the box lands at the same shared-memory offset in every CTA
+// of the cluster named in cta_mask, and each of those CTAs' mbarrier at `bar`'s offset
+// receives the bytes that landed in that CTA.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void *map, int c0, int c1,
+                                               uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "h"(cta_mask)
+        : "memory");
+}
+
+// ---------------------------------------------------------------- clusters
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// All threads of every CTA of the cluster; orders shared-memory writes (barrier
+// initialisation included) before the peers' accesses after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Byte offset of element (row, col) inside a TMA box of 64-column (128-byte)
 // bf16 rows written with CU_TENSOR_MAP_SWIZZLE_128B: the 16-byte chunk index
 // is XORed with (row mod 8).  The box base must be 1024-byte aligned.

@@ -87,6 +87,7 @@ __device__ __forceinline__ uint32_t sw128_chunk(int row, int chunk) {
 
 }  // namespace
 
+template <int kCluster>
 __global__ void __launch_bounds__(kThreads, 1)
 k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
              const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -97,6 +98,10 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
     const int qt = A.n_qtiles_max - 1 - (int)blockIdx.y;     // longest tiles first
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = p.Hq / p.Hkv, hk = h / g;
+    // with kCluster = 2 the CTAs of heads 2i and 2i + 1 (same KV head) form a cluster; each
+    // loads one 64-key half of every K/V tile and multicasts it to both
+    const uint32_t crank = kCluster > 1 ? cluster_ctarank() : 0u;
+    constexpr uint16_t kPeers = (uint16_t)((1u << kCluster) - 1u);
 
     // ---- sequence and tile geometry (uniform over the CTA)
     const int start = p.cu_seqlens_q[b], end = p.cu_seqlens_q[b + 1];
@@ -144,7 +149,7 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         mbar_init(bar(B_Q), 1);
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(bar(B_KV_FULL + s), 1);
-            mbar_init(bar(B_KV_EMPTY + s), 1);
+            mbar_init(bar(B_KV_EMPTY + s), kCluster);         // released by every CTA's MMAs
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(B_S_FULL + s), 1);
@@ -168,6 +173,7 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
+    if constexpr (kCluster > 1) cluster_sync();          // peers' barriers exist before any multicast
     const uint32_t tmem = *tmem_slot;
 
     const float lam = (p.log_scale_base > 1.f) ? fmaxf(1.f, logf((float)T) / logf(p.log_scale_base)) : 1.f;
@@ -212,10 +218,11 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                 const int t = t_hi - n;
                 const uint32_t dst = s_base + kOffKV + slot * kSlotBytes;
                 const uint32_t fb = bar(B_KV_FULL + slot);
-                mbar_arrive_expect_tx(fb, kSlotBytes);
+                mbar_arrive_expect_tx(fb, kSlotBytes);       // both halves land in every CTA
                 const void *map = isv ? static_cast<const void *>(&vmap) : static_cast<const void *>(&kmap);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                for (int hh = 0; hh < 3 - kCluster; ++hh) {
+                    const int half = kCluster > 1 ? (int)crank : hh;
                     const int lb = 2 * t + half;                 // logical cache block
                     long long row = A.kv_rows;                   // past the tensor: TMA fills zeros
                     if ((long long)lb * kBlock < T) {
@@ -224,8 +231,13 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                         if (blk >= 0 && blk < p.num_blocks) row = ((long long)blk * p.Hkv + hk) * kBlock;
                         else set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
                     }
-                    tma_load_2d(dst + half * 8192, map, 0, (int)row, fb);
-                    tma_load_2d(dst + 16384 + half * 8192, map, 64, (int)row, fb);
+                    if constexpr (kCluster > 1) {
+                        tma_load_2d_mc(dst + half * 8192, map, 0, (int)row, fb, kPeers);
+                        tma_load_2d_mc(dst + 16384 + half * 8192, map, 64, (int)row, fb, kPeers);
+                    } else {
+                        tma_load_2d(dst + half * 8192, map, 0, (int)row, fb);
+                        tma_load_2d(dst + 16384 + half * 8192, map, 64, (int)row, fb);
+                    }
                 }
             }
             __syncwarp();
@@ -285,15 +297,24 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             return true;
         };
         int kv_used = 0;                         // K/V tiles consumed, same order as loaded
-        auto next_tile = [&](int &slot) -> bool {
+        auto next_tile = [&](int &slot, bool &last) -> bool {
             const int L = kv_used++;
             slot = L % kSlots;
+            last = L + kSlots >= 2 * N;          // no later load reuses the slot
             return wwait(bar(B_KV_FULL + slot), (L / kSlots) & 1);
+        };
+        // lane 0: the slot may be refilled once the MMAs issued so far have read it; a slot
+        // with no later load is not released, so no arrival reaches a peer that has finished
+        auto release = [&](int slot, bool last) {
+            if (last) return;
+            if constexpr (kCluster > 1) tc::commit_mc(bar(B_KV_EMPTY + slot), kPeers);
+            else tc::commit(bar(B_KV_EMPTY + slot));
         };
         auto issue_pv = [&](int m) -> bool {
             if (!wwait(bar(B_P_FULL + (m & 1)), (m >> 1) & 1)) return false;
             int slot;
-            if (!next_tile(slot)) return false;
+            bool last;
+            if (!next_tile(slot, last)) return false;
             // keys at or past the sequence end inside a loaded block: zero their V rows so
             // that P = 0 there contributes exact zeros whatever the cache slots hold
             const int j0 = (t_hi - m) * kKeys;
@@ -319,7 +340,7 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                 for (int kk = 1; kk < 8; ++kk)
                     tc::mma_bf16_ts(tmem + kTmemO, ps + kk * 8, db + (uint64_t)(kk * 128), id_pv, 1u);
                 tc::commit(bar(B_PV_DONE + (m & 1)));
-                tc::commit(bar(B_KV_EMPTY + slot));
+                release(slot, last);
             }
             __syncwarp();
             return true;
@@ -328,7 +349,8 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         if (ok && n_band > 0) ok = issue_r(0);
         for (int n = 0; n < N && ok; ++n) {
             int slot;
-            ok = next_tile(slot);
+            bool last;
+            ok = next_tile(slot, last);
             if (!ok) break;
             tc::fence_after();
             if (lane == 0) {
@@ -340,7 +362,7 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                     tc::mma_bf16_ss(sd, dq + off, db + off, id_qk, kk > 0 ? 1u : 0u);
                 }
                 tc::commit(bar(B_S_FULL + (n & 1)));
-                tc::commit(bar(B_KV_EMPTY + slot));
+                release(slot, last);
             }
             __syncwarp();
             if (n < n_band) ok = issue_r(n + 1);
@@ -595,6 +617,8 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         tc::fence_after();
         tc::tmem_dealloc(tmem, 512);
     }
+    // a CTA leaves only when its peer no longer writes into its shared memory
+    if constexpr (kCluster > 1) cluster_sync();
 }
 
 cudaError_t launch_prefill_tc(const inkattn_attn_params &p, const AttnScalars &s, const CUtensorMap &qmap,
@@ -605,11 +629,30 @@ cudaError_t launch_prefill_tc(const inkattn_attn_params &p, const AttnScalars &s
     a.scale = s.scale;
     a.n_qtiles_max = (p.max_seqlen_q + kRows - 1) / kRows;
     a.kv_rows = (long long)p.num_blocks * p.Hkv * kBlock;
-    cudaError_t err = cudaFuncSetAttribute(k_prefill_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (err != cudaSuccess) return err;
     dim3 grid(p.Hq, a.n_qtiles_max, p.B);
-    k_prefill_tc<<<grid, kThreads, kSmem, stream>>>(a, qmap, kmap, vmap, pmap);
-    return cudaGetLastError();
+    // head pairs (2i, 2i + 1) share a KV head when the group size is even
+    const bool pair = (p.Hq / p.Hkv) % 2 == 0;
+    if (!pair) {
+        cudaError_t err = cudaFuncSetAttribute(k_prefill_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+        if (err != cudaSuccess) return err;
+        k_prefill_tc<1><<<grid, kThreads, kSmem, stream>>>(a, qmap, kmap, vmap, pmap);
+        return cudaGetLastError();
+    }
+    cudaError_t err = cudaFuncSetAttribute(k_prefill_tc<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_prefill_tc<2>, a, qmap, kmap, vmap, pmap);
 }
 
 }  // namespace inkattn

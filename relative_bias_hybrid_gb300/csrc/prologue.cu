@@ -16,7 +16,10 @@
 // its tokens, the g = Hq/Hkv query heads of that KV head (RMSNorm only), the K stream
 // of head hk (conv, round to bf16, RMSNorm, cache write) and the V stream (conv,
 // round, cache write).  Each 128-value row is owned by a half-warp: 16 lanes x 16 bytes,
-// so every global access is a full 256-byte row, coalesced.
+// so every global access is a full 256-byte row, coalesced.  The query rows (most of the
+// bytes) are loaded first, eight per half-warp in flight; the K and V input rows of the
+// tile and the three rows before it are staged once in shared memory, so each conv tap
+// is a shared-memory read instead of a fourth global read of the same row.
 //
 // Conv-state carry without races: tiles are aligned to sequence starts, so every read of
 // the carried rows (tokens 0..2) happens in tile 0 of the sequence; that same CTA, after
@@ -29,7 +32,7 @@ namespace inkattn {
 
 constexpr int kPrologueTokens = 16;
 constexpr int kPrologueThreads = 256;
-constexpr int kRowsInFlight = 2;   // rows a half-warp loads before it computes
+constexpr int kQInFlight = 8;      // query rows a half-warp loads before it computes
 
 __device__ __forceinline__ void unpack8(const uint4 &u, float (&x)[8]) {
     x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x);
@@ -87,25 +90,33 @@ __device__ __forceinline__ float conv4_bf16(const float (&w)[4], const float (&x
     return round_pair_bf16(hi, lo);
 }
 
-__global__ void __launch_bounds__(kPrologueThreads)
+// The same correctly rounded value, cheaply in almost every case: an fp32 multiply-add
+// chain s is within 4u * sum|w_k x_k| of the exact sum (u = 2^-24), so when s is farther
+// than 8u * sum|w_k x_k| from the nearest bf16 rounding boundary (the midpoint above or
+// below it, or a quarter bf16 ulp when a power of two is near) its rounding is the exact
+// sum's; otherwise the error-free path decides.
+__device__ __forceinline__ float conv4_bf16_fast(const float (&w)[4], const float (&x)[4]) {
+    const float s = fmaf(w[3], x[3], fmaf(w[2], x[2], fmaf(w[1], x[1], w[0] * x[0])));
+    const float a = fmaf(fabsf(w[3]), fabsf(x[3]),
+                         fmaf(fabsf(w[2]), fabsf(x[2]), fmaf(fabsf(w[1]), fabsf(x[1]), fabsf(w[0] * x[0]))));
+    const float mid = __uint_as_float((__float_as_uint(s) & 0xFFFF0000u) | 0x8000u);
+    if (fabsf(s - mid) * 2097152.f > a && fabsf(s) * 2048.f > a)        // 2^21, 2^11
+        return __bfloat162float(__float2bfloat16_rn(s));
+    return conv4_bf16(w, x);
+}
+
+__global__ void __launch_bounds__(kPrologueThreads, 3)
 k_prologue(const inkattn_prologue_params p) {
     __shared__ __align__(16) float s_wk[kHeadDim * 4];
     __shared__ __align__(16) float s_wv[kHeadDim * 4];
     __shared__ float s_gq[kHeadDim], s_gk[kHeadDim];
+    // this head's K and V input rows [t0 - 3, t0 + nt) of [3 carried rows ; new rows]
+    __shared__ uint4 s_x[2][kPrologueTokens + 3][16];
 
     const int tile = blockIdx.x, b = blockIdx.y, hk = blockIdx.z;
     const int tid = threadIdx.x;
     const int C = p.Hkv * kHeadDim;
     const int g = p.Hq / p.Hkv;
-
-    for (int i = tid; i < kHeadDim * 4; i += kPrologueThreads) {
-        s_wk[i] = p.conv_w_k[(size_t)hk * kHeadDim * 4 + i];
-        s_wv[i] = p.conv_w_v[(size_t)hk * kHeadDim * 4 + i];
-    }
-    if (tid < kHeadDim) {
-        s_gq[tid] = p.q_norm_w[tid];
-        s_gk[tid] = p.k_norm_w[tid];
-    }
 
     const int start = p.cu_seqlens_q[b];
     const int end = p.cu_seqlens_q[b + 1];
@@ -119,103 +130,138 @@ k_prologue(const inkattn_prologue_params p) {
     const int t0 = tile * kPrologueTokens;
     if (t0 >= q_len) return;   // (an empty sequence keeps its state unchanged)
     const int nt = min(kPrologueTokens, q_len - t0);
+
+    const int half = tid >> 4;                // 16 half-warps per CTA
+    const int lane16 = tid & 15;
+    const int c0 = lane16 * 8;                // 8 channels per lane within the head
+    const size_t head_off = (size_t)hk * kHeadDim + c0;
+
+    // ---- query rows first: up to kQInFlight loads per lane before any arithmetic
+    const int q_rows = nt * g;
+    // row -> token within the tile (shifts for power-of-two group sizes)
+    const int g_shift = (g & (g - 1)) == 0 ? __ffs(g) - 1 : -1;
+    auto div_g = [&](int row) { return g_shift >= 0 ? row >> g_shift : row / g; };
+    uint4 qraw[kQInFlight];
+#pragma unroll
+    for (int j = 0; j < kQInFlight; ++j) {
+        const int row = half + 16 * j;
+        qraw[j] = make_uint4(0, 0, 0, 0);
+        if (row < q_rows) {
+            const int tt = div_g(row), h = hk * g + (row - tt * g);
+            qraw[j] = __ldg(reinterpret_cast<const uint4 *>(
+                p.q + ((size_t)(start + t0 + tt) * p.Hq + h) * kHeadDim + c0));
+        }
+    }
+    // ---- conv weights, norm gains, and the K/V input rows with their 3-row halo
+    for (int i = tid; i < kHeadDim * 4; i += kPrologueThreads) {
+        // channel c = 8 * lane + e, tap k stored at [(e * 16 + lane) * 4 + k]: the 16 lanes
+        // of a half-warp read 16 consecutive float4s for each e (no bank conflicts)
+        const int c = i >> 2, k = i & 3;
+        const int j = (((c & 7) * 16 + (c >> 3)) << 2) + k;
+        s_wk[j] = p.conv_w_k[(size_t)hk * kHeadDim * 4 + i];
+        s_wv[j] = p.conv_w_v[(size_t)hk * kHeadDim * 4 + i];
+    }
+    if (tid < kHeadDim) {
+        const int j = (tid & 7) * 16 + (tid >> 3);        // same interleave for the gains
+        s_gq[j] = p.q_norm_w[tid];
+        s_gk[j] = p.k_norm_w[tid];
+    }
+    for (int i = tid; i < 2 * (nt + 3) * 16; i += kPrologueThreads) {
+        const int stream = i / ((nt + 3) * 16), r = (i >> 4) % (nt + 3), chunk = i & 15;
+        const int idx = t0 + r;               // index into [3 carried rows ; new rows]
+        const size_t ch = (size_t)hk * kHeadDim + chunk * 8;
+        uint4 v;
+        if (idx < 3) {
+            const inkattn_bf16 *st = stream == 0 ? p.conv_state_k : p.conv_state_v;
+            v = *reinterpret_cast<const uint4 *>(st + ((size_t)slot * 3 + idx) * C + ch);
+        } else {
+            const inkattn_bf16 *src = stream == 0 ? p.k : p.v;
+            v = __ldg(reinterpret_cast<const uint4 *>(src + ((size_t)start + idx - 3) * C + ch));
+        }
+        s_x[stream][r][chunk] = v;
+    }
     __syncthreads();
 
-    const int kinds = g + 2;                  // g query rows, the K row, the V row
-    const int rows = nt * kinds;
-    const int half = tid >> 4;                // 16 half-warps per CTA
-    const int c0 = (tid & 15) * 8;            // 8 channels per lane within the head
-    const size_t head_off = (size_t)hk * kHeadDim + c0;
-    const long long slot_limit = (long long)p.num_blocks * kBlock;
-
-    for (int base = 0; base < rows; base += 16 * kRowsInFlight) {
-        float x[kRowsInFlight][8];
-        int kind_of[kRowsInFlight], tok_of[kRowsInFlight];
-        // phase 1: loads (and the conv, which only needs loads)
+    // ---- query rows: RMSNorm and store (the loads were issued at the start)
+    for (int j0 = 0; j0 * 16 < q_rows; j0 += kQInFlight) {
 #pragma unroll
-        for (int u = 0; u < kRowsInFlight; ++u) {
-            const int row = base + u * 16 + half;
-            kind_of[u] = -1;
-            tok_of[u] = 0;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[u][e] = 0.f;
-            if (row >= rows) continue;
-            const int tt = row / kinds, kind = row - tt * kinds;
-            const int t = t0 + tt;
-            const long long tok = (long long)start + t;
-            kind_of[u] = kind;
-            tok_of[u] = (int)tok;
-            if (kind < g) {
-                const int h = hk * g + kind;
-                const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
-                    p.q + ((size_t)tok * p.Hq + h) * kHeadDim + c0));
-                unpack8(raw, x[u]);
-            } else {
-                const bool isk = (kind == g);
-                const inkattn_bf16 *src = isk ? p.k : p.v;
-                const inkattn_bf16 *st = isk ? p.conv_state_k : p.conv_state_v;
-                const float *w = isk ? s_wk : s_wv;
-                float xt[4][8];
-#pragma unroll
-                for (int tap = 0; tap < 4; ++tap) {
-                    const int idx = t + tap;      // index into [3 carried rows ; new rows]
-                    uint4 raw;
-                    if (idx < 3) {
-                        raw = *reinterpret_cast<const uint4 *>(
-                            st + ((size_t)slot * 3 + idx) * C + head_off);
-                    } else {
-                        raw = __ldg(reinterpret_cast<const uint4 *>(
-                            src + ((size_t)start + idx - 3) * C + head_off));
-                    }
-                    unpack8(raw, xt[tap]);
-                }
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {   // the conv output is rounded to bf16
-                    const float4 w4 = *reinterpret_cast<const float4 *>(w + (c0 + e) * 4);
-                    const float we[4] = {w4.x, w4.y, w4.z, w4.w};
-                    const float xe[4] = {xt[0][e], xt[1][e], xt[2][e], xt[3][e]};
-                    x[u][e] = conv4_bf16(we, xe);
+        for (int j = 0; j < kQInFlight; ++j) {
+            const int row = half + 16 * (j0 + j);
+            if (j0 > 0) {                      // rows beyond the first batch (g > 8)
+                qraw[j] = make_uint4(0, 0, 0, 0);
+                if (row < q_rows) {
+                    const int tt = div_g(row), h = hk * g + (row - tt * g);
+                    qraw[j] = __ldg(reinterpret_cast<const uint4 *>(
+                        p.q + ((size_t)(start + t0 + tt) * p.Hq + h) * kHeadDim + c0));
                 }
             }
         }
-        // phase 2: RMSNorm (all lanes take part in the shuffles) and stores
 #pragma unroll
-        for (int u = 0; u < kRowsInFlight; ++u) {
+        for (int j = 0; j < kQInFlight; ++j) {
+            const int row = half + 16 * (j0 + j);
+            float x[8];
+            unpack8(qraw[j], x);
             float ss = 0.f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ss = fmaf(x[u][e], x[u][e], ss);
+            for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
             ss += __shfl_xor_sync(0xffffffffu, ss, 8);
             ss += __shfl_xor_sync(0xffffffffu, ss, 4);
             ss += __shfl_xor_sync(0xffffffffu, ss, 2);
             ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-            const int kind = kind_of[u];
-            if (kind < 0) continue;
-            const int tok = tok_of[u];
-            const float inv = __frsqrt_rn(ss * (1.0f / kHeadDim) + p.eps);
-            if (kind < g) {
-                float y[8];
+            if (row >= q_rows) continue;
+            const int tt = div_g(row), h = hk * g + (row - tt * g);
+            const float inv = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
+            float y[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) y[e] = x[u][e] * inv * s_gq[c0 + e];
-                const int h = hk * g + kind;
-                *reinterpret_cast<uint4 *>(p.q_out + ((size_t)tok * p.Hq + h) * kHeadDim + c0) =
-                    pack8(y);
-            } else {
-                const int sm = p.slot_mapping[tok];
-                if (sm < 0 || (long long)sm >= slot_limit) {
-                    set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
-                    continue;
-                }
-                const size_t dst = (((size_t)(sm / kBlock) * p.Hkv + hk) * kBlock + (sm % kBlock)) *
-                                   kHeadDim + c0;
-                if (kind == g) {
-                    float y[8];
+            for (int e = 0; e < 8; ++e) y[e] = x[e] * inv * s_gq[e * 16 + lane16];
+            *reinterpret_cast<uint4 *>(p.q_out + ((size_t)(start + t0 + tt) * p.Hq + h) * kHeadDim + c0) = pack8(y);
+        }
+    }
+
+
+    // ---- K and V rows: conv (rounded to bf16), K RMSNorm, cache write.  Half-warps 0-7
+    // take the K stream and 8-15 the V stream.
+    const long long slot_limit = (long long)p.num_blocks * kBlock;
+    const int stream = half >> 3;
+    const float *wsm = stream == 0 ? s_wk : s_wv;
+    for (int base = 0; base < nt; base += 8) {       // uniform trip count: all lanes shuffle
+        const int tt = base + (half & 7);
+        const bool valid = tt < nt;
+        const int ts = valid ? tt : 0;
+        float xt[4][8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) y[e] = x[u][e] * inv * s_gk[c0 + e];
-                    *reinterpret_cast<uint4 *>(p.k_cache + dst) = pack8(y);
-                } else {
-                    *reinterpret_cast<uint4 *>(p.v_cache + dst) = pack8(x[u]);
-                }
-            }
+        for (int tap = 0; tap < 4; ++tap) unpack8(s_x[stream][ts + tap][lane16], xt[tap]);
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float4 w4 = *reinterpret_cast<const float4 *>(wsm + (e * 16 + lane16) * 4);
+            const float we[4] = {w4.x, w4.y, w4.z, w4.w};
+            const float xe[4] = {xt[0][e], xt[1][e], xt[2][e], xt[3][e]};
+            x[e] = conv4_bf16_fast(we, xe);
+        }
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        if (!valid) continue;
+        const int tok = start + t0 + tt;
+        const int sm = p.slot_mapping[tok];
+        if (sm < 0 || (long long)sm >= slot_limit) {
+            if (lane16 == 0) set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
+            continue;
+        }
+        const size_t dst = (((size_t)(sm / kBlock) * p.Hkv + hk) * kBlock + (sm % kBlock)) * kHeadDim + c0;
+        if (stream == 0) {
+            const float inv = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = x[e] * inv * s_gk[e * 16 + lane16];
+            *reinterpret_cast<uint4 *>(p.k_cache + dst) = pack8(y);
+        } else {
+            *reinterpret_cast<uint4 *>(p.v_cache + dst) = pack8(x);
         }
     }
 
@@ -224,19 +270,19 @@ k_prologue(const inkattn_prologue_params p) {
     uint4 nv = make_uint4(0, 0, 0, 0);
     int task = tid;                              // 2 streams x 3 rows x 16 chunks
     const bool active = task < 2 * 3 * 16;
-    const int stream = task / 48, r = (task / 16) % 3, chunk = task % 16;
+    const int sstream = task / 48, r = (task / 16) % 3, chunk = task % 16;
     const size_t ch = (size_t)hk * kHeadDim + chunk * 8;
-    inkattn_bf16 *st = stream == 0 ? p.conv_state_k : p.conv_state_v;
+    inkattn_bf16 *st = sstream == 0 ? p.conv_state_k : p.conv_state_v;
     if (active) {
         const int idx = q_len + r;
         if (idx < 3) {
             nv = *reinterpret_cast<const uint4 *>(st + ((size_t)slot * 3 + idx) * C + ch);
         } else {
-            const inkattn_bf16 *src = stream == 0 ? p.k : p.v;
+            const inkattn_bf16 *src = sstream == 0 ? p.k : p.v;
             nv = __ldg(reinterpret_cast<const uint4 *>(src + ((size_t)start + idx - 3) * C + ch));
         }
     }
-    __syncthreads();   // every read of the old state (conv taps and the rows above) is done
+    __syncthreads();   // every read of the old state (the staged rows and the rows above) is done
     if (active) *reinterpret_cast<uint4 *>(st + ((size_t)slot * 3 + r) * C + ch) = nv;
 }
 

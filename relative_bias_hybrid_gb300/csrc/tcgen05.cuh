@@ -75,6 +75,13 @@ __device__ __forceinline__ void commit(uint32_t bar) {
                  :: "r"(bar) : "memory");
 }
 
+// As commit, arriving on the mbarrier at the same shared-memory offset in every CTA of
+// the cluster named in cta_mask.
+__device__ __forceinline__ void commit_mc(uint32_t bar, uint16_t cta_mask) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+                 :: "r"(bar), "h"(cta_mask) : "memory");
+}
+
 // ---------------------------------------------------------------- TMEM <-> registers
 // 32x32b shape: thread i of the warp reads/writes TMEM lane (quarter base + i), 32
 // consecutive 32-bit columns starting at the address's column.

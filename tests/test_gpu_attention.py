@@ -98,7 +98,8 @@ def test_prefill_tiny_all_rows(env):
     _check_all_rows(env, w, *_run(env, w))
 
 
-@pytest.mark.parametrize("case", ["swa_ragged", "full_logscale", "no_bias", "extent_past_T", "gqa4"])
+@pytest.mark.parametrize("case", ["swa_ragged", "full_logscale", "no_bias", "extent_past_T", "gqa4",
+                                  "gqa3_unpaired", "mha"])
 def test_prefill_small_mixed(env, case):
     gen = env[0]
     kw = dict(Hq=8, Hkv=2, q_lens=[200, 77, 300, 1], prefix_lens=[0, 150, 37, 9])
@@ -110,9 +111,16 @@ def test_prefill_small_mixed(env, case):
         w = gen.custom(case, window=0, rel_extent=0, **kw)
     elif case == "extent_past_T":
         w = gen.custom(case, window=0, rel_extent=600, **kw)
-    else:
+    elif case == "gqa4":
         w = gen.custom(case, Hq=16, Hkv=4, q_lens=[257, 129], prefix_lens=[64, 0], window=192,
                        rel_extent=96, d_r=32)
+    elif case == "gqa3_unpaired":
+        # odd group size: head pairs do not share a KV head, so no CTA pairing
+        w = gen.custom(case, Hq=6, Hkv=2, q_lens=[300, 45], prefix_lens=[20, 0], window=0,
+                       rel_extent=200)
+    else:
+        w = gen.custom(case, Hq=3, Hkv=3, q_lens=[190, 260], prefix_lens=[0, 70], window=128,
+                       rel_extent=50)
     _check_all_rows(env, w, *_run(env, w, seed=11))
 
 
