@@ -32,6 +32,7 @@ namespace inkattn {
 
 constexpr int kPrologueTokens = 16;
 constexpr int kPrologueThreads = 256;
+static_assert(kPrologueThreads == 256, "the row mapping assumes 16 half-warps per CTA");
 constexpr int kQInFlight = 8;      // query rows a half-warp loads before it computes
 
 __device__ __forceinline__ void unpack8(const uint4 &u, float (&x)[8]) {
@@ -103,6 +104,26 @@ __device__ __forceinline__ float conv4_bf16_fast(const float (&w)[4], const floa
     if (fabsf(s - mid) * 2097152.f > a && fabsf(s) * 2048.f > a)        // 2^21, 2^11
         return __bfloat162float(__float2bfloat16_rn(s));
     return conv4_bf16(w, x);
+}
+
+// conv4_bf16_fast on two channels at once: the multiply-add chains and the sums of
+// magnitudes run on paired fp32 instructions.
+__device__ __forceinline__ void conv4_bf16_fast2(const float (&wa)[4], const float (&xa)[4],
+                                                 const float (&wb)[4], const float (&xb)[4],
+                                                 float &ya, float &yb) {
+    float2 s = fmul2(make_float2(wa[0], wb[0]), make_float2(xa[0], xb[0]));
+    float2 a = make_float2(fabsf(s.x), fabsf(s.y));
+#pragma unroll
+    for (int k = 1; k < 4; ++k) {
+        s = ffma2(make_float2(wa[k], wb[k]), make_float2(xa[k], xb[k]), s);
+        a = ffma2(make_float2(fabsf(wa[k]), fabsf(wb[k])), make_float2(fabsf(xa[k]), fabsf(xb[k])), a);
+    }
+    const float ma = __uint_as_float((__float_as_uint(s.x) & 0xFFFF0000u) | 0x8000u);
+    const float mb = __uint_as_float((__float_as_uint(s.y) & 0xFFFF0000u) | 0x8000u);
+    ya = (fabsf(s.x - ma) * 2097152.f > a.x && fabsf(s.x) * 2048.f > a.x)
+        ? __bfloat162float(__float2bfloat16_rn(s.x)) : conv4_bf16(wa, xa);
+    yb = (fabsf(s.y - mb) * 2097152.f > a.y && fabsf(s.y) * 2048.f > a.y)
+        ? __bfloat162float(__float2bfloat16_rn(s.y)) : conv4_bf16(wb, xb);
 }
 
 __global__ void __launch_bounds__(kPrologueThreads, 3)
@@ -183,6 +204,9 @@ k_prologue(const inkattn_prologue_params p) {
     __syncthreads();
 
     // ---- query rows: RMSNorm and store (the loads were issued at the start)
+    float2 gq[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) gq[e] = make_float2(s_gq[(2 * e) * 16 + lane16], s_gq[(2 * e + 1) * 16 + lane16]);
     for (int j0 = 0; j0 * 16 < q_rows; j0 += kQInFlight) {
 #pragma unroll
         for (int j = 0; j < kQInFlight; ++j) {
@@ -211,9 +235,14 @@ k_prologue(const inkattn_prologue_params p) {
             if (row >= q_rows) continue;
             const int tt = div_g(row), h = hk * g + (row - tt * g);
             const float inv = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
+            const float2 inv2 = make_float2(inv, inv);
             float y[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) y[e] = x[e] * inv * s_gq[e * 16 + lane16];
+            for (int e = 0; e < 4; ++e) {
+                const float2 v = fmul2(fmul2(make_float2(x[2 * e], x[2 * e + 1]), inv2), gq[e]);
+                y[2 * e] = v.x;
+                y[2 * e + 1] = v.y;
+            }
             *reinterpret_cast<uint4 *>(p.q_out + ((size_t)(start + t0 + tt) * p.Hq + h) * kHeadDim + c0) = pack8(y);
         }
     }
@@ -233,11 +262,13 @@ k_prologue(const inkattn_prologue_params p) {
         for (int tap = 0; tap < 4; ++tap) unpack8(s_x[stream][ts + tap][lane16], xt[tap]);
         float x[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float4 w4 = *reinterpret_cast<const float4 *>(wsm + (e * 16 + lane16) * 4);
-            const float we[4] = {w4.x, w4.y, w4.z, w4.w};
-            const float xe[4] = {xt[0][e], xt[1][e], xt[2][e], xt[3][e]};
-            x[e] = conv4_bf16_fast(we, xe);
+        for (int e = 0; e < 8; e += 2) {
+            const float4 wa = *reinterpret_cast<const float4 *>(wsm + (e * 16 + lane16) * 4);
+            const float4 wb = *reinterpret_cast<const float4 *>(wsm + ((e + 1) * 16 + lane16) * 4);
+            const float wea[4] = {wa.x, wa.y, wa.z, wa.w}, web[4] = {wb.x, wb.y, wb.z, wb.w};
+            const float xea[4] = {xt[0][e], xt[1][e], xt[2][e], xt[3][e]};
+            const float xeb[4] = {xt[0][e + 1], xt[1][e + 1], xt[2][e + 1], xt[3][e + 1]};
+            conv4_bf16_fast2(wea, xea, web, xeb, x[e], x[e + 1]);
         }
         float ss = 0.f;
 #pragma unroll
