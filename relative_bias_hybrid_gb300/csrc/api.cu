@@ -213,6 +213,18 @@ bool make_q_map(CUtensorMap *map, const void *base, int n_tok, int hq, int box_r
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_q_group_map(CUtensorMap *map, const void *base, int n_tok, int hq, int group, int tokens) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hq, (cuuint64_t)(n_tok > 0 ? n_tok : 1)};
+    cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)hq * kHeadDim * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)tokens};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_rel_map(CUtensorMap *map, const void *base, int hq, int rel_extent, int d_r) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
     if (!enc) return false;
@@ -301,12 +313,13 @@ inkattn_status inkattn_decode(const inkattn_attn_params *p, int num_splits, void
         ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + ws_o_bytes(*p, S));
     }
     if (p->N_tok == 0) return INKATTN_OK;
-    CUtensorMap kmap, vmap;
+    CUtensorMap qmap, kmap, vmap;
     const long long rows = (long long)p->num_blocks * p->Hkv * kBlock;
-    if (!make_cache_map(&kmap, p->k_cache, rows) || !make_cache_map(&vmap, p->v_cache, rows))
+    if (!make_cache_map(&kmap, p->k_cache, rows) || !make_cache_map(&vmap, p->v_cache, rows) ||
+        !make_q_group_map(&qmap, p->q, p->N_tok, p->Hq, p->Hq / p->Hkv, p->max_seqlen_q))
         return INKATTN_ERR_CUDA;
-    return launch_status(launch_decode(*p, scalars(*p), S, ws_o, ws_lse, kmap, vmap,
-                                       static_cast<cudaStream_t>(stream)));
+    return launch_status(launch_decode_tc(*p, scalars(*p), S, ws_o, ws_lse, qmap, kmap, vmap,
+                                          static_cast<cudaStream_t>(stream)));
 }
 
 inkattn_status inkattn_combine(const inkattn_attn_params *p, int num_splits, const void *workspace,

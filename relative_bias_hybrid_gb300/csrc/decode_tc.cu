@@ -1,0 +1,543 @@
+// decode_tc.cu -- split-KV decode on the 5th-generation tensor cores (tcgen05 + TMEM + TMA),
+// sm_103a, with the relative-position bias.
+//
+// [vLLM TML Inkling サポート, §低レイテンシコレクティブとカーネル "FA4 Kernel"] and
+// [vLLM hỗ trợ TML Inkling ..., §FA4 với sheared bias]: the attention kernel splits the KV
+// length (num_splits picked from batch size, TP size and KV length); the partial results are
+// merged afterwards (k_combine in decode.cu).
+// [SGLang と Miles が Inkling を初日からサポート, §相対位置バイアス付き Attention]: the logit is
+// the scaled dot product plus the bias r_i . P_h[:, i-j] for 0 <= i-j < rel_extent.
+//
+// One CTA per (split, KV head hk, sequence b).  Its MMA rows are the (token t, query head
+// h = hk*g + hh) pairs of the sequence, row = t*g + hh (72 rows for 9 MTP-verify tokens x 8
+// heads, padded to 128), so every K/V tile is read once for all the query heads that share
+// it.  The Q tile arrives as one 3D TMA box {64 dims, g heads, ql tokens} per half of the
+// head dimension, which lands exactly in that row order.  Roles, as in the prefill kernel:
+//   warp 0      producer: TMA loads of 128-key K/V tiles (two 64-key cache blocks) of this
+//               split's key range into a 3-slot ring, in the order the MMAs consume them.
+//   warp 1      MMA issuer (one lane): S = Q K^T into a double-buffered S in TMEM, O += P V
+//               with P (bf16) read from TMEM.
+//   warps 2-9   softmax: two warpgroups; row a (TMEM lane a) is shared by one thread of each,
+//               which own its key columns [0, 64) and [64, 128).
+// TMEM: O [0,128) | S0 [128,256) | S1 [256,384).
+//
+// Relative bias: only tiles within rel_extent of the queries carry it (the last ones of the
+// sequence).  For such a tile the softmax warps first build, per query head, the table
+// R[t][x] = r_t . P_h[:, dlo + x] over the tile's 128 + ql distances with mma.sync (bf16
+// operands, fp32 accumulation), then each thread adds its row's 64 entries.
+//
+// The softmax runs in the log2 domain with the lazy rescale of the prefill kernel (O is
+// rescaled only when the running maximum grows by more than 8).  The epilogue writes O / l
+// and the natural-log LSE: straight to `out` with one split, else to the split workspace.
+#include "common.cuh"
+#include "internal.h"
+#include "tcgen05.cuh"
+
+namespace inkattn {
+
+namespace {
+
+constexpr int kRows = 128;                 // MMA M: (token, query head) rows, padded
+constexpr int kKeys = 128;                 // keys per tile (two cache blocks)
+constexpr int kSlots = 3;                  // K/V ring slots
+constexpr int kSlotBytes = 32768;          // one K or V tile: [d half][128 keys][128 B]
+constexpr int kThreads = 320;              // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
+constexpr int kTabW = 144;                 // distances per table row: 128 keys + up to 16 tokens
+constexpr int kTabRows = kDecodeMaxRows;   // g * ql <= 128
+
+constexpr int kOffQ = 0;
+constexpr int kOffKV = 32768;
+constexpr int kOffTab = kOffKV + kSlots * kSlotBytes;              // fp32 [g][ql][kTabW]
+constexpr int kOffXchg = kOffTab + kTabRows * kTabW * 4;           // row maxima / sums
+constexpr int kOffBar = kOffXchg + 3 * 2 * kRows * 4;
+
+enum Bar {
+    B_Q = 0, B_KV_FULL = 1, B_KV_EMPTY = 4, B_S_FULL = 7, B_P_FULL = 9, B_PV_DONE = 11,
+    B_TAB_FULL = 13, B_TAB_FREE = 14, B_DRAIN = 15, B_PAIR = 16, B_COUNT = 20
+};
+constexpr int kSmem = kOffBar + B_COUNT * 8 + 16;
+static_assert(kSmem <= 232448, "shared memory budget");
+
+constexpr uint32_t kTmemO = 0, kTmemS0 = 128;
+
+struct DecTcArgs {
+    inkattn_attn_params p;
+    float scale;            // softmax scale
+    int S;                  // number of splits
+    int ql;                 // rows of the Q box per head (max_seqlen_q)
+    float *ws_o;
+    float *ws_lse;
+    long long kv_rows;      // rows of the cache tensor maps (OOB row = this)
+};
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
+            const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const inkattn_attn_params &p = A.p;
+    const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = p.Hq / p.Hkv;
+
+    // ---- sequence geometry and this split's key range (uniform over the CTA)
+    const int start = p.cu_seqlens_q[b], end = p.cu_seqlens_q[b + 1];
+    const int T = p.seqlen_k[b];
+    const int q_len = end - start;
+    if (start < 0 || end < start || end > p.N_tok || q_len > A.ql || T < q_len ||
+        T > p.max_seqlen_k || q_len * g > kRows) {
+        if (threadIdx.x == 0) set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
+        return;
+    }
+    if (q_len == 0) return;
+    const int n_rows = q_len * g;
+    const int pos0 = T - q_len;                       // position of token 0
+    int blk_first = 0;
+    if (p.window > 0) blk_first = max(0, pos0 - p.window + 1) / kBlock;
+    const int blk_end = (T + kBlock - 1) / kBlock;    // exclusive
+    const int nblk = blk_end - blk_first;
+    const int per = (nblk + A.S - 1) / A.S;
+    const int my_lo = blk_first + split * per;
+    const int my_hi = min(blk_end, my_lo + per);
+    const int my_n = max(0, my_hi - my_lo);
+    const int N = (my_n + 1) / 2;                     // 128-key tiles
+    const int kr_lo = my_lo * kBlock, kr_hi = my_hi * kBlock;
+    const int g_shift = (g & (g - 1)) == 0 ? __ffs(g) - 1 : -1;
+
+    if (N == 0) {
+        // an empty split: its partial result is empty (O = 0, LSE = -inf)
+        for (int idx = threadIdx.x; idx < n_rows * (kHeadDim / 4); idx += kThreads) {
+            const int row = idx / (kHeadDim / 4), c4 = idx - row * (kHeadDim / 4);
+            const int t = g_shift >= 0 ? row >> g_shift : row / g, hh = row - t * g;
+            const size_t qrow = (size_t)(start + t) * p.Hq + hk * g + hh;
+            *reinterpret_cast<float4 *>(A.ws_o + (qrow * A.S + split) * kHeadDim + c4 * 4) =
+                make_float4(0.f, 0.f, 0.f, 0.f);
+            if (c4 == 0) A.ws_lse[qrow * A.S + split] = -INFINITY;
+        }
+        return;
+    }
+
+    const uint32_t s_base = smem_u32(smem);
+    if ((s_base & 1023u) != 0u) {
+        if (threadIdx.x == 0) set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
+        return;
+    }
+    auto bar = [&](int i) { return s_base + kOffBar + 8u * (uint32_t)i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffBar + B_COUNT * 8);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffBar + B_COUNT * 8 + 4);
+    auto wwait = [&](uint32_t addr, uint32_t parity) -> bool {
+        const bool r = mbar_wait(addr, parity, p.dev_status, abort_flag);
+        return __all_sync(0xffffffffu, r);
+    };
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(B_Q), 1);
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(bar(B_KV_FULL + s), 1);
+            mbar_init(bar(B_KV_EMPTY + s), 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(B_S_FULL + s), 1);
+            mbar_init(bar(B_P_FULL + s), 256);
+            mbar_init(bar(B_PV_DONE + s), 1);
+        }
+        mbar_init(bar(B_TAB_FULL), 256);
+        mbar_init(bar(B_TAB_FREE), 256);
+        mbar_init(bar(B_DRAIN), 1);
+        for (int q = 0; q < 4; ++q) mbar_init(bar(B_PAIR + q), 64);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(smem_u32(tmem_slot), 512);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const float lam = (p.log_scale_base > 1.f) ? fmaxf(1.f, logf((float)T) / logf(p.log_scale_base)) : 1.f;
+    const float c_qk = lam * A.scale * kLog2e;       // S (with the bias folded in) -> log2 logit
+    const float inv_scale = 1.f / A.scale;           // bias in S units
+
+    if (warp == 0) {
+        // ================================ producer ================================
+        bool ok = true;
+        if (lane == 0) {
+            tma_prefetch_desc(&qmap);
+            tma_prefetch_desc(&kmap);
+            tma_prefetch_desc(&vmap);
+            const uint32_t qbytes = (uint32_t)(2 * 64 * 2 * g * A.ql);
+            mbar_arrive_expect_tx(bar(B_Q), qbytes);
+            tma_load_3d(s_base + kOffQ, &qmap, 0, hk * g, start, bar(B_Q));
+            tma_load_3d(s_base + kOffQ + 16384, &qmap, 64, hk * g, start, bar(B_Q));
+        }
+        int kv_loads = 0;
+        auto load_kv = [&](int n, int isv) -> bool {
+            const int L = kv_loads++, slot = L % kSlots;
+            if (L >= kSlots && !wwait(bar(B_KV_EMPTY + slot), ((L / kSlots) - 1) & 1))
+                return false;
+            if (lane == 0) {
+                const uint32_t dst = s_base + kOffKV + slot * kSlotBytes;
+                const uint32_t fb = bar(B_KV_FULL + slot);
+                mbar_arrive_expect_tx(fb, kSlotBytes);
+                const void *map = isv ? static_cast<const void *>(&vmap) : static_cast<const void *>(&kmap);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int lb = my_lo + 2 * n + half;       // logical cache block
+                    long long row = A.kv_rows;                   // past the tensor: TMA fills zeros
+                    if (lb < my_hi) {
+                        const int blk = lb < p.max_blocks_per_seq
+                            ? p.block_table[(size_t)b * p.max_blocks_per_seq + lb] : -1;
+                        if (blk >= 0 && blk < p.num_blocks) row = ((long long)blk * p.Hkv + hk) * kBlock;
+                        else set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
+                    }
+                    tma_load_2d(dst + half * 8192, map, 0, (int)row, fb);
+                    tma_load_2d(dst + 16384 + half * 8192, map, 64, (int)row, fb);
+                }
+            }
+            __syncwarp();
+            return true;
+        };
+        // consumption order of the MMA warp: K_0, then per tile n >= 1: K_n, V_{n-1}; then V_{N-1}
+        ok = load_kv(0, 0);
+        for (int n = 1; n < N && ok; ++n) {
+            ok = load_kv(n, 0);
+            if (ok) ok = load_kv(n - 1, 1);
+        }
+        if (ok) ok = load_kv(N - 1, 1);
+        // nothing may still be landing in shared memory when the CTA tears down
+        if (lane == 0) {
+            mbar_wait(bar(B_Q), 0, p.dev_status, abort_flag);
+            for (int L = max(0, kv_loads - kSlots); L < kv_loads; ++L)
+                mbar_wait(bar(B_KV_FULL + L % kSlots), (L / kSlots) & 1, p.dev_status, abort_flag);
+        }
+    } else if (warp == 1) {
+        // ================================ MMA issuer ================================
+        const uint32_t id_qk = tc::idesc(128, 128, tc::kFmtBF16, 0, 0);
+        const uint32_t id_pv = tc::idesc(128, 128, tc::kFmtBF16, 0, 1);
+        const uint64_t dq = tc::sdesc_sw128(s_base + kOffQ, 16, 1024);
+        uint64_t dk[kSlots], dv[kSlots];
+#pragma unroll
+        for (int sl = 0; sl < kSlots; ++sl) {
+            dk[sl] = tc::sdesc_sw128(s_base + kOffKV + sl * kSlotBytes, 16, 1024);
+            dv[sl] = tc::sdesc_sw128(s_base + kOffKV + sl * kSlotBytes, 16384, 1024);
+        }
+        bool ok = wwait(bar(B_Q), 0);
+        int kv_used = 0;
+        auto next_tile = [&](int &slot, bool &last) -> bool {
+            const int L = kv_used++;
+            slot = L % kSlots;
+            last = L + kSlots >= 2 * N;
+            return wwait(bar(B_KV_FULL + slot), (L / kSlots) & 1);
+        };
+        auto issue_pv = [&](int m) -> bool {
+            if (!wwait(bar(B_P_FULL + (m & 1)), (m >> 1) & 1)) return false;
+            int slot;
+            bool last;
+            if (!next_tile(slot, last)) return false;
+            // keys at or past the sequence end inside a loaded block: zero their V rows so
+            // that P = 0 there contributes exact zeros whatever the cache slots hold
+            const int j0 = kr_lo + m * kKeys;
+            const int nvalid = max(0, min(kKeys, T - j0));
+            const int nload = min(kKeys, (my_hi - my_lo - 2 * m) * kBlock);
+            if (nvalid < nload) {
+                unsigned char *vp = smem + kOffKV + slot * kSlotBytes;
+                const int rows = nload - nvalid;
+                for (int idx = lane; idx < rows * 16; idx += 32) {
+                    const int key = nvalid + idx / 16, dh = (idx >> 3) & 1, ch = idx & 7;
+                    *reinterpret_cast<uint4 *>(vp + dh * 16384 + (key >> 6) * 8192 + (key & 63) * 128 + ch * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            tc::fence_after();
+            if (lane == 0) {
+                const uint32_t ps = tmem + kTmemS0 + (uint32_t)(m & 1) * 128;
+                const uint64_t db = dv[slot];
+                tc::mma_bf16_ts(tmem + kTmemO, ps, db, id_pv, m > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 1; kk < 8; ++kk)
+                    tc::mma_bf16_ts(tmem + kTmemO, ps + kk * 8, db + (uint64_t)(kk * 128), id_pv, 1u);
+                tc::commit(bar(B_PV_DONE + (m & 1)));
+                if (!last) tc::commit(bar(B_KV_EMPTY + slot));
+            }
+            __syncwarp();
+            return true;
+        };
+        for (int n = 0; n < N && ok; ++n) {
+            int slot;
+            bool last;
+            ok = next_tile(slot, last);
+            if (!ok) break;
+            tc::fence_after();
+            if (lane == 0) {
+                const uint32_t sd = tmem + kTmemS0 + (uint32_t)(n & 1) * 128;
+                const uint64_t db = dk[slot];
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                    tc::mma_bf16_ss(sd, dq + off, db + off, id_qk, kk > 0 ? 1u : 0u);
+                }
+                tc::commit(bar(B_S_FULL + (n & 1)));
+                if (!last) tc::commit(bar(B_KV_EMPTY + slot));
+            }
+            __syncwarp();
+            if (n >= 1) ok = issue_pv(n - 1);
+        }
+        if (ok) ok = issue_pv(N - 1);
+        if (lane == 0) tc::commit(bar(B_DRAIN));
+        __syncwarp();
+        (void)wwait(bar(B_DRAIN), 0);
+    } else {
+        // ================================ softmax ================================
+        const int quad = warp & 3;
+        const int hw = (warp - 2) >> 2;                       // column half
+        const int sw = warp - 2;                              // softmax warp index 0..7
+        const int a = quad * 32 + lane;                       // MMA row = TMEM lane
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        const bool valid_row = a < n_rows;
+        const int t = valid_row ? (g_shift >= 0 ? a >> g_shift : a / g) : 0;
+        const int hh = a - t * g;
+        const int i_pos = pos0 + t;
+        const int cb = 64 * hw;
+        float *tab = reinterpret_cast<float *>(smem + kOffTab);
+        float *xchg = reinterpret_cast<float *>(smem + kOffXchg);
+        int pair_phase = 0;
+        auto pair_sync = [&]() -> bool {
+            mbar_arrive(bar(B_PAIR + quad));
+            return wwait(bar(B_PAIR + quad), (pair_phase++) & 1);
+        };
+        const bool has_bias = p.rel_extent > 0;
+        const int gq = lane >> 2, tq = lane & 3;              // mma.sync fragment coordinates
+        int band_round = 0;
+        bool ok = true;
+
+        float m_run = -INFINITY, l_run = 0.f;
+        auto wait_pv = [&](int m) -> bool { return wwait(bar(B_PV_DONE + (m & 1)), (m >> 1) & 1); };
+        for (int n = 0; n < N; ++n) {
+            const int j0 = kr_lo + n * kKeys;
+            const bool band = has_bias && (pos0 - (j0 + kKeys - 1) < p.rel_extent);
+            const int dlo = pos0 - j0 - (kKeys - 1);          // distance at table column 0
+            if (band) {
+                // ---- relative rows of this tile, one query head per warp, into the table
+                if (band_round > 0 && !(ok = wwait(bar(B_TAB_FREE), (band_round - 1) & 1))) break;
+                for (int hq = sw; hq < g; hq += 8) {
+                    const int h = hk * g + hq;
+                    const float *Ph = p.P + (size_t)h * p.rel_extent * p.d_r;
+                    const inkattn_bf16 *rh = p.r + ((size_t)start * p.Hq + h) * p.d_r;
+                    uint32_t rf[4][4];
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int tt = gq + ((e & 1) << 3);
+                            const int col = kk * 16 + 2 * tq + ((e >> 1) << 3);
+                            rf[kk][e] = (kk * 16 < p.d_r && tt < q_len)
+                                ? __ldg(reinterpret_cast<const uint32_t *>(rh + (size_t)tt * p.Hq * p.d_r + col))
+                                : 0u;
+                        }
+                    for (int nt = 0; nt < kTabW / 8; ++nt) {
+                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                        const int dl = dlo + nt * 8 + gq;
+                        const bool dv = dl >= 0 && dl < p.rel_extent;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            if (kk * 16 >= p.d_r) continue;
+                            const int e0 = kk * 16 + 2 * tq;
+                            float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+                            if (dv) {
+                                const float2 lo = __ldg(reinterpret_cast<const float2 *>(Ph + (size_t)dl * p.d_r + e0));
+                                const float2 hi = __ldg(reinterpret_cast<const float2 *>(Ph + (size_t)dl * p.d_r + e0 + 8));
+                                p0 = lo.x; p1 = lo.y; p2 = hi.x; p3 = hi.y;
+                            }
+                            mma_16816(acc, rf[kk], pack_bf16(p0, p1), pack_bf16(p2, p3));
+                        }
+                        const int c = nt * 8 + 2 * tq;
+                        if (gq < q_len) {
+                            float *dst = tab + ((size_t)hq * A.ql + gq) * kTabW + c;
+                            dst[0] = acc[0] * inv_scale;
+                            dst[1] = acc[1] * inv_scale;
+                        }
+                        if (gq + 8 < q_len) {
+                            float *dst = tab + ((size_t)hq * A.ql + gq + 8) * kTabW + c;
+                            dst[0] = acc[2] * inv_scale;
+                            dst[1] = acc[3] * inv_scale;
+                        }
+                    }
+                }
+                mbar_arrive(bar(B_TAB_FULL));
+                if (!(ok = wwait(bar(B_TAB_FULL), band_round & 1))) break;
+            }
+
+            if (!(ok = wwait(bar(B_S_FULL + (n & 1)), (n >> 1) & 1))) break;
+            tc::fence_after();
+            const uint32_t sbuf = tmem + kTmemS0 + (uint32_t)(n & 1) * 128 + lane_off;
+            float s[64];
+            {
+                uint32_t *su = reinterpret_cast<uint32_t *>(s);
+                tc::ld32(sbuf + cb, *reinterpret_cast<uint32_t(*)[32]>(su));
+                tc::ld32(sbuf + cb + 32, *reinterpret_cast<uint32_t(*)[32]>(su + 32));
+                tc::wait_ld();
+            }
+            if (band) {
+                if (valid_row) {
+                    // column b of the tile is at distance i - j = dlo + (t + 127 - b)
+                    const float *trow = tab + ((size_t)hh * A.ql + t) * kTabW + t + (kKeys - 1) - cb;
+#pragma unroll
+                    for (int bb = 0; bb < 64; ++bb) s[bb] += trow[-bb];
+                }
+                mbar_arrive(bar(B_TAB_FREE));
+                ++band_round;
+            }
+            // mask: key j visible iff it is in this split's range, j <= i and (SWA) i - j < window
+            int b_lo, span;
+            {
+                int jv_lo = kr_lo, jv_hi = min(i_pos, kr_hi - 1);
+                if (p.window > 0) jv_lo = max(jv_lo, i_pos - p.window + 1);
+                const bool any = valid_row && jv_hi >= jv_lo;
+                b_lo = any ? jv_lo - j0 - cb : (1 << 20);
+                span = any ? jv_hi - jv_lo : 0;
+            }
+            const bool need_mask = !valid_row || (j0 + kKeys - 1 > pos0) || (j0 + kKeys > kr_hi) ||
+                                   (p.window > 0 && pos0 + q_len - 1 - j0 >= p.window);
+            if (need_mask) {
+#pragma unroll
+                for (int bb = 0; bb < 64; ++bb)
+                    s[bb] = ((unsigned)(bb - b_lo) <= (unsigned)span) ? s[bb] : -INFINITY;
+            }
+            float m4[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float m = fmax3(s[16 * c], s[16 * c + 1], s[16 * c + 2]);
+#pragma unroll
+                for (int e = 3; e < 15; e += 2) m = fmax3(m, s[16 * c + e], s[16 * c + e + 1]);
+                m4[c] = fmaxf(m, s[16 * c + 15]);
+            }
+            float mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
+            float *xc = xchg + (n & 1) * 256;
+            xc[hw * 128 + a] = mx;
+            if (!(ok = pair_sync())) break;
+            mx = fmaxf(mx, xc[(1 - hw) * 128 + a]);
+            mx = mx == -INFINITY ? -INFINITY : mx * c_qk;        // log2 units
+            const bool need = mx > m_run + 8.f;
+            if (__any_sync(0xffffffffu, need)) {
+                const float m_new = need ? fmaxf(m_run, mx) : m_run;
+                const float corr = m_new == -INFINITY ? 1.f : fast_exp2(m_run - m_new);
+                if (n > 0) {
+                    if (!(ok = wait_pv(n - 1))) break;
+                    tc::fence_after();
+                    uint32_t o[32];
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        tc::ld32(tmem + kTmemO + lane_off + cb + c * 32, o);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+                        tc::st32(tmem + kTmemO + lane_off + cb + c * 32, o);
+                    }
+                    tc::wait_st();
+                }
+                l_run *= corr;
+                m_run = m_new;
+            }
+            const float ref = m_run == -INFINITY ? 0.f : m_run;
+            const float2 cq = make_float2(c_qk, c_qk), nref = make_float2(-ref, -ref);
+            float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                            make_float2(0.f, 0.f)};
+            uint32_t pk[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const float2 x = ffma2(make_float2(s[2 * e], s[2 * e + 1]), cq, nref);
+                const int k8 = e & 7;
+                const float2 y = (k8 == 1 || k8 == 4 || k8 == 6)
+                    ? soft_exp2x2(x) : make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                l4[e & 3] = fadd2(l4[e & 3], y);
+                pk[e] = pack_bf16(y.x, y.y);
+            }
+            tc::st32(sbuf + 32 * hw, pk);
+            const float2 l2 = fadd2(fadd2(l4[0], l4[1]), fadd2(l4[2], l4[3]));
+            l_run += l2.x + l2.y;
+            tc::wait_st();
+            tc::fence_before();
+            mbar_arrive(bar(B_P_FULL + (n & 1)));
+        }
+        // epilogue: the row sum of both halves, then O / l for this thread's 64 columns
+        float *xl = xchg + 512;
+        xl[hw * 128 + a] = l_run;
+        if (ok) ok = pair_sync();
+        const float l_tot = l_run + xl[(1 - hw) * 128 + a];
+        if (ok) ok = wait_pv(N - 1);
+        if (ok) {
+            tc::fence_after();
+            const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+            const size_t qrow = (size_t)(start + t) * p.Hq + hk * g + hh;
+            const float ref = m_run == -INFINITY ? 0.f : m_run;
+            const float lse_nat = l_tot > 0.f ? (ref + log2f(l_tot)) * 0.6931471805599453f : -INFINITY;
+            uint32_t o[32];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                tc::ld32(tmem + kTmemO + lane_off + cb + c * 32, o);
+                tc::wait_ld();
+                if (!valid_row) continue;
+                const int col = cb + c * 32;
+                if (A.S > 1) {
+                    float4 *dst = reinterpret_cast<float4 *>(A.ws_o + (qrow * A.S + split) * kHeadDim + col);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv, __uint_as_float(o[4 * e + 1]) * inv,
+                                             __uint_as_float(o[4 * e + 2]) * inv, __uint_as_float(o[4 * e + 3]) * inv);
+                } else if (p.out_dtype == INKATTN_DTYPE_F32) {
+                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + qrow * kHeadDim + col);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        dst[e] = make_float4(__uint_as_float(o[4 * e]) * inv, __uint_as_float(o[4 * e + 1]) * inv,
+                                             __uint_as_float(o[4 * e + 2]) * inv, __uint_as_float(o[4 * e + 3]) * inv);
+                } else {
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<inkattn_bf16 *>(p.out) + qrow * kHeadDim + col);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        dst[e] = make_uint4(
+                            pack_bf16(__uint_as_float(o[8 * e]) * inv, __uint_as_float(o[8 * e + 1]) * inv),
+                            pack_bf16(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv),
+                            pack_bf16(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv),
+                            pack_bf16(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv));
+                }
+            }
+            if (valid_row && hw == 0) {
+                if (A.S > 1) A.ws_lse[qrow * A.S + split] = lse_nat;
+                else if (p.lse) p.lse[qrow] = lse_nat;
+            }
+        }
+    }
+
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+cudaError_t launch_decode_tc(const inkattn_attn_params &p, const AttnScalars &s, int num_splits,
+                             float *ws_o, float *ws_lse, const CUtensorMap &qmap, const CUtensorMap &kmap,
+                             const CUtensorMap &vmap, cudaStream_t stream) {
+    DecTcArgs a;
+    a.p = p;
+    a.scale = s.scale;
+    a.S = num_splits;
+    a.ql = p.max_seqlen_q;
+    a.ws_o = ws_o;
+    a.ws_lse = ws_lse;
+    a.kv_rows = (long long)p.num_blocks * p.Hkv * kBlock;
+    cudaError_t err = cudaFuncSetAttribute(k_decode_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (err != cudaSuccess) return err;
+    dim3 grid(num_splits, p.Hkv, p.B);
+    k_decode_tc<<<grid, kThreads, kSmem, stream>>>(a, qmap, kmap, vmap);
+    return cudaGetLastError();
+}
+
+}  // namespace inkattn

@@ -47,5 +47,11 @@ bool make_rel_map(CUtensorMap *map, const void *base, int hq, int rel_extent, in
 bool make_cache_map(CUtensorMap *map, const void *base, long long rows);
 // TMA descriptor for q viewed as [N_tok][Hq][128] bf16, box {64, 1, box_rows}, 128-byte swizzle.
 bool make_q_map(CUtensorMap *map, const void *base, int n_tok, int hq, int box_rows);
+// Q as [N_tok][Hq][128] with a box of {64 dims, `group` heads, `tokens` tokens}: the rows of
+// one KV head's query heads for consecutive tokens, in (token, head) order.
+bool make_q_group_map(CUtensorMap *map, const void *base, int n_tok, int hq, int group, int tokens);
+cudaError_t launch_decode_tc(const inkattn_attn_params &p, const AttnScalars &s, int num_splits,
+                             float *ws_o, float *ws_lse, const CUtensorMap &qmap, const CUtensorMap &kmap,
+                             const CUtensorMap &vmap, cudaStream_t stream);
 
 }  // namespace inkattn
