@@ -40,7 +40,8 @@ L2_FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = {
     "k_prefill_tc": ["relative_bias_hybrid_gb300/csrc/prefill_tc.cu", "relative_bias_hybrid_gb300/csrc/tcgen05.cuh",
                      "relative_bias_hybrid_gb300/csrc/common.cuh"],
-    "k_decode": ["relative_bias_hybrid_gb300/csrc/decode.cu", "relative_bias_hybrid_gb300/csrc/common.cuh"],
+    "k_decode_tc": ["relative_bias_hybrid_gb300/csrc/decode_tc.cu", "relative_bias_hybrid_gb300/csrc/tcgen05.cuh",
+                    "relative_bias_hybrid_gb300/csrc/common.cuh"],
     "k_prologue": ["relative_bias_hybrid_gb300/csrc/prologue.cu", "relative_bias_hybrid_gb300/csrc/common.cuh"],
 }
 
@@ -432,8 +433,8 @@ def run_gpu(args, world, rank, local):
             "k_prologue": {"bound": "hbm", "achieved": pro_gbs, "peak": peaks["hbm"], "unit": "GB/s",
                            "frac": pro_gbs / peaks["hbm"], "traffic": ncu_traffic("k_prologue", "swa"),
                            "algorithmic_bytes_per_launch": prologue_bytes(w), "ms": pro_ms},
-            "k_decode+k_combine": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm"], "unit": "GB/s",
-                                   "frac": dec_gbs / peaks["hbm"], "traffic": ncu_traffic("k_decode", "decode"),
+            "k_decode_tc+k_combine": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                                      "frac": dec_gbs / peaks["hbm"], "traffic": ncu_traffic("k_decode_tc", "decode"),
                                    "algorithmic_bytes_per_launch": dbytes, "ms": dec_ms,
                                    "num_splits": dstep.num_splits},
         },

@@ -124,9 +124,12 @@ AttnScalars scalars(const inkattn_attn_params &p) {
 
 inkattn_status launch_status(cudaError_t e) { return e == cudaSuccess ? INKATTN_OK : INKATTN_ERR_CUDA; }
 
-// Decode split heuristic.  Cost model, in units of "one 64-key K+V block streamed by one
-// CTA slot": the KV stream takes waves(S) * ceil(nblk / S); the split partials add their
-// write + read traffic spread over all slots, plus a fixed cost for the combine launch.
+// Decode split heuristic ([vLLM TML Inkling サポート, §低レイテンシコレクティブとカーネル
+// "FA4 Kernel"]: num_splits from batch size, TP size and KV length; TP = 1 here).
+// Cost model in units of one 64-key K+V block moved at the full HBM rate: a CTA streams
+// `per` blocks at min(its own rate, HBM / active CTAs), so a wave with a CTAs costs
+// per * max(r, a), where r is the number of CTAs that saturate HBM; the split partials add
+// their write + read traffic and the combine launch a fixed cost.
 int pick_splits(const inkattn_attn_params &p, int num_sms) {
     const int g = p.Hq / p.Hkv;
     long long nblk = (p.max_seqlen_k + kBlock - 1) / kBlock;
@@ -137,7 +140,7 @@ int pick_splits(const inkattn_attn_params &p, int num_sms) {
     if (nblk < 1) nblk = 1;
     const long long units = (long long)p.B * p.Hkv;
     const long long slots = (long long)(num_sms > 0 ? num_sms : 1) * kDecodeCtasPerSm;
-    if (units >= 2 * slots) return 1;
+    const double r = kDecodeHbmSmFrac * (double)slots;
     const long long rows_per_unit = (long long)p.max_seqlen_q * g;
     const double block_bytes = 2.0 * kBlock * kHeadDim * 2;   // K + V of one block
     int best = 1;
@@ -145,11 +148,14 @@ int pick_splits(const inkattn_attn_params &p, int num_sms) {
     for (int S = 1; S <= kDecodeMaxSplits; ++S) {
         const long long per = (nblk + S - 1) / S;
         if (S > 1 && per < kDecodeMinSplitBlocks) break;
-        const long long waves = (units * S + slots - 1) / slots;
-        double cost = (double)waves * (double)per;
+        const long long ctas = units * S;
+        const long long full = ctas / slots, rest = ctas - full * slots;
+        double waves = (double)full * fmax(r, (double)slots);
+        if (rest > 0) waves += fmax(r, (double)rest);
+        double cost = (double)per * waves;
         if (S > 1) {
             const double ws_bytes = 2.0 * units * rows_per_unit * S * (kHeadDim + 1) * 4.0;
-            cost += ws_bytes / block_bytes / (double)slots + kCombineCostBlocks;
+            cost += ws_bytes / block_bytes + kCombineCostBlocks;
         }
         if (cost < best_cost * (1.0 - 1e-9)) {
             best_cost = cost;

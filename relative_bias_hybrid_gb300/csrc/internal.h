@@ -26,10 +26,10 @@ constexpr int kDecodeMaxRows = 128;     // max_seqlen_q * group
 constexpr int kDecodeMaxSplits = 64;
 constexpr int kDecodeCtasPerSm = 1;     // design occupancy used by the split heuristic
 constexpr int kDecodeMinSplitBlocks = 8; // a split streams at least 8 cache blocks (512 keys)
-constexpr double kCombineCostBlocks = 2.0; // fixed cost of the combine launch, in block loads
-cudaError_t launch_decode(const inkattn_attn_params &p, const AttnScalars &s, int num_splits,
-                          float *ws_o, float *ws_lse, const CUtensorMap &kmap,
-                          const CUtensorMap &vmap, cudaStream_t stream);
+// Fraction of the SMs whose decode CTAs together saturate HBM: one CTA streams K/V at about
+// 40 B/clk (its MMAs take ~1600 cycles per 64 KB tile), HBM gives ~23 B/clk per SM.
+constexpr double kDecodeHbmSmFrac = 0.6;
+constexpr double kCombineCostBlocks = 600.0; // fixed cost of the combine launch (~3 us), in block loads
 cudaError_t launch_combine(const inkattn_attn_params &p, int num_splits, const float *ws_o,
                            const float *ws_lse, cudaStream_t stream);
 

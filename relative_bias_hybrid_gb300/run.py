@@ -26,6 +26,7 @@ def main(argv=None):
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--seqs", type=int, default=0, help="keep only the first N sequences")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--splits", type=int, default=0, help="decode splits (0 = the library's heuristic)")
     args = ap.parse_args(argv)
 
     w = gen.workload(args.workload)
@@ -34,7 +35,8 @@ def main(argv=None):
                                 prefix_lens=w.prefix_lens[:args.seqs])
     dev = torch.device("cuda", torch.cuda.current_device())
     x = gen.make_inputs(w, seed=args.seed, device=dev)
-    step = AttentionStep(w, x, mode="decode" if args.workload == "decode" else "prefill")
+    step = AttentionStep(w, x, mode="decode" if args.workload == "decode" else "prefill",
+                         num_splits=args.splits)
     stream = torch.cuda.Stream(device=dev)
     print(w.describe(), f"num_splits={step.num_splits}" if step.mode == "decode" else "")
     with torch.cuda.stream(stream):

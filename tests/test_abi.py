@@ -119,12 +119,17 @@ def test_host_validation_rejects_before_any_launch(ia):
 
 def test_split_heuristic_and_workspace_size(ia):
     p = _attn(ia)
-    S = ia.inkattn_decode_num_splits(p, 152)
-    assert 1 < S <= 64
+    # 32 sequences x 8 KV heads = 256 CTAs already keep HBM busy on 152 SMs: no split
+    assert ia.inkattn_decode_num_splits(p, 152) == 1
+    assert ia.inkattn_decode_num_splits(_attn(ia, B=16, N_tok=16 * 9), 152) == 1
+    # a few sequences: split the KV length until the GPU is full
+    few = _attn(ia, B=2, N_tok=2 * 9)
+    S = ia.inkattn_decode_num_splits(few, 152)
+    assert 4 <= S <= 64 and 2 * 8 * S >= 0.6 * 152   # enough CTAs to keep HBM busy
     nblk = 32768 // 64
     assert -(-nblk // S) >= 8                      # each split streams >= 8 blocks
-    # enough (sequence, KV head) units to fill two waves: no split
-    assert ia.inkattn_decode_num_splits(_attn(ia, B=64, N_tok=64 * 9), 152) == 1
+    # 160 units: one full wave plus 8 CTAs would idle most SMs in the second wave
+    assert ia.inkattn_decode_num_splits(_attn(ia, B=20, N_tok=20 * 9), 152) > 1
     # short KV: few blocks, few splits
     short = _attn(ia, B=1, N_tok=9, max_seqlen_k=1024, max_blocks_per_seq=16)
     assert ia.inkattn_decode_num_splits(short, 152) <= 2
