@@ -12,19 +12,19 @@
 // The conv sum of each channel is formed exactly (error-free products and sums in fp32)
 // and rounded once to bf16, which is the correctly rounded value of the definition.
 //
-// Work split: one CTA per (16-token tile of one sequence, KV head hk).  It handles, for
-// its tokens, the g = Hq/Hkv query heads of that KV head (RMSNorm only), the K stream
-// of head hk (conv, round to bf16, RMSNorm, cache write) and the V stream (conv,
-// round, cache write).  Each 128-value row is owned by a half-warp: 16 lanes x 16 bytes,
-// so every global access is a full 256-byte row, coalesced.  The query rows (most of the
-// bytes) are loaded first, eight per half-warp in flight; the K and V input rows of the
-// tile and the three rows before it are staged once in shared memory, so each conv tap
-// is a shared-memory read instead of a fourth global read of the same row.
-//
+// Work split: two CTAs per (16-token tile of one sequence, KV head hk), neighbours in the
+// grid.  One streams the tile's query rows of the g = Hq/Hkv query heads of hk (RMSNorm
+// only; eight rows per half-warp in flight).  The other takes the K and V streams of head
+// hk: it stages the tile's input rows and the three rows before it in shared memory once,
+// then computes the conv (rounded to bf16), the K RMSNorm and the cache writes.  The
+// latency-bound K/V work thus runs beside the bandwidth-bound query stream, four CTAs per
+// SM.  Each 128-value row is owned by a half-warp: 16 lanes x 16 bytes, so every global
+// access is a full 256-byte row, coalesced.
+
 // Conv-state carry without races: tiles are aligned to sequence starts, so every read of
-// the carried rows (tokens 0..2) happens in tile 0 of the sequence; that same CTA, after
-// a block barrier, writes the new state for its own 128 channels.  No other CTA touches
-// those channels of that state slot.
+// the carried rows (tokens 0..2) happens in the K/V CTA of tile 0 of the sequence; that
+// same CTA, after a block barrier, writes the new state for its own 128 channels.  No other
+// CTA touches those channels of that state slot.
 #include "common.cuh"
 #include "internal.h"
 
@@ -126,15 +126,18 @@ __device__ __forceinline__ void conv4_bf16_fast2(const float (&wa)[4], const flo
         ? __bfloat162float(__float2bfloat16_rn(s.y)) : conv4_bf16(wb, xb);
 }
 
-__global__ void __launch_bounds__(kPrologueThreads, 3)
+__global__ void __launch_bounds__(kPrologueThreads, 4)
 k_prologue(const inkattn_prologue_params p) {
     __shared__ __align__(16) float s_wk[kHeadDim * 4];
     __shared__ __align__(16) float s_wv[kHeadDim * 4];
-    __shared__ float s_gq[kHeadDim], s_gk[kHeadDim];
+    __shared__ float s_gk[kHeadDim];
     // this head's K and V input rows [t0 - 3, t0 + nt) of [3 carried rows ; new rows]
     __shared__ uint4 s_x[2][kPrologueTokens + 3][16];
 
-    const int tile = blockIdx.x, b = blockIdx.y, hk = blockIdx.z;
+    // even x: the query rows of the tile (RMSNorm only, a pure stream); odd x: the K and V
+    // rows (conv, norm, cache write, state carry).  Neighbouring CTAs take the two roles, so
+    // the latency-bound K/V work runs beside the bandwidth-bound query stream.
+    const int tile = blockIdx.x >> 1, role_kv = blockIdx.x & 1, b = blockIdx.y, hk = blockIdx.z;
     const int tid = threadIdx.x;
     const int C = p.Hkv * kHeadDim;
     const int g = p.Hq / p.Hkv;
@@ -155,38 +158,71 @@ k_prologue(const inkattn_prologue_params p) {
     const int half = tid >> 4;                // 16 half-warps per CTA
     const int lane16 = tid & 15;
     const int c0 = lane16 * 8;                // 8 channels per lane within the head
-    const size_t head_off = (size_t)hk * kHeadDim + c0;
 
-    // ---- query rows first: up to kQInFlight loads per lane before any arithmetic
-    const int q_rows = nt * g;
-    // row -> token within the tile (shifts for power-of-two group sizes)
-    const int g_shift = (g & (g - 1)) == 0 ? __ffs(g) - 1 : -1;
-    auto div_g = [&](int row) { return g_shift >= 0 ? row >> g_shift : row / g; };
-    uint4 qraw[kQInFlight];
-#pragma unroll
-    for (int j = 0; j < kQInFlight; ++j) {
-        const int row = half + 16 * j;
-        qraw[j] = make_uint4(0, 0, 0, 0);
-        if (row < q_rows) {
-            const int tt = div_g(row), h = hk * g + (row - tt * g);
-            qraw[j] = __ldg(reinterpret_cast<const uint4 *>(
-                p.q + ((size_t)(start + t0 + tt) * p.Hq + h) * kHeadDim + c0));
+    if (!role_kv) {
+        // ======================= query rows: RMSNorm, kQInFlight rows per lane in flight
+        const int q_rows = nt * g;
+        const int g_shift = (g & (g - 1)) == 0 ? __ffs(g) - 1 : -1;
+        auto div_g = [&](int row) { return g_shift >= 0 ? row >> g_shift : row / g; };
+        float2 gq[4];
+        {
+            const float4 g0 = __ldg(reinterpret_cast<const float4 *>(p.q_norm_w + c0));
+            const float4 g1 = __ldg(reinterpret_cast<const float4 *>(p.q_norm_w + c0 + 4));
+            gq[0] = make_float2(g0.x, g0.y); gq[1] = make_float2(g0.z, g0.w);
+            gq[2] = make_float2(g1.x, g1.y); gq[3] = make_float2(g1.z, g1.w);
         }
+        for (int j0 = 0; j0 * 16 < q_rows; j0 += kQInFlight) {   // uniform over the CTA
+            uint4 qraw[kQInFlight];
+#pragma unroll
+            for (int j = 0; j < kQInFlight; ++j) {
+                const int row = half + 16 * (j0 + j);
+                qraw[j] = make_uint4(0, 0, 0, 0);
+                if (row < q_rows) {
+                    const int tt = div_g(row), h = hk * g + (row - tt * g);
+                    qraw[j] = __ldg(reinterpret_cast<const uint4 *>(
+                        p.q + ((size_t)(start + t0 + tt) * p.Hq + h) * kHeadDim + c0));
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kQInFlight; ++j) {
+                const int row = half + 16 * (j0 + j);
+                float x[8];
+                unpack8(qraw[j], x);
+                float ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+                ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+                ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+                ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                if (row >= q_rows) continue;
+                const int tt = div_g(row), h = hk * g + (row - tt * g);
+                const float inv = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
+                const float2 inv2 = make_float2(inv, inv);
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 v = fmul2(fmul2(make_float2(x[2 * e], x[2 * e + 1]), inv2), gq[e]);
+                    y[2 * e] = v.x;
+                    y[2 * e + 1] = v.y;
+                }
+                *reinterpret_cast<uint4 *>(p.q_out + ((size_t)(start + t0 + tt) * p.Hq + h) * kHeadDim + c0) =
+                    pack8(y);
+            }
+        }
+        return;
     }
-    // ---- conv weights, norm gains, and the K/V input rows with their 3-row halo
+
+    // ======================= K and V rows
+    // conv weights and the K gains, interleaved by lane: channel c = 8 * lane + e, tap k at
+    // [(e * 16 + lane) * 4 + k], so the 16 lanes of a half-warp read consecutive float4s
     for (int i = tid; i < kHeadDim * 4; i += kPrologueThreads) {
-        // channel c = 8 * lane + e, tap k stored at [(e * 16 + lane) * 4 + k]: the 16 lanes
-        // of a half-warp read 16 consecutive float4s for each e (no bank conflicts)
         const int c = i >> 2, k = i & 3;
         const int j = (((c & 7) * 16 + (c >> 3)) << 2) + k;
         s_wk[j] = p.conv_w_k[(size_t)hk * kHeadDim * 4 + i];
         s_wv[j] = p.conv_w_v[(size_t)hk * kHeadDim * 4 + i];
     }
-    if (tid < kHeadDim) {
-        const int j = (tid & 7) * 16 + (tid >> 3);        // same interleave for the gains
-        s_gq[j] = p.q_norm_w[tid];
-        s_gk[j] = p.k_norm_w[tid];
-    }
+    if (tid < kHeadDim) s_gk[(tid & 7) * 16 + (tid >> 3)] = p.k_norm_w[tid];
     for (int i = tid; i < 2 * (nt + 3) * 16; i += kPrologueThreads) {
         const int stream = i / ((nt + 3) * 16), r = (i >> 4) % (nt + 3), chunk = i & 15;
         const int idx = t0 + r;               // index into [3 carried rows ; new rows]
@@ -201,55 +237,18 @@ k_prologue(const inkattn_prologue_params p) {
         }
         s_x[stream][r][chunk] = v;
     }
+    // slot mapping of the rows this thread writes (tokens half&7 and half&7 + 8), fetched
+    // before the barrier so the cache write does not wait for it
+    int sm_pre[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int tt = u * 8 + (half & 7);
+        sm_pre[u] = tt < nt ? __ldg(p.slot_mapping + start + t0 + tt) : 0;
+    }
     __syncthreads();
 
-    // ---- query rows: RMSNorm and store (the loads were issued at the start)
-    float2 gq[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) gq[e] = make_float2(s_gq[(2 * e) * 16 + lane16], s_gq[(2 * e + 1) * 16 + lane16]);
-    for (int j0 = 0; j0 * 16 < q_rows; j0 += kQInFlight) {
-#pragma unroll
-        for (int j = 0; j < kQInFlight; ++j) {
-            const int row = half + 16 * (j0 + j);
-            if (j0 > 0) {                      // rows beyond the first batch (g > 8)
-                qraw[j] = make_uint4(0, 0, 0, 0);
-                if (row < q_rows) {
-                    const int tt = div_g(row), h = hk * g + (row - tt * g);
-                    qraw[j] = __ldg(reinterpret_cast<const uint4 *>(
-                        p.q + ((size_t)(start + t0 + tt) * p.Hq + h) * kHeadDim + c0));
-                }
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < kQInFlight; ++j) {
-            const int row = half + 16 * (j0 + j);
-            float x[8];
-            unpack8(qraw[j], x);
-            float ss = 0.f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
-            ss += __shfl_xor_sync(0xffffffffu, ss, 8);
-            ss += __shfl_xor_sync(0xffffffffu, ss, 4);
-            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-            if (row >= q_rows) continue;
-            const int tt = div_g(row), h = hk * g + (row - tt * g);
-            const float inv = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
-            const float2 inv2 = make_float2(inv, inv);
-            float y[8];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 v = fmul2(fmul2(make_float2(x[2 * e], x[2 * e + 1]), inv2), gq[e]);
-                y[2 * e] = v.x;
-                y[2 * e + 1] = v.y;
-            }
-            *reinterpret_cast<uint4 *>(p.q_out + ((size_t)(start + t0 + tt) * p.Hq + h) * kHeadDim + c0) = pack8(y);
-        }
-    }
-
-
-    // ---- K and V rows: conv (rounded to bf16), K RMSNorm, cache write.  Half-warps 0-7
-    // take the K stream and 8-15 the V stream.
+    // conv (rounded to bf16), K RMSNorm, cache write.  Half-warps 0-7 take the K stream and
+    // 8-15 the V stream.
     const long long slot_limit = (long long)p.num_blocks * kBlock;
     const int stream = half >> 3;
     const float *wsm = stream == 0 ? s_wk : s_wv;
@@ -278,8 +277,7 @@ k_prologue(const inkattn_prologue_params p) {
         ss += __shfl_xor_sync(0xffffffffu, ss, 2);
         ss += __shfl_xor_sync(0xffffffffu, ss, 1);
         if (!valid) continue;
-        const int tok = start + t0 + tt;
-        const int sm = p.slot_mapping[tok];
+        const int sm = base == 0 ? sm_pre[0] : sm_pre[1];
         if (sm < 0 || (long long)sm >= slot_limit) {
             if (lane16 == 0) set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
             continue;
@@ -319,7 +317,7 @@ k_prologue(const inkattn_prologue_params p) {
 
 cudaError_t launch_prologue(const inkattn_prologue_params &p, cudaStream_t stream) {
     const int tiles = p.max_seqlen_q > 0 ? (p.max_seqlen_q + kPrologueTokens - 1) / kPrologueTokens : 1;
-    dim3 grid(tiles, p.B, p.Hkv);
+    dim3 grid(2 * tiles, p.B, p.Hkv);
     k_prologue<<<grid, kPrologueThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
