@@ -30,7 +30,9 @@
 
 namespace inkattn {
 
-constexpr int kPrologueTokens = 16;
+constexpr int kPrologueTokens = 16;      // tokens of a query-stream CTA
+constexpr int kKvTilesMax = 4;           // query tiles per K/V CTA: 2, or 4 for large grids
+constexpr int kKvTokens = kKvTilesMax * kPrologueTokens;   // most tokens of a K/V CTA
 constexpr int kPrologueThreads = 256;
 static_assert(kPrologueThreads == 256, "the row mapping assumes 16 half-warps per CTA");
 constexpr int kQInFlight = 8;      // query rows a half-warp loads before it computes
@@ -127,17 +129,20 @@ __device__ __forceinline__ void conv4_bf16_fast2(const float (&wa)[4], const flo
 }
 
 __global__ void __launch_bounds__(kPrologueThreads, 4)
-k_prologue(const inkattn_prologue_params p) {
+k_prologue(const inkattn_prologue_params p, const int kv_tiles) {
     __shared__ __align__(16) float s_wk[kHeadDim * 4];
     __shared__ __align__(16) float s_wv[kHeadDim * 4];
     __shared__ float s_gk[kHeadDim];
     // this head's K and V input rows [t0 - 3, t0 + nt) of [3 carried rows ; new rows]
-    __shared__ uint4 s_x[2][kPrologueTokens + 3][16];
+    __shared__ uint4 s_x[2][kKvTokens + 3][16];
 
-    // even x: the query rows of the tile (RMSNorm only, a pure stream); odd x: the K and V
-    // rows (conv, norm, cache write, state carry).  Neighbouring CTAs take the two roles, so
-    // the latency-bound K/V work runs beside the bandwidth-bound query stream.
-    const int tile = blockIdx.x >> 1, role_kv = blockIdx.x & 1, b = blockIdx.y, hk = blockIdx.z;
+    // Groups of kv_tiles + 1 neighbouring CTAs along x: the first kv_tiles stream the query
+    // rows of one 16-token tile each (RMSNorm only); the last takes the K and V rows of the
+    // group's 16 * kv_tiles tokens (conv, norm, cache write, state carry).  The
+    // latency-bound K/V work thus runs beside the bandwidth-bound query stream.
+    const int grp = blockIdx.x / (kv_tiles + 1), sub = blockIdx.x - grp * (kv_tiles + 1);
+    const int role_kv = sub == kv_tiles, b = blockIdx.y, hk = blockIdx.z;
+    const int tile = role_kv ? grp * kv_tiles : grp * kv_tiles + sub;
     const int tid = threadIdx.x;
     const int C = p.Hkv * kHeadDim;
     const int g = p.Hq / p.Hkv;
@@ -153,7 +158,7 @@ k_prologue(const inkattn_prologue_params p) {
     const int q_len = end - start;
     const int t0 = tile * kPrologueTokens;
     if (t0 >= q_len) return;   // (an empty sequence keeps its state unchanged)
-    const int nt = min(kPrologueTokens, q_len - t0);
+    const int nt = min(role_kv ? kv_tiles * kPrologueTokens : kPrologueTokens, q_len - t0);
 
     const int half = tid >> 4;                // 16 half-warps per CTA
     const int lane16 = tid & 15;
@@ -237,11 +242,12 @@ k_prologue(const inkattn_prologue_params p) {
         }
         s_x[stream][r][chunk] = v;
     }
-    // slot mapping of the rows this thread writes (tokens half&7 and half&7 + 8), fetched
-    // before the barrier so the cache write does not wait for it
-    int sm_pre[2];
+    // slot mapping of the rows this thread writes (tokens half&7 + 8u), fetched before the
+    // barrier so the cache write does not wait for it
+    constexpr int kRowsPerHalf = kKvTokens / 8;
+    int sm_pre[kRowsPerHalf];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < kRowsPerHalf; ++u) {
         const int tt = u * 8 + (half & 7);
         sm_pre[u] = tt < nt ? __ldg(p.slot_mapping + start + t0 + tt) : 0;
     }
@@ -252,8 +258,10 @@ k_prologue(const inkattn_prologue_params p) {
     const long long slot_limit = (long long)p.num_blocks * kBlock;
     const int stream = half >> 3;
     const float *wsm = stream == 0 ? s_wk : s_wv;
-    for (int base = 0; base < nt; base += 8) {       // uniform trip count: all lanes shuffle
-        const int tt = base + (half & 7);
+#pragma unroll 1
+    for (int u = 0; u < kRowsPerHalf; ++u) {         // uniform trip count: all lanes shuffle
+        if (u * 8 >= nt) break;                      // uniform over the CTA
+        const int tt = u * 8 + (half & 7);
         const bool valid = tt < nt;
         const int ts = valid ? tt : 0;
         float xt[4][8];
@@ -277,7 +285,9 @@ k_prologue(const inkattn_prologue_params p) {
         ss += __shfl_xor_sync(0xffffffffu, ss, 2);
         ss += __shfl_xor_sync(0xffffffffu, ss, 1);
         if (!valid) continue;
-        const int sm = base == 0 ? sm_pre[0] : sm_pre[1];
+        int sm = sm_pre[0];
+#pragma unroll
+        for (int v = 1; v < kRowsPerHalf; ++v) sm = (u == v) ? sm_pre[v] : sm;
         if (sm < 0 || (long long)sm >= slot_limit) {
             if (lane16 == 0) set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
             continue;
@@ -317,8 +327,12 @@ k_prologue(const inkattn_prologue_params p) {
 
 cudaError_t launch_prologue(const inkattn_prologue_params &p, cudaStream_t stream) {
     const int tiles = p.max_seqlen_q > 0 ? (p.max_seqlen_q + kPrologueTokens - 1) / kPrologueTokens : 1;
-    dim3 grid(2 * tiles, p.B, p.Hkv);
-    k_prologue<<<grid, kPrologueThreads, 0, stream>>>(p);
+    // larger K/V groups amortise their fixed cost on large grids; smaller ones keep the
+    // K/V work spread out on short ones
+    const int kv_tiles = ((long long)tiles * p.B >= 2048) ? 4 : 2;
+    const int groups = (tiles + kv_tiles - 1) / kv_tiles;
+    dim3 grid(groups * (kv_tiles + 1), p.B, p.Hkv);
+    k_prologue<<<grid, kPrologueThreads, 0, stream>>>(p, kv_tiles);
     return cudaGetLastError();
 }
 

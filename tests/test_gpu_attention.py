@@ -99,7 +99,7 @@ def test_prefill_tiny_all_rows(env):
 
 
 @pytest.mark.parametrize("case", ["swa_ragged", "full_logscale", "no_bias", "extent_past_T", "gqa4",
-                                  "gqa3_unpaired", "mha"])
+                                  "gqa3_unpaired", "mha", "empty_sequence"])
 def test_prefill_small_mixed(env, case):
     gen = env[0]
     kw = dict(Hq=8, Hkv=2, q_lens=[200, 77, 300, 1], prefix_lens=[0, 150, 37, 9])
@@ -118,9 +118,13 @@ def test_prefill_small_mixed(env, case):
         # odd group size: head pairs do not share a KV head, so no CTA pairing
         w = gen.custom(case, Hq=6, Hkv=2, q_lens=[300, 45], prefix_lens=[20, 0], window=0,
                        rel_extent=200)
-    else:
+    elif case == "mha":
         w = gen.custom(case, Hq=3, Hkv=3, q_lens=[190, 260], prefix_lens=[0, 70], window=128,
                        rel_extent=50)
+    else:
+        # a sequence with no new tokens between two others (its cached prefix stays unread)
+        w = gen.custom(case, Hq=8, Hkv=2, q_lens=[130, 0, 129], prefix_lens=[5, 64, 0],
+                       window=0, rel_extent=100)
     _check_all_rows(env, w, *_run(env, w, seed=11))
 
 

@@ -66,10 +66,22 @@ def test_prologue_ragged_short_sequences(env):
     _check(env, w, *_run(env, w, seed=3))
 
 
-def test_prologue_swa_layer_full_size(env):
+@pytest.mark.parametrize("name", ["swa", "full"])
+def test_prologue_layer_full_size(env, name):
+    """One prefill layer at full size (8192 / 32768 tokens): the two K/V group sizes the
+    launch picks (32 tokens on the short grid, 64 on the long one)."""
     gen = env[0]
-    w = gen.workload("swa")
+    w = gen.workload(name)
     _check(env, w, *_run(env, w, seed=1))
+
+
+def test_prologue_many_sequences_uneven_tiles(env):
+    """Long enough that K/V groups of 64 tokens are used, with sequence lengths that end
+    inside a group and inside a query tile, and a carried state on every sequence."""
+    gen = env[0]
+    w = gen.custom("many", Hq=8, Hkv=2, q_lens=[1000, 77, 4097, 63, 2048, 5, 3001, 130] * 2,
+                   prefix_lens=[0, 3, 50, 2, 7, 1, 900, 4] * 2)
+    _check(env, w, *_run(env, w, seed=4))
 
 
 def test_prologue_decode_shape(env):
