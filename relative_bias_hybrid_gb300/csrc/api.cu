@@ -281,11 +281,9 @@ inkattn_status inkattn_prefill(const inkattn_attn_params *p, void *stream) {
     if (!make_q_map(&qmap, p->q, p->N_tok, p->Hq, kPrefillTcRows) ||
         !make_cache_map(&kmap, p->k_cache, rows) || !make_cache_map(&vmap, p->v_cache, rows))
         return INKATTN_ERR_CUDA;
-    if (p->rel_extent > 0) {
-        if (!make_rel_map(&pmap, p->P, p->Hq, p->rel_extent, p->d_r)) return INKATTN_ERR_CUDA;
-    } else {
-        pmap = kmap;   // unused without a bias band
-    }
+    if (p->rel_extent == 0)   // no bias band: two query tiles per CTA
+        return launch_status(launch_prefill_2q(*p, scalars(*p), qmap, kmap, vmap, static_cast<cudaStream_t>(stream)));
+    if (!make_rel_map(&pmap, p->P, p->Hq, p->rel_extent, p->d_r)) return INKATTN_ERR_CUDA;
     return launch_status(launch_prefill_tc(*p, scalars(*p), qmap, kmap, vmap, pmap,
                                            static_cast<cudaStream_t>(stream)));
 }
