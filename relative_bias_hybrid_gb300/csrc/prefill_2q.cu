@@ -321,22 +321,26 @@ k_prefill_2q(const Tc2Args A, const __grid_constant__ CUtensorMap qmap,
             }
             const bool need_mask = (j0 + kKeys - 1 > p_lo_x) || (j0 + kKeys - 1 >= T) ||
                                    (p.window > 0 && p_lo_x + kRows - 1 - j0 >= p.window);
-            // pass 1: row maximum over the 128 columns, 32 at a time
+            // pass 1: row maximum over the 128 columns, 64 at a time (two loads per wait)
             float mx = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float sc[32];
-                tc::ld32(sbuf + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sc));
+            for (int c2 = 0; c2 < 2; ++c2) {
+                float sc[64];
+                tc::ld32(sbuf + 64 * c2, *reinterpret_cast<uint32_t(*)[32]>(sc));
+                tc::ld32(sbuf + 64 * c2 + 32, *reinterpret_cast<uint32_t(*)[32]>(sc + 32));
                 tc::wait_ld();
                 if (need_mask) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        sc[e] = ((unsigned)(32 * c + e - b_lo) <= (unsigned)span) ? sc[e] : -INFINITY;
+                    for (int e = 0; e < 64; ++e)
+                        sc[e] = ((unsigned)(64 * c2 + e - b_lo) <= (unsigned)span) ? sc[e] : -INFINITY;
                 }
-                float m = fmax3(sc[0], sc[1], sc[2]);
+                float m0 = fmax3(sc[0], sc[1], sc[2]), m1 = fmax3(sc[32], sc[33], sc[34]);
 #pragma unroll
-                for (int e = 3; e < 31; e += 2) m = fmax3(m, sc[e], sc[e + 1]);
-                mx = fmax3(mx, m, sc[31]);
+                for (int e = 3; e < 31; e += 2) {
+                    m0 = fmax3(m0, sc[e], sc[e + 1]);
+                    m1 = fmax3(m1, sc[32 + e], sc[32 + e + 1]);
+                }
+                mx = fmax3(mx, fmaxf(m0, sc[31]), fmaxf(m1, sc[63]));
             }
             mx = mx == -INFINITY ? -INFINITY : mx * c_qk;     // log2 units
             const bool need = mx > m_run + 8.f;
@@ -368,11 +372,15 @@ k_prefill_2q(const Tc2Args A, const __grid_constant__ CUtensorMap qmap,
             const float2 cq = make_float2(c_qk, c_qk), nref = make_float2(-ref, -ref);
             float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                             make_float2(0.f, 0.f)};
+            float scn[32];                                   // the next chunk, loading
+            tc::ld32(sbuf, *reinterpret_cast<uint32_t(*)[32]>(scn));
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                float sc[32];
-                tc::ld32(sbuf + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sc));
                 tc::wait_ld();
+                float sc[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) sc[e] = scn[e];
+                if (c < 3) tc::ld32(sbuf + 32 * (c + 1), *reinterpret_cast<uint32_t(*)[32]>(scn));
                 if (need_mask) {
 #pragma unroll
                     for (int e = 0; e < 32; ++e)

@@ -98,8 +98,8 @@ def test_prefill_tiny_all_rows(env):
     _check_all_rows(env, w, *_run(env, w))
 
 
-@pytest.mark.parametrize("case", ["swa_ragged", "full_logscale", "no_bias", "extent_past_T", "gqa4",
-                                  "gqa3_unpaired", "mha", "empty_sequence"])
+@pytest.mark.parametrize("case", ["swa_ragged", "full_logscale", "no_bias", "no_bias_window", "extent_past_T",
+                                  "gqa4", "gqa3_unpaired", "mha", "empty_sequence"])
 def test_prefill_small_mixed(env, case):
     gen = env[0]
     kw = dict(Hq=8, Hkv=2, q_lens=[200, 77, 300, 1], prefix_lens=[0, 150, 37, 9])
@@ -109,6 +109,10 @@ def test_prefill_small_mixed(env, case):
         w = gen.custom(case, window=0, rel_extent=130, log_scale_base=64.0, **kw)
     elif case == "no_bias":
         w = gen.custom(case, window=0, rel_extent=0, **kw)
+    elif case == "no_bias_window":
+        # two query tiles per CTA with different key ranges at both window edges
+        w = gen.custom(case, Hq=8, Hkv=2, q_lens=[700, 129, 256], prefix_lens=[30, 0, 500], window=200,
+                       rel_extent=0)
     elif case == "extent_past_T":
         w = gen.custom(case, window=0, rel_extent=600, **kw)
     elif case == "gqa4":
@@ -128,13 +132,16 @@ def test_prefill_small_mixed(env, case):
     _check_all_rows(env, w, *_run(env, w, seed=11))
 
 
-@pytest.mark.parametrize("name", ["swa", "full", "ragged"])
+@pytest.mark.parametrize("name", ["swa", "full", "ragged", "full_nobias"])
 def test_prefill_full_size_sampled(env, name):
+    import dataclasses
     gen = env[0]
-    w = gen.workload(name)
+    w = gen.workload(name.replace("_nobias", ""))
+    if name.endswith("_nobias"):
+        w = dataclasses.replace(w, name=name, rel_extent=0)
     _, x, step = _run(env, w, device_inputs=True, seed=1)
     rows = _sample_rows(w)
-    if name == "full":
+    if name.startswith("full"):
         rows = rows[:: max(1, len(rows) // 24)]
     _check_rows(env, w, x, step, rows)
 
