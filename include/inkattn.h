@@ -10,8 +10,9 @@
  *
  * General conventions
  *   - Every pointer inside a params struct is a DEVICE pointer owned by the caller.
- *     The library allocates no device memory; the only scratch memory (the split-KV
- *     partials of inkattn_decode) is a caller-provided workspace.
+ *     The library allocates no device memory at run time: the split-KV partials of
+ *     inkattn_decode live in a caller-provided workspace, those of
+ *     inkattn_decode_noalloc in a fixed 64 MiB buffer that is part of the library image.
  *   - bf16 tensors are IEEE bfloat16 (inkattn_bf16 holds the raw 16-bit pattern);
  *     all arrays are dense and row-major in the layouts stated per field.
  *   - Every call is asynchronous on the caller's CUDA stream (passed as void*, a

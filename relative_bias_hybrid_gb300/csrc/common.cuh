@@ -1,7 +1,7 @@
 // common.cuh -- device helpers shared by the inkattn kernels (sm_103a).
 //
 // Everything here is plain PTX wrapped in inline functions: mbarriers with
-// bounded waits, TMA tensor loads, ldmatrix / mma.sync fragments, bf16 packing.
+// bounded waits, TMA tensor and bulk copies, clusters, mma.sync, bf16 packing, paired fp32.
 #pragma once
 
 #include <cuda.h>
@@ -148,24 +148,7 @@ __device__ __forceinline__ void cluster_sync() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Byte offset of element (row, col) inside a TMA box of 64-column (128-byte)
-// bf16 rows written with CU_TENSOR_MAP_SWIZZLE_128B: the 16-byte chunk index
-// is XORed with (row mod 8).  The box base must be 1024-byte aligned.
-__device__ __forceinline__ uint32_t sw128_offset(int row, int col) {
-    return static_cast<uint32_t>(row * 128 + ((((col >> 3) ^ row) & 7) << 4) + ((col & 7) << 1));
-}
-
 // ---------------------------------------------------------------- mma.sync
-
-__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
-}
-
-__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
-}
 
 // D (16x8 fp32) += A (16x16 bf16, row) * B (16x8 bf16, col)
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -192,19 +175,11 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-// exp2 on the FMA/ALU pipes, to share the load of the special-function unit.
-// x = n + f with n = round(x) (adding 1.5 * 2^23 leaves n in the low mantissa bits) and
-// f in [-1/2, 1/2]; 2^f by a degree-3 polynomial with minimax relative error 7.5e-5 on
+// exp2 on the FMA/ALU pipes (soft_exp2x2 below), to share the load of the special-function
+// unit.  x = n + f with n = round(x) (adding 1.5 * 2^23 leaves n in the low mantissa bits)
+// and f in [-1/2, 1/2]; 2^f by a degree-3 polynomial with minimax relative error 7.5e-5 on
 // that interval (coefficients fitted by csrc/fit_exp2_poly.py); 2^n is added to the
 // exponent field.  Inputs below -125 are clamped (the result is then ~2^-125, not 0).
-__device__ __forceinline__ float soft_exp2(float x) {
-    x = fmaxf(x, -125.f);
-    const float t = x + 12582912.f;
-    const float f = x - (t - 12582912.f);
-    const float p = fmaf(fmaf(fmaf(0.0551716685295105f, f, 0.2426111251115799f), f, 0.6932609677314758f), f,
-                         0.9999280571937561f);
-    return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
-}
 
 // ---------------------------------------------------------------- paired fp32 (sm_100 family)
 // Two fp32 lanes per instruction (fma/add/mul .f32x2), each lane rounded to nearest even
@@ -241,9 +216,8 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
-// soft_exp2 on two lanes at once: the same range reduction and polynomial, with the
-// additions and multiply-adds paired; 2^n enters the exponent field by an integer
-// shift-add (n << 23 plus the bits of p, modulo 2^32).
+// Two lanes at once: the additions and multiply-adds are paired; 2^n enters the exponent
+// field by an integer shift-add (n << 23 plus the bits of p, modulo 2^32).
 __device__ __forceinline__ float2 soft_exp2x2(float2 x) {
     x.x = fmaxf(x.x, -125.f);
     x.y = fmaxf(x.y, -125.f);
@@ -259,8 +233,5 @@ __device__ __forceinline__ float2 soft_exp2x2(float2 x) {
                        __uint_as_float((__float_as_uint(t.y) << 23) + __float_as_uint(p.y)));
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int threads) {
-    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
-}
 
 }  // namespace inkattn

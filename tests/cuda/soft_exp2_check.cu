@@ -1,5 +1,6 @@
-// Checks soft_exp2 (the polynomial exp2 of the prefill softmax) against CUDA's exp2f on
-// a dense grid of [-125, 8] plus special inputs; prints the maximum relative error.
+// Checks soft_exp2x2 (the polynomial exp2 of the attention softmax, two lanes at once)
+// against CUDA's exp2f on a dense grid of [-125, 8] plus special inputs; prints the
+// maximum relative error.
 #include <cstdio>
 #include <cmath>
 #include <vector>
@@ -8,8 +9,11 @@
 __global__ void k(const float *x, float *a, float *b, int n) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n) {
-        a[i] = inkattn::soft_exp2(x[i]);
+        // lane pairs (x[i], x[n - 1 - i]): both lanes of the paired instructions are checked
+        const float2 y = inkattn::soft_exp2x2(make_float2(x[i], x[n - 1 - i]));
+        a[i] = y.x;
         b[i] = exp2f(x[i]);
+        if (y.y != inkattn::soft_exp2x2(make_float2(x[n - 1 - i], x[i])).x) a[i] = NAN;
     }
 }
 
@@ -27,7 +31,9 @@ int main() {
     cudaMemcpy(ha.data(), a, n * 4, cudaMemcpyDeviceToHost);
     cudaMemcpy(hb.data(), b, n * 4, cudaMemcpyDeviceToHost);
     double worst = 0; float at = 0;
+    long lane_mismatch = 0;                  // the two lanes disagreed on the same input
     for (int i = 0; i < n; ++i) {
+        if (std::isnan(ha[i])) { ++lane_mismatch; continue; }
         const double r = std::fabs((double)ha[i] / (double)hb[i] - 1.0);
         if (r > worst) { worst = r; at = hx[i]; }
     }
@@ -36,6 +42,6 @@ int main() {
     cudaMemcpy(x, &ninf, 4, cudaMemcpyHostToDevice);
     k<<<1, 1>>>(x, a, b, 1);
     cudaMemcpy(&hres, a, 4, cudaMemcpyDeviceToHost);
-    printf("max_rel_err %.6e at %.6f neg_inf %.3e\n", worst, at, hres);
+    printf("max_rel_err %.6e at %.6f neg_inf %.3e lane_mismatch %ld\n", worst, at, hres, lane_mismatch);
     return 0;
 }

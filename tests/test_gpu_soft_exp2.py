@@ -1,6 +1,7 @@
-"""The polynomial exp2 used by the prefill softmax, against CUDA's exp2f: maximum
-relative error below 1e-4 over [-125, 8] (the fitted bound is 7.5e-5; exp2f itself is
-accurate to a couple of fp32 ulps), and a negligible value for -inf."""
+"""The polynomial exp2 of the attention softmax (two lanes per paired instruction),
+against CUDA's exp2f: maximum relative error below 1e-4 over [-125, 8] (the fitted bound
+is 7.5e-5; exp2f itself is accurate to a couple of fp32 ulps), both lanes identical, and a
+negligible value for -inf."""
 import os
 import subprocess
 
@@ -21,4 +22,5 @@ def test_soft_exp2_matches_exp2f(tmp_path):
     err = float(out[out.index("max_rel_err") + 1])
     neg_inf = float(out[out.index("neg_inf") + 1])
     assert err < 1e-4, out
+    assert int(out[out.index("lane_mismatch") + 1]) == 0, out
     assert 0.0 <= neg_inf < 1e-37
