@@ -231,18 +231,6 @@ bool make_q_group_map(CUtensorMap *map, const void *base, int n_tok, int hq, int
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_rel_map(CUtensorMap *map, const void *base, int hq, int rel_extent, int d_r) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)d_r, (cuuint64_t)rel_extent, (cuuint64_t)hq};
-    cuuint64_t strides[2] = {(cuuint64_t)d_r * 4, (cuuint64_t)rel_extent * d_r * 4};
-    cuuint32_t box[3] = {(cuuint32_t)d_r, 128, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace inkattn
 
 using namespace inkattn;
@@ -276,16 +264,14 @@ inkattn_status inkattn_prefill(const inkattn_attn_params *p, void *stream) {
     if (st != INKATTN_OK) return st;
     if ((st = check_device(nullptr)) != INKATTN_OK) return st;
     if (p->N_tok == 0) return INKATTN_OK;
-    CUtensorMap qmap, kmap, vmap, pmap;
+    CUtensorMap qmap, kmap, vmap;
     const long long rows = (long long)p->num_blocks * p->Hkv * kBlock;
     if (!make_q_map(&qmap, p->q, p->N_tok, p->Hq, kPrefillTcRows) ||
         !make_cache_map(&kmap, p->k_cache, rows) || !make_cache_map(&vmap, p->v_cache, rows))
         return INKATTN_ERR_CUDA;
     if (p->rel_extent == 0)   // no bias band: two query tiles per CTA
         return launch_status(launch_prefill_2q(*p, scalars(*p), qmap, kmap, vmap, static_cast<cudaStream_t>(stream)));
-    if (!make_rel_map(&pmap, p->P, p->Hq, p->rel_extent, p->d_r)) return INKATTN_ERR_CUDA;
-    return launch_status(launch_prefill_tc(*p, scalars(*p), qmap, kmap, vmap, pmap,
-                                           static_cast<cudaStream_t>(stream)));
+    return launch_status(launch_prefill_tc(*p, scalars(*p), qmap, kmap, vmap, static_cast<cudaStream_t>(stream)));
 }
 
 int inkattn_decode_num_splits(const inkattn_attn_params *p, int num_sms) {

@@ -36,14 +36,10 @@ cudaError_t launch_combine(const inkattn_attn_params &p, int num_splits, const f
 // tcgen05 prefill: 128 query rows per CTA, d_r = 32.
 constexpr int kPrefillTcRows = 128;
 cudaError_t launch_prefill_tc(const inkattn_attn_params &p, const AttnScalars &s, const CUtensorMap &qmap,
-                              const CUtensorMap &kmap, const CUtensorMap &vmap, const CUtensorMap &pmap,
-                              cudaStream_t stream);
+                              const CUtensorMap &kmap, const CUtensorMap &vmap, cudaStream_t stream);
 // prefill without relative bias: two query tiles per CTA
 cudaError_t launch_prefill_2q(const inkattn_attn_params &p, const AttnScalars &s, const CUtensorMap &qmap,
                               const CUtensorMap &kmap, const CUtensorMap &vmap, cudaStream_t stream);
-// TMA descriptor for P viewed as [Hq][rel_extent][d_r] fp32, box {d_r, 128, 1}, 128-byte swizzle
-// (128 distances of one head: the K-major B operand of the relative-row MMA).
-bool make_rel_map(CUtensorMap *map, const void *base, int hq, int rel_extent, int d_r);
 
 // TMA descriptor for a paged cache viewed as [num_blocks*Hkv*64 rows][128] bf16,
 // box 64 rows x 64 columns, 128-byte swizzle.  Returns false on failure.

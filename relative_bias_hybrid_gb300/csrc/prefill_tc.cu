@@ -9,14 +9,18 @@
 // sheared bias]: a warp-specialized attention kernel that applies the relative term as a
 // sheared bias band.
 //
-// One CTA per (128-query tile of one sequence, query head).  Roles:
-//   warp 0      producer: TMA loads of the Q tile and of 128-key K/V tiles (two 64-key
-//               cache blocks, two 64-column boxes each, 128-byte swizzle) into a 3-slot
-//               ring; the relative-projection windows (128 distances of P_h) for the band.
-//   warp 1      MMA issuer (one lane): S = Q K^T (operands in shared memory), O += P V
-//               (P read from TMEM), R = r P_h (tf32, both operands K-major) for the band.
-//   warps 2-9   softmax: two warpgroups; row i (TMEM lane i) is shared by one thread of
+// One CTA per (128-query tile of one sequence, query head), 16 warps in four warpgroups:
+//   warps 0-3   relative bias: the band's R chunks (below), issued by one lane of warp 0,
+//               and their move from TMEM into the bias rows.
+//   warps 4-11  softmax: two warpgroups; row i (TMEM lane i) is shared by one thread of
 //               each, which own its key columns [0, 64) and [64, 128).
+//   warp 12     producer: TMA loads of the Q tile and of 128-key K/V tiles (two 64-key
+//               cache blocks, two 64-column boxes each, 128-byte swizzle) into a 3-slot ring.
+//   warp 13     MMA issuer (one lane): S = Q K^T (operands in shared memory), O += P V
+//               (P read from TMEM).
+//   warps 14-15 idle (they complete the last warpgroup's register hand-back).
+// Registers are moved between warpgroups at the start (setmaxnreg): the softmax threads,
+// which keep 64 logits and their P live, get 176 each; the bias warps 96; TMA and MMA 64.
 // TMEM (512 columns): O [0,128) | S0 [128,256) | S1 [256,384) | R [384,512).  P (bf16)
 // overwrites the first 64 columns of its S buffer.  S is double-buffered so Q K^T of the
 // next tile runs while the softmax works on this one.
@@ -26,13 +30,16 @@
 // row a of tile n needs distances D_n + a - b for its 128 keys b: a window that shifts with
 // the row (the shear).  The windows of consecutive tiles abut, so the band is covered by
 // chunks C_n = [D_n + 1, D_n + 128] of 128 distances, one new chunk per tile (plus
-// C_{-1} = [D_0 - 127, D_0] before the first).  For each chunk the MMA warp computes
-// R[a][x] = r_a . P_h[:, D_n + 1 + x] (M=128, N=128, K=d_r) into TMEM.  Row a owns one
-// row of a 128-entry fp16 buffer indexed by key column; it resolves the shear as it moves
-// its values there: value x is the bias of column a - 1 - x in tile n when x < a (moved
-// before tile n reads its bias) and of column a + 127 - x in tile n + 1 when x >= a (moved
-// after).  Each tile then reads its bias row with sequential 16-byte loads.  Tiles farther
-// than rel_extent skip all of this.
+// C_{-1} = [D_0 - 127, D_0] before the first).  For each chunk the bias warps compute
+// R^T[x][a] = P_h[:, D_n + 1 + x] . r_a (M = 128 distances, N = 128 rows, K = d_r) into
+// TMEM; value x of row a is the bias of key column a - 1 - x of tile n when x < a and of
+// column a + 127 - x of tile n + 1 when x >= a.  The thread of TMEM lane x writes both into
+// 128-entry fp16 rows indexed by key column, one per tile, alternating between two
+// buffers: tile n's row is complete once C_n is moved, and C_{n+1} can be computed as soon
+// as C_n has left TMEM, so the chunks run ahead of the softmax, which reads its bias row
+// with sequential 16-byte loads.  Tiles farther than rel_extent skip all of this.
+// The bias MMA takes bf16 operands: r as given, and P_h (times 1/scale, so that R is in
+// the units of S) split into high and low bf16 parts, two products accumulated in fp32.
 //
 // The softmax runs in the log2 domain and keeps a stale row maximum unless the new one
 // exceeds it by more than 8 (P stays below 2^8); only then is O rescaled in TMEM.  Column
@@ -52,23 +59,26 @@ constexpr int kRows = 128;                 // query rows per CTA (MMA M)
 constexpr int kKeys = 128;                 // keys per tile (MMA N of Q K^T, K of P V)
 constexpr int kSlots = 3;                  // K/V ring slots
 constexpr int kSlotBytes = 32768;          // one K or V tile: [d half][128 keys][128 B]
-constexpr int kThreads = 320;            // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
+constexpr int kThreads = 512;            // warps 0-3 bias, 4-11 softmax, 12 TMA, 13 MMA, 14-15 idle
+constexpr int kWarpProducer = 12, kWarpMma = 13;
 constexpr int kStageStride = 136;          // halves per row of the bias buffer
-constexpr int kMaxDr = 32;                 // d_r (the relative features fill one 128-byte row)
-constexpr int kPwinBytes = 128 * 128;      // [128 distances][32 fp32] (K-major)
+constexpr int kMaxDr = 32;                 // d_r (the relative features fill one 64-byte bf16 row)
+constexpr int kWin64 = 128 * kMaxDr * 2;  // [128 rows][32 bf16], K-major 64-byte rows
 
 constexpr int kOffQ = 0;
 constexpr int kOffKV = 32768;
-constexpr int kOffPwin = kOffKV + kSlots * kSlotBytes;
-constexpr int kOffRfeat = kOffPwin + 2 * kPwinBytes;
-constexpr int kOffStage = kOffRfeat + 16384;
-constexpr int kOffXchg = kOffStage + kRows * kStageStride * 2;   // row maxima / sums of the two halves
+constexpr int kOffPwHi = kOffKV + kSlots * kSlotBytes;        // P window, bf16 high parts
+constexpr int kOffPwLo = kOffPwHi + kWin64;                     // P window, bf16 low parts
+constexpr int kOffRfeat = kOffPwLo + kWin64;                    // relative features (bf16)
+constexpr int kOffStage = kOffRfeat + kWin64;                   // two bias buffers
+constexpr int kStageBuf = kRows * kStageStride;                 // halves per bias buffer
+constexpr int kOffXchg = kOffStage + 2 * kStageBuf * 2;         // row maxima / sums of the two halves
 constexpr int kOffBar = kOffXchg + 3 * 2 * kRows * 4;
 
 enum Bar {
     B_Q = 0, B_KV_FULL = 1, B_KV_EMPTY = 4, B_S_FULL = 7, B_P_FULL = 9, B_PV_DONE = 11,
-    B_R_FULL = 13, B_R_EMPTY = 14, B_PW_FULL = 15, B_PW_EMPTY = 17, B_RFEAT = 19, B_DRAIN = 20,
-    B_PAIR = 21, B_COUNT = 25
+    B_R_FULL = 13, B_R_EMPTY = 14, B_PW_READY = 15, B_DRAIN = 16, B_PAIR = 17,
+    B_STAGE_FULL = 21, B_STAGE_EMPTY = 23, B_BDRAIN = 25, B_COUNT = 26
 };
 constexpr int kSmem = kOffBar + B_COUNT * 8 + 16;
 
@@ -81,8 +91,10 @@ struct TcArgs {
     long long kv_rows;      // rows of the cache tensor maps (OOB row = this)
 };
 
-__device__ __forceinline__ uint32_t sw128_chunk(int row, int chunk) {
-    return (uint32_t)(row * 128 + (((chunk ^ row) & 7) << 4));
+// byte offset of 16-byte chunk j of row r in a K-major tile of 64-byte rows with the 64-byte
+// swizzle (address bits 4-5 XOR bits 7-8)
+__device__ __forceinline__ uint32_t sw64_chunk(int r, int j) {
+    return (uint32_t)(r * 64 + (((j ^ (r >> 1)) & 3) << 4));
 }
 
 }  // namespace
@@ -90,8 +102,7 @@ __device__ __forceinline__ uint32_t sw128_chunk(int row, int chunk) {
 template <int kCluster>
 __global__ void __launch_bounds__(kThreads, 1)
 k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
-             const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-             const __grid_constant__ CUtensorMap pmap) {
+             const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
     extern __shared__ __align__(1024) unsigned char smem[];
     const inkattn_attn_params &p = A.p;
     const int h = blockIdx.x, b = blockIdx.z;
@@ -154,19 +165,20 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(B_S_FULL + s), 1);
             mbar_init(bar(B_P_FULL + s), 256);
-            mbar_init(bar(B_PW_FULL + s), 1);
-            mbar_init(bar(B_PW_EMPTY + s), 1);
+            mbar_init(bar(B_STAGE_FULL + s), 128);
+            mbar_init(bar(B_STAGE_EMPTY + s), 256);
             mbar_init(bar(B_PV_DONE + s), 1);
         }
         mbar_init(bar(B_R_FULL), 1);
-        mbar_init(bar(B_R_EMPTY), 256);
-        mbar_init(bar(B_RFEAT), 256);
+        mbar_init(bar(B_R_EMPTY), 128);
+        mbar_init(bar(B_PW_READY), 128);
         mbar_init(bar(B_DRAIN), 1);
+        mbar_init(bar(B_BDRAIN), 1);
         for (int q = 0; q < 4; ++q) mbar_init(bar(B_PAIR + q), 64);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == kWarpMma) {
         tc::tmem_alloc(smem_u32(tmem_slot), 512);
         tc::tmem_relinquish();
     }
@@ -180,7 +192,12 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
     const float c_qk = lam * A.scale * kLog2e;       // S (with the bias folded in) -> log2 logit
     const float inv_scale = 1.f / A.scale;           // bias in S units
 
-    if (warp == 0) {
+    // Registers: the kernel is launched with 128 a thread (64 K in all).  Each warpgroup sets
+    // its own budget first thing in its branch: the softmax threads keep 64 logits and their
+    // P live (176), the bias warps one 32-column TMEM load (104), TMA and MMA little (56).
+    if (warp >= kWarpProducer) {
+      tc::reg_dealloc<64>();
+      if (warp == kWarpProducer) {
         // ================================ producer ================================
         bool ok = true;
         const uint32_t q_dst = s_base + kOffQ;
@@ -188,27 +205,10 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             tma_prefetch_desc(&qmap);
             tma_prefetch_desc(&kmap);
             tma_prefetch_desc(&vmap);
-            if (n_band > 0) tma_prefetch_desc(&pmap);
             mbar_arrive_expect_tx(bar(B_Q), 2 * 16384);
             tma_load_3d(q_dst, &qmap, 0, h, start + row0, bar(B_Q));
             tma_load_3d(q_dst + 16384, &qmap, 64, h, start + row0, bar(B_Q));
         }
-        // relative-projection window of chunk rho-1 (rho = 0 is C_{-1}): P_h rows of the 128
-        // distances from D_{rho-1} + 1, one TMA box [128][d_r] fp32 that lands K-major with
-        // the 128-byte swizzle, as the tf32 MMA reads it; distances outside [0, rel_extent)
-        // are out of the tensor and arrive as zeros
-        auto load_pwin = [&](int rho) -> bool {
-            const int slot = rho & 1;
-            if (rho >= 2 && !wwait(bar(B_PW_EMPTY + slot), ((rho >> 1) - 1) & 1))
-                return false;
-            if (lane == 0) {
-                const int x0 = p_lo - kKeys * (t_hi - (rho - 1)) + 1;
-                mbar_arrive_expect_tx(bar(B_PW_FULL + slot), kPwinBytes);
-                tma_load_3d(s_base + kOffPwin + slot * kPwinBytes, &pmap, 0, x0, h, bar(B_PW_FULL + slot));
-            }
-            __syncwarp();
-            return true;
-        };
         int kv_loads = 0;                       // K/V tiles issued, in the MMA warp's order
         auto load_kv = [&](int n, int isv) -> bool {
             const int L = kv_loads++, slot = L % kSlots;
@@ -243,15 +243,12 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             __syncwarp();
             return true;
         };
-        // the MMA warp consumes K_0, [W_1], then per tile n >= 1: K_n, [W_{n+1}], V_{n-1},
-        // and finally V_{N-1} (W = relative-projection window); loading in that order lets
-        // K_{n+1} reuse the slot of V_{n-2} instead of waiting for V_{n-1} to be consumed
-        if (n_band > 0) ok = load_pwin(0);
-        if (ok) ok = load_kv(0, 0);
-        if (ok && 0 < n_band) ok = load_pwin(1);
+        // the MMA warp consumes K_0, then per tile n >= 1: K_n, V_{n-1}, and finally V_{N-1};
+        // loading in that order lets K_{n+1} reuse the slot of V_{n-2} instead of waiting for
+        // V_{n-1} to be consumed
+        ok = load_kv(0, 0);
         for (int n = 1; n < N && ok; ++n) {
             ok = load_kv(n, 0);
-            if (ok && n < n_band) ok = load_pwin(n + 1);
             if (ok) ok = load_kv(n - 1, 1);
         }
         if (ok) ok = load_kv(N - 1, 1);
@@ -261,11 +258,10 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             for (int L = max(0, kv_loads - kSlots); L < kv_loads; ++L)
                 mbar_wait(bar(B_KV_FULL + L % kSlots), (L / kSlots) & 1, p.dev_status, abort_flag);
         }
-    } else if (warp == 1) {
+      } else if (warp == kWarpMma) {
         // ================================ MMA issuer ================================
         const uint32_t id_qk = tc::idesc(128, 128, tc::kFmtBF16, 0, 0);
         const uint32_t id_pv = tc::idesc(128, 128, tc::kFmtBF16, 0, 1);
-        const uint32_t id_r = tc::idesc(128, 128, tc::kFmtTF32, 0, 0);
         // Base descriptors, built once; the per-k-step ones differ only in the start
         // address field (bits 0-13, 16-byte units), which never carries out of its 14 bits
         // since shared-memory addresses stay below 256 KB.
@@ -276,26 +272,8 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             dk[sl] = tc::sdesc_sw128(s_base + kOffKV + sl * kSlotBytes, 16, 1024);
             dv[sl] = tc::sdesc_sw128(s_base + kOffKV + sl * kSlotBytes, 16384, 1024);
         }
-        const uint64_t dr = tc::sdesc_sw128(s_base + kOffRfeat, 16, 1024);
-        const uint64_t dw0 = tc::sdesc_sw128(s_base + kOffPwin, 16, 1024);
         bool ok = wwait(bar(B_Q), 0);
-        if (ok && n_band > 0) ok = wwait(bar(B_RFEAT), 0);
 
-        auto issue_r = [&](int rho) -> bool {
-            if (rho >= 1 && !wwait(bar(B_R_EMPTY), (rho - 1) & 1)) return false;
-            const int slot = rho & 1;
-            if (!wwait(bar(B_PW_FULL + slot), (rho >> 1) & 1)) return false;
-            tc::fence_after();
-            if (lane == 0) {
-                const uint64_t dw = dw0 + (uint64_t)(slot * kPwinBytes >> 4);
-                for (int kk = 0; kk < d_r / 8; ++kk)
-                    tc::mma_tf32_ss(tmem + kTmemR, dr + (uint64_t)(kk * 2), dw + (uint64_t)(kk * 2), id_r, kk > 0);
-                tc::commit(bar(B_R_FULL));
-                tc::commit(bar(B_PW_EMPTY + slot));
-            }
-            __syncwarp();
-            return true;
-        };
         int kv_used = 0;                         // K/V tiles consumed, same order as loaded
         auto next_tile = [&](int &slot, bool &last) -> bool {
             const int L = kv_used++;
@@ -346,7 +324,6 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             return true;
         };
 
-        if (ok && n_band > 0) ok = issue_r(0);
         for (int n = 0; n < N && ok; ++n) {
             int slot;
             bool last;
@@ -365,22 +342,174 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                 release(slot, last);
             }
             __syncwarp();
-            if (n < n_band) ok = issue_r(n + 1);
-            if (ok && n >= 1) ok = issue_pv(n - 1);
+            if (n >= 1) ok = issue_pv(n - 1);
         }
         if (ok) ok = issue_pv(N - 1);
         // every MMA of this CTA has completed before TMEM is released
         if (lane == 0) tc::commit(bar(B_DRAIN));
         __syncwarp();
         (void)wwait(bar(B_DRAIN), 0);
+      }
+    } else if (warp < 4) {
+        // ============================== relative bias ==============================
+        tc::reg_dealloc<96>();
+        // R is computed transposed, R^T[x][a] = P_h[:, D + 1 + x] . r_a (M = 128 distances,
+        // N = 128 rows), so this thread (TMEM lane x) holds position x of the chunk for every
+        // row a, in column a.  Its value for row a goes to column a - 1 - x of tile n's bias
+        // row when x < a and to column a + 127 - x of tile n + 1's when x >= a: for a fixed
+        // thread both are one base address plus a per-row constant, so every value is one
+        // store with an immediate offset, and the 32 lanes of a store write 32 consecutive
+        // columns of one row.  Tiles alternate between two bias buffers, so a chunk is
+        // moved out of TMEM as soon as it is computed and the next one can follow: the chunks
+        // run a tile ahead of the softmax.
+        //
+        // The MMA takes bf16 operands: r exactly, and P_h split into a high and a low bf16
+        // part (P = hi + lo to 16 significant bits), two products accumulated in fp32.
+        const int w = warp;                                   // TMEM lane quarter
+        const int x = 32 * w + lane;
+        const uint32_t lane_off = (uint32_t)(w * 32) << 16;
+        bool ok = true;
+        if (n_band > 0) {
+            // row x's relative features (bf16 as given)
+            {
+                const int row = row0 + x;
+                uint4 u[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                              make_uint4(0, 0, 0, 0)};
+                if (row < q_len) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(p.r + ((size_t)(start + row) * p.Hq + h) * d_r);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) u[j] = __ldg(src + j);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4 *>(smem + kOffRfeat + sw64_chunk(x, j)) = u[j];
+            }
+            // row x of the P window of chunk rho - 1 (rho = 0 is C_{-1}): distance
+            // D_{rho-1} + 1 + x; distances outside [0, rel_extent) have no bias (zeros)
+            const float *Ph = p.P + (size_t)h * p.rel_extent * d_r;
+            auto load_p = [&](int rho, float4 (&v)[8]) {
+                const long long d = (long long)p_lo - (long long)kKeys * (t_hi - (rho - 1)) + 1 + x;
+                if (d >= 0 && d < p.rel_extent) {
+                    const float4 *src = reinterpret_cast<const float4 *>(Ph + (size_t)d * d_r);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) v[j] = __ldg(src + j);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            };
+            auto store_p = [&](const float4 (&v)[8]) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float f[8] = {v[2 * j].x * inv_scale, v[2 * j].y * inv_scale, v[2 * j].z * inv_scale,
+                                        v[2 * j].w * inv_scale, v[2 * j + 1].x * inv_scale, v[2 * j + 1].y * inv_scale,
+                                        v[2 * j + 1].z * inv_scale, v[2 * j + 1].w * inv_scale};
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        hi[e] = pack_bf16(f[2 * e], f[2 * e + 1]);
+                        lo[e] = pack_bf16(f[2 * e] - bf16_lo(hi[e]), f[2 * e + 1] - bf16_hi(hi[e]));
+                    }
+                    *reinterpret_cast<uint4 *>(smem + kOffPwHi + sw64_chunk(x, j)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4 *>(smem + kOffPwLo + sw64_chunk(x, j)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(bar(B_PW_READY));
+            };
+
+            const uint32_t id_r = tc::idesc(128, 128, tc::kFmtBF16, 0, 0);
+            const uint64_t dhi = tc::sdesc_sw64(s_base + kOffPwHi, 16, 512);
+            const uint64_t dlo = tc::sdesc_sw64(s_base + kOffPwLo, 16, 512);
+            const uint64_t dr = tc::sdesc_sw64(s_base + kOffRfeat, 16, 512);
+            // warp 0 issues chunk rho - 1 once its window is in place and every thread has
+            // moved the previous chunk out of TMEM; K = 32 in two steps of 16 (32 bytes)
+            auto issue = [&](int rho) -> bool {
+                if (warp != 0) return true;
+                if (rho >= 1 && !wwait(bar(B_R_EMPTY), (rho - 1) & 1)) return false;
+                if (!wwait(bar(B_PW_READY), rho & 1)) return false;
+                tc::fence_after();
+                if (lane == 0) {
+                    tc::mma_bf16_ss(tmem + kTmemR, dhi, dr, id_r, 0u);
+                    tc::mma_bf16_ss(tmem + kTmemR, dhi + 2, dr + 2, id_r, 1u);
+                    tc::mma_bf16_ss(tmem + kTmemR, dlo, dr, id_r, 1u);
+                    tc::mma_bf16_ss(tmem + kTmemR, dlo + 2, dr + 2, id_r, 1u);
+                    tc::commit(bar(B_R_FULL));
+                }
+                __syncwarp();
+                return true;
+            };
+            constexpr int kRowStep = kStageStride + 1;        // (row a, column a - 1 - x) -> next row
+            __half *const stage = reinterpret_cast<__half *>(smem + kOffStage);
+            // rows [32 j, 32 j + 32) of the chunk: the part for tile n (first) or for tile
+            // n + 1 (second), into bias buffer buf
+            auto drain_block = [&](int j, bool first, int buf) {
+                uint32_t r[32];
+                tc::ld32(tmem + kTmemR + lane_off + 32 * j, r);
+                tc::wait_ld();
+                __half *base = stage + buf * kStageBuf + (first ? -1 - x : 127 - x) + 32 * j * kRowStep;
+                if (j != w) {                                  // every lane's x is on one side
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const __half2 v = __floats2half2_rn(__uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+                        base[e * kRowStep] = __low2half(v);
+                        base[(e + 1) * kRowStep] = __high2half(v);
+                    }
+                } else {                                       // row 32 w + e vs x = 32 w + lane
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const __half2 v = __floats2half2_rn(__uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+                        if ((lane < e) == first) base[e * kRowStep] = __low2half(v);
+                        if ((lane < e + 1) == first) base[(e + 1) * kRowStep] = __high2half(v);
+                    }
+                }
+            };
+            float4 pv[8];
+            load_p(0, pv);
+            store_p(pv);                                       // window of C_{-1}
+            if (ok) ok = issue(0);
+            load_p(1, pv);                                     // window of C_0, in flight
+            if (ok) ok = wwait(bar(B_R_FULL), 0);
+            if (ok) {
+                tc::fence_after();
+                store_p(pv);                                   // the MMA has read window 0
+                for (int j = 0; j <= w; ++j) drain_block(j, false, 0);   // C_{-1}: tile 0, columns [a, 128)
+                tc::fence_before();
+                mbar_arrive(bar(B_R_EMPTY));
+            }
+            for (int n = 0; n < n_band && ok; ++n) {
+                const int rho = n + 1;                         // chunk C_n
+                const bool more = n + 1 < n_band;              // tile n + 1 is in the band
+                if (!(ok = issue(rho))) break;
+                if (more) load_p(rho + 1, pv);
+                if (!(ok = wwait(bar(B_R_FULL), rho & 1))) break;
+                tc::fence_after();
+                const int bn = n & 1;
+                for (int j = w; j < 4; ++j) drain_block(j, true, bn);    // tile n, columns [0, a)
+                mbar_arrive(bar(B_STAGE_FULL + bn));          // tile n's bias is complete
+                if (more) store_p(pv);                         // the MMA has read this window
+                if (more) {
+                    // tile n + 1 shares its buffer with tile n - 1, whose reads must be done
+                    if (n >= 1 && !(ok = wwait(bar(B_STAGE_EMPTY + (bn ^ 1)), ((n - 1) >> 1) & 1))) break;
+                    for (int j = 0; j <= w; ++j) drain_block(j, false, bn ^ 1);  // tile n + 1, columns [a, 128)
+                }
+                tc::fence_before();
+                mbar_arrive(bar(B_R_EMPTY));
+            }
+            // the issuing thread's MMAs (and their barrier arrivals) end before teardown
+            if (warp == 0) {
+                if (lane == 0) tc::commit(bar(B_BDRAIN));
+                __syncwarp();
+                (void)wwait(bar(B_BDRAIN), 0);
+            }
+        }
     } else {
         // ================================ softmax ================================
-        // Two warpgroups share the 128 rows: warps 2-5 (half 0) and 6-9 (half 1) read the
+        tc::reg_alloc<176>();
+        // Two warpgroups share the 128 rows: warps 4-7 (half 0) and 8-11 (half 1) read the
         // same TMEM lane quarters; thread (half w, row a) owns key columns [64 w, 64 w + 64)
         // of row a.  The two threads of a row exchange row maxima (and, at the end, row
         // sums) through shared memory with a 64-thread named barrier per lane quarter.
         const int quad = warp & 3;
-        const int hw = (warp - 2) >> 2;                       // column half
+        const int hw = (warp - 4) >> 2;                       // column half
         const int a = quad * 32 + lane;                       // query row = TMEM lane
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const int row = row0 + a;                             // row within the sequence
@@ -396,54 +525,7 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         };
         bool ok = true;
 
-        if (n_band > 0) {
-            // this row's relative features as fp32, K-major with the 128-byte swizzle; each
-            // half writes 4 of the 8 16-byte chunks
-            if (row < q_len) {
-                const inkattn_bf16 *src = p.r + ((size_t)(start + row) * p.Hq + h) * d_r;
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int cc = 2 * hw + c;                // 8-element group of the features
-                    float4 f0 = make_float4(0.f, 0.f, 0.f, 0.f), f1 = f0;
-                    if (cc * 8 < d_r) {
-                        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(src + cc * 8));
-                        f0 = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
-                        f1 = make_float4(bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w));
-                    }
-                    *reinterpret_cast<float4 *>(smem + kOffRfeat + sw128_chunk(a, 2 * cc)) = f0;
-                    *reinterpret_cast<float4 *>(smem + kOffRfeat + sw128_chunk(a, 2 * cc + 1)) = f1;
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<float4 *>(smem + kOffRfeat + sw128_chunk(a, 4 * hw + c)) =
-                        make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(bar(B_RFEAT));
-        }
-
-        // Move this thread's half (positions [cb, cb + 64)) of the chunk in TMEM R (times
-        // inv_scale) into the row's bias buffer, indexed by key column: value x of chunk C_n
-        // is the bias of key column a - 1 - x in tile n (x < a, first part) and of key
-        // column a + 127 - x in tile n + 1 (x >= a).
-        auto drain = [&](bool first_part) {
-            __half *base = stage + (first_part ? a - 1 : a + 127) - cb;
-            uint32_t r[32];
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                tc::ld32(tmem + kTmemR + lane_off + cb + c * 32, r);
-                tc::wait_ld();
-                const int lim = a - cb - 32 * c;              // e < lim  <=>  x < a
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    if ((e < lim) == first_part)
-                        base[-(32 * c + e)] = __float2half_rn(__uint_as_float(r[e]) * inv_scale);
-            }
-        };
-
         float m_run = -INFINITY, l_run = 0.f;
-        int r_round = 0;
         // P V of tile m signals PV_DONE[m & 1], phase m >> 1.  The MMA warp issues Q K^T of
         // tile m + 2 after P V of tile m, so once this thread has seen S of tile m + 2 the
         // phase before tile m's (tile m - 2) is complete: a parity wait is then unambiguous
@@ -461,21 +543,12 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                 tc::wait_ld();
             }
             if (n < n_band) {
-                if (n == 0) {
-                    if (!(ok = wwait(bar(B_R_FULL), r_round & 1))) break;
-                    tc::fence_after();
-                    drain(false);                                 // C_{-1}: positions >= a
-                    tc::fence_before();
-                    mbar_arrive(bar(B_R_EMPTY));
-                    ++r_round;
-                }
-                if (!(ok = wwait(bar(B_R_FULL), r_round & 1))) break;
-                tc::fence_after();
-                drain(true);                                      // C_n: positions < a
-                if (!(ok = pair_sync())) break;                   // both halves moved
+                const int bn = n & 1;
+                if (!(ok = wwait(bar(B_STAGE_FULL + bn), (n >> 1) & 1))) break;
+                const __half *bias_row = stage + bn * kStageBuf;
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) {
-                    const uint4 u = *reinterpret_cast<const uint4 *>(stage + cb + 8 * c8);
+                    const uint4 u = *reinterpret_cast<const uint4 *>(bias_row + cb + 8 * c8);
                     const __half2 *hp = reinterpret_cast<const __half2 *>(&u);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -485,11 +558,7 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                         s[8 * c8 + 2 * e + 1] = f.y;
                     }
                 }
-                if (!(ok = pair_sync())) break;                   // both halves read tile n
-                drain(false);                                     // C_n: positions >= a (tile n+1)
-                tc::fence_before();
-                mbar_arrive(bar(B_R_EMPTY));
-                ++r_round;
+                mbar_arrive(bar(B_STAGE_EMPTY + bn));
             }
             // mask and row maximum over this thread's 64 columns (unscaled; the scale is > 0)
             const int j0 = (t_hi - n) * kKeys;
@@ -613,7 +682,7 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
 
     tc::fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kWarpMma) {
         tc::fence_after();
         tc::tmem_dealloc(tmem, 512);
     }
@@ -622,8 +691,18 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
 }
 
 cudaError_t launch_prefill_tc(const inkattn_attn_params &p, const AttnScalars &s, const CUtensorMap &qmap,
-                              const CUtensorMap &kmap, const CUtensorMap &vmap, const CUtensorMap &pmap,
-                              cudaStream_t stream) {
+                              const CUtensorMap &kmap, const CUtensorMap &vmap, cudaStream_t stream) {
+    // the warpgroups' register budgets (64 + 96 + 2 x 176 per thread of a warpgroup) add
+    // up to the 64 K registers that 512 threads at 128 each are launched with
+    static int regs_ok = -1;
+    if (regs_ok < 0) {
+        cudaFuncAttributes fa1, fa2;
+        if (cudaFuncGetAttributes(&fa1, k_prefill_tc<1>) != cudaSuccess ||
+            cudaFuncGetAttributes(&fa2, k_prefill_tc<2>) != cudaSuccess)
+            return cudaErrorInvalidDeviceFunction;
+        regs_ok = (fa1.numRegs == 128 && fa2.numRegs == 128) ? 1 : 0;
+    }
+    if (!regs_ok) return cudaErrorInvalidConfiguration;
     TcArgs a;
     a.p = p;
     a.scale = s.scale;
@@ -635,7 +714,7 @@ cudaError_t launch_prefill_tc(const inkattn_attn_params &p, const AttnScalars &s
     if (!pair) {
         cudaError_t err = cudaFuncSetAttribute(k_prefill_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (err != cudaSuccess) return err;
-        k_prefill_tc<1><<<grid, kThreads, kSmem, stream>>>(a, qmap, kmap, vmap, pmap);
+        k_prefill_tc<1><<<grid, kThreads, kSmem, stream>>>(a, qmap, kmap, vmap);
         return cudaGetLastError();
     }
     cudaError_t err = cudaFuncSetAttribute(k_prefill_tc<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
@@ -652,7 +731,7 @@ cudaError_t launch_prefill_tc(const inkattn_attn_params &p, const AttnScalars &s
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_prefill_tc<2>, a, qmap, kmap, vmap, pmap);
+    return cudaLaunchKernelEx(&cfg, k_prefill_tc<2>, a, qmap, kmap, vmap);
 }
 
 }  // namespace inkattn
