@@ -59,14 +59,13 @@ __device__ __forceinline__ uint64_t sdesc_sw64(uint32_t addr, uint32_t lbo_bytes
 }
 
 // Instruction descriptor: D fp32 (bits 4-5 = 1), A/B element format (bits 7-9, 10-12:
-// 1 = bf16 for kind::f16, 2 = tf32 for kind::tf32), A/B major (bits 15, 16: 1 = MN-major),
+// 1 = bf16 for kind::f16), A/B major (bits 15, 16: 1 = MN-major),
 // N >> 3 (bits 17-22), M >> 4 (bits 24-28).
 __host__ __device__ constexpr uint32_t idesc(int M, int N, uint32_t ab_format, int a_mn, int b_mn) {
     return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((uint32_t)a_mn << 15) |
            ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 constexpr uint32_t kFmtBF16 = 1;
-constexpr uint32_t kFmtTF32 = 2;
 
 // ---------------------------------------------------------------- MMA + commit
 
@@ -81,12 +80,6 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d, uint32_t a_tmem, uint64_
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
                  "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
                  :: "r"(d), "r"(a_tmem), "l"(b), "r"(id), "r"(acc) : "memory");
-}
-// D[tmem] (+)= A[smem desc] * B[smem desc], kind::tf32 (fp32 operands read as tf32).
-__device__ __forceinline__ void mma_tf32_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
-                 :: "r"(d), "l"(a), "l"(b), "r"(id), "r"(acc) : "memory");
 }
 // Arrives once on the mbarrier when every tcgen05 operation issued so far by this
 // thread has completed.
