@@ -194,7 +194,8 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
 
     // Registers: the kernel is launched with 128 a thread (64 K in all).  Each warpgroup sets
     // its own budget first thing in its branch: the softmax threads keep 64 logits and their
-    // P live (176), the bias warps one 32-column TMEM load (104), TMA and MMA little (56).
+    // P live (176), the bias warps a 32-column TMEM load and a P row in flight (96), TMA and
+    // MMA little (64).
     if (warp >= kWarpProducer) {
       tc::reg_dealloc<64>();
       if (warp == kWarpProducer) {
@@ -694,15 +695,15 @@ cudaError_t launch_prefill_tc(const inkattn_attn_params &p, const AttnScalars &s
                               const CUtensorMap &kmap, const CUtensorMap &vmap, cudaStream_t stream) {
     // the warpgroups' register budgets (64 + 96 + 2 x 176 per thread of a warpgroup) add
     // up to the 64 K registers that 512 threads at 128 each are launched with
-    static int regs_ok = -1;
-    if (regs_ok < 0) {
+    // (checked once per process; the static's initialisation is thread-safe)
+    static const cudaError_t regs_check = [] {
         cudaFuncAttributes fa1, fa2;
         if (cudaFuncGetAttributes(&fa1, k_prefill_tc<1>) != cudaSuccess ||
             cudaFuncGetAttributes(&fa2, k_prefill_tc<2>) != cudaSuccess)
             return cudaErrorInvalidDeviceFunction;
-        regs_ok = (fa1.numRegs == 128 && fa2.numRegs == 128) ? 1 : 0;
-    }
-    if (!regs_ok) return cudaErrorInvalidConfiguration;
+        return (fa1.numRegs == 128 && fa2.numRegs == 128) ? cudaSuccess : cudaErrorInvalidConfiguration;
+    }();
+    if (regs_check != cudaSuccess) return regs_check;
     TcArgs a;
     a.p = p;
     a.scale = s.scale;
