@@ -29,11 +29,12 @@
 // i0 - j0 of tile n (i0 = the tile's first query position, j0 = the key tile's first key),
 // row a of tile n needs distances D_n + a - b for its 128 keys b: a window that shifts with
 // the row (the shear).  The windows of consecutive tiles abut, so the band is covered by
-// chunks C_n = [D_n + 1, D_n + 128] of 128 distances, one new chunk per tile (plus
-// C_{-1} = [D_0 - 127, D_0] before the first).  For each chunk the bias warps compute
-// R^T[x][a] = P_h[:, D_n + 1 + x] . r_a (M = 128 distances, N = 128 rows, K = d_r) into
-// TMEM; value x of row a is the bias of key column a - 1 - x of tile n when x < a and of
-// column a + 127 - x of tile n + 1 when x >= a.  The thread of TMEM lane x writes both into
+// chunks C_n = [D_n, D_n + 127] of 128 distances, one new chunk per tile (plus
+// C_{-1} = [D_0 - 128, D_0 - 1] before the first, which only reaches keys past the diagonal
+// and is skipped when D_0 = 0).  For each chunk the bias warps compute
+// R^T[x][a] = P_h[:, D_n + x] . r_a (M = 128 distances, N = 128 rows, K = d_r) into TMEM;
+// value x of row a is the bias of key column a - x of tile n when x <= a and of column
+// a + 128 - x of tile n + 1 when x > a.  The thread of TMEM lane x writes both into
 // 128-entry fp16 rows indexed by key column, one per tile, alternating between two
 // buffers: tile n's row is complete once C_n is moved, and C_{n+1} can be computed as soon
 // as C_n has left TMEM, so the chunks run ahead of the softmax, which reads its bias row
@@ -356,8 +357,8 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         tc::reg_dealloc<96>();
         // R is computed transposed, R^T[x][a] = P_h[:, D + 1 + x] . r_a (M = 128 distances,
         // N = 128 rows), so this thread (TMEM lane x) holds position x of the chunk for every
-        // row a, in column a.  Its value for row a goes to column a - 1 - x of tile n's bias
-        // row when x < a and to column a + 127 - x of tile n + 1's when x >= a: for a fixed
+        // row a, in column a.  Its value for row a goes to column a - x of tile n's bias row
+        // when x <= a and to column a + 128 - x of tile n + 1's when x > a: for a fixed
         // thread both are one base address plus a per-row constant, so every value is one
         // store with an immediate offset, and the 32 lanes of a store write 32 consecutive
         // columns of one row.  Tiles alternate between two bias buffers, so a chunk is
@@ -385,10 +386,10 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                 for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4 *>(smem + kOffRfeat + sw64_chunk(x, j)) = u[j];
             }
             // row x of the P window of chunk rho - 1 (rho = 0 is C_{-1}): distance
-            // D_{rho-1} + 1 + x; distances outside [0, rel_extent) have no bias (zeros)
+            // D_{rho-1} + x; distances outside [0, rel_extent) have no bias (zeros)
             const float *Ph = p.P + (size_t)h * p.rel_extent * d_r;
             auto load_p = [&](int rho, float4 (&v)[8]) {
-                const long long d = (long long)p_lo - (long long)kKeys * (t_hi - (rho - 1)) + 1 + x;
+                const long long d = (long long)p_lo - (long long)kKeys * (t_hi - (rho - 1)) + x;
                 if (d >= 0 && d < p.rel_extent) {
                     const float4 *src = reinterpret_cast<const float4 *>(Ph + (size_t)d * d_r);
 #pragma unroll
@@ -421,12 +422,12 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             const uint64_t dhi = tc::sdesc_sw64(s_base + kOffPwHi, 16, 512);
             const uint64_t dlo = tc::sdesc_sw64(s_base + kOffPwLo, 16, 512);
             const uint64_t dr = tc::sdesc_sw64(s_base + kOffRfeat, 16, 512);
-            // warp 0 issues chunk rho - 1 once its window is in place and every thread has
+            // warp 0 issues the ci-th chunk once its window is in place and every thread has
             // moved the previous chunk out of TMEM; K = 32 in two steps of 16 (32 bytes)
-            auto issue = [&](int rho) -> bool {
+            auto issue = [&](int ci) -> bool {
                 if (warp != 0) return true;
-                if (rho >= 1 && !wwait(bar(B_R_EMPTY), (rho - 1) & 1)) return false;
-                if (!wwait(bar(B_PW_READY), rho & 1)) return false;
+                if (ci >= 1 && !wwait(bar(B_R_EMPTY), (ci - 1) & 1)) return false;
+                if (!wwait(bar(B_PW_READY), ci & 1)) return false;
                 tc::fence_after();
                 if (lane == 0) {
                     tc::mma_bf16_ss(tmem + kTmemR, dhi, dr, id_r, 0u);
@@ -438,7 +439,7 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                 __syncwarp();
                 return true;
             };
-            constexpr int kRowStep = kStageStride + 1;        // (row a, column a - 1 - x) -> next row
+            constexpr int kRowStep = kStageStride + 1;        // (row a, column a - x) -> next row
             __half *const stage = reinterpret_cast<__half *>(smem + kOffStage);
             // rows [32 j, 32 j + 32) of the chunk: the part for tile n (first) or for tile
             // n + 1 (second), into bias buffer buf
@@ -446,7 +447,7 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                 uint32_t r[32];
                 tc::ld32(tmem + kTmemR + lane_off + 32 * j, r);
                 tc::wait_ld();
-                __half *base = stage + buf * kStageBuf + (first ? -1 - x : 127 - x) + 32 * j * kRowStep;
+                __half *base = stage + buf * kStageBuf + (first ? -x : 128 - x) + 32 * j * kRowStep;
                 if (j != w) {                                  // every lane's x is on one side
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
@@ -458,39 +459,50 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
                         const __half2 v = __floats2half2_rn(__uint_as_float(r[e]), __uint_as_float(r[e + 1]));
-                        if ((lane < e) == first) base[e * kRowStep] = __low2half(v);
-                        if ((lane < e + 1) == first) base[(e + 1) * kRowStep] = __high2half(v);
+                        if ((lane <= e) == first) base[e * kRowStep] = __low2half(v);
+                        if ((lane <= e + 1) == first) base[(e + 1) * kRowStep] = __high2half(v);
                     }
                 }
             };
+            // C_{-1} gives tile 0 its columns past the diagonal (a + 1 .. 127), at distances
+            // D_0 - 128 + x; when the tile sits on the diagonal (D_0 = 0) they are all future
+            // keys, masked, and C_{-1} is skipped
+            const bool need_prev = p_lo - kKeys * t_hi != 0;
+            int ci = 0;                                        // chunks issued
             float4 pv[8];
-            load_p(0, pv);
-            store_p(pv);                                       // window of C_{-1}
-            if (ok) ok = issue(0);
-            load_p(1, pv);                                     // window of C_0, in flight
-            if (ok) ok = wwait(bar(B_R_FULL), 0);
-            if (ok) {
-                tc::fence_after();
-                store_p(pv);                                   // the MMA has read window 0
-                for (int j = 0; j <= w; ++j) drain_block(j, false, 0);   // C_{-1}: tile 0, columns [a, 128)
-                tc::fence_before();
-                mbar_arrive(bar(B_R_EMPTY));
+            if (need_prev) {
+                load_p(0, pv);
+                store_p(pv);                                   // window of C_{-1}
+                if (ok) ok = issue(0);
+                load_p(1, pv);                                 // window of C_0, in flight
+                if (ok) ok = wwait(bar(B_R_FULL), 0);
+                if (ok) {
+                    tc::fence_after();
+                    store_p(pv);                               // the MMA has read window 0
+                    for (int j = 0; j <= w; ++j) drain_block(j, false, 0);   // C_{-1}: tile 0, columns (a, 128)
+                    tc::fence_before();
+                    mbar_arrive(bar(B_R_EMPTY));
+                }
+                ci = 1;
+            } else {
+                load_p(1, pv);
+                store_p(pv);                                   // window of C_0
             }
-            for (int n = 0; n < n_band && ok; ++n) {
+            for (int n = 0; n < n_band && ok; ++n, ++ci) {
                 const int rho = n + 1;                         // chunk C_n
                 const bool more = n + 1 < n_band;              // tile n + 1 is in the band
-                if (!(ok = issue(rho))) break;
+                if (!(ok = issue(ci))) break;
                 if (more) load_p(rho + 1, pv);
-                if (!(ok = wwait(bar(B_R_FULL), rho & 1))) break;
+                if (!(ok = wwait(bar(B_R_FULL), ci & 1))) break;
                 tc::fence_after();
                 const int bn = n & 1;
-                for (int j = w; j < 4; ++j) drain_block(j, true, bn);    // tile n, columns [0, a)
+                for (int j = w; j < 4; ++j) drain_block(j, true, bn);    // tile n, columns [0, a]
                 mbar_arrive(bar(B_STAGE_FULL + bn));          // tile n's bias is complete
                 if (more) store_p(pv);                         // the MMA has read this window
                 if (more) {
                     // tile n + 1 shares its buffer with tile n - 1, whose reads must be done
                     if (n >= 1 && !(ok = wwait(bar(B_STAGE_EMPTY + (bn ^ 1)), ((n - 1) >> 1) & 1))) break;
-                    for (int j = 0; j <= w; ++j) drain_block(j, false, bn ^ 1);  // tile n + 1, columns [a, 128)
+                    for (int j = 0; j <= w; ++j) drain_block(j, false, bn ^ 1);  // tile n + 1, columns (a, 128)
                 }
                 tc::fence_before();
                 mbar_arrive(bar(B_R_EMPTY));
