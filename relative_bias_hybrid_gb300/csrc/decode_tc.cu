@@ -14,7 +14,8 @@
 // it.  The Q tile arrives as one 3D TMA box {64 dims, g heads, ql tokens} per half of the
 // head dimension, which lands exactly in that row order.  Roles, as in the prefill kernel:
 //   warp 0      producer: TMA loads of 128-key K/V tiles (two 64-key cache blocks) of this
-//               split's key range into a 3-slot ring, in the order the MMAs consume them.
+//               split's key range into a 4-slot ring, in the order the MMAs consume them
+//               (every tile comes from HBM: the ring's depth sets the bytes in flight).
 //   warp 1      MMA issuer (one lane): S = Q K^T into a double-buffered S in TMEM, O += P V
 //               with P (bf16) read from TMEM.
 //   warps 2-9   softmax: two warpgroups; row a (TMEM lane a) is shared by one thread of each,
@@ -24,7 +25,8 @@
 // Relative bias: only tiles within rel_extent of the queries carry it (the last ones of the
 // sequence).  For such a tile the softmax warps first build, per query head, the table
 // R[t][x] = r_t . P_h[:, dlo + x] over the tile's 128 + ql distances with mma.sync (bf16
-// operands, fp32 accumulation), then each thread adds its row's 64 entries.
+// operands, fp32 accumulation, stored as fp16 in S units), then each thread adds its row's
+// 64 entries.
 //
 // The softmax runs in the log2 domain with the lazy rescale of the prefill kernel (O is
 // rescaled only when the running maximum grows by more than 8).  The epilogue writes O / l
@@ -39,7 +41,7 @@ namespace {
 
 constexpr int kRows = 128;                 // MMA M: (token, query head) rows, padded
 constexpr int kKeys = 128;                 // keys per tile (two cache blocks)
-constexpr int kSlots = 3;                  // K/V ring slots
+constexpr int kSlots = 4;                  // K/V ring slots
 constexpr int kSlotBytes = 32768;          // one K or V tile: [d half][128 keys][128 B]
 constexpr int kThreads = 320;              // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
 constexpr int kTabW = 144;                 // distances per table row: 128 keys + up to 16 tokens
@@ -47,13 +49,23 @@ constexpr int kTabRows = kDecodeMaxRows;   // g * ql <= 128
 
 constexpr int kOffQ = 0;
 constexpr int kOffKV = 32768;
-constexpr int kOffTab = kOffKV + kSlots * kSlotBytes;              // fp32 [g][ql][kTabW]
-constexpr int kOffXchg = kOffTab + kTabRows * kTabW * 4;           // row maxima / sums
+constexpr int kOffTab = kOffKV + kSlots * kSlotBytes;              // fp16 [g][ql][kTabW]
+constexpr int kOffXchg = kOffTab + kTabRows * kTabW * 2;           // row maxima / sums
 constexpr int kOffBar = kOffXchg + 3 * 2 * kRows * 4;
 
+// mbarrier indices, laid out from the slot count
 enum Bar {
-    B_Q = 0, B_KV_FULL = 1, B_KV_EMPTY = 4, B_S_FULL = 7, B_P_FULL = 9, B_PV_DONE = 11,
-    B_TAB_FULL = 13, B_TAB_FREE = 14, B_DRAIN = 15, B_PAIR = 16, B_COUNT = 20
+    B_Q = 0,
+    B_KV_FULL = 1,
+    B_KV_EMPTY = B_KV_FULL + kSlots,
+    B_S_FULL = B_KV_EMPTY + kSlots,
+    B_P_FULL = B_S_FULL + 2,
+    B_PV_DONE = B_P_FULL + 2,
+    B_TAB_FULL = B_PV_DONE + 2,
+    B_TAB_FREE = B_TAB_FULL + 1,
+    B_DRAIN = B_TAB_FREE + 1,
+    B_PAIR = B_DRAIN + 1,
+    B_COUNT = B_PAIR + 4
 };
 constexpr int kSmem = kOffBar + B_COUNT * 8 + 16;
 static_assert(kSmem <= 232448, "shared memory budget");
@@ -304,7 +316,7 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
         const int hh = a - t * g;
         const int i_pos = pos0 + t;
         const int cb = 64 * hw;
-        float *tab = reinterpret_cast<float *>(smem + kOffTab);
+        __half *tab = reinterpret_cast<__half *>(smem + kOffTab);
         float *xchg = reinterpret_cast<float *>(smem + kOffXchg);
         int pair_phase = 0;
         auto pair_sync = [&]() -> bool {
@@ -327,45 +339,55 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
                 if (band_round > 0 && !(ok = wwait(bar(B_TAB_FREE), (band_round - 1) & 1))) break;
                 for (int hq = sw; hq < g; hq += 8) {
                     const int h = hk * g + hq;
-                    const float *Ph = p.P + (size_t)h * p.rel_extent * p.d_r;
-                    const inkattn_bf16 *rh = p.r + ((size_t)start * p.Hq + h) * p.d_r;
-                    uint32_t rf[4][4];
+                    const float *Ph = p.P + (size_t)h * p.rel_extent * 32;
+                    const inkattn_bf16 *rh = p.r + ((size_t)start * p.Hq + h) * 32;
+                    // d_r = 32 (checked on the host): two k steps of 16
+                    uint32_t rf[2][4];
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
+                    for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int tt = gq + ((e & 1) << 3);
                             const int col = kk * 16 + 2 * tq + ((e >> 1) << 3);
-                            rf[kk][e] = (kk * 16 < p.d_r && tt < q_len)
-                                ? __ldg(reinterpret_cast<const uint32_t *>(rh + (size_t)tt * p.Hq * p.d_r + col))
+                            rf[kk][e] = tt < q_len
+                                ? __ldg(reinterpret_cast<const uint32_t *>(rh + (size_t)tt * 32 * p.Hq + col))
                                 : 0u;
                         }
-                    for (int nt = 0; nt < kTabW / 8; ++nt) {
-                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                        const int dl = dlo + nt * 8 + gq;
-                        const bool dv = dl >= 0 && dl < p.rel_extent;
+                    // the table in two rounds of nine groups of 8 distances: a round's P loads
+                    // are all issued before its first MMA, so the table waits for two L2 round
+                    // trips (the first also covers r above), not one per group; while K/V
+                    // streams saturate the memory system a round trip costs thousands of cycles
+                    constexpr int kGrp = 9;
+                    static_assert((kTabW / 8) % kGrp == 0, "whole rounds");
+                    for (int nt0 = 0; nt0 < kTabW / 8; nt0 += kGrp) {
+                        uint32_t pb[kGrp][2][2];
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            if (kk * 16 >= p.d_r) continue;
-                            const int e0 = kk * 16 + 2 * tq;
-                            float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-                            if (dv) {
-                                const float2 lo = __ldg(reinterpret_cast<const float2 *>(Ph + (size_t)dl * p.d_r + e0));
-                                const float2 hi = __ldg(reinterpret_cast<const float2 *>(Ph + (size_t)dl * p.d_r + e0 + 8));
-                                p0 = lo.x; p1 = lo.y; p2 = hi.x; p3 = hi.y;
+                        for (int u = 0; u < kGrp; ++u) {
+                            const int dl = dlo + (nt0 + u) * 8 + gq;
+                            const bool dv = dl >= 0 && dl < p.rel_extent;
+#pragma unroll
+                            for (int kk = 0; kk < 2; ++kk) {
+                                pb[u][kk][0] = pb[u][kk][1] = 0u;
+                                if (!dv) continue;
+                                const int e0 = kk * 16 + 2 * tq;
+                                const float2 lo = __ldg(reinterpret_cast<const float2 *>(Ph + (size_t)dl * 32 + e0));
+                                const float2 hi = __ldg(reinterpret_cast<const float2 *>(Ph + (size_t)dl * 32 + e0 + 8));
+                                pb[u][kk][0] = pack_bf16(lo.x, lo.y);
+                                pb[u][kk][1] = pack_bf16(hi.x, hi.y);
                             }
-                            mma_16816(acc, rf[kk], pack_bf16(p0, p1), pack_bf16(p2, p3));
                         }
-                        const int c = nt * 8 + 2 * tq;
-                        if (gq < q_len) {
-                            float *dst = tab + ((size_t)hq * A.ql + gq) * kTabW + c;
-                            dst[0] = acc[0] * inv_scale;
-                            dst[1] = acc[1] * inv_scale;
-                        }
-                        if (gq + 8 < q_len) {
-                            float *dst = tab + ((size_t)hq * A.ql + gq + 8) * kTabW + c;
-                            dst[0] = acc[2] * inv_scale;
-                            dst[1] = acc[3] * inv_scale;
+#pragma unroll
+                        for (int u = 0; u < kGrp; ++u) {
+                            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                            for (int kk = 0; kk < 2; ++kk) mma_16816(acc, rf[kk], pb[u][kk][0], pb[u][kk][1]);
+                            const int c = (nt0 + u) * 8 + 2 * tq;
+                            if (gq < q_len)
+                                *reinterpret_cast<__half2 *>(tab + ((size_t)hq * A.ql + gq) * kTabW + c) =
+                                    __floats2half2_rn(acc[0] * inv_scale, acc[1] * inv_scale);
+                            if (gq + 8 < q_len)
+                                *reinterpret_cast<__half2 *>(tab + ((size_t)hq * A.ql + gq + 8) * kTabW + c) =
+                                    __floats2half2_rn(acc[2] * inv_scale, acc[3] * inv_scale);
                         }
                     }
                 }
@@ -386,9 +408,9 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
             if (band) {
                 if (valid_row) {
                     // column b of the tile is at distance i - j = dlo + (t + 127 - b)
-                    const float *trow = tab + ((size_t)hh * A.ql + t) * kTabW + t + (kKeys - 1) - cb;
+                    const __half *trow = tab + ((size_t)hh * A.ql + t) * kTabW + t + (kKeys - 1) - cb;
 #pragma unroll
-                    for (int bb = 0; bb < 64; ++bb) s[bb] += trow[-bb];
+                    for (int bb = 0; bb < 64; ++bb) s[bb] += __half2float(trow[-bb]);
                 }
                 mbar_arrive(bar(B_TAB_FREE));
                 ++band_round;
