@@ -230,13 +230,13 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
         // ================================ MMA issuer ================================
         const uint32_t id_qk = tc::idesc(128, 128, tc::kFmtBF16, 0, 0);
         const uint32_t id_pv = tc::idesc(128, 128, tc::kFmtBF16, 0, 1);
+        // the whole warp runs this loop with the same values in every lane (the MMAs and
+        // commits are warp-collective); per-slot descriptors differ only in the start address
+        // field, which stays below its 14 bits (shared memory < 256 KB)
         const uint64_t dq = tc::sdesc_sw128(s_base + kOffQ, 16, 1024);
-        uint64_t dk[kSlots], dv[kSlots];
-#pragma unroll
-        for (int sl = 0; sl < kSlots; ++sl) {
-            dk[sl] = tc::sdesc_sw128(s_base + kOffKV + sl * kSlotBytes, 16, 1024);
-            dv[sl] = tc::sdesc_sw128(s_base + kOffKV + sl * kSlotBytes, 16384, 1024);
-        }
+        const uint64_t dk0 = tc::sdesc_sw128(s_base + kOffKV, 16, 1024);
+        const uint64_t dv0 = tc::sdesc_sw128(s_base + kOffKV, 16384, 1024);
+        auto slot_off = [](int slot) { return (uint64_t)(slot * (kSlotBytes >> 4)); };
         bool ok = wwait(bar(B_Q), 0);
         int kv_used = 0;
         auto next_tile = [&](int &slot, bool &last) -> bool {
@@ -267,9 +267,9 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
                 __syncwarp();
             }
             tc::fence_after();
-            if (lane == 0) {
+            {
                 const uint32_t ps = tmem + kTmemS0 + (uint32_t)(m & 1) * 128;
-                const uint64_t db = dv[slot];
+                const uint64_t db = dv0 + slot_off(slot);
                 tc::mma_bf16_ts(tmem + kTmemO, ps, db, id_pv, m > 0 ? 1u : 0u);
 #pragma unroll
                 for (int kk = 1; kk < 8; ++kk)
@@ -286,9 +286,9 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
             ok = next_tile(slot, last);
             if (!ok) break;
             tc::fence_after();
-            if (lane == 0) {
+            {
                 const uint32_t sd = tmem + kTmemS0 + (uint32_t)(n & 1) * 128;
-                const uint64_t db = dk[slot];
+                const uint64_t db = dk0 + slot_off(slot);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
@@ -301,7 +301,7 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
             if (n >= 1) ok = issue_pv(n - 1);
         }
         if (ok) ok = issue_pv(N - 1);
-        if (lane == 0) tc::commit(bar(B_DRAIN));
+        tc::commit(bar(B_DRAIN));
         __syncwarp();
         (void)wwait(bar(B_DRAIN), 0);
     } else {

@@ -189,15 +189,13 @@ k_prefill_2q(const Tc2Args A, const __grid_constant__ CUtensorMap qmap,
         // ================================ MMA issuer ================================
         const uint32_t id_qk = tc::idesc(128, 128, tc::kFmtBF16, 0, 0);
         const uint32_t id_pv = tc::idesc(128, 128, tc::kFmtBF16, 0, 1);
-        uint64_t dq[2];
-        dq[0] = tc::sdesc_sw128(s_base + kOffQ, 16, 1024);
-        dq[1] = tc::sdesc_sw128(s_base + kOffQ + 32768, 16, 1024);
-        uint64_t dk[kSlots], dv[kSlots];
-#pragma unroll
-        for (int sl = 0; sl < kSlots; ++sl) {
-            dk[sl] = tc::sdesc_sw128(s_base + kOffKV + sl * kSlotBytes, 16, 1024);
-            dv[sl] = tc::sdesc_sw128(s_base + kOffKV + sl * kSlotBytes, 16384, 1024);
-        }
+        // the whole warp runs this loop with the same values in every lane (the MMAs and
+        // commits are warp-collective); per-tile and per-slot descriptors differ only in the
+        // start address field, which stays below its 14 bits (shared memory < 256 KB)
+        const uint64_t dq0 = tc::sdesc_sw128(s_base + kOffQ, 16, 1024);
+        const uint64_t dk0 = tc::sdesc_sw128(s_base + kOffKV, 16, 1024);
+        const uint64_t dv0 = tc::sdesc_sw128(s_base + kOffKV, 16384, 1024);
+        auto slot_off = [](int slot) { return (uint64_t)(slot * (kSlotBytes >> 4)); };
         bool ok = wwait(bar(B_Q), 0);
         int kv_used = 0;
         auto acquire = [&](int &slot, bool &last) -> bool {
@@ -207,15 +205,16 @@ k_prefill_2q(const Tc2Args A, const __grid_constant__ CUtensorMap qmap,
             return wwait(bar(B_KV_FULL + slot), (L / kSlots) & 1);
         };
         auto release = [&](int slot, bool last) {
-            if (lane == 0 && !last) tc::commit(bar(B_KV_EMPTY + slot));
+            if (!last) tc::commit(bar(B_KV_EMPTY + slot));
         };
         auto qk = [&](int x, int slot) {
-            if (lane == 0) {
-                const uint64_t db = dk[slot];
+            {
+                const uint64_t db = dk0 + slot_off(slot);
+                const uint64_t da = dq0 + (uint64_t)(x * (32768 >> 4));
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                    tc::mma_bf16_ss(tmem + kTmemS + x * 128, dq[x] + off, db + off, id_qk, kk > 0 ? 1u : 0u);
+                    tc::mma_bf16_ss(tmem + kTmemS + x * 128, da + off, db + off, id_qk, kk > 0 ? 1u : 0u);
                 }
                 tc::commit(bar(B_S_FULL + x));
             }
@@ -225,9 +224,9 @@ k_prefill_2q(const Tc2Args A, const __grid_constant__ CUtensorMap qmap,
         auto pv = [&](int x, int slot) -> bool {
             if (!wwait(bar(B_P_FULL + x), kp[x] & 1)) return false;
             tc::fence_after();
-            if (lane == 0) {
+            {
                 const uint32_t ps = tmem + kTmemS + x * 128;
-                const uint64_t db = dv[slot];
+                const uint64_t db = dv0 + slot_off(slot);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     tc::mma_bf16_ts(tmem + kTmemO + x * 128, ps + kk * 8, db + (uint64_t)(kk * 128), id_pv,
@@ -287,7 +286,7 @@ k_prefill_2q(const Tc2Args A, const __grid_constant__ CUtensorMap qmap,
                 release(kslot, klast);
             }
         }
-        if (lane == 0) tc::commit(bar(B_DRAIN));
+        tc::commit(bar(B_DRAIN));
         __syncwarp();
         (void)wwait(bar(B_DRAIN), 0);
     } else {

@@ -264,16 +264,14 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         // ================================ MMA issuer ================================
         const uint32_t id_qk = tc::idesc(128, 128, tc::kFmtBF16, 0, 0);
         const uint32_t id_pv = tc::idesc(128, 128, tc::kFmtBF16, 0, 1);
-        // Base descriptors, built once; the per-k-step ones differ only in the start
-        // address field (bits 0-13, 16-byte units), which never carries out of its 14 bits
-        // since shared-memory addresses stay below 256 KB.
+        // Base descriptors, built once; the per-slot and per-k-step ones differ only in the
+        // start address field (bits 0-13, 16-byte units), which never carries out of its 14
+        // bits since shared-memory addresses stay below 256 KB.  The whole warp runs this
+        // loop with the same values in every lane (the MMAs and commits are warp-collective).
         const uint64_t dq = tc::sdesc_sw128(s_base + kOffQ, 16, 1024);
-        uint64_t dk[kSlots], dv[kSlots];
-#pragma unroll
-        for (int sl = 0; sl < kSlots; ++sl) {
-            dk[sl] = tc::sdesc_sw128(s_base + kOffKV + sl * kSlotBytes, 16, 1024);
-            dv[sl] = tc::sdesc_sw128(s_base + kOffKV + sl * kSlotBytes, 16384, 1024);
-        }
+        const uint64_t dk0 = tc::sdesc_sw128(s_base + kOffKV, 16, 1024);
+        const uint64_t dv0 = tc::sdesc_sw128(s_base + kOffKV, 16384, 1024);
+        auto slot_off = [](int slot) { return (uint64_t)(slot * (kSlotBytes >> 4)); };
         bool ok = wwait(bar(B_Q), 0);
 
         int kv_used = 0;                         // K/V tiles consumed, same order as loaded
@@ -283,8 +281,8 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             last = L + kSlots >= 2 * N;          // no later load reuses the slot
             return wwait(bar(B_KV_FULL + slot), (L / kSlots) & 1);
         };
-        // lane 0: the slot may be refilled once the MMAs issued so far have read it; a slot
-        // with no later load is not released, so no arrival reaches a peer that has finished
+        // the slot may be refilled once the MMAs issued so far have read it; a slot with no
+        // later load is not released, so no arrival reaches a peer that has finished
         auto release = [&](int slot, bool last) {
             if (last) return;
             if constexpr (kCluster > 1) tc::commit_mc(bar(B_KV_EMPTY + slot), kPeers);
@@ -312,9 +310,9 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                 __syncwarp();
             }
             tc::fence_after();
-            if (lane == 0) {
+            {
                 const uint32_t ps = tmem + kTmemS0 + (uint32_t)(m & 1) * 128;
-                const uint64_t db = dv[slot];
+                const uint64_t db = dv0 + slot_off(slot);
                 tc::mma_bf16_ts(tmem + kTmemO, ps, db, id_pv, m > 0 ? 1u : 0u);
 #pragma unroll
                 for (int kk = 1; kk < 8; ++kk)
@@ -332,9 +330,9 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             ok = next_tile(slot, last);
             if (!ok) break;
             tc::fence_after();
-            if (lane == 0) {
+            {
                 const uint32_t sd = tmem + kTmemS0 + (uint32_t)(n & 1) * 128;
-                const uint64_t db = dk[slot];
+                const uint64_t db = dk0 + slot_off(slot);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
@@ -348,7 +346,7 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         }
         if (ok) ok = issue_pv(N - 1);
         // every MMA of this CTA has completed before TMEM is released
-        if (lane == 0) tc::commit(bar(B_DRAIN));
+        tc::commit(bar(B_DRAIN));
         __syncwarp();
         (void)wwait(bar(B_DRAIN), 0);
       }
@@ -429,13 +427,11 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                 if (ci >= 1 && !wwait(bar(B_R_EMPTY), (ci - 1) & 1)) return false;
                 if (!wwait(bar(B_PW_READY), ci & 1)) return false;
                 tc::fence_after();
-                if (lane == 0) {
-                    tc::mma_bf16_ss(tmem + kTmemR, dhi, dr, id_r, 0u);
-                    tc::mma_bf16_ss(tmem + kTmemR, dhi + 2, dr + 2, id_r, 1u);
-                    tc::mma_bf16_ss(tmem + kTmemR, dlo, dr, id_r, 1u);
-                    tc::mma_bf16_ss(tmem + kTmemR, dlo + 2, dr + 2, id_r, 1u);
-                    tc::commit(bar(B_R_FULL));
-                }
+                tc::mma_bf16_ss(tmem + kTmemR, dhi, dr, id_r, 0u);
+                tc::mma_bf16_ss(tmem + kTmemR, dhi + 2, dr + 2, id_r, 1u);
+                tc::mma_bf16_ss(tmem + kTmemR, dlo, dr, id_r, 1u);
+                tc::mma_bf16_ss(tmem + kTmemR, dlo + 2, dr + 2, id_r, 1u);
+                tc::commit(bar(B_R_FULL));
                 __syncwarp();
                 return true;
             };
@@ -509,7 +505,7 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             }
             // the issuing thread's MMAs (and their barrier arrivals) end before teardown
             if (warp == 0) {
-                if (lane == 0) tc::commit(bar(B_BDRAIN));
+                tc::commit(bar(B_BDRAIN));
                 __syncwarp();
                 (void)wwait(bar(B_BDRAIN), 0);
             }

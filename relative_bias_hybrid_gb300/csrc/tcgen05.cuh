@@ -68,30 +68,40 @@ __host__ __device__ constexpr uint32_t idesc(int M, int N, uint32_t ab_format, i
 constexpr uint32_t kFmtBF16 = 1;
 
 // ---------------------------------------------------------------- MMA + commit
+// Warp-collective: all 32 lanes of a converged warp make the call with the same operands,
+// and one lane, elected inside the instruction sequence, issues.  A lone thread issuing
+// from a divergent branch (if (lane == 0)) spends several instructions of its own on every
+// MMA; while the other warps of its SM sub-partition keep the issue port busy (softmax
+// arithmetic), those delay each MMA past the 64 cycles the tensor pipe needs for an
+// M = 128, N = 128, K = 16 step, and the step takes ~130 cycles instead.  With the operands
+// warp-uniform the issue keeps up with the pipe.  The commits elect the same lane, so they
+// track the MMAs that lane issued.
 
 // D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (bf16 inputs), cta_group::1.
 __device__ __forceinline__ void mma_bf16_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+    asm volatile("{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
                  :: "r"(d), "l"(a), "l"(b), "r"(id), "r"(acc) : "memory");
 }
 // D[tmem] (+)= A[tmem] * B[smem desc], kind::f16.
 __device__ __forceinline__ void mma_bf16_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t acc) {
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+    asm volatile("{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
                  :: "r"(d), "r"(a_tmem), "l"(b), "r"(id), "r"(acc) : "memory");
 }
-// Arrives once on the mbarrier when every tcgen05 operation issued so far by this
-// thread has completed.
+// Arrives once on the mbarrier when every tcgen05 operation issued so far by the elected
+// lane has completed.
 __device__ __forceinline__ void commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
                  :: "r"(bar) : "memory");
 }
 
 // As commit, arriving on the mbarrier at the same shared-memory offset in every CTA of
 // the cluster named in cta_mask.
 __device__ __forceinline__ void commit_mc(uint32_t bar, uint16_t cta_mask) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}"
                  :: "r"(bar), "h"(cta_mask) : "memory");
 }
 
