@@ -189,6 +189,16 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
         int kv_loads = 0;
         auto load_kv = [&](int n, int isv) -> bool {
             const int L = kv_loads++, slot = L % kSlots;
+            // the tile's block-table entries are read before the wait for the slot, so that
+            // their round trip to memory overlaps it instead of delaying the copy
+            int blk[2];                                      // -2: past this split's range
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int lb = my_lo + 2 * n + half;         // logical cache block
+                blk[half] = lb >= my_hi ? -2
+                          : lb < p.max_blocks_per_seq ? __ldg(p.block_table + (size_t)b * p.max_blocks_per_seq + lb)
+                          : -1;
+            }
             if (L >= kSlots && !wwait(bar(B_KV_EMPTY + slot), ((L / kSlots) - 1) & 1))
                 return false;
             if (lane == 0) {
@@ -198,12 +208,9 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
                 const void *map = isv ? static_cast<const void *>(&vmap) : static_cast<const void *>(&kmap);
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
-                    const int lb = my_lo + 2 * n + half;       // logical cache block
                     long long row = A.kv_rows;                   // past the tensor: TMA fills zeros
-                    if (lb < my_hi) {
-                        const int blk = lb < p.max_blocks_per_seq
-                            ? p.block_table[(size_t)b * p.max_blocks_per_seq + lb] : -1;
-                        if (blk >= 0 && blk < p.num_blocks) row = ((long long)blk * p.Hkv + hk) * kBlock;
+                    if (blk[half] != -2) {
+                        if (blk[half] >= 0 && blk[half] < p.num_blocks) row = ((long long)blk[half] * p.Hkv + hk) * kBlock;
                         else set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
                     }
                     tma_load_2d(dst + half * 8192, map, 0, (int)row, fb);

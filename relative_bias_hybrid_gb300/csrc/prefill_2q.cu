@@ -151,22 +151,29 @@ k_prefill_2q(const Tc2Args A, const __grid_constant__ CUtensorMap qmap,
         int kv_loads = 0;
         auto load_kv = [&](int n, int isv) -> bool {
             const int L = kv_loads++, slot = L % kSlots;
+            const int t = t_top - n;
+            // the tile's block-table entries are read before the wait for the slot, so that
+            // their round trip to memory overlaps it instead of delaying the copy
+            int blk[2];                                      // -2: past the sequence end
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int lb = 2 * t + half;                 // logical cache block
+                blk[half] = (long long)lb * kBlock >= T ? -2
+                          : lb < p.max_blocks_per_seq ? __ldg(p.block_table + (size_t)b * p.max_blocks_per_seq + lb)
+                          : -1;
+            }
             if (L >= kSlots && !wwait(bar(B_KV_EMPTY + slot), ((L / kSlots) - 1) & 1))
                 return false;
             if (lane == 0) {
-                const int t = t_top - n;
                 const uint32_t dst = s_base + kOffKV + slot * kSlotBytes;
                 const uint32_t fb = bar(B_KV_FULL + slot);
                 mbar_arrive_expect_tx(fb, kSlotBytes);
                 const void *map = isv ? static_cast<const void *>(&vmap) : static_cast<const void *>(&kmap);
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
-                    const int lb = 2 * t + half;
                     long long row = A.kv_rows;
-                    if ((long long)lb * kBlock < T) {
-                        const int blk = lb < p.max_blocks_per_seq
-                            ? p.block_table[(size_t)b * p.max_blocks_per_seq + lb] : -1;
-                        if (blk >= 0 && blk < p.num_blocks) row = ((long long)blk * p.Hkv + hk) * kBlock;
+                    if (blk[half] != -2) {
+                        if (blk[half] >= 0 && blk[half] < p.num_blocks) row = ((long long)blk[half] * p.Hkv + hk) * kBlock;
                         else set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
                     }
                     tma_load_2d(dst + half * 8192, map, 0, (int)row, fb);

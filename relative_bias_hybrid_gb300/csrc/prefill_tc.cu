@@ -10,15 +10,19 @@
 // sheared bias band.
 //
 // One CTA per (128-query tile of one sequence, query head), 16 warps in four warpgroups:
-//   warps 0-3   relative bias: the band's R chunks (below), issued by one lane of warp 0,
-//               and their move from TMEM into the bias rows.
-//   warps 4-11  softmax: two warpgroups; row i (TMEM lane i) is shared by one thread of
-//               each, which own its key columns [0, 64) and [64, 128).
-//   warp 12     producer: TMA loads of the Q tile and of 128-key K/V tiles (two 64-key
+//   warp 0      MMA issuer (the whole warp, one elected lane issuing): S = Q K^T (operands
+//               in shared memory), O += P V (P read from TMEM).
+//   warp 1      producer: TMA loads of the Q tile and of 128-key K/V tiles (two 64-key
 //               cache blocks, two 64-column boxes each, 128-byte swizzle) into a 3-slot ring.
-//   warp 13     MMA issuer (one lane): S = Q K^T (operands in shared memory), O += P V
-//               (P read from TMEM).
-//   warps 14-15 idle (they complete the last warpgroup's register hand-back).
+//   warps 2-3   idle (they complete the first warpgroup's register hand-back).
+//   warps 4-7   relative bias: the band's R chunks (below), issued by warp 4, and their move
+//               from TMEM into the bias rows.
+//   warps 8-15  softmax: two warpgroups; row i (TMEM lane i) is shared by one thread of
+//               each, which own its key columns [0, 64) and [64, 128).
+// The MMA and TMA warps have the lowest warp numbers: among warps ready to issue, the
+// scheduler favours those, and every instruction on the MMA warp's path (barrier checks,
+// commits, loop) is on the critical path of the tile pipeline, while the softmax warps
+// beside it on each SM sub-partition always have independent work.
 // Registers are moved between warpgroups at the start (setmaxnreg): the softmax threads,
 // which keep 64 logits and their P live, get 176 each; the bias warps 96; TMA and MMA 64.
 // TMEM (512 columns): O [0,128) | S0 [128,256) | S1 [256,384) | R [384,512).  P (bf16)
@@ -60,8 +64,8 @@ constexpr int kRows = 128;                 // query rows per CTA (MMA M)
 constexpr int kKeys = 128;                 // keys per tile (MMA N of Q K^T, K of P V)
 constexpr int kSlots = 3;                  // K/V ring slots
 constexpr int kSlotBytes = 32768;          // one K or V tile: [d half][128 keys][128 B]
-constexpr int kThreads = 512;            // warps 0-3 bias, 4-11 softmax, 12 TMA, 13 MMA, 14-15 idle
-constexpr int kWarpProducer = 12, kWarpMma = 13;
+constexpr int kThreads = 512;            // warp 0 MMA, 1 TMA, 2-3 idle, 4-7 bias, 8-15 softmax
+constexpr int kWarpMma = 0, kWarpProducer = 1, kWarpBias = 4, kWarpSoftmax = 8;
 constexpr int kStageStride = 136;          // halves per row of the bias buffer
 constexpr int kMaxDr = 32;                 // d_r (the relative features fill one 64-byte bf16 row)
 constexpr int kWin64 = 128 * kMaxDr * 2;  // [128 rows][32 bf16], K-major 64-byte rows
@@ -197,7 +201,7 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
     // its own budget first thing in its branch: the softmax threads keep 64 logits and their
     // P live (176), the bias warps a 32-column TMEM load and a P row in flight (96), TMA and
     // MMA little (64).
-    if (warp >= kWarpProducer) {
+    if (warp < kWarpBias) {
       tc::reg_dealloc<64>();
       if (warp == kWarpProducer) {
         // ================================ producer ================================
@@ -214,23 +218,31 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         int kv_loads = 0;                       // K/V tiles issued, in the MMA warp's order
         auto load_kv = [&](int n, int isv) -> bool {
             const int L = kv_loads++, slot = L % kSlots;
+            const int t = t_hi - n;
+            // the tile's block-table entries are read before the wait for the slot, so that
+            // their round trip to memory overlaps it instead of delaying the copy
+            constexpr int kHalves = 3 - kCluster;
+            int blk[kHalves];                                // -2: past the sequence end
+#pragma unroll
+            for (int hh = 0; hh < kHalves; ++hh) {
+                const int lb = 2 * t + (kCluster > 1 ? (int)crank : hh);   // logical cache block
+                blk[hh] = (long long)lb * kBlock >= T ? -2
+                        : lb < p.max_blocks_per_seq ? __ldg(p.block_table + (size_t)b * p.max_blocks_per_seq + lb)
+                        : -1;
+            }
             if (L >= kSlots && !wwait(bar(B_KV_EMPTY + slot), ((L / kSlots) - 1) & 1))
                 return false;
             if (lane == 0) {
-                const int t = t_hi - n;
                 const uint32_t dst = s_base + kOffKV + slot * kSlotBytes;
                 const uint32_t fb = bar(B_KV_FULL + slot);
                 mbar_arrive_expect_tx(fb, kSlotBytes);       // both halves land in every CTA
                 const void *map = isv ? static_cast<const void *>(&vmap) : static_cast<const void *>(&kmap);
 #pragma unroll
-                for (int hh = 0; hh < 3 - kCluster; ++hh) {
+                for (int hh = 0; hh < kHalves; ++hh) {
                     const int half = kCluster > 1 ? (int)crank : hh;
-                    const int lb = 2 * t + half;                 // logical cache block
                     long long row = A.kv_rows;                   // past the tensor: TMA fills zeros
-                    if ((long long)lb * kBlock < T) {
-                        const int blk = lb < p.max_blocks_per_seq
-                            ? p.block_table[(size_t)b * p.max_blocks_per_seq + lb] : -1;
-                        if (blk >= 0 && blk < p.num_blocks) row = ((long long)blk * p.Hkv + hk) * kBlock;
+                    if (blk[hh] != -2) {
+                        if (blk[hh] >= 0 && blk[hh] < p.num_blocks) row = ((long long)blk[hh] * p.Hkv + hk) * kBlock;
                         else set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
                     }
                     if constexpr (kCluster > 1) {
@@ -350,7 +362,7 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         __syncwarp();
         (void)wwait(bar(B_DRAIN), 0);
       }
-    } else if (warp < 4) {
+    } else if (warp < kWarpSoftmax) {
         // ============================== relative bias ==============================
         tc::reg_dealloc<96>();
         // R is computed transposed, R^T[x][a] = P_h[:, D + 1 + x] . r_a (M = 128 distances,
@@ -365,7 +377,7 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         //
         // The MMA takes bf16 operands: r exactly, and P_h split into a high and a low bf16
         // part (P = hi + lo to 16 significant bits), two products accumulated in fp32.
-        const int w = warp;                                   // TMEM lane quarter
+        const int w = warp - kWarpBias;                       // TMEM lane quarter
         const int x = 32 * w + lane;
         const uint32_t lane_off = (uint32_t)(w * 32) << 16;
         bool ok = true;
@@ -420,10 +432,10 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             const uint64_t dhi = tc::sdesc_sw64(s_base + kOffPwHi, 16, 512);
             const uint64_t dlo = tc::sdesc_sw64(s_base + kOffPwLo, 16, 512);
             const uint64_t dr = tc::sdesc_sw64(s_base + kOffRfeat, 16, 512);
-            // warp 0 issues the ci-th chunk once its window is in place and every thread has
-            // moved the previous chunk out of TMEM; K = 32 in two steps of 16 (32 bytes)
+            // the first bias warp issues the ci-th chunk once its window is in place and every
+            // thread has moved the previous chunk out of TMEM; K = 32 in two steps of 16 (32 B)
             auto issue = [&](int ci) -> bool {
-                if (warp != 0) return true;
+                if (w != 0) return true;
                 if (ci >= 1 && !wwait(bar(B_R_EMPTY), (ci - 1) & 1)) return false;
                 if (!wwait(bar(B_PW_READY), ci & 1)) return false;
                 tc::fence_after();
@@ -504,7 +516,7 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                 mbar_arrive(bar(B_R_EMPTY));
             }
             // the issuing thread's MMAs (and their barrier arrivals) end before teardown
-            if (warp == 0) {
+            if (w == 0) {
                 tc::commit(bar(B_BDRAIN));
                 __syncwarp();
                 (void)wwait(bar(B_BDRAIN), 0);
@@ -518,7 +530,7 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         // of row a.  The two threads of a row exchange row maxima (and, at the end, row
         // sums) through shared memory with a 64-thread named barrier per lane quarter.
         const int quad = warp & 3;
-        const int hw = (warp - 4) >> 2;                       // column half
+        const int hw = (warp - kWarpSoftmax) >> 2;            // column half
         const int a = quad * 32 + lane;                       // query row = TMEM lane
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const int row = row0 + a;                             // row within the sequence
