@@ -175,12 +175,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-// exp2 on the FMA/ALU pipes (soft_exp2x2 below), to share the load of the special-function
-// unit.  x = n + f with n = round(x) (adding 1.5 * 2^23 leaves n in the low mantissa bits)
-// and f in [-1/2, 1/2]; 2^f by a degree-3 polynomial with minimax relative error 7.5e-5 on
-// that interval (coefficients fitted by csrc/fit_exp2_poly.py); 2^n is added to the
-// exponent field.  Inputs below -125 are clamped (the result is then ~2^-125, not 0).
-
 // ---------------------------------------------------------------- paired fp32 (sm_100 family)
 // Two fp32 lanes per instruction (fma/add/mul .f32x2), each lane rounded to nearest even
 // exactly like its scalar form.
@@ -216,22 +210,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
-// Two lanes at once: the additions and multiply-adds are paired; 2^n enters the exponent
-// field by an integer shift-add (n << 23 plus the bits of p, modulo 2^32).
-__device__ __forceinline__ float2 soft_exp2x2(float2 x) {
-    x.x = fmaxf(x.x, -125.f);
-    x.y = fmaxf(x.y, -125.f);
-    const float2 magic = make_float2(12582912.f, 12582912.f);
-    const float2 t = fadd2(x, magic);
-    const float2 r = fadd2(t, make_float2(-12582912.f, -12582912.f));
-    const float2 f = ffma2(r, make_float2(-1.f, -1.f), x);
-    float2 p = ffma2(make_float2(0.0551716685295105f, 0.0551716685295105f), f,
-                     make_float2(0.2426111251115799f, 0.2426111251115799f));
-    p = ffma2(p, f, make_float2(0.6932609677314758f, 0.6932609677314758f));
-    p = ffma2(p, f, make_float2(0.9999280571937561f, 0.9999280571937561f));
-    return make_float2(__uint_as_float((__float_as_uint(t.x) << 23) + __float_as_uint(p.x)),
-                       __uint_as_float((__float_as_uint(t.y) << 23) + __float_as_uint(p.y)));
-}
 
 
 }  // namespace inkattn

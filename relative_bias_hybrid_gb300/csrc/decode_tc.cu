@@ -481,9 +481,7 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
                 const float2 x = ffma2(make_float2(s[2 * e], s[2 * e + 1]), cq, nref);
-                const int k8 = e & 7;
-                const float2 y = (k8 == 1 || k8 == 4 || k8 == 6)
-                    ? soft_exp2x2(x) : make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                const float2 y = make_float2(fast_exp2(x.x), fast_exp2(x.y));
                 l4[e & 3] = fadd2(l4[e & 3], y);
                 pk[e] = pack_bf16(y.x, y.y);
             }

@@ -19,8 +19,8 @@
 // one in the tensor pipe, so the overwrite is ordered.
 //
 // The softmax runs in the log2 domain with a lazy rescale (O is rescaled only when the row
-// maximum grows by more than 8); column pairs use paired fp32 instructions, and three pairs
-// in eight take the polynomial exp2 on the FMA pipe.
+// maximum grows by more than 8); column pairs use paired fp32 instructions, and every exp2
+// goes through the special-function unit.
 #include "common.cuh"
 #include "internal.h"
 #include "tcgen05.cuh"
@@ -396,9 +396,7 @@ k_prefill_2q(const Tc2Args A, const __grid_constant__ CUtensorMap qmap,
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const float2 xv = ffma2(make_float2(sc[2 * e], sc[2 * e + 1]), cq, nref);
-                    const int k8 = (8 * c + e) & 7;
-                    const float2 y = (k8 == 1 || k8 == 4 || k8 == 6)
-                        ? soft_exp2x2(xv) : make_float2(fast_exp2(xv.x), fast_exp2(xv.y));
+                    const float2 y = make_float2(fast_exp2(xv.x), fast_exp2(xv.y));
                     l4[e & 3] = fadd2(l4[e & 3], y);
                     pk[e] = pack_bf16(y.x, y.y);
                 }

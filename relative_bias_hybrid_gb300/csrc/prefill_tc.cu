@@ -48,10 +48,10 @@
 //
 // The softmax runs in the log2 domain and keeps a stale row maximum unless the new one
 // exceeds it by more than 8 (P stays below 2^8); only then is O rescaled in TMEM.  Column
-// pairs go through paired fp32 instructions (fma/add .f32x2); three pairs in eight take a
-// polynomial exp2 on the FMA pipe and the rest the special-function unit: 16 exp2 per clock
-// per SM would alone take about as long as the MMAs of a tile, while the polynomial costs
-// issue slots the softmax warps share.
+// pairs go through paired fp32 instructions (fma/add .f32x2) and every exp2 through the
+// special-function unit: its 16 a clock per SM leave it below the tile period, while each
+// extra instruction of the softmax warps takes an issue slot from the MMA warp beside them.
+// (A polynomial exp2 on the FMA pipe for three pairs in eight was 5-6% slower.)
 #include "common.cuh"
 #include "internal.h"
 #include "tcgen05.cuh"
@@ -642,12 +642,9 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             uint32_t pk[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-                // column pairs, logits to log2 units relative to the running maximum; three
-                // pairs in eight take the polynomial exp2, the rest the special-function unit
+                // column pairs, logits to log2 units relative to the running maximum
                 const float2 x = ffma2(make_float2(s[2 * e], s[2 * e + 1]), cq, nref);
-                const int k8 = e & 7;
-                const float2 y = (k8 == 1 || k8 == 4 || k8 == 6)
-                    ? soft_exp2x2(x) : make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                const float2 y = make_float2(fast_exp2(x.x), fast_exp2(x.y));
                 l4[e & 3] = fadd2(l4[e & 3], y);
                 pk[e] = pack_bf16(y.x, y.y);
             }
