@@ -286,13 +286,24 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         auto slot_off = [](int slot) { return (uint64_t)(slot * (kSlotBytes >> 4)); };
         bool ok = wwait(bar(B_Q), 0);
 
-        int kv_used = 0;                         // K/V tiles consumed, same order as loaded
+        // K/V tiles consumed, in load order: slot and phase kept as counters (this warp's
+        // instructions are on the critical path of every tile)
+        int c_slot = 0, c_L = 0;
+        uint32_t c_par = 0;
+        const int first_last = 2 * N - kSlots;   // loads from here on are not reused
         auto next_tile = [&](int &slot, bool &last) -> bool {
-            const int L = kv_used++;
-            slot = L % kSlots;
-            last = L + kSlots >= 2 * N;          // no later load reuses the slot
-            return wwait(bar(B_KV_FULL + slot), (L / kSlots) & 1);
+            slot = c_slot;
+            const uint32_t par = c_par;
+            last = c_L++ >= first_last;
+            if (++c_slot == kSlots) {
+                c_slot = 0;
+                c_par ^= 1u;
+            }
+            return wwait(bar(B_KV_FULL + slot), par);
         };
+        // only the nearest key tile can hold keys at or past the sequence end inside a
+        // loaded cache block (when T is not a multiple of the block size)
+        const bool zero_tail = (T % kBlock) != 0 && t_hi == (T - 1) / kKeys;
         // the slot may be refilled once the MMAs issued so far have read it; a slot with no
         // later load is not released, so no arrival reaches a peer that has finished
         auto release = [&](int slot, bool last) {
@@ -307,10 +318,10 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             if (!next_tile(slot, last)) return false;
             // keys at or past the sequence end inside a loaded block: zero their V rows so
             // that P = 0 there contributes exact zeros whatever the cache slots hold
-            const int j0 = (t_hi - m) * kKeys;
-            const int nvalid = min(kKeys, T - j0);
-            const int nload = min(kKeys, (int)(((long long)((T + kBlock - 1) / kBlock)) * kBlock - j0));
-            if (nvalid < nload) {
+            if (m == 0 && zero_tail) {
+                const int j0 = t_hi * kKeys;
+                const int nvalid = T - j0;
+                const int nload = min(kKeys, (int)(((long long)((T + kBlock - 1) / kBlock)) * kBlock - j0));
                 unsigned char *vp = smem + kOffKV + slot * kSlotBytes;
                 const int rows = nload - nvalid;
                 for (int idx = lane; idx < rows * 16; idx += 32) {
@@ -322,16 +333,9 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                 __syncwarp();
             }
             tc::fence_after();
-            {
-                const uint32_t ps = tmem + kTmemS0 + (uint32_t)(m & 1) * 128;
-                const uint64_t db = dv0 + slot_off(slot);
-                tc::mma_bf16_ts(tmem + kTmemO, ps, db, id_pv, m > 0 ? 1u : 0u);
-#pragma unroll
-                for (int kk = 1; kk < 8; ++kk)
-                    tc::mma_bf16_ts(tmem + kTmemO, ps + kk * 8, db + (uint64_t)(kk * 128), id_pv, 1u);
-                tc::commit(bar(B_PV_DONE + (m & 1)));
-                release(slot, last);
-            }
+            tc::mma_bf16_ts_k128_commit(tmem + kTmemO, tmem + kTmemS0 + (uint32_t)(m & 1) * 128,
+                                        dv0 + slot_off(slot), id_pv, m > 0 ? 1u : 0u, bar(B_PV_DONE + (m & 1)));
+            release(slot, last);
             __syncwarp();
             return true;
         };
@@ -342,17 +346,9 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             ok = next_tile(slot, last);
             if (!ok) break;
             tc::fence_after();
-            {
-                const uint32_t sd = tmem + kTmemS0 + (uint32_t)(n & 1) * 128;
-                const uint64_t db = dk0 + slot_off(slot);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                    tc::mma_bf16_ss(sd, dq + off, db + off, id_qk, kk > 0 ? 1u : 0u);
-                }
-                tc::commit(bar(B_S_FULL + (n & 1)));
-                release(slot, last);
-            }
+            tc::mma_bf16_ss_k128_commit(tmem + kTmemS0 + (uint32_t)(n & 1) * 128, dq, dk0 + slot_off(slot), id_qk,
+                                        0u, bar(B_S_FULL + (n & 1)));
+            release(slot, last);
             __syncwarp();
             if (n >= 1) ok = issue_pv(n - 1);
         }
