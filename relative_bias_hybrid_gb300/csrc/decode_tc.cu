@@ -274,16 +274,9 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
                 __syncwarp();
             }
             tc::fence_after();
-            {
-                const uint32_t ps = tmem + kTmemS0 + (uint32_t)(m & 1) * 128;
-                const uint64_t db = dv0 + slot_off(slot);
-                tc::mma_bf16_ts(tmem + kTmemO, ps, db, id_pv, m > 0 ? 1u : 0u);
-#pragma unroll
-                for (int kk = 1; kk < 8; ++kk)
-                    tc::mma_bf16_ts(tmem + kTmemO, ps + kk * 8, db + (uint64_t)(kk * 128), id_pv, 1u);
-                tc::commit(bar(B_PV_DONE + (m & 1)));
-                if (!last) tc::commit(bar(B_KV_EMPTY + slot));
-            }
+            tc::mma_bf16_ts_k128_commit(tmem + kTmemO, tmem + kTmemS0 + (uint32_t)(m & 1) * 128,
+                                        dv0 + slot_off(slot), id_pv, m > 0 ? 1u : 0u, bar(B_PV_DONE + (m & 1)));
+            if (!last) tc::commit(bar(B_KV_EMPTY + slot));
             __syncwarp();
             return true;
         };
@@ -293,17 +286,9 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
             ok = next_tile(slot, last);
             if (!ok) break;
             tc::fence_after();
-            {
-                const uint32_t sd = tmem + kTmemS0 + (uint32_t)(n & 1) * 128;
-                const uint64_t db = dk0 + slot_off(slot);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                    tc::mma_bf16_ss(sd, dq + off, db + off, id_qk, kk > 0 ? 1u : 0u);
-                }
-                tc::commit(bar(B_S_FULL + (n & 1)));
-                if (!last) tc::commit(bar(B_KV_EMPTY + slot));
-            }
+            tc::mma_bf16_ss_k128_commit(tmem + kTmemS0 + (uint32_t)(n & 1) * 128, dq, dk0 + slot_off(slot), id_qk,
+                                        0u, bar(B_S_FULL + (n & 1)));
+            if (!last) tc::commit(bar(B_KV_EMPTY + slot));
             __syncwarp();
             if (n >= 1) ok = issue_pv(n - 1);
         }

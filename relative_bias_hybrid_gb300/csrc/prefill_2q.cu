@@ -215,31 +215,16 @@ k_prefill_2q(const Tc2Args A, const __grid_constant__ CUtensorMap qmap,
             if (!last) tc::commit(bar(B_KV_EMPTY + slot));
         };
         auto qk = [&](int x, int slot) {
-            {
-                const uint64_t db = dk0 + slot_off(slot);
-                const uint64_t da = dq0 + (uint64_t)(x * (32768 >> 4));
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                    tc::mma_bf16_ss(tmem + kTmemS + x * 128, da + off, db + off, id_qk, kk > 0 ? 1u : 0u);
-                }
-                tc::commit(bar(B_S_FULL + x));
-            }
+            tc::mma_bf16_ss_k128_commit(tmem + kTmemS + x * 128, dq0 + (uint64_t)(x * (32768 >> 4)),
+                                        dk0 + slot_off(slot), id_qk, 0u, bar(B_S_FULL + x));
             __syncwarp();
         };
         int kp[2] = {0, 0};                                   // P V issued per tile
         auto pv = [&](int x, int slot) -> bool {
             if (!wwait(bar(B_P_FULL + x), kp[x] & 1)) return false;
             tc::fence_after();
-            {
-                const uint32_t ps = tmem + kTmemS + x * 128;
-                const uint64_t db = dv0 + slot_off(slot);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    tc::mma_bf16_ts(tmem + kTmemO + x * 128, ps + kk * 8, db + (uint64_t)(kk * 128), id_pv,
-                                    (kp[x] > 0 || kk > 0) ? 1u : 0u);
-                tc::commit(bar(B_PV_DONE + x));
-            }
+            tc::mma_bf16_ts_k128_commit(tmem + kTmemO + x * 128, tmem + kTmemS + x * 128, dv0 + slot_off(slot),
+                                        id_pv, kp[x] > 0 ? 1u : 0u, bar(B_PV_DONE + x));
             __syncwarp();
             ++kp[x];
             return true;
