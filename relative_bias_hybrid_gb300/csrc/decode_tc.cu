@@ -274,9 +274,9 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
                 __syncwarp();
             }
             tc::fence_after();
-            tc::mma_bf16_ts_k128_commit(tmem + kTmemO, tmem + kTmemS0 + (uint32_t)(m & 1) * 128,
-                                        dv0 + slot_off(slot), id_pv, m > 0 ? 1u : 0u, bar(B_PV_DONE + (m & 1)));
-            if (!last) tc::commit(bar(B_KV_EMPTY + slot));
+            tc::mma_bf16_ts_k128_commit<false>(tmem + kTmemO, tmem + kTmemS0 + (uint32_t)(m & 1) * 128,
+                                               dv0 + slot_off(slot), id_pv, m > 0 ? 1u : 0u, bar(B_PV_DONE + (m & 1)),
+                                               bar(B_KV_EMPTY + slot), last ? 0u : 1u);
             __syncwarp();
             return true;
         };
@@ -286,9 +286,9 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
             ok = next_tile(slot, last);
             if (!ok) break;
             tc::fence_after();
-            tc::mma_bf16_ss_k128_commit(tmem + kTmemS0 + (uint32_t)(n & 1) * 128, dq, dk0 + slot_off(slot), id_qk,
-                                        0u, bar(B_S_FULL + (n & 1)));
-            if (!last) tc::commit(bar(B_KV_EMPTY + slot));
+            tc::mma_bf16_ss_k128_commit<false>(tmem + kTmemS0 + (uint32_t)(n & 1) * 128, dq, dk0 + slot_off(slot),
+                                               id_qk, 0u, bar(B_S_FULL + (n & 1)), bar(B_KV_EMPTY + slot),
+                                               last ? 0u : 1u);
             __syncwarp();
             if (n >= 1) ok = issue_pv(n - 1);
         }

@@ -215,7 +215,7 @@ k_prefill_2q(const Tc2Args A, const __grid_constant__ CUtensorMap qmap,
             if (!last) tc::commit(bar(B_KV_EMPTY + slot));
         };
         auto qk = [&](int x, int slot) {
-            tc::mma_bf16_ss_k128_commit(tmem + kTmemS + x * 128, dq0 + (uint64_t)(x * (32768 >> 4)),
+            tc::mma_bf16_ss_k128_commit<false>(tmem + kTmemS + x * 128, dq0 + (uint64_t)(x * (32768 >> 4)),
                                         dk0 + slot_off(slot), id_qk, 0u, bar(B_S_FULL + x));
             __syncwarp();
         };
@@ -223,7 +223,7 @@ k_prefill_2q(const Tc2Args A, const __grid_constant__ CUtensorMap qmap,
         auto pv = [&](int x, int slot) -> bool {
             if (!wwait(bar(B_P_FULL + x), kp[x] & 1)) return false;
             tc::fence_after();
-            tc::mma_bf16_ts_k128_commit(tmem + kTmemO + x * 128, tmem + kTmemS + x * 128, dv0 + slot_off(slot),
+            tc::mma_bf16_ts_k128_commit<false>(tmem + kTmemO + x * 128, tmem + kTmemS + x * 128, dv0 + slot_off(slot),
                                         id_pv, kp[x] > 0 ? 1u : 0u, bar(B_PV_DONE + x));
             __syncwarp();
             ++kp[x];

@@ -304,13 +304,9 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         // only the nearest key tile can hold keys at or past the sequence end inside a
         // loaded cache block (when T is not a multiple of the block size)
         const bool zero_tail = (T % kBlock) != 0 && t_hi == (T - 1) / kKeys;
-        // the slot may be refilled once the MMAs issued so far have read it; a slot with no
-        // later load is not released, so no arrival reaches a peer that has finished
-        auto release = [&](int slot, bool last) {
-            if (last) return;
-            if constexpr (kCluster > 1) tc::commit_mc(bar(B_KV_EMPTY + slot), kPeers);
-            else tc::commit(bar(B_KV_EMPTY + slot));
-        };
+        // A K/V slot may be refilled once the MMAs issued so far have read it: each MMA group
+        // ends with that release (in every CTA of the cluster), except for a slot with no
+        // later load, so that no arrival reaches a peer that has finished.
         auto issue_pv = [&](int m) -> bool {
             if (!wwait(bar(B_P_FULL + (m & 1)), (m >> 1) & 1)) return false;
             int slot;
@@ -333,9 +329,9 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                 __syncwarp();
             }
             tc::fence_after();
-            tc::mma_bf16_ts_k128_commit(tmem + kTmemO, tmem + kTmemS0 + (uint32_t)(m & 1) * 128,
-                                        dv0 + slot_off(slot), id_pv, m > 0 ? 1u : 0u, bar(B_PV_DONE + (m & 1)));
-            release(slot, last);
+            tc::mma_bf16_ts_k128_commit<(kCluster > 1)>(
+                tmem + kTmemO, tmem + kTmemS0 + (uint32_t)(m & 1) * 128, dv0 + slot_off(slot), id_pv,
+                m > 0 ? 1u : 0u, bar(B_PV_DONE + (m & 1)), bar(B_KV_EMPTY + slot), last ? 0u : 1u, kPeers);
             __syncwarp();
             return true;
         };
@@ -346,9 +342,9 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             ok = next_tile(slot, last);
             if (!ok) break;
             tc::fence_after();
-            tc::mma_bf16_ss_k128_commit(tmem + kTmemS0 + (uint32_t)(n & 1) * 128, dq, dk0 + slot_off(slot), id_qk,
-                                        0u, bar(B_S_FULL + (n & 1)));
-            release(slot, last);
+            tc::mma_bf16_ss_k128_commit<(kCluster > 1)>(
+                tmem + kTmemS0 + (uint32_t)(n & 1) * 128, dq, dk0 + slot_off(slot), id_qk, 0u,
+                bar(B_S_FULL + (n & 1)), bar(B_KV_EMPTY + slot), last ? 0u : 1u, kPeers);
             __syncwarp();
             if (n >= 1) ok = issue_pv(n - 1);
         }

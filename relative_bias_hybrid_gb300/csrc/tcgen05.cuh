@@ -105,63 +105,104 @@ __device__ __forceinline__ void commit_mc(uint32_t bar, uint16_t cta_mask) {
                  :: "r"(bar), "h"(cta_mask) : "memory");
 }
 
-// A whole K = 128 step (eight K = 16 MMAs) and a commit of it to `bar`, in one instruction
-// sequence with one election: the issuing lane spends no instructions of its own between the
-// MMAs.  acc0 = 0 makes the first MMA overwrite D.  Warp-collective like the single forms.
+// A whole K = 128 step (eight K = 16 MMAs), a commit of it to `bar` and, when `rel` is
+// nonzero, a second commit to `rel_bar` (in every CTA named in `rel_mask` when kMc), all in
+// one instruction sequence with one election: the issuing lane spends no instructions of
+// its own between them.  acc0 = 0 makes the first MMA overwrite D.  Warp-collective like
+// the single forms.
 //
 // SS: A and B are 128-byte-swizzled K-major tiles stored as two 64-column halves 16 KB
 // apart; the k-step start addresses advance by 32 bytes within a half (2 in the
 // descriptor's 16-byte units) and by 16 KB (1024) to the second half.
-__device__ __forceinline__ void mma_bf16_ss_k128_commit(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
-                                                         uint32_t acc0, uint32_t bar) {
-    asm volatile(
-        "{\n\t.reg .pred e, p0, pt;\n\t.reg .b64 a1, b1;\n\t"
-        "setp.ne.b32 p0, %4, 0;\n\tsetp.eq.u32 pt, 0, 0;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n\t"
-        "add.s64 a1, %1, 2;\n\tadd.s64 b1, %2, 2;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t"
-        "add.s64 a1, %1, 4;\n\tadd.s64 b1, %2, 4;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t"
-        "add.s64 a1, %1, 6;\n\tadd.s64 b1, %2, 6;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t"
-        "add.s64 a1, %1, 1024;\n\tadd.s64 b1, %2, 1024;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t"
-        "add.s64 a1, %1, 1026;\n\tadd.s64 b1, %2, 1026;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t"
-        "add.s64 a1, %1, 1028;\n\tadd.s64 b1, %2, 1028;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t"
-        "add.s64 a1, %1, 1030;\n\tadd.s64 b1, %2, 1030;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t}"
-        :: "r"(d), "l"(a), "l"(b), "r"(id), "r"(acc0), "r"(bar) : "memory");
-}
+#define INKATTN_MMA_SS_K128 \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n\t" \
+    "add.s64 a1, %1, 2;\n\t" \
+    "add.s64 b1, %2, 2;\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t" \
+    "add.s64 a1, %1, 4;\n\t" \
+    "add.s64 b1, %2, 4;\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t" \
+    "add.s64 a1, %1, 6;\n\t" \
+    "add.s64 b1, %2, 6;\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t" \
+    "add.s64 a1, %1, 1024;\n\t" \
+    "add.s64 b1, %2, 1024;\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t" \
+    "add.s64 a1, %1, 1026;\n\t" \
+    "add.s64 b1, %2, 1026;\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t" \
+    "add.s64 a1, %1, 1028;\n\t" \
+    "add.s64 b1, %2, 1028;\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t" \
+    "add.s64 a1, %1, 1030;\n\t" \
+    "add.s64 b1, %2, 1030;\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t"
 
 // TS: A (P, bf16) in TMEM, 8 columns per k step; B is a 128-byte-swizzled MN-major tile
 // whose k steps (16 rows of 128 bytes) lie 2 KB apart (128 in 16-byte units).
+#define INKATTN_MMA_TS_K128 \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p0;\n\t" \
+    "add.u32 a1, %1, 8;\n\t" \
+    "add.s64 b1, %2, 128;\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, pt;\n\t" \
+    "add.u32 a1, %1, 16;\n\t" \
+    "add.s64 b1, %2, 256;\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, pt;\n\t" \
+    "add.u32 a1, %1, 24;\n\t" \
+    "add.s64 b1, %2, 384;\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, pt;\n\t" \
+    "add.u32 a1, %1, 32;\n\t" \
+    "add.s64 b1, %2, 512;\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, pt;\n\t" \
+    "add.u32 a1, %1, 40;\n\t" \
+    "add.s64 b1, %2, 640;\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, pt;\n\t" \
+    "add.u32 a1, %1, 48;\n\t" \
+    "add.s64 b1, %2, 768;\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, pt;\n\t" \
+    "add.u32 a1, %1, 56;\n\t" \
+    "add.s64 b1, %2, 896;\n\t" \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, pt;\n\t"
+
+#define INKATTN_K128_PROLOGUE \
+    "setp.ne.b32 p0, %4, 0;\n\tsetp.eq.u32 pt, 0, 0;\n\tsetp.ne.b32 pr, %7, 0;\n\t" \
+    "elect.sync _|e, 0xffffffff;\n\tand.pred pr, pr, e;\n\t"
+#define INKATTN_K128_COMMITS(MC) \
+    "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t" \
+    "@pr tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster" MC ";\n\t}"
+
+template <bool kMc>
+__device__ __forceinline__ void mma_bf16_ss_k128_commit(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
+                                                         uint32_t acc0, uint32_t bar, uint32_t rel_bar = 0,
+                                                         uint32_t rel = 0, uint16_t rel_mask = 0) {
+    if constexpr (kMc) {
+        asm volatile("{\n\t.reg .pred e, p0, pt, pr;\n\t.reg .b64 a1, b1;\n\t" INKATTN_K128_PROLOGUE
+                     INKATTN_MMA_SS_K128 INKATTN_K128_COMMITS(".multicast::cluster.b64 [%6], %8")
+                     :: "r"(d), "l"(a), "l"(b), "r"(id), "r"(acc0), "r"(bar), "r"(rel_bar), "r"(rel),
+                        "h"(rel_mask) : "memory");
+    } else {
+        asm volatile("{\n\t.reg .pred e, p0, pt, pr;\n\t.reg .b64 a1, b1;\n\t" INKATTN_K128_PROLOGUE
+                     INKATTN_MMA_SS_K128 INKATTN_K128_COMMITS(".b64 [%6]")
+                     :: "r"(d), "l"(a), "l"(b), "r"(id), "r"(acc0), "r"(bar), "r"(rel_bar), "r"(rel),
+                        "h"(rel_mask) : "memory");
+    }
+}
+
+template <bool kMc>
 __device__ __forceinline__ void mma_bf16_ts_k128_commit(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id,
-                                                         uint32_t acc0, uint32_t bar) {
-    asm volatile(
-        "{\n\t.reg .pred e, p0, pt;\n\t.reg .b32 a1;\n\t.reg .b64 b1;\n\t"
-        "setp.ne.b32 p0, %4, 0;\n\tsetp.eq.u32 pt, 0, 0;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p0;\n\t"
-        "add.u32 a1, %1, 8;\n\tadd.s64 b1, %2, 128;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, pt;\n\t"
-        "add.u32 a1, %1, 16;\n\tadd.s64 b1, %2, 256;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, pt;\n\t"
-        "add.u32 a1, %1, 24;\n\tadd.s64 b1, %2, 384;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, pt;\n\t"
-        "add.u32 a1, %1, 32;\n\tadd.s64 b1, %2, 512;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, pt;\n\t"
-        "add.u32 a1, %1, 40;\n\tadd.s64 b1, %2, 640;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, pt;\n\t"
-        "add.u32 a1, %1, 48;\n\tadd.s64 b1, %2, 768;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, pt;\n\t"
-        "add.u32 a1, %1, 56;\n\tadd.s64 b1, %2, 896;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, pt;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t}"
-        :: "r"(d), "r"(a_tmem), "l"(b), "r"(id), "r"(acc0), "r"(bar) : "memory");
+                                                         uint32_t acc0, uint32_t bar, uint32_t rel_bar = 0,
+                                                         uint32_t rel = 0, uint16_t rel_mask = 0) {
+    if constexpr (kMc) {
+        asm volatile("{\n\t.reg .pred e, p0, pt, pr;\n\t.reg .b32 a1;\n\t.reg .b64 b1;\n\t" INKATTN_K128_PROLOGUE
+                     INKATTN_MMA_TS_K128 INKATTN_K128_COMMITS(".multicast::cluster.b64 [%6], %8")
+                     :: "r"(d), "r"(a_tmem), "l"(b), "r"(id), "r"(acc0), "r"(bar), "r"(rel_bar), "r"(rel),
+                        "h"(rel_mask) : "memory");
+    } else {
+        asm volatile("{\n\t.reg .pred e, p0, pt, pr;\n\t.reg .b32 a1;\n\t.reg .b64 b1;\n\t" INKATTN_K128_PROLOGUE
+                     INKATTN_MMA_TS_K128 INKATTN_K128_COMMITS(".b64 [%6]")
+                     :: "r"(d), "r"(a_tmem), "l"(b), "r"(id), "r"(acc0), "r"(bar), "r"(rel_bar), "r"(rel),
+                        "h"(rel_mask) : "memory");
+    }
 }
 
 // ---------------------------------------------------------------- TMEM <-> registers
