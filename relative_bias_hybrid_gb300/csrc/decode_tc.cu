@@ -16,8 +16,8 @@
 //   warp 0      producer: TMA loads of 128-key K/V tiles (two 64-key cache blocks) of this
 //               split's key range into a 4-slot ring, in the order the MMAs consume them
 //               (every tile comes from HBM: the ring's depth sets the bytes in flight).
-//   warp 1      MMA issuer (one lane): S = Q K^T into a double-buffered S in TMEM, O += P V
-//               with P (bf16) read from TMEM.
+//   warp 1      MMA issuer (the whole warp, one elected lane issuing): S = Q K^T into a
+//               double-buffered S in TMEM, O += P V with P (bf16) read from TMEM.
 //   warps 2-9   softmax: two warpgroups; row a (TMEM lane a) is shared by one thread of each,
 //               which own its key columns [0, 64) and [64, 128).
 // TMEM: O [0,128) | S0 [128,256) | S1 [256,384).

@@ -11,7 +11,7 @@
 // and Q K^T of tile n) run, and the other way round.  Roles:
 //   warp 0      producer: TMA loads of Q_A, Q_B and of 128-key K/V tiles into a 3-slot ring,
 //               in the order the MMAs first use them (K_0, V_0, K_1, V_1, ...).
-//   warp 1      MMA issuer (one lane).
+//   warp 1      MMA issuer (the whole warp, one elected lane issuing).
 //   warps 2-5   softmax of tile A, warps 6-9 softmax of tile B: one thread per query row,
 //               all 128 key columns of the tile (no exchange between threads).
 // TMEM (512 columns): O_A [0,128) | O_B [128,256) | S_A [256,384) | S_B [384,512).  P (bf16)

@@ -83,26 +83,12 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d, uint64_t a, uint64_t b, 
                  "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
                  :: "r"(d), "l"(a), "l"(b), "r"(id), "r"(acc) : "memory");
 }
-// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t acc) {
-    asm volatile("{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-                 :: "r"(d), "r"(a_tmem), "l"(b), "r"(id), "r"(acc) : "memory");
-}
 // Arrives once on the mbarrier when every tcgen05 operation issued so far by the elected
 // lane has completed.
 __device__ __forceinline__ void commit(uint32_t bar) {
     asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
                  "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
                  :: "r"(bar) : "memory");
-}
-
-// As commit, arriving on the mbarrier at the same shared-memory offset in every CTA of
-// the cluster named in cta_mask.
-__device__ __forceinline__ void commit_mc(uint32_t bar, uint16_t cta_mask) {
-    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}"
-                 :: "r"(bar), "h"(cta_mask) : "memory");
 }
 
 // A whole K = 128 step (eight K = 16 MMAs), a commit of it to `bar` and, when `rel` is
