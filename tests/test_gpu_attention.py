@@ -282,3 +282,40 @@ def test_bf16_output_is_the_fp32_output_rounded_once(env, mode, splits):
         ia.inkattn_combine(p, step.num_splits, step.workspace)
     torch.cuda.synchronize()
     assert torch.equal(out_bf.view(torch.int16), step.out.to(torch.bfloat16).view(torch.int16))
+
+
+# ---------------------------------------------------------------- poisoned cache tails
+
+def _poison_tails(x):
+    """NaN into every K and V slot past a sequence's end inside its last cache block."""
+    nan = torch.tensor(float("nan"), dtype=x["k_cache"].dtype, device=x["k_cache"].device)
+    table = x["block_table"].cpu()
+    for b, T in enumerate(x["seqlen_k"].cpu().tolist()):
+        for pos in range(T, (T + 63) // 64 * 64):
+            blk = int(table[b, pos // 64])
+            x["k_cache"][blk, :, pos % 64, :] = nan
+            x["v_cache"][blk, :, pos % 64, :] = nan
+
+
+@pytest.mark.parametrize("mode,rel_extent", [("prefill", 150), ("prefill", 0), ("decode", 200)])
+def test_nan_past_sequence_end_is_ignored(env, mode, rel_extent):
+    """Keys past a sequence's end inside its last loaded block are masked; their V rows are
+    zeroed before P V, so NaN there (0 * NaN = NaN otherwise) leaves the output finite and
+    equal to the oracle's, which reads only the valid keys."""
+    gen, AttentionStep, _ = env
+    if mode == "decode":
+        w = gen.custom("nan-tail-dec", Hq=16, Hkv=2, q_lens=[9, 4], prefix_lens=[900, 2000],
+                       rel_extent=rel_extent, log_scale_base=256.0)
+    else:
+        w = gen.custom("nan-tail", Hq=8, Hkv=2, q_lens=[301, 140], prefix_lens=[20, 3], window=200,
+                       rel_extent=rel_extent)
+    x_cpu = gen.make_inputs(w, seed=31, device="cpu")
+    x = {k: v.cuda() for k, v in x_cpu.items()}
+    assert all(T % 64 != 0 for T in x_cpu["seqlen_k"].tolist())
+    step = AttentionStep(w, x, mode=mode, out_dtype=torch.float32)
+    step.run_prologue()
+    _poison_tails(x)
+    step.run_attention()
+    torch.cuda.synchronize()
+    assert step.device_status() == 0
+    _check_all_rows(env, w, x_cpu, x, step)
