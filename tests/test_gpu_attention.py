@@ -156,6 +156,17 @@ def test_decode_small(env, splits):
     _check_all_rows(env, w, *_run(env, w, mode="decode", seed=4, num_splits=splits))
 
 
+@pytest.mark.parametrize("Hq,Hkv,ql", [(32, 2, 8), (16, 2, 16)])
+def test_decode_at_the_row_limit(env, Hq, Hkv, ql):
+    """(token, query head) rows of a KV head at their limit of 128 (the MMA's M, every TMEM
+    lane and every bias-table row in use), with uneven prefixes and 3 splits."""
+    gen = env[0]
+    w = gen.custom("dec-rows", Hq=Hq, Hkv=Hkv, q_lens=[ql, ql], prefix_lens=[1000, 2989], rel_extent=300,
+                   log_scale_base=256.0)
+    assert (Hq // Hkv) * ql == 128
+    _check_all_rows(env, w, *_run(env, w, mode="decode", seed=8, num_splits=3))
+
+
 def test_decode_sliding_window(env):
     gen = env[0]
     w = gen.custom("dec-swa", Hq=64, Hkv=8, q_lens=[9, 9], prefix_lens=[5000, 300], rel_extent=512,
