@@ -242,14 +242,15 @@ k_prologue(const inkattn_prologue_params p, const int kv_tiles) {
         }
         s_x[stream][r][chunk] = v;
     }
-    // slot mapping of the rows this thread writes (tokens half&7 + 8u), fetched before the
-    // barrier so the cache write does not wait for it
+    // slot mapping of the rows this half-warp writes (tokens half&7 + 8u): lane u of the
+    // half-warp fetches the one for step u before the barrier, so the cache write neither
+    // waits for it nor selects it from a register array
     constexpr int kRowsPerHalf = kKvTokens / 8;
-    int sm_pre[kRowsPerHalf];
-#pragma unroll
-    for (int u = 0; u < kRowsPerHalf; ++u) {
-        const int tt = u * 8 + (half & 7);
-        sm_pre[u] = tt < nt ? __ldg(p.slot_mapping + start + t0 + tt) : 0;
+    static_assert(kRowsPerHalf <= 16, "one entry per lane of a half-warp");
+    int sm_mine = 0;
+    {
+        const int tt = lane16 * 8 + (half & 7);
+        if (lane16 < kRowsPerHalf && tt < nt) sm_mine = __ldg(p.slot_mapping + start + t0 + tt);
     }
     __syncthreads();
 
@@ -284,10 +285,8 @@ k_prologue(const inkattn_prologue_params p, const int kv_tiles) {
         ss += __shfl_xor_sync(0xffffffffu, ss, 4);
         ss += __shfl_xor_sync(0xffffffffu, ss, 2);
         ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        const int sm = __shfl_sync(0xffffffffu, sm_mine, ((half & 1) << 4) + u);
         if (!valid) continue;
-        int sm = sm_pre[0];
-#pragma unroll
-        for (int v = 1; v < kRowsPerHalf; ++v) sm = (u == v) ? sm_pre[v] : sm;
         if (sm < 0 || (long long)sm >= slot_limit) {
             if (lane16 == 0) set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
             continue;
