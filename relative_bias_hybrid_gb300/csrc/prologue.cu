@@ -114,11 +114,14 @@ __device__ __forceinline__ void conv4_bf16_fast2(const float (&wa)[4], const flo
                                                  const float (&wb)[4], const float (&xb)[4],
                                                  float &ya, float &yb) {
     float2 s = fmul2(make_float2(wa[0], wb[0]), make_float2(xa[0], xb[0]));
+    // the sums of magnitudes in scalar form: the absolute values then ride on the
+    // multiply-adds' operands instead of taking instructions of their own
     float2 a = make_float2(fabsf(s.x), fabsf(s.y));
 #pragma unroll
     for (int k = 1; k < 4; ++k) {
         s = ffma2(make_float2(wa[k], wb[k]), make_float2(xa[k], xb[k]), s);
-        a = ffma2(make_float2(fabsf(wa[k]), fabsf(wb[k])), make_float2(fabsf(xa[k]), fabsf(xb[k])), a);
+        a.x = fmaf(fabsf(wa[k]), fabsf(xa[k]), a.x);
+        a.y = fmaf(fabsf(wb[k]), fabsf(xb[k]), a.y);
     }
     const float ma = __uint_as_float((__float_as_uint(s.x) & 0xFFFF0000u) | 0x8000u);
     const float mb = __uint_as_float((__float_as_uint(s.y) & 0xFFFF0000u) | 0x8000u);
