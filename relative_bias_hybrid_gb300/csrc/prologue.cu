@@ -231,19 +231,23 @@ k_prologue(const inkattn_prologue_params p, const int kv_tiles) {
         s_wv[j] = p.conv_w_v[(size_t)hk * kHeadDim * 4 + i];
     }
     if (tid < kHeadDim) s_gk[(tid & 7) * 16 + (tid >> 3)] = p.k_norm_w[tid];
-    for (int i = tid; i < 2 * (nt + 3) * 16; i += kPrologueThreads) {
-        const int stream = i / ((nt + 3) * 16), r = (i >> 4) % (nt + 3), chunk = i & 15;
+    // one 16-byte chunk of one row of both streams per step (no division by the row count)
+    for (int i = tid; i < (nt + 3) * 16; i += kPrologueThreads) {
+        const int r = i >> 4, chunk = i & 15;
         const int idx = t0 + r;               // index into [3 carried rows ; new rows]
         const size_t ch = (size_t)hk * kHeadDim + chunk * 8;
-        uint4 v;
+        uint4 vk, vv;
         if (idx < 3) {
-            const inkattn_bf16 *st = stream == 0 ? p.conv_state_k : p.conv_state_v;
-            v = *reinterpret_cast<const uint4 *>(st + ((size_t)slot * 3 + idx) * C + ch);
+            const size_t o = ((size_t)slot * 3 + idx) * C + ch;
+            vk = *reinterpret_cast<const uint4 *>(p.conv_state_k + o);
+            vv = *reinterpret_cast<const uint4 *>(p.conv_state_v + o);
         } else {
-            const inkattn_bf16 *src = stream == 0 ? p.k : p.v;
-            v = __ldg(reinterpret_cast<const uint4 *>(src + ((size_t)start + idx - 3) * C + ch));
+            const size_t o = ((size_t)start + idx - 3) * C + ch;
+            vk = __ldg(reinterpret_cast<const uint4 *>(p.k + o));
+            vv = __ldg(reinterpret_cast<const uint4 *>(p.v + o));
         }
-        s_x[stream][r][chunk] = v;
+        s_x[0][r][chunk] = vk;
+        s_x[1][r][chunk] = vv;
     }
     // slot mapping of the rows this half-warp writes (tokens half&7 + 8u): lane u of the
     // half-warp fetches the one for step u before the barrier, so the cache write neither
