@@ -1,26 +1,28 @@
 #!/usr/bin/env python3
-"""Benchmark of the Inkling attention hot path on GB300.
+"""Benchmark of the Inkling attention hot path on one GB300.
 
-One step = one pass of the whole path over the sliding-window prefill layer
-(8192 tokens, Hq=64, Hkv=8, window 4096, rel_extent 512): inkattn_prologue then
-inkattn_prefill, inputs resident in HBM.  value = algorithmic attention TFLOP/s of
-the step.  The same line carries the MTP-verify decode workload (32 x 9 queries,
-KV 32768, split-KV decode + combine) as KV GB/s, per-kernel rooflines, the
-end-to-end number through the C ABI with pinned host buffers, the SM clocks seen
-during the timed region, and the fp64 oracle timed on a bounded sample on the host
-cores.
+One step = one pass of the whole path over one workload, inputs resident in HBM:
+inkattn_prologue then inkattn_prefill (prefill layers), or inkattn_prologue then
+inkattn_decode + inkattn_combine (decode).  The headline is the full-attention prefill
+layer (B=1, T=32768, Hq=64, Hkv=8, rel_extent=1024, logits scaled by ln T / ln 8192):
+value = its algorithmic attention TFLOP/s per step.  The same JSON line carries the
+sliding-window layer, the ragged mixed-prefill batch and the MTP-verify decode under
+"workloads", each with its kernel rooflines, the end-to-end number through the C ABI
+with host buffers, and the fp64 oracle timed on a bounded sample on the host cores;
+plus the SM clocks sampled during the timed regions.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+  python bench.py [--steps K] [--warmup W] [--impl reference] [--only NAME ...]
 
-With N > 1 (launched by torch.distributed.run) every rank runs an independent
-replica of the workload on its own GPU; value = units of all ranks / max time.
+One GPU only.  The prefill kernel multicasts K/V tiles inside a CTA pair, which this
+build keeps to single-GPU runs: --gpus N > 1 (or a torch.distributed launch with more
+than one rank) is refused before any GPU is touched.  The reference arm (the CPU
+oracle) touches no GPU; under a multi-rank launch its rank 0 alone runs.
 """
 from __future__ import annotations
 
 import argparse
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -134,7 +136,9 @@ def ncu_traffic(kernel: str, workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    """nvidia-smi sampling of SM clocks, power and throttle reasons during the timed regions
+    (every 100 ms).  sm_mhz is the median over the samples taken under load (power at
+    least half of the largest seen)."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -154,7 +158,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self.target, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
         time.sleep(0.3)
@@ -167,7 +171,7 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         try:
             with open(self.path) as f:
@@ -178,6 +182,7 @@ class ClockSampler:
                     try:
                         sm.append(float(parts[0]))
                         mx.append(float(parts[1]))
+                        pw.append(float(parts[2]))
                     except ValueError:
                         continue
                     for name, val in zip(names, parts[4:8]):
@@ -188,64 +193,16 @@ class ClockSampler:
             pass
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        top = max(pw)
+        loaded = [c for c, w in zip(sm, pw) if w >= 0.5 * top]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm), "samples_under_load": len(loaded),
+                "sm_mhz_median_all": statistics.median(sm), "power_w_max": top}
 
 
-def dist_setup(args):
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        import torch.distributed as dist
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
-        if torch.cuda.is_available():
-            torch.cuda.set_device(local)
-        dist.init_process_group(backend=backend)
-    elif torch.cuda.is_available():
-        torch.cuda.set_device(0)
-    return world, rank, local
-
-
-def barrier(world):
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-
-
-def aggregate_over_ranks(local_ms: float, local_units: float, world: int):
-    """(max time over ranks in ms, total units over ranks).  Replicas: no data exchange;
-    this reduction is on two scalars for the report only."""
-    if world == 1:
-        return local_ms, local_units
-    import torch.distributed as dist
-    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
-    t = torch.tensor([local_ms], dtype=torch.float64, device=dev)
-    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    dist.all_reduce(u, op=dist.ReduceOp.SUM)
-    return float(t.item()), float(u.item())
-
-
-# ---------------------------------------------------------------- oracle arm
-
-def oracle_sample(w, x_cpu, q_bits, kc_bits, vc_bits, rows, n_threads):
-    import oracle
-    t0 = time.perf_counter()
-    oracle.attention_for_inputs(x_cpu, w, q_bits, kc_bits, vc_bits, rows=rows, n_threads=n_threads)
-    return time.perf_counter() - t0
-
-
-def sample_flops(w, rows, cu):
-    """Algorithmic FLOPs of the attention for the listed token rows (all heads)."""
-    total = 0.0
-    seq = np.searchsorted(cu, rows, side="right") - 1
-    for t, b in zip(rows, seq):
-        i = w.prefix_lens[b] + (t - cu[b])
-        vis = i + 1 if w.window == 0 else min(i + 1, w.window)
-        lim = w.rel_extent if w.window == 0 else min(w.rel_extent, w.window)
-        total += (4.0 * w.head_dim * vis + 2.0 * w.d_r * min(i + 1, lim)) * w.Hq
-    return total
+def world_from_env():
+    """(world size, rank) of a torch.distributed launch, (1, 0) otherwise."""
+    return int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
 
 
 def host_cores():
@@ -255,48 +212,131 @@ def host_cores():
         return os.cpu_count() or 1
 
 
-def cpu_oracle_baseline(w, x_dev, target_s=12.0, seed=0):
-    """fp64 oracle on a bounded sample of the workload's query rows (all heads), timed
-    on all host cores; returns the cpu_baseline object in the bench's unit."""
-    import oracle  # noqa: F401  (test infrastructure; only this leg of the bench uses it)
-    from relative_bias_hybrid_gb300 import inputs as gen
-    x_cpu = {k: x_dev[k].cpu() for k in ("cu_seqlens_q", "seqlen_k", "r", "P", "block_table")}
-    q_bits = gen.bits(x_dev["q"])
-    kc, vc = gen.bits(x_dev["k_cache"]), gen.bits(x_dev["v_cache"])
-    cu = x_cpu["cu_seqlens_q"].numpy()
+# ---------------------------------------------------------------- oracle (CPU) samples
+
+def sample_flops(w, rows, cu):
+    """Algorithmic FLOPs of the attention for the listed token rows (all heads)."""
+    total = 0.0
+    seq = np.searchsorted(cu, rows, side="right") - 1
+    lim = w.rel_extent if w.window == 0 else min(w.rel_extent, w.window)
+    for t, b in zip(rows, seq):
+        i = w.prefix_lens[b] + (t - cu[b])
+        vis = i + 1 if w.window == 0 else min(i + 1, w.window)
+        total += (4.0 * w.head_dim * vis + 2.0 * w.d_r * min(i + 1, lim)) * w.Hq
+    return total
+
+
+class HostCopy:
+    """What the oracle needs of a measured workload, copied to the host before the device
+    buffers are freed: normalised queries and caches (bf16 bits), r, P, lengths, table."""
+
+    def __init__(self, w, x, q_out, seqs=None):
+        from relative_bias_hybrid_gb300 import inputs as gen
+        self.w = w
+        self.B_full = w.B
+        if seqs is None:
+            self.x = {k: x[k].cpu() for k in ("cu_seqlens_q", "seqlen_k", "r", "P", "block_table")}
+            self.q = gen.bits(q_out)
+            self.kc, self.vc = gen.bits(x["k_cache"]), gen.bits(x["v_cache"])
+            return
+        # decode: a few whole sequences, their cache blocks gathered and renumbered
+        import dataclasses
+        bt = x["block_table"].cpu().numpy()
+        sk = x["seqlen_k"].cpu().numpy()
+        cu = x["cu_seqlens_q"].cpu().numpy()
+        blocks, table = [], np.full((len(seqs), bt.shape[1]), -1, np.int32)
+        for i, b in enumerate(seqs):
+            n = (int(sk[b]) + w.block_size - 1) // w.block_size
+            table[i, :n] = np.arange(len(blocks), len(blocks) + n)
+            blocks.extend(bt[b, :n].tolist())
+        idx = torch.as_tensor(np.asarray(blocks, np.int64), device=x["k_cache"].device)
+        self.kc = gen.bits(x["k_cache"].index_select(0, idx))
+        self.vc = gen.bits(x["v_cache"].index_select(0, idx))
+        rows = np.concatenate([np.arange(cu[b], cu[b + 1]) for b in seqs]).astype(np.int64)
+        ridx = torch.as_tensor(rows, device=q_out.device)
+        self.q = gen.bits(q_out.index_select(0, ridx))
+        q_lens = [int(cu[b + 1] - cu[b]) for b in seqs]
+        self.w = dataclasses.replace(w, name=f"{w.name}[{len(seqs)} seqs]", q_lens=q_lens,
+                                     prefix_lens=[int(sk[b]) - q for b, q in zip(seqs, q_lens)])
+        cus = np.zeros(len(seqs) + 1, np.int32)
+        cus[1:] = np.cumsum(q_lens)
+        self.x = {"cu_seqlens_q": torch.from_numpy(cus), "seqlen_k": torch.from_numpy(sk[list(seqs)].copy()),
+                  "r": x["r"].index_select(0, ridx).cpu(), "P": x["P"].cpu(),
+                  "block_table": torch.from_numpy(table)}
+
+
+def _oracle_time(h, rows, n_threads):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.attention_for_inputs(h.x, h.w, h.q, h.kc, h.vc, rows=rows, n_threads=n_threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline_prefill(h, target_s, seed=0):
+    """fp64 oracle on a bounded sample of a prefill workload's query rows (all heads), on
+    all host cores; scaled to TFLOP/s by the sample's algorithmic FLOP."""
+    import oracle
+    oracle.build()
+    w = h.w
+    cu = h.x["cu_seqlens_q"].numpy()
     rng = np.random.default_rng(seed)
     cores = host_cores()
-    n = 16
+    n = 8
     rows = np.sort(rng.choice(w.N_tok, size=n, replace=False)).astype(np.int32)
-    dt = oracle_sample(w, x_cpu, q_bits, kc, vc, rows, cores)
-    if dt < target_s / 4:
+    dt = _oracle_time(h, rows, cores)
+    if dt < target_s / 3:
         n = int(min(w.N_tok, max(n, n * target_s / max(dt, 1e-3))))
         rows = np.sort(rng.choice(w.N_tok, size=n, replace=False)).astype(np.int32)
-        dt = oracle_sample(w, x_cpu, q_bits, kc, vc, rows, cores)
+        dt = _oracle_time(h, rows, cores)
     fl = sample_flops(w, rows, cu)
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{len(rows)} of {w.N_tok} query rows (all {w.Hq} heads), {fl:.3g} FLOP in {dt:.1f} s"}
 
 
+def cpu_baseline_decode(h, target_s):
+    """fp64 oracle on the first sequences of the copied decode sample (all their rows and
+    heads), as many as fit about target_s; scaled to GB/s by their algorithmic bytes."""
+    import dataclasses
+    import oracle
+    oracle.build()
+    cores = host_cores()
+    cu = h.x["cu_seqlens_q"].numpy()
+    n_seq = 1
+    while True:
+        rows = np.arange(0, cu[n_seq], dtype=np.int32)
+        dt = _oracle_time(h, rows, cores)
+        if dt >= target_s / 3 or n_seq == h.w.B:
+            break
+        n_seq = int(min(h.w.B, max(n_seq + 1, n_seq * target_s / max(dt, 1e-3))))
+    sub = dataclasses.replace(h.w, q_lens=h.w.q_lens[:n_seq], prefix_lens=h.w.prefix_lens[:n_seq])
+    nbytes = decode_bytes(sub)
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n_seq} of {h.B_full} sequences (all {cu[n_seq]} query rows, all {h.w.Hq} heads), "
+                      f"{nbytes:.3g} algorithmic bytes in {dt:.1f} s"}
+
+
 def run_reference(args, world, rank):
-    """--impl reference: the fp64 CPU oracle, timed on the host cores, on the same
+    """--impl reference: the fp64 CPU oracle, timed on the host cores, on the headline
     workload and metric (each step a bounded sample of query rows)."""
     if rank != 0:
         return
     from relative_bias_hybrid_gb300 import inputs as gen
     import oracle
     oracle.build()
-    w = gen.workload("swa")
+    w = gen.workload("full")
     x = gen.make_inputs(w, seed=0, device="cpu")
     ref = oracle.prologue_for_inputs(x, w)
+    h = HostCopy.__new__(HostCopy)
+    h.w, h.q, h.kc, h.vc = w, ref["q_out"], ref["k_cache"], ref["v_cache"]
+    h.x = {k: x[k] for k in ("cu_seqlens_q", "seqlen_k", "r", "P", "block_table")}
     cu = x["cu_seqlens_q"].numpy()
     cores = host_cores()
     rng = np.random.default_rng(1)
-    rows_per_step = 96
+    rows_per_step = 16
     times, flops = [], []
     for it in range(args.warmup + args.steps):
         rows = np.sort(rng.choice(w.N_tok, size=rows_per_step, replace=False)).astype(np.int32)
-        dt = oracle_sample(w, x, ref["q_out"], ref["k_cache"], ref["v_cache"], rows, cores)
+        dt = _oracle_time(h, rows, cores)
         if it >= args.warmup:
             times.append(dt)
             flops.append(sample_flops(w, rows, cu))
@@ -314,14 +354,15 @@ def run_reference(args, world, rank):
 
 # ---------------------------------------------------------------- GPU arm
 
-def timed_steps(step, steps, warmup, flush, stream, kernel_split=True):
+def timed_steps(step, steps, warmup, flush, stream):
     """Runs warmup + steps passes; each timed pass is bracketed by CUDA events on the
     launching stream, with an L2 flush (a 256 MiB write) between passes, outside the
-    events.  Returns (per-step ms list, per-step attention-kernel ms list)."""
-    for _ in range(warmup):
-        step.run(stream)
+    events.  Returns per-step ms lists: whole step, attention call(s), prologue."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush.zero_()
+            step.run(stream)
     torch.cuda.synchronize()
-    tot, att = [], []
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
             torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     with torch.cuda.stream(stream):
@@ -333,15 +374,14 @@ def timed_steps(step, steps, warmup, flush, stream, kernel_split=True):
             step.run_attention(stream)
             e2.record(stream)
     torch.cuda.synchronize()
-    for e0, e1, e2 in evs:
-        tot.append(e0.elapsed_time(e2))
-        att.append(e1.elapsed_time(e2))
+    tot = [e0.elapsed_time(e2) for e0, _, e2 in evs]
+    att = [e1.elapsed_time(e2) for _, e1, e2 in evs]
     pro = [t - a for t, a in zip(tot, att)]
     return tot, att, pro
 
 
 def e2e_steps(steps_pair, x_host, steps, warmup, stream):
-    """Per step: pinned host -> device copies of the step's inputs, the two C-ABI calls and
+    """Per step: pinned host -> device copies of the step's inputs, the C-ABI calls and
     the device -> pinned host copy of its output, every one inside the timed events.  Two
     sets of input and output buffers alternate, so that the copies of step i + 1 (in) and
     step i - 1 (out) run on their own streams while step i computes; the calls themselves
@@ -394,97 +434,117 @@ def e2e_steps(steps_pair, x_host, steps, warmup, stream):
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
 
-def run_gpu(args, world, rank, local):
-    from relative_bias_hybrid_gb300 import build as _b
+DECODE_ORACLE_SEQS = 16
+
+
+def measure(name, args, peaks, dev, stream, flush):
+    """Device-timed steps, then end-to-end steps, of one workload.  Returns its report
+    (without cpu_baseline), the launches inside its timed regions and the host copy the
+    oracle sample needs."""
     from relative_bias_hybrid_gb300 import inputs as gen
     from relative_bias_hybrid_gb300.step import AttentionStep
-    _b.build()
-    peaks = load_peaks()
-    dev = torch.device("cuda", torch.cuda.current_device())
-    stream = torch.cuda.Stream(device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-
-    # ---- prefill layer (the headline workload)
-    w = gen.workload("swa")
-    x = gen.make_inputs(w, seed=rank, device=dev)
-    step = AttentionStep(w, x, mode="prefill")
-    fl = attention_flops(w)
-
-    # ---- decode workload
-    wd = gen.workload("decode")
-    xd = gen.make_inputs(wd, seed=rank, device=dev)
-    dstep = AttentionStep(wd, xd, mode="decode")
-    dbytes = decode_bytes(wd)
-
-    clocks = ClockSampler(dev.index)
-    barrier(world)
-    torch.cuda.synchronize()
-    clocks.start()
+    w = gen.workload(name)
+    mode = "decode" if name == "decode" else "prefill"
+    x = gen.make_inputs(w, seed=0, device=dev)
+    step = AttentionStep(w, x, mode=mode)
     tot, att, pro = timed_steps(step, args.steps, args.warmup, flush, stream)
-    dtot, datt, dpro = timed_steps(dstep, args.steps, args.warmup, flush, stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
-    status = step.device_status() | dstep.device_status()
-    if status != 0:
-        raise RuntimeError(f"device status {status} during the bench")
+    if step.device_status() != 0:
+        raise RuntimeError(f"{name}: device status {step.device_status()} during the timed steps")
+    ms, att_ms, pro_ms = (sum(v) / len(v) for v in (tot, att, pro))
 
-    ms = sum(tot) / len(tot)
-    ms_max, units = aggregate_over_ranks(ms, fl, world)
-    value = units / (ms_max * 1e-3) / 1e12
-
-    # ---- end to end through the C ABI with pinned host buffers
+    # end to end through the C ABI: a second set of input/output buffers over the same
+    # cache and conv state
     x_host = {n: x[n].cpu().pin_memory() for n in ("q", "k", "v", "r")}
-    # a second set of input/output buffers over the same cache and conv state
     x2 = dict(x)
     for n in ("q", "k", "v", "r"):
         x2[n] = torch.empty_like(x[n])
-    step2 = AttentionStep(w, x2, mode="prefill")
+    step2 = AttentionStep(w, x2, mode=mode, num_splits=step.num_splits)
     e2e_ms, h2d, d2h = e2e_steps((step, step2), x_host, args.steps, args.warmup, stream)
     if step.device_status() | step2.device_status():
-        raise RuntimeError("device status set during the end-to-end steps")
-    e2e_ms_max, e2e_units = aggregate_over_ranks(e2e_ms, fl, world)
+        raise RuntimeError(f"{name}: device status set during the end-to-end steps")
+    launches = args.steps * 2 * step.launches_per_run()
 
-    att_ms = sum(att) / len(att)
-    pro_ms = sum(pro) / len(pro)
-    dec_ms = sum(datt) / len(datt)
-    prefill_tf = fl / (att_ms * 1e-3) / 1e12
-    pro_gbs = prologue_bytes(w) / (pro_ms * 1e-3) / 1e9
-    dec_gbs = dbytes / (dec_ms * 1e-3) / 1e9
-    traffic = ncu_traffic("k_prefill_tc", "swa")
-    roof = {"bound": "tensor", "kernel": "k_prefill_tc", "achieved": prefill_tf, "peak": peaks["bf16"],
-            "unit": "TFLOP/s", "frac": prefill_tf / peaks["bf16"], "peak_src": peaks["src"] + " (burst bf16)",
-            "traffic": traffic, "algorithmic_flop_per_launch": fl}
+    pro_bytes = prologue_bytes(w)
+    prologue = {"bound": "hbm", "kernel": "k_prologue", "achieved": pro_bytes / (pro_ms * 1e-3) / 1e9,
+                "peak": peaks["hbm"], "unit": "GB/s", "traffic": ncu_traffic("k_prologue", name),
+                "algorithmic_bytes_per_launch": pro_bytes, "ms": pro_ms}
+    prologue["frac"] = prologue["achieved"] / peaks["hbm"]
+    if mode == "prefill":
+        fl = attention_flops(w)
+        tf = fl / (att_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": "k_prefill_tc", "achieved": tf, "peak": peaks["bf16"],
+                "unit": "TFLOP/s", "frac": tf / peaks["bf16"], "peak_src": peaks["src"] + " (burst bf16)",
+                "frac_of_sustained": tf / peaks["bf16_sustained"], "traffic": ncu_traffic("k_prefill_tc", name),
+                "algorithmic_flop_per_launch": fl, "ms": att_ms}
+        rep = {"workload": w.describe() + "; step = inkattn_prologue + inkattn_prefill",
+               "value": fl / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+               "roofline": roof, "rooflines": {"k_prologue": prologue},
+               "e2e": {"value": fl / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}}
+        host = HostCopy(w, x, step.q_out)
+    else:
+        nbytes = decode_bytes(w)
+        gbs = nbytes / (att_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "kernel": "k_decode_tc" + ("+k_combine" if step.num_splits > 1 else ""),
+                "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"],
+                "peak_src": peaks["src"] + " (copy bandwidth)", "traffic": ncu_traffic("k_decode_tc", name),
+                "algorithmic_bytes_per_launch": nbytes, "ms": att_ms, "num_splits": step.num_splits}
+        rep = {"workload": w.describe() + "; step = inkattn_prologue + inkattn_decode (+ inkattn_combine)",
+               "value": nbytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+               "roofline": roof, "rooflines": {"k_prologue": prologue},
+               "e2e": {"value": nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}}
+        host = HostCopy(w, x, step.q_out, seqs=list(range(DECODE_ORACLE_SEQS)))
+    return rep, launches, host
+
+
+WORKLOADS = ("full", "swa", "ragged", "decode")
+
+
+def run_gpu(args):
+    from relative_bias_hybrid_gb300 import build as _b
+    _b.build()
+    torch.cuda.set_device(0)
+    peaks = load_peaks()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    names = [n for n in WORKLOADS if not args.only or n in args.only]
+
+    reps, hosts, launches = {}, {}, 0
+    clocks = ClockSampler(dev.index)
+    torch.cuda.synchronize()
+    clocks.start()
+    for name in names:
+        reps[name], n_launch, hosts[name] = measure(name, args, peaks, dev, stream, flush)
+        launches += n_launch
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    clk = clocks.stop()
+    if not args.no_cpu_baseline:
+        per = args.cpu_seconds / len(names)
+        for name in names:
+            h = hosts.pop(name)
+            reps[name]["cpu_baseline"] = (cpu_baseline_decode(h, per) if name == "decode"
+                                          else cpu_baseline_prefill(h, per))
+    head_name = names[0]
+    head = reps.pop(head_name)
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.describe() + "; step = inkattn_prologue + inkattn_prefill",
-                   "global_batch": w.B * world, "seq_len": w.N_tok, "parallelism": f"replicas x{world}",
+        "metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": head["workload"], "global_batch": 1, "parallelism": "single GPU",
                    "l2": "flushed between steps (256 MiB write, outside the timed events)"},
-        "roofline": roof,
-        "rooflines": {
-            "k_prologue": {"bound": "hbm", "achieved": pro_gbs, "peak": peaks["hbm"], "unit": "GB/s",
-                           "frac": pro_gbs / peaks["hbm"], "traffic": ncu_traffic("k_prologue", "swa"),
-                           "algorithmic_bytes_per_launch": prologue_bytes(w), "ms": pro_ms},
-            "k_decode_tc+k_combine": {"bound": "hbm", "achieved": dec_gbs, "peak": peaks["hbm"], "unit": "GB/s",
-                                      "frac": dec_gbs / peaks["hbm"], "traffic": ncu_traffic("k_decode_tc", "decode"),
-                                   "algorithmic_bytes_per_launch": dbytes, "ms": dec_ms,
-                                   "num_splits": dstep.num_splits},
-        },
-        "decode": {"workload": wd.describe() + "; step = inkattn_prologue + inkattn_decode + inkattn_combine",
-                   "value": dec_gbs, "unit": "GB/s", "kv_bytes_per_step": dbytes,
-                   "ms_per_step": sum(dtot) / len(dtot), "ms_attention": dec_ms,
-                   "num_splits": dstep.num_splits, "frac_of_hbm": dec_gbs / peaks["hbm"]},
-        "e2e": {"value": e2e_units / (e2e_ms_max * 1e-3) / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms_max},
-        "gpu_launches": args.steps * (step.launches_per_run() + dstep.launches_per_run()),
+        "roofline": head["roofline"],
+        "rooflines": head["rooflines"],
+        "e2e": head["e2e"],
+        "workloads": reps,
+        "gpu_launches": launches,
         "clocks": clk,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_oracle_baseline(w, x)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    if "cpu_baseline" in head:
+        line["cpu_baseline"] = head["cpu_baseline"]
+    print(json.dumps(line), flush=True)
 
 
 def main(argv=None):
@@ -493,20 +553,24 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["inkattn", "reference"], default="inkattn")
+    ap.add_argument("--only", nargs="*", choices=list(WORKLOADS), default=None,
+                    help="measure only these workloads (the first one listed in the default order heads the line)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=24.0,
+                    help="host-core seconds of oracle work over all workloads' cpu_baseline samples")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)     # at least 3 untimed warm-up steps, reported as used
-    world, rank, local = dist_setup(args)
-    try:
-        if args.impl == "reference":
-            run_reference(args, world, rank)
-        else:
-            run_gpu(args, world, rank, local)
-    finally:
-        if world > 1:
-            import torch.distributed as dist
-            dist.destroy_process_group()
+    world, rank = world_from_env()
+    if args.impl == "reference":
+        run_reference(args, max(world, args.gpus), rank)
+        return 0
+    if args.gpus != 1 or world != 1:
+        sys.stderr.write("bench.py: one GPU only.  The prefill kernel multicasts K/V tiles inside a CTA pair, "
+                         "which this build keeps to single-GPU runs; --gpus must be 1 (no multi-rank launch).\n")
+        return 2
+    run_gpu(args)
+    return 0
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main())

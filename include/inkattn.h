@@ -27,6 +27,11 @@
  *     write INKATTN_ERR_DEVICE_TIMEOUT.  The first error written wins; the caller
  *     zeroes *dev_status before the call and reads it after synchronising.
  *   - head_dim must be 128 and block_size 64, else INKATTN_ERR_UNSUPPORTED.
+ *   - Bounded device waits give up after 1 s.  For tests of that failure path only, two
+ *     environment variables are read once per process: INKATTN_TEST_WAIT_LIMIT_US
+ *     (100 .. 10000000: a shorter limit) and INKATTN_TEST_WITHHOLD_ARRIVAL=1 (the
+ *     attention kernels' softmax withholds its first arrival before P V, so that the MMA
+ *     warp's wait runs out).  Leave both unset in normal use.
  */
 #ifndef INKATTN_H
 #define INKATTN_H
@@ -134,6 +139,14 @@ INKATTN_API inkattn_status inkattn_prologue(const inkattn_prologue_params *p, vo
  *             (full layers' length-dependent logit scaling), else 1,
  *   out_i = sum_j softmax_j(s_ij) v_j,  lse_i = ln sum_j exp(s_ij)  (natural log).
  * softmax_scale <= 0 selects 1/sqrt(128).
+ *
+ * q, k_cache and v_cache are read by TMA through tensor maps and must be device memory of
+ * the current device (cudaMalloc or a memory pool of that device); host memory, managed
+ * memory and another GPU's memory are rejected with INKATTN_ERR_INVALID_ARG.  The prefill
+ * kernel multicasts each K/V tile to the two CTAs of a head pair inside one cluster: the
+ * tensor maps cover this GPU's memory alone.
+ * The bias enters the logits with 11 significant bits (it is staged in fp16, in units of
+ * softmax_scale * q.k); |bias| must stay below 65504 * softmax_scale.
  * ------------------------------------------------------------------------------ */
 typedef struct inkattn_attn_params {
     size_t struct_size;        /* = sizeof(inkattn_attn_params)                          */
@@ -204,21 +217,26 @@ INKATTN_API inkattn_status inkattn_combine(const inkattn_attn_params *p, int num
  * Decode without a caller-provided workspace.  The pages have no counterpart: this
  * is a library convenience.
  *
- * For callers that cannot allocate device memory where they decode: code running in a
- * host function enqueued on a stream (no CUDA API calls are allowed there), plugin
- * hosts that own all device memory and pass only inputs and outputs, and serving loops
- * that must not allocate on the hot path (an allocation can synchronise the device).
+ * For callers that cannot allocate device memory where they decode: plugin hosts that
+ * own all device memory and pass only inputs and outputs, and serving loops that must not
+ * allocate on the hot path (an allocation can synchronise the device).  The call itself
+ * still makes CUDA runtime calls (device and pointer queries, tensor-map encoding) and
+ * launches kernels.
  *
  * Same computation and result as inkattn_decode followed by inkattn_combine with the
- * same num_splits (0 = the heuristic), writing out/lse.  The split partials go to a
- * static device buffer of INKATTN_DECODE_NOALLOC_MAX_BYTES inside the library instead
- * of a workspace; the call allocates nothing (no cudaMalloc, cudaFree or allocating
- * library routine).
- *   - Returns INKATTN_ERR_INVALID_ARG when the partials for the resolved split count
- *     need more than INKATTN_DECODE_NOALLOC_MAX_BYTES, i.e. when
- *     inkattn_decode_workspace_bytes(p, S) exceeds it; pass a smaller num_splits.
- *   - The buffer's device address is looked up once per device, by the first call made
- *     with that device current; make that first call before any stream capture.
+ * same split count, writing out/lse: with an explicit num_splits the results are
+ * bit-identical to theirs.  The split partials go to a static device buffer of
+ * INKATTN_DECODE_NOALLOC_MAX_BYTES inside the library instead of a workspace; the call
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ *   - num_splits = 0 takes the heuristic's split count and lowers it until the partials
+ *     fit the buffer (down to 1, which needs none).
+ *   - An explicit num_splits whose partials exceed the buffer, i.e. whose
+ *     inkattn_decode_workspace_bytes(p, S) is above INKATTN_DECODE_NOALLOC_MAX_BYTES, is
+ *     rejected with INKATTN_ERR_INVALID_ARG.
+ *   - The buffer's device address belongs to a CUDA context; it is looked up with the
+ *     caller's context current and cached per context (a new context, e.g. after
+ *     cudaDeviceReset, looks it up again).  The first call in a context may load the
+ *     library's device code: make it before any stream capture.
  *   - Every call on a device shares the one buffer and it keeps the last call's
  *     contents.  Each call writes every partial it reads, so nothing needs clearing,
  *     but calls whose GPU work overlaps (on different streams, or from several host

@@ -11,6 +11,7 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <mutex>
 
 #include "../../include/inkattn.h"
@@ -20,6 +21,7 @@ namespace inkattn {
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr uint64_t kWaitLimitNsDefault = 1000000000ull;   // 1 s, as the kernels' default
 
 // ---------------------------------------------------------------- device checks
 
@@ -115,6 +117,29 @@ inkattn_status validate_attn(const inkattn_attn_params *p) {
     return INKATTN_OK;
 }
 
+// q, k_cache and v_cache are read by TMA through tensor maps, and the prefill kernel
+// multicasts each K/V tile to the two CTAs of a head pair: the maps must cover memory of
+// this GPU alone.  Each must be device memory of the current device; host memory (pinned
+// or not), managed memory and another GPU's memory reached through unified addressing are
+// rejected.  A pointer whose location the runtime cannot report is rejected too.
+inkattn_status validate_locations(const inkattn_attn_params *p) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return INKATTN_ERR_INVALID_ARG;
+    }
+    const void *ptrs[] = {p->q, p->k_cache, p->v_cache};
+    for (const void *ptr : ptrs) {
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return INKATTN_ERR_INVALID_ARG;
+        }
+        if (a.type != cudaMemoryTypeDevice || a.device != dev) return INKATTN_ERR_INVALID_ARG;
+    }
+    return INKATTN_OK;
+}
+
 AttnScalars scalars(const inkattn_attn_params &p) {
     AttnScalars s;
     s.scale = p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)kHeadDim);
@@ -123,6 +148,8 @@ AttnScalars scalars(const inkattn_attn_params &p) {
 }
 
 inkattn_status launch_status(cudaError_t e) { return e == cudaSuccess ? INKATTN_OK : INKATTN_ERR_CUDA; }
+
+}  // namespace
 
 // Decode split heuristic ([vLLM TML Inkling サポート, §低レイテンシコレクティブとカーネル
 // "FA4 Kernel"]: num_splits from batch size, TP size and KV length; TP = 1 here).
@@ -165,6 +192,8 @@ int pick_splits(const inkattn_attn_params &p, int num_sms) {
     return best;
 }
 
+namespace {
+
 size_t ws_o_bytes(const inkattn_attn_params &p, int S) {
     const size_t b = (size_t)p.N_tok * p.Hq * S * kHeadDim * 4;
     return (b + 255) & ~(size_t)255;
@@ -194,6 +223,31 @@ inkattn_status resolve_splits(const inkattn_attn_params &p, int requested, int *
 }
 
 }  // namespace
+
+size_t decode_workspace_bytes(const inkattn_attn_params &p, int S) {
+    return S > 1 ? ws_o_bytes(p, S) + ws_lse_bytes(p, S) : 0;
+}
+
+inkattn_status validate_decode_call(const inkattn_attn_params *p, int *sms) {
+    inkattn_status st = validate_attn(p);
+    if (st != INKATTN_OK) return st;
+    if ((st = validate_decode_shape(*p)) != INKATTN_OK) return st;
+    if ((st = validate_locations(p)) != INKATTN_OK) return st;
+    return check_device(sms);
+}
+
+const KernelDebug &kernel_debug() {
+    static const KernelDebug d = [] {
+        KernelDebug k{kWaitLimitNsDefault, 0};
+        if (const char *s = std::getenv("INKATTN_TEST_WAIT_LIMIT_US")) {
+            const long long us = std::atoll(s);
+            if (us >= 100 && us <= 10000000) k.wait_ns = (uint64_t)us * 1000ull;
+        }
+        if (const char *s = std::getenv("INKATTN_TEST_WITHHOLD_ARRIVAL")) k.withhold = std::atoi(s) == 1;
+        return k;
+    }();
+    return d;
+}
 
 bool make_cache_map(CUtensorMap *map, const void *base, long long rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
@@ -262,6 +316,7 @@ inkattn_status inkattn_prologue(const inkattn_prologue_params *p, void *stream) 
 inkattn_status inkattn_prefill(const inkattn_attn_params *p, void *stream) {
     inkattn_status st = validate_attn(p);
     if (st != INKATTN_OK) return st;
+    if ((st = validate_locations(p)) != INKATTN_OK) return st;
     if ((st = check_device(nullptr)) != INKATTN_OK) return st;
     if (p->N_tok == 0) return INKATTN_OK;
     CUtensorMap qmap, kmap, vmap;
@@ -292,6 +347,7 @@ inkattn_status inkattn_decode(const inkattn_attn_params *p, int num_splits, void
     if (st != INKATTN_OK) return st;
     if ((st = validate_decode_shape(*p)) != INKATTN_OK) return st;
     if (num_splits < 0 || num_splits > kDecodeMaxSplits) return INKATTN_ERR_INVALID_ARG;
+    if ((st = validate_locations(p)) != INKATTN_OK) return st;
     if ((st = check_device(nullptr)) != INKATTN_OK) return st;
     int S = 0;
     if ((st = resolve_splits(*p, num_splits, &S)) != INKATTN_OK) return st;

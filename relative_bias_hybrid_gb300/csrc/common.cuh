@@ -1,7 +1,7 @@
 // common.cuh -- device helpers shared by the inkattn kernels (sm_103a).
 //
 // Everything here is plain PTX wrapped in inline functions: mbarriers with
-// bounded waits, TMA tensor and bulk copies, clusters, mma.sync, bf16 packing, paired fp32.
+// bounded waits, TMA tensor copies, clusters, mma.sync (fp16), bf16/fp16 packing, paired fp32.
 #pragma once
 
 #include <cuda.h>
@@ -17,7 +17,8 @@ namespace inkattn {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // A device wait that has not completed after this many nanoseconds gives up,
-// records INKATTN_ERR_DEVICE_TIMEOUT and lets the kernel wind down.
+// records INKATTN_ERR_DEVICE_TIMEOUT and lets the kernel wind down.  Kernels take the
+// limit as an argument (this value unless a test of the failure path sets a shorter one).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s
 constexpr uint32_t kWaitSleepNs = 100000u;         // longest single suspension of a waiting thread
 
@@ -81,21 +82,31 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 }
 
 // Waits for the phase with the given parity to complete.  Returns false (and
-// records a timeout) if it has not completed within kWaitLimitNs, or soon after
-// *abort is set by another role of the same CTA.
+// records a timeout) if it has not completed within limit_ns, or soon after *abort
+// is set by another role of the same CTA.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t *status,
-                                          volatile int *abort) {
+                                          volatile int *abort, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (;;) {
         if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
         if (abort && *abort) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
+        if (globaltimer() - t0 > limit_ns) {
             set_status(status, INKATTN_ERR_DEVICE_TIMEOUT);
             if (abort) *abort = 1;
             return false;
         }
     }
+}
+
+// Teardown wait for asynchronous work this CTA has already issued (TMA copies landing in
+// its shared memory, tensor-core operations on its TMEM): unlike mbar_wait it does not
+// stop when another role gives up, since the CTA may release neither while that work is in
+// flight.  Still bounded by limit_ns: issued copies and MMAs complete in microseconds, and
+// a phase that needs a copy nobody issued (a peer that gave up first) never completes.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, int32_t *status,
+                                           uint64_t limit_ns) {
+    return mbar_wait(bar, parity, status, nullptr, limit_ns);
 }
 
 // ---------------------------------------------------------------- TMA
@@ -148,16 +159,30 @@ __device__ __forceinline__ void cluster_sync() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// ---------------------------------------------------------------- mma.sync
+// ---------------------------------------------------------------- mma.sync and packing
 
-// D (16x8 fp32) += A (16x16 bf16, row) * B (16x8 bf16, col)
-__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                          uint32_t b1) {
+// D (16x8 fp32) += A (16x16 fp16, row) * B (16x8 fp16, col)
+__device__ __forceinline__ void mma_16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
     asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
         "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// two floats -> packed fp16x2 (lo in the low half), round to nearest even
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// 2^-k for the k that brings m (>= 0) to at most 2^15, 1 when m is below that: a scale by
+// which values of magnitude <= m convert to fp16 without overflow (exact, being a power of 2)
+__device__ __forceinline__ float fp16_prescale(float m) {
+    const int e = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127;   // floor(log2 m) for normal m
+    const int k = e > 14 ? e - 14 : 0;
+    return __uint_as_float((uint32_t)(127 - k) << 23);
 }
 
 // two floats -> packed bf16x2 (lo in the low half), round to nearest even
@@ -210,6 +235,31 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
-
+// ---------------------------------------------------------------- 16-bit fixed-point bias
+// The relative bias is staged in shared memory as 16-bit offset-binary fixed point,
+// value = (u - 32768) * sigma, with sigma chosen per tile (or table row) from a bound on
+// |bias|, so that the staged value keeps an absolute error of at most sigma / 2
+// (16 bits over the bound) instead of fp16's 11 significant bits.
+//
+// Encoding: v = x / sigma must satisfy |v| < 32768.  Adding 1.5 * 2^23 + 32768 in fp32
+// rounds v to the nearest integer (the spacing of floats there is 1) and leaves
+// round(v) + 32768 in the low 16 bits of the result.
+constexpr float kFixMagic = 12582912.0f + 32768.0f;
+__device__ __forceinline__ float2 fix16_encode2(float2 x, float inv_sigma) {
+    return ffma2(x, make_float2(inv_sigma, inv_sigma), make_float2(kFixMagic, kFixMagic));
+}
+__device__ __forceinline__ unsigned short fix16_bits(float encoded) {
+    return (unsigned short)(__float_as_uint(encoded) & 0xFFFFu);
+}
+// The two values packed in w (low half first) as exact integers round(v): the bits are
+// placed under the exponent of 2^23 (byte permute), giving 2^23 + u, and 2^23 + 32768 is
+// subtracted exactly.
+__device__ __forceinline__ float2 fix16_decode2(uint32_t w) {
+    uint32_t lo, hi;
+    asm("prmt.b32 %0, %1, %2, 0x7610;" : "=r"(lo) : "r"(w), "r"(0x4B000000u));
+    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi) : "r"(w), "r"(0x4B000000u));
+    return fadd2(make_float2(__uint_as_float(lo), __uint_as_float(hi)),
+                 make_float2(-8421376.0f, -8421376.0f));
+}
 
 }  // namespace inkattn

@@ -24,9 +24,16 @@
 //
 // Relative bias: only tiles within rel_extent of the queries carry it (the last ones of the
 // sequence).  For such a tile the softmax warps first build, per query head, the table
-// R[t][x] = r_t . P_h[:, dlo + x] over the tile's 128 + ql distances with mma.sync (bf16
-// operands, fp32 accumulation, stored as fp16 in S units), then each thread adds its row's
-// 64 entries.
+// R[t][x] = r_t . P_h[:, dlo + x] over the tile's 128 + ql distances with mma.sync (one warp
+// per head; fp16 operands, fp32 accumulation), then each thread adds its row's 64 entries.
+// fp16 keeps 11 significant bits of P (bf16 would keep 8) and represents the bf16 r exactly;
+// r and each round of P are first scaled by powers of two that keep them inside fp16's
+// range (exact, undone on the fp32 results).  The table holds 16-bit fixed point with one
+// step per (head, token) row and round of 72 distances, sigma = (largest |entry| of that
+// part of the row) / 32000; the staged bias is within sigma / 2 of the fp32 value.
+// Normalisation: O accumulates P V with P rounded to bf16, and each tile's largest P (its
+// row maximum's) is the dominant term whose bf16 rounding matters; that rounding error is
+// added to the row's normaliser, while the LSE uses the sum of the fp32 P.
 //
 // The softmax runs in the log2 domain with the lazy rescale of the prefill kernel (O is
 // rescaled only when the running maximum grows by more than 8).  The epilogue writes O / l
@@ -49,9 +56,10 @@ constexpr int kTabRows = kDecodeMaxRows;   // g * ql <= 128
 
 constexpr int kOffQ = 0;
 constexpr int kOffKV = 32768;
-constexpr int kOffTab = kOffKV + kSlots * kSlotBytes;              // fp16 [g][ql][kTabW]
+constexpr int kOffTab = kOffKV + kSlots * kSlotBytes;              // 16-bit fixed point [g][ql][kTabW]
 constexpr int kOffXchg = kOffTab + kTabRows * kTabW * 2;           // row maxima / sums
-constexpr int kOffBar = kOffXchg + 3 * 2 * kRows * 4;
+constexpr int kOffTsig = kOffXchg + 3 * 2 * kRows * 4;             // fp32 steps [g][ql][2 rounds]
+constexpr int kOffBar = kOffTsig + kTabRows * 2 * 4;
 
 // mbarrier indices, laid out from the slot count
 enum Bar {
@@ -80,6 +88,8 @@ struct DecTcArgs {
     float *ws_o;
     float *ws_lse;
     long long kv_rows;      // rows of the cache tensor maps (OOB row = this)
+    uint64_t wait_ns;       // limit of every bounded wait
+    int withhold;           // failure-path test: the softmax withholds its first P arrival
 };
 
 }  // namespace
@@ -139,7 +149,7 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffBar + B_COUNT * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffBar + B_COUNT * 8 + 4);
     auto wwait = [&](uint32_t addr, uint32_t parity) -> bool {
-        const bool r = mbar_wait(addr, parity, p.dev_status, abort_flag);
+        const bool r = mbar_wait(addr, parity, p.dev_status, abort_flag, A.wait_ns);
         return __all_sync(0xffffffffu, r);
     };
 
@@ -199,8 +209,10 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
                           : lb < p.max_blocks_per_seq ? __ldg(p.block_table + (size_t)b * p.max_blocks_per_seq + lb)
                           : -1;
             }
-            if (L >= kSlots && !wwait(bar(B_KV_EMPTY + slot), ((L / kSlots) - 1) & 1))
+            if (L >= kSlots && !wwait(bar(B_KV_EMPTY + slot), ((L / kSlots) - 1) & 1)) {
+                --kv_loads;                                  // not issued
                 return false;
+            }
             if (lane == 0) {
                 const uint32_t dst = s_base + kOffKV + slot * kSlotBytes;
                 const uint32_t fb = bar(B_KV_FULL + slot);
@@ -227,11 +239,12 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
             if (ok) ok = load_kv(n - 1, 1);
         }
         if (ok) ok = load_kv(N - 1, 1);
-        // nothing may still be landing in shared memory when the CTA tears down
+        // nothing may still be landing in shared memory when the CTA tears down, also when a
+        // role gave up: the copies issued and not yet consumed are the last kSlots
         if (lane == 0) {
-            mbar_wait(bar(B_Q), 0, p.dev_status, abort_flag);
+            mbar_drain(bar(B_Q), 0, p.dev_status, A.wait_ns);
             for (int L = max(0, kv_loads - kSlots); L < kv_loads; ++L)
-                mbar_wait(bar(B_KV_FULL + L % kSlots), (L / kSlots) & 1, p.dev_status, abort_flag);
+                mbar_drain(bar(B_KV_FULL + L % kSlots), (L / kSlots) & 1, p.dev_status, A.wait_ns);
         }
     } else if (warp == 1) {
         // ================================ MMA issuer ================================
@@ -293,9 +306,11 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
             if (n >= 1) ok = issue_pv(n - 1);
         }
         if (ok) ok = issue_pv(N - 1);
+        // every MMA of this CTA has completed before TMEM is released (also after a role gave up)
         tc::commit(bar(B_DRAIN));
         __syncwarp();
-        (void)wwait(bar(B_DRAIN), 0);
+        (void)mbar_drain(bar(B_DRAIN), 0, p.dev_status, A.wait_ns);
+        __syncwarp();
     } else {
         // ================================ softmax ================================
         const int quad = warp & 3;
@@ -308,7 +323,8 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
         const int hh = a - t * g;
         const int i_pos = pos0 + t;
         const int cb = 64 * hw;
-        __half *tab = reinterpret_cast<__half *>(smem + kOffTab);
+        unsigned short *tab = reinterpret_cast<unsigned short *>(smem + kOffTab);
+        float *tsig = reinterpret_cast<float *>(smem + kOffTsig);
         float *xchg = reinterpret_cast<float *>(smem + kOffXchg);
         int pair_phase = 0;
         auto pair_sync = [&]() -> bool {
@@ -320,7 +336,8 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
         int band_round = 0;
         bool ok = true;
 
-        float m_run = -INFINITY, l_run = 0.f;
+        float m_run = -INFINITY, l_run = 0.f;   // l_run: sum of the fp32 P (for the LSE)
+        float lc_run = 0.f;                      // bf16 rounding of each tile's largest P (normaliser)
         auto wait_pv = [&](int m) -> bool { return wwait(bar(B_PV_DONE + (m & 1)), (m >> 1) & 1); };
         for (int n = 0; n < N; ++n) {
             const int j0 = kr_lo + n * kKeys;
@@ -333,53 +350,111 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
                     const int h = hk * g + hq;
                     const float *Ph = p.P + (size_t)h * p.rel_extent * 32;
                     const inkattn_bf16 *rh = p.r + ((size_t)start * p.Hq + h) * 32;
-                    // d_r = 32 (checked on the host): two k steps of 16
-                    uint32_t rf[2][4];
+                    // d_r = 32 (checked on the host): two k steps of 16.  A fragments: tokens gq
+                    // (e even) and gq + 8 (e odd), each lane 8 of a token's 32 features; the four
+                    // lanes of a token (tq = 0..3) hold all of them.
+                    float rv[2][4][2];
+                    float rm[2] = {0.f, 0.f};
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int tt = gq + ((e & 1) << 3);
                             const int col = kk * 16 + 2 * tq + ((e >> 1) << 3);
-                            rf[kk][e] = tt < q_len
+                            const uint32_t w2 = tt < q_len
                                 ? __ldg(reinterpret_cast<const uint32_t *>(rh + (size_t)tt * 32 * p.Hq + col))
                                 : 0u;
+                            rv[kk][e][0] = bf16_lo(w2);
+                            rv[kk][e][1] = bf16_hi(w2);
+                            rm[e & 1] = fmaxf(rm[e & 1], fmaxf(fabsf(rv[kk][e][0]), fabsf(rv[kk][e][1])));
                         }
+                    float rsc[2], rusc[2];                     // per token row: fp16 prescale and its inverse
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        rm[i] = fmaxf(rm[i], __shfl_xor_sync(0xffffffffu, rm[i], 1));
+                        rm[i] = fmaxf(rm[i], __shfl_xor_sync(0xffffffffu, rm[i], 2));
+                        rsc[i] = fp16_prescale(rm[i]);
+                        rusc[i] = 1.f / rsc[i];
+                    }
+                    uint32_t rf[2][4];
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            rf[kk][e] = pack_f16(rv[kk][e][0] * rsc[e & 1], rv[kk][e][1] * rsc[e & 1]);
                     // the table in two rounds of nine groups of 8 distances: a round's P loads
                     // are all issued before its first MMA, so the table waits for two L2 round
                     // trips (the first also covers r above), not one per group; while K/V
-                    // streams saturate the memory system a round trip costs thousands of cycles
+                    // streams saturate the memory system a round trip costs thousands of cycles.
+                    // Each round's results set the steps of its part of the rows and are stored.
                     constexpr int kGrp = 9;
-                    static_assert((kTabW / 8) % kGrp == 0, "whole rounds");
-                    for (int nt0 = 0; nt0 < kTabW / 8; nt0 += kGrp) {
-                        uint32_t pb[kGrp][2][2];
+                    static_assert(kTabW / 8 == 2 * kGrp, "two rounds");
+#pragma unroll
+                    for (int rd = 0; rd < 2; ++rd) {
+                        float res[kGrp][4];
+                        float2 pl[kGrp][2], ph[kGrp][2];
+                        float pmx = 0.f;
 #pragma unroll
                         for (int u = 0; u < kGrp; ++u) {
-                            const int dl = dlo + (nt0 + u) * 8 + gq;
+                            const int dl = dlo + (rd * kGrp + u) * 8 + gq;
                             const bool dv = dl >= 0 && dl < p.rel_extent;
 #pragma unroll
                             for (int kk = 0; kk < 2; ++kk) {
-                                pb[u][kk][0] = pb[u][kk][1] = 0u;
-                                if (!dv) continue;
                                 const int e0 = kk * 16 + 2 * tq;
-                                const float2 lo = __ldg(reinterpret_cast<const float2 *>(Ph + (size_t)dl * 32 + e0));
-                                const float2 hi = __ldg(reinterpret_cast<const float2 *>(Ph + (size_t)dl * 32 + e0 + 8));
-                                pb[u][kk][0] = pack_bf16(lo.x, lo.y);
-                                pb[u][kk][1] = pack_bf16(hi.x, hi.y);
+                                pl[u][kk] = dv ? __ldg(reinterpret_cast<const float2 *>(Ph + (size_t)dl * 32 + e0))
+                                               : make_float2(0.f, 0.f);
+                                ph[u][kk] = dv ? __ldg(reinterpret_cast<const float2 *>(Ph + (size_t)dl * 32 + e0 + 8))
+                                               : make_float2(0.f, 0.f);
+                                pmx = fmaxf(pmx, fmaxf(fmaxf(fabsf(pl[u][kk].x), fabsf(pl[u][kk].y)),
+                                                       fmaxf(fabsf(ph[u][kk].x), fabsf(ph[u][kk].y))));
                             }
                         }
+                        // one prescale for the round's P (magnitudes order like their bit patterns)
+                        pmx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(pmx)));
+                        const float psc = fp16_prescale(pmx), pusc = 1.f / psc;
 #pragma unroll
                         for (int u = 0; u < kGrp; ++u) {
                             float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                            for (int kk = 0; kk < 2; ++kk) mma_16816(acc, rf[kk], pb[u][kk][0], pb[u][kk][1]);
-                            const int c = (nt0 + u) * 8 + 2 * tq;
-                            if (gq < q_len)
-                                *reinterpret_cast<__half2 *>(tab + ((size_t)hq * A.ql + gq) * kTabW + c) =
-                                    __floats2half2_rn(acc[0] * inv_scale, acc[1] * inv_scale);
-                            if (gq + 8 < q_len)
-                                *reinterpret_cast<__half2 *>(tab + ((size_t)hq * A.ql + gq + 8) * kTabW + c) =
-                                    __floats2half2_rn(acc[2] * inv_scale, acc[3] * inv_scale);
+                            for (int kk = 0; kk < 2; ++kk)
+                                mma_16816_f16(acc, rf[kk], pack_f16(pl[u][kk].x * psc, pl[u][kk].y * psc),
+                                              pack_f16(ph[u][kk].x * psc, ph[u][kk].y * psc));
+                            res[u][0] = acc[0] * (pusc * rusc[0]);
+                            res[u][1] = acc[1] * (pusc * rusc[0]);
+                            res[u][2] = acc[2] * (pusc * rusc[1]);
+                            res[u][3] = acc[3] * (pusc * rusc[1]);
+                        }
+                        // each token row's largest |entry| in this round (its four lanes hold all
+                        // of its columns here)
+                        float mx[2] = {0.f, 0.f};
+#pragma unroll
+                        for (int u = 0; u < kGrp; ++u) {
+                            mx[0] = fmaxf(mx[0], fmaxf(fabsf(res[u][0]), fabsf(res[u][1])));
+                            mx[1] = fmaxf(mx[1], fmaxf(fabsf(res[u][2]), fabsf(res[u][3])));
+                        }
+                        float enc[2];
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
+                            mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
+                            const float mm = fmaxf(mx[i], 1e-30f);
+                            const int tt = gq + 8 * i;
+                            // the step in S units (the table holds R / scale); entries encode to
+                            // R * (32000 / max) in [-32000, 32000]
+                            if (tq == 0 && tt < q_len) tsig[(hq * A.ql + tt) * 2 + rd] = mm * inv_scale * (1.f / 32000.f);
+                            enc[i] = 32000.f / mm;
+                        }
+#pragma unroll
+                        for (int u = 0; u < kGrp; ++u) {
+                            const int c = (rd * kGrp + u) * 8 + 2 * tq;
+#pragma unroll
+                            for (int i = 0; i < 2; ++i) {
+                                const int tt = gq + 8 * i;
+                                if (tt >= q_len) continue;
+                                const float2 v = fix16_encode2(make_float2(res[u][2 * i], res[u][2 * i + 1]), enc[i]);
+                                *reinterpret_cast<uint32_t *>(tab + ((size_t)hq * A.ql + tt) * kTabW + c) =
+                                    (__float_as_uint(v.x) & 0xFFFFu) | (__float_as_uint(v.y) << 16);
+                            }
                         }
                     }
                 }
@@ -400,9 +475,14 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
             if (band) {
                 if (valid_row) {
                     // column b of the tile is at distance i - j = dlo + (t + 127 - b)
-                    const __half *trow = tab + ((size_t)hh * A.ql + t) * kTabW + t + (kKeys - 1) - cb;
+                    const int c0 = t + (kKeys - 1) - cb;             // table column of key column cb
+                    const unsigned short *trow = tab + ((size_t)hh * A.ql + t) * kTabW + c0;
+                    const float sg0 = tsig[(hh * A.ql + t) * 2], sg1 = tsig[(hh * A.ql + t) * 2 + 1];
 #pragma unroll
-                    for (int bb = 0; bb < 64; ++bb) s[bb] += __half2float(trow[-bb]);
+                    for (int bb = 0; bb < 64; ++bb) {
+                        const float q = __uint_as_float(0x4B000000u | (uint32_t)trow[-bb]) - 8421376.0f;
+                        s[bb] = fmaf(q, c0 - bb < 72 ? sg0 : sg1, s[bb]);   // columns [0, 72): first round
+                    }
                 }
                 mbar_arrive(bar(B_TAB_FREE));
                 ++band_round;
@@ -436,6 +516,7 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
             xc[hw * 128 + a] = mx;
             if (!(ok = pair_sync())) break;
             mx = fmaxf(mx, xc[(1 - hw) * 128 + a]);
+            const float mx_raw = mx;                             // the row's largest logit of the tile (S units)
             mx = mx == -INFINITY ? -INFINITY : mx * c_qk;        // log2 units
             const bool need = mx > m_run + 8.f;
             if (__any_sync(0xffffffffu, need)) {
@@ -456,10 +537,16 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
                     tc::wait_st();
                 }
                 l_run *= corr;
+                lc_run *= corr;
                 m_run = m_new;
             }
             const float ref = m_run == -INFINITY ? 0.f : m_run;
             const float2 cq = make_float2(c_qk, c_qk), nref = make_float2(-ref, -ref);
+            if (hw == 0 && mx_raw != -INFINITY) {
+                // the tile's largest P of this row, computed as its element is, and its bf16 rounding
+                const float pm = fast_exp2(fmaf(mx_raw, c_qk, -ref));
+                lc_run += bf16_lo(pack_bf16(pm, 0.f)) - pm;
+            }
             float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                             make_float2(0.f, 0.f)};
             uint32_t pk[32];
@@ -475,17 +562,21 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
             l_run += l2.x + l2.y;
             tc::wait_st();
             tc::fence_before();
-            mbar_arrive(bar(B_P_FULL + (n & 1)));
+            if (!(A.withhold && n == 0)) mbar_arrive(bar(B_P_FULL + (n & 1)));
         }
         // epilogue: the row sum of both halves, then O / l for this thread's 64 columns
+        // the column-half 0 thread of a row alone holds the correction (lc_run is 0 in the other)
+        // and alone writes the LSE: it publishes l + lc, the other thread l
         float *xl = xchg + 512;
-        xl[hw * 128 + a] = l_run;
+        xl[hw * 128 + a] = l_run + lc_run;
         if (ok) ok = pair_sync();
-        const float l_tot = l_run + xl[(1 - hw) * 128 + a];
+        const float l_other = xl[(1 - hw) * 128 + a];
+        const float l_tot = l_run + l_other;                  // the fp32 sum (read by half 0 only)
+        const float l_norm = l_run + lc_run + l_other;        // normaliser of P V's bf16 P
         if (ok) ok = wait_pv(N - 1);
         if (ok) {
             tc::fence_after();
-            const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+            const float inv = l_norm > 0.f ? 1.f / l_norm : 0.f;
             const size_t qrow = (size_t)(start + t) * p.Hq + hk * g + hh;
             const float ref = m_run == -INFINITY ? 0.f : m_run;
             const float lse_nat = l_tot > 0.f ? (ref + log2f(l_tot)) * 0.6931471805599453f : -INFINITY;
@@ -545,6 +636,8 @@ cudaError_t launch_decode_tc(const inkattn_attn_params &p, const AttnScalars &s,
     a.ws_o = ws_o;
     a.ws_lse = ws_lse;
     a.kv_rows = (long long)p.num_blocks * p.Hkv * kBlock;
+    a.wait_ns = kernel_debug().wait_ns;
+    a.withhold = kernel_debug().withhold;
     cudaError_t err = cudaFuncSetAttribute(k_decode_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (err != cudaSuccess) return err;
     dim3 grid(num_splits, p.Hkv, p.B);

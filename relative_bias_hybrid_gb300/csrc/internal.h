@@ -5,6 +5,8 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
 
 #include "../../include/inkattn.h"
 
@@ -12,6 +14,25 @@ namespace inkattn {
 
 constexpr int kHeadDim = 128;
 constexpr int kBlock = 64;          // paged-cache block (tokens)
+
+// Settings of the bounded device waits, read once per process.  In normal use every wait
+// gives up after 1 s and nothing is withheld.  A test of the failure path sets the
+// environment variables INKATTN_TEST_WAIT_LIMIT_US (a shorter limit, 100 us .. 10 s) and
+// INKATTN_TEST_WITHHOLD_ARRIVAL=1 (the attention kernels' softmax withholds its first
+// arrival on the barrier the MMA warp waits on before P V, so that wait runs out and the
+// kernel winds down through its error path).
+struct KernelDebug {
+    uint64_t wait_ns;
+    int withhold;
+};
+const KernelDebug &kernel_debug();
+
+// Host checks shared by the entry points (api.cu).  validate_decode_call makes, in order,
+// the checks inkattn_decode makes before it resolves the split count: the params, the
+// decode shape, where q / k_cache / v_cache live, and the device (its SM count to *sms).
+inkattn_status validate_decode_call(const inkattn_attn_params *p, int *sms);
+int pick_splits(const inkattn_attn_params &p, int num_sms);
+size_t decode_workspace_bytes(const inkattn_attn_params &p, int S);   // 0 when S <= 1
 
 // Resolved per-call scalars of an attention call (host-computed).
 struct AttnScalars {

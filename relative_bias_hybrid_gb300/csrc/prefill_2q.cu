@@ -20,7 +20,9 @@
 //
 // The softmax runs in the log2 domain with a lazy rescale (O is rescaled only when the row
 // maximum grows by more than 8); column pairs use paired fp32 instructions, and every exp2
-// goes through the special-function unit.
+// goes through the special-function unit.  The bf16 rounding error of each tile's largest P
+// (a row's dominant term once P V rounds P to bf16) is added to the row's normaliser; the
+// LSE uses the sum of the fp32 P.
 #include "common.cuh"
 #include "internal.h"
 #include "tcgen05.cuh"
@@ -39,11 +41,20 @@ constexpr int kOffQ = 0;                   // Q_A, Q_B: 32 KB each
 constexpr int kOffKV = 65536;
 constexpr int kOffBar = kOffKV + kSlots * kSlotBytes;
 
+// mbarrier indices, laid out from the slot count so that no two ranges overlap
 enum Bar {
-    B_Q = 0, B_KV_FULL = 1, B_KV_EMPTY = 4, B_S_FULL = 7, B_P_FULL = 9, B_PV_DONE = 11,
-    B_DRAIN = 13, B_COUNT = 14
+    B_Q = 0,
+    B_KV_FULL = 1,
+    B_KV_EMPTY = B_KV_FULL + kSlots,
+    B_S_FULL = B_KV_EMPTY + kSlots,
+    B_P_FULL = B_S_FULL + 2,
+    B_PV_DONE = B_P_FULL + 2,
+    B_DRAIN = B_PV_DONE + 2,
+    B_COUNT = B_DRAIN + 1
 };
 constexpr int kSmem = kOffBar + B_COUNT * 8 + 16;
+static_assert(kSmem <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
+static_assert(kOffKV % 1024 == 0 && kOffBar % 8 == 0, "alignment of the regions");
 
 constexpr uint32_t kTmemO = 0, kTmemS = 256;
 
@@ -52,6 +63,8 @@ struct Tc2Args {
     float scale;
     int n_pairs_max;        // gridDim.y
     long long kv_rows;
+    uint64_t wait_ns;       // limit of every bounded wait
+    int withhold;           // failure-path test: tile A's softmax withholds its first P arrival
 };
 
 }  // namespace
@@ -103,7 +116,7 @@ k_prefill_2q(const Tc2Args A, const __grid_constant__ CUtensorMap qmap,
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffBar + B_COUNT * 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffBar + B_COUNT * 8 + 4);
     auto wwait = [&](uint32_t addr, uint32_t parity) -> bool {
-        const bool r = mbar_wait(addr, parity, p.dev_status, abort_flag);
+        const bool r = mbar_wait(addr, parity, p.dev_status, abort_flag, A.wait_ns);
         return __all_sync(0xffffffffu, r);
     };
 
@@ -162,8 +175,10 @@ k_prefill_2q(const Tc2Args A, const __grid_constant__ CUtensorMap qmap,
                           : lb < p.max_blocks_per_seq ? __ldg(p.block_table + (size_t)b * p.max_blocks_per_seq + lb)
                           : -1;
             }
-            if (L >= kSlots && !wwait(bar(B_KV_EMPTY + slot), ((L / kSlots) - 1) & 1))
+            if (L >= kSlots && !wwait(bar(B_KV_EMPTY + slot), ((L / kSlots) - 1) & 1)) {
+                --kv_loads;                                  // not issued
                 return false;
+            }
             if (lane == 0) {
                 const uint32_t dst = s_base + kOffKV + slot * kSlotBytes;
                 const uint32_t fb = bar(B_KV_FULL + slot);
@@ -187,10 +202,12 @@ k_prefill_2q(const Tc2Args A, const __grid_constant__ CUtensorMap qmap,
             ok = load_kv(n, 0);
             if (ok) ok = load_kv(n, 1);
         }
+        // nothing may still be landing in shared memory when the CTA tears down, also when a
+        // role gave up: the copies issued and not yet consumed are the last kSlots
         if (lane == 0) {
-            mbar_wait(bar(B_Q), 0, p.dev_status, abort_flag);
+            mbar_drain(bar(B_Q), 0, p.dev_status, A.wait_ns);
             for (int L = max(0, kv_loads - kSlots); L < kv_loads; ++L)
-                mbar_wait(bar(B_KV_FULL + L % kSlots), (L / kSlots) & 1, p.dev_status, abort_flag);
+                mbar_drain(bar(B_KV_FULL + L % kSlots), (L / kSlots) & 1, p.dev_status, A.wait_ns);
         }
     } else if (warp == 1) {
         // ================================ MMA issuer ================================
@@ -278,9 +295,11 @@ k_prefill_2q(const Tc2Args A, const __grid_constant__ CUtensorMap qmap,
                 release(kslot, klast);
             }
         }
+        // every MMA of this CTA has completed before TMEM is released (also after a role gave up)
         tc::commit(bar(B_DRAIN));
         __syncwarp();
-        (void)wwait(bar(B_DRAIN), 0);
+        (void)mbar_drain(bar(B_DRAIN), 0, p.dev_status, A.wait_ns);
+        __syncwarp();
     } else {
         // ================================ softmax ================================
         const int x = (warp - 2) >> 2;                        // tile A or B
@@ -295,7 +314,8 @@ k_prefill_2q(const Tc2Args A, const __grid_constant__ CUtensorMap qmap,
         const uint32_t sbuf = tmem + kTmemS + x * 128 + lane_off;
         const uint32_t obuf = tmem + kTmemO + x * 128 + lane_off;
         bool ok = true;
-        float m_run = -INFINITY, l_run = 0.f;
+        float m_run = -INFINITY, l_run = 0.f;   // l_run: sum of the fp32 P (for the LSE)
+        float lc_run = 0.f;                      // bf16 rounding of each tile's largest P (normaliser)
         int kx = 0;
         for (int n = 0; n < N && tile_valid; ++n) {
             const int t = t_top - n;
@@ -333,6 +353,7 @@ k_prefill_2q(const Tc2Args A, const __grid_constant__ CUtensorMap qmap,
                 }
                 mx = fmax3(mx, fmaxf(m0, sc[31]), fmaxf(m1, sc[63]));
             }
+            const float mx_raw = mx;                          // the row's largest logit of the tile (S units)
             mx = mx == -INFINITY ? -INFINITY : mx * c_qk;     // log2 units
             const bool need = mx > m_run + 8.f;
             if (__any_sync(0xffffffffu, need)) {
@@ -355,12 +376,18 @@ k_prefill_2q(const Tc2Args A, const __grid_constant__ CUtensorMap qmap,
                     tc::wait_st();
                 }
                 l_run *= corr;
+                lc_run *= corr;
                 m_run = m_new;
             }
             // pass 2: P = exp2(S * c - m) per 32 columns; P chunk c (bf16 pairs) goes to packed
             // columns [16 c, 16 c + 16), which only overlap S columns already read
             const float ref = m_run == -INFINITY ? 0.f : m_run;
             const float2 cq = make_float2(c_qk, c_qk), nref = make_float2(-ref, -ref);
+            if (mx_raw != -INFINITY) {
+                // the tile's largest P of this row, computed as its element is, and its bf16 rounding
+                const float pm = fast_exp2(fmaf(mx_raw, c_qk, -ref));
+                lc_run += bf16_lo(pack_bf16(pm, 0.f)) - pm;
+            }
             float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                             make_float2(0.f, 0.f)};
             float scn[32];                                   // the next chunk, loading
@@ -391,14 +418,14 @@ k_prefill_2q(const Tc2Args A, const __grid_constant__ CUtensorMap qmap,
             l_run += l2.x + l2.y;
             tc::wait_st();
             tc::fence_before();
-            mbar_arrive(bar(B_P_FULL + x));
+            if (!(A.withhold && x == 0 && kx == 0)) mbar_arrive(bar(B_P_FULL + x));
             ++kx;
         }
         // epilogue: O / l for this row
         if (ok && tile_valid && kx > 0) ok = wwait(bar(B_PV_DONE + x), (kx - 1) & 1);
         if (ok && tile_valid && kx > 0) {
             tc::fence_after();
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            const float inv = (l_run + lc_run) > 0.f ? 1.f / (l_run + lc_run) : 0.f;
             const bool valid = row < q_len;
             const size_t qrow = (size_t)(start + row) * p.Hq + h;
             uint32_t o[32];
@@ -448,6 +475,8 @@ cudaError_t launch_prefill_2q(const inkattn_attn_params &p, const AttnScalars &s
     const int n_qtiles = (p.max_seqlen_q + kRows - 1) / kRows;
     a.n_pairs_max = (n_qtiles + 1) / 2;
     a.kv_rows = (long long)p.num_blocks * p.Hkv * kBlock;
+    a.wait_ns = kernel_debug().wait_ns;
+    a.withhold = kernel_debug().withhold;
     cudaError_t err = cudaFuncSetAttribute(k_prefill_2q, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (err != cudaSuccess) return err;
     dim3 grid(p.Hq, a.n_pairs_max, p.B);

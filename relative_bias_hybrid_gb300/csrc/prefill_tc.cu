@@ -39,12 +39,27 @@
 // R^T[x][a] = P_h[:, D_n + x] . r_a (M = 128 distances, N = 128 rows, K = d_r) into TMEM;
 // value x of row a is the bias of key column a - x of tile n when x <= a and of column
 // a + 128 - x of tile n + 1 when x > a.  The thread of TMEM lane x writes both into
-// 128-entry fp16 rows indexed by key column, one per tile, alternating between two
+// 128-entry 16-bit rows indexed by key column, one per tile, alternating between two
 // buffers: tile n's row is complete once C_n is moved, and C_{n+1} can be computed as soon
 // as C_n has left TMEM, so the chunks run ahead of the softmax, which reads its bias row
 // with sequential 16-byte loads.  Tiles farther than rel_extent skip all of this.
 // The bias MMA takes bf16 operands: r as given, and P_h (times 1/scale, so that R is in
 // the units of S) split into high and low bf16 parts, two products accumulated in fp32.
+// The bias rows hold 16-bit fixed point (offset binary) with one step per chunk:
+// |R[a][delta]| <= |r_a| |P_h[delta]| (Cauchy-Schwarz), so with B_c = max_a |r_a| times the
+// largest |P_h[delta]| of chunk c's window, sigma_c = B_c / 32000 bounds every value of
+// chunk c with room for rounding.  Row a of tile n holds chunk n's values in columns b <= a
+// and chunk n - 1's in columns b > a, so the softmax takes the step of each column from the
+// side of the diagonal it is on.  The staged bias is within sigma / 2 of the fp32 value, 16
+// bits below the bound; fp16 (11 significant bits) moved logits of |bias| ~ 15 by ~4e-3.
+// Each warp publishes its part of B_c when it stores chunk c's window, before its arrival
+// on the barrier that the chunk's MMA waits on, so B_c is complete before the chunk is.
+//
+// Normalisation: O accumulates P V with P rounded to bf16.  With the lazy rescale the
+// largest P of a tile is rarely exactly a power of two, and when it dominates the row,
+// dividing by the sum of the unrounded P leaves its bf16 rounding (up to 2^-9 of |o|) in the
+// output.  So the rounding error of each tile's largest P is added to the row's normaliser
+// (a few instructions per tile); the LSE uses the sum of the fp32 P.
 //
 // The softmax runs in the log2 domain and keeps a stale row maximum unless the new one
 // exceeds it by more than 8 (P stays below 2^8); only then is O rescaled in TMEM.  Column
@@ -78,14 +93,34 @@ constexpr int kOffRfeat = kOffPwLo + kWin64;                    // relative feat
 constexpr int kOffStage = kOffRfeat + kWin64;                   // two bias buffers
 constexpr int kStageBuf = kRows * kStageStride;                 // halves per bias buffer
 constexpr int kOffXchg = kOffStage + 2 * kStageBuf * 2;         // row maxima / sums of the two halves
-constexpr int kOffBar = kOffXchg + 3 * 2 * kRows * 4;
+constexpr int kOffNorm = kOffXchg + 3 * 2 * kRows * 4;          // bias bounds and tile scales (below)
+constexpr int kOffBar = kOffNorm + 64;
+// kOffNorm: float wmax[2][4] (per window parity and bias warp: max |P_h row|^2 of the window,
+// S units), float rmax[4] (per bias warp: max |r row|^2), float sigma[4] (the fixed-point
+// step of chunk c in entry (c + 1) & 3, c >= -1)
 
+// mbarrier indices, laid out from the slot count so that no two ranges overlap
 enum Bar {
-    B_Q = 0, B_KV_FULL = 1, B_KV_EMPTY = 4, B_S_FULL = 7, B_P_FULL = 9, B_PV_DONE = 11,
-    B_R_FULL = 13, B_R_EMPTY = 14, B_PW_READY = 15, B_DRAIN = 16, B_PAIR = 17,
-    B_STAGE_FULL = 21, B_STAGE_EMPTY = 23, B_BDRAIN = 25, B_COUNT = 26
+    B_Q = 0,
+    B_KV_FULL = 1,
+    B_KV_EMPTY = B_KV_FULL + kSlots,
+    B_S_FULL = B_KV_EMPTY + kSlots,
+    B_P_FULL = B_S_FULL + 2,
+    B_PV_DONE = B_P_FULL + 2,
+    B_R_FULL = B_PV_DONE + 2,
+    B_R_EMPTY = B_R_FULL + 1,
+    B_PW_READY = B_R_EMPTY + 1,
+    B_DRAIN = B_PW_READY + 1,
+    B_PAIR = B_DRAIN + 1,
+    B_STAGE_FULL = B_PAIR + 4,
+    B_STAGE_EMPTY = B_STAGE_FULL + 2,
+    B_BDRAIN = B_STAGE_EMPTY + 2,
+    B_NORM = B_BDRAIN + 1,
+    B_COUNT = B_NORM + 1
 };
 constexpr int kSmem = kOffBar + B_COUNT * 8 + 16;
+static_assert(kSmem <= 232448, "dynamic shared memory above the 227 KB a CTA may use");
+static_assert(kOffBar % 8 == 0 && kOffKV % 1024 == 0 && kOffStage % 16 == 0, "alignment of the regions");
 
 constexpr uint32_t kTmemO = 0, kTmemS0 = 128, kTmemR = 384;
 
@@ -94,6 +129,8 @@ struct TcArgs {
     float scale;            // softmax scale
     int n_qtiles_max;       // gridDim.y
     long long kv_rows;      // rows of the cache tensor maps (OOB row = this)
+    uint64_t wait_ns;       // limit of every bounded wait
+    int withhold;           // failure-path test: the softmax withholds its first P arrival
 };
 
 // byte offset of 16-byte chunk j of row r in a K-major tile of 64-byte rows with the 64-byte
@@ -157,7 +194,7 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
     // every lane waits; the outcome is made uniform over the warp, because the warps that
     // act on it next issue warp-collective (.sync.aligned) tcgen05 instructions
     auto wwait = [&](uint32_t addr, uint32_t parity) -> bool {
-        const bool r = mbar_wait(addr, parity, p.dev_status, abort_flag);
+        const bool r = mbar_wait(addr, parity, p.dev_status, abort_flag, A.wait_ns);
         return __all_sync(0xffffffffu, r);
     };
 
@@ -179,6 +216,7 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         mbar_init(bar(B_PW_READY), 128);
         mbar_init(bar(B_DRAIN), 1);
         mbar_init(bar(B_BDRAIN), 1);
+        mbar_init(bar(B_NORM), 128);
         for (int q = 0; q < 4; ++q) mbar_init(bar(B_PAIR + q), 64);
         *abort_flag = 0;
         fence_mbar_init();
@@ -230,8 +268,10 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                         : lb < p.max_blocks_per_seq ? __ldg(p.block_table + (size_t)b * p.max_blocks_per_seq + lb)
                         : -1;
             }
-            if (L >= kSlots && !wwait(bar(B_KV_EMPTY + slot), ((L / kSlots) - 1) & 1))
+            if (L >= kSlots && !wwait(bar(B_KV_EMPTY + slot), ((L / kSlots) - 1) & 1)) {
+                --kv_loads;                                  // not issued
                 return false;
+            }
             if (lane == 0) {
                 const uint32_t dst = s_base + kOffKV + slot * kSlotBytes;
                 const uint32_t fb = bar(B_KV_FULL + slot);
@@ -266,11 +306,13 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             if (ok) ok = load_kv(n - 1, 1);
         }
         if (ok) ok = load_kv(N - 1, 1);
-        // nothing may still be landing in shared memory when the CTA tears down
+        // nothing may still be landing in shared memory when the CTA tears down, also when a
+        // role gave up: every copy issued and not yet consumed is waited for (a slot is only
+        // reloaded after its previous copy was consumed, so those are the last kSlots)
         if (lane == 0) {
-            mbar_wait(bar(B_Q), 0, p.dev_status, abort_flag);
+            mbar_drain(bar(B_Q), 0, p.dev_status, A.wait_ns);
             for (int L = max(0, kv_loads - kSlots); L < kv_loads; ++L)
-                mbar_wait(bar(B_KV_FULL + L % kSlots), (L / kSlots) & 1, p.dev_status, abort_flag);
+                mbar_drain(bar(B_KV_FULL + L % kSlots), (L / kSlots) & 1, p.dev_status, A.wait_ns);
         }
       } else if (warp == kWarpMma) {
         // ================================ MMA issuer ================================
@@ -349,10 +391,11 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             if (n >= 1) ok = issue_pv(n - 1);
         }
         if (ok) ok = issue_pv(N - 1);
-        // every MMA of this CTA has completed before TMEM is released
+        // every MMA of this CTA has completed before TMEM is released (also after a role gave up)
         tc::commit(bar(B_DRAIN));
         __syncwarp();
-        (void)wwait(bar(B_DRAIN), 0);
+        (void)mbar_drain(bar(B_DRAIN), 0, p.dev_status, A.wait_ns);
+        __syncwarp();
       }
     } else if (warp < kWarpSoftmax) {
         // ============================== relative bias ==============================
@@ -373,8 +416,11 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         const int x = 32 * w + lane;
         const uint32_t lane_off = (uint32_t)(w * 32) << 16;
         bool ok = true;
+        float *wmax = reinterpret_cast<float *>(smem + kOffNorm);       // [2][4]
+        float *rmax = wmax + 8;                                          // [4]
+        float *sigma_s = wmax + 12;                                      // [4]
         if (n_band > 0) {
-            // row x's relative features (bf16 as given)
+            // row x's relative features (bf16 as given), and the largest |r_a|^2 of each warp
             {
                 const int row = row0 + x;
                 uint4 u[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
@@ -384,8 +430,20 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
 #pragma unroll
                     for (int j = 0; j < 4; ++j) u[j] = __ldg(src + j);
                 }
+                float n2 = 0.f;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4 *>(smem + kOffRfeat + sw64_chunk(x, j)) = u[j];
+                for (int j = 0; j < 4; ++j) {
+                    *reinterpret_cast<uint4 *>(smem + kOffRfeat + sw64_chunk(x, j)) = u[j];
+                    const uint32_t wd[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        n2 = fmaf(bf16_lo(wd[e]), bf16_lo(wd[e]), n2);
+                        n2 = fmaf(bf16_hi(wd[e]), bf16_hi(wd[e]), n2);
+                    }
+                }
+                // squares are >= 0, so their bit patterns order like the values
+                const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(n2));
+                if (lane == 0) rmax[w] = __uint_as_float(m);
             }
             // row x of the P window of chunk rho - 1 (rho = 0 is C_{-1}): distance
             // D_{rho-1} + x; distances outside [0, rel_extent) have no bias (zeros)
@@ -401,7 +459,12 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                     for (int j = 0; j < 8; ++j) v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             };
+            // windows stored so far; window k publishes its per-warp max |P row|^2 in wmax[k & 1]
+            // and completes phase k of B_NORM
+            int n_win = 0;
             auto store_p = [&](const float4 (&v)[8]) {
+                float2 a2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                make_float2(0.f, 0.f)};   // |row|^2 in four independent chains
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const float f[8] = {v[2 * j].x * inv_scale, v[2 * j].y * inv_scale, v[2 * j].z * inv_scale,
@@ -412,12 +475,36 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                     for (int e = 0; e < 4; ++e) {
                         hi[e] = pack_bf16(f[2 * e], f[2 * e + 1]);
                         lo[e] = pack_bf16(f[2 * e] - bf16_lo(hi[e]), f[2 * e + 1] - bf16_hi(hi[e]));
+                        const float2 fe = make_float2(f[2 * e], f[2 * e + 1]);
+                        a2[e] = ffma2(fe, fe, a2[e]);
                     }
                     *reinterpret_cast<uint4 *>(smem + kOffPwHi + sw64_chunk(x, j)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                     *reinterpret_cast<uint4 *>(smem + kOffPwLo + sw64_chunk(x, j)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 }
+                const float2 t2 = fadd2(fadd2(a2[0], a2[1]), fadd2(a2[2], a2[3]));
+                const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(t2.x + t2.y));
+                if (lane == 0) wmax[(n_win & 1) * 4 + w] = __uint_as_float(m);
+                mbar_arrive(bar(B_NORM));
+                ++n_win;
                 fence_proxy_async_smem();
                 mbar_arrive(bar(B_PW_READY));
+            };
+            // bound B_k = max_a |r_a| * max |P row| over window k (S units), once all four warps
+            // have published it
+            auto bound = [&](int k, float &out) -> bool {
+                if (!wwait(bar(B_NORM), k & 1)) return false;
+                const float *wm = wmax + (k & 1) * 4;
+                const float pm = fmaxf(fmaxf(wm[0], wm[1]), fmaxf(wm[2], wm[3]));
+                const float rm = fmaxf(fmaxf(rmax[0], rmax[1]), fmaxf(rmax[2], rmax[3]));
+                out = sqrtf(pm) * sqrtf(rm);
+                return true;
+            };
+            // fixed-point step of chunk c (bounded by b_c; no value of a zero bound), published for
+            // the softmax in sigma entry (c + 1) & 3; returns 1 / step
+            auto set_step = [&](int c, float b) {
+                const float sg = fmaxf(b, 1e-30f) * (1.f / 32000.f);
+                if (x == 0) sigma_s[(c + 1) & 3] = sg;
+                return 1.f / sg;
             };
 
             const uint32_t id_r = tc::idesc(128, 128, tc::kFmtBF16, 0, 0);
@@ -440,27 +527,27 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                 return true;
             };
             constexpr int kRowStep = kStageStride + 1;        // (row a, column a - x) -> next row
-            __half *const stage = reinterpret_cast<__half *>(smem + kOffStage);
+            unsigned short *const stage = reinterpret_cast<unsigned short *>(smem + kOffStage);
             // rows [32 j, 32 j + 32) of the chunk: the part for tile n (first) or for tile
-            // n + 1 (second), into bias buffer buf
-            auto drain_block = [&](int j, bool first, int buf) {
+            // n + 1 (second), into bias buffer buf, as fixed point with step 1 / inv_sig
+            auto drain_block = [&](int j, bool first, int buf, float inv_sig) {
                 uint32_t r[32];
                 tc::ld32(tmem + kTmemR + lane_off + 32 * j, r);
                 tc::wait_ld();
-                __half *base = stage + buf * kStageBuf + (first ? -x : 128 - x) + 32 * j * kRowStep;
+                unsigned short *base = stage + buf * kStageBuf + (first ? -x : 128 - x) + 32 * j * kRowStep;
                 if (j != w) {                                  // every lane's x is on one side
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const __half2 v = __floats2half2_rn(__uint_as_float(r[e]), __uint_as_float(r[e + 1]));
-                        base[e * kRowStep] = __low2half(v);
-                        base[(e + 1) * kRowStep] = __high2half(v);
+                        const float2 v = fix16_encode2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), inv_sig);
+                        base[e * kRowStep] = fix16_bits(v.x);
+                        base[(e + 1) * kRowStep] = fix16_bits(v.y);
                     }
                 } else {                                       // row 32 w + e vs x = 32 w + lane
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const __half2 v = __floats2half2_rn(__uint_as_float(r[e]), __uint_as_float(r[e + 1]));
-                        if ((lane <= e) == first) base[e * kRowStep] = __low2half(v);
-                        if ((lane <= e + 1) == first) base[(e + 1) * kRowStep] = __high2half(v);
+                        const float2 v = fix16_encode2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), inv_sig);
+                        if ((lane <= e) == first) base[e * kRowStep] = fix16_bits(v.x);
+                        if ((lane <= e + 1) == first) base[(e + 1) * kRowStep] = fix16_bits(v.y);
                     }
                 }
             };
@@ -470,16 +557,23 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             const bool need_prev = p_lo - kKeys * t_hi != 0;
             int ci = 0;                                        // chunks issued
             float4 pv[8];
+            // window k of the chunks (k = c + 1 with C_{-1}, k = c without) is stored before its
+            // chunk's MMA, so its bound is complete once the chunk is (see above)
+            const int k_of_c0 = need_prev ? 1 : 0;
+            float inv_c = 0.f;                                 // 1 / step of the chunk being moved
             if (need_prev) {
                 load_p(0, pv);
                 store_p(pv);                                   // window of C_{-1}
                 if (ok) ok = issue(0);
                 load_p(1, pv);                                 // window of C_0, in flight
                 if (ok) ok = wwait(bar(B_R_FULL), 0);
+                float b = 0.f;
+                if (ok) ok = bound(0, b);
                 if (ok) {
                     tc::fence_after();
                     store_p(pv);                               // the MMA has read window 0
-                    for (int j = 0; j <= w; ++j) drain_block(j, false, 0);   // C_{-1}: tile 0, columns (a, 128)
+                    inv_c = set_step(-1, b);
+                    for (int j = 0; j <= w; ++j) drain_block(j, false, 0, inv_c);   // C_{-1}: tile 0, columns (a, 128)
                     tc::fence_before();
                     mbar_arrive(bar(B_R_EMPTY));
                 }
@@ -495,14 +589,17 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                 if (more) load_p(rho + 1, pv);
                 if (!(ok = wwait(bar(B_R_FULL), ci & 1))) break;
                 tc::fence_after();
+                float b = 0.f;
+                if (!(ok = bound(n + k_of_c0, b))) break;      // complete: C_n's MMA has run
+                inv_c = set_step(n, b);
                 const int bn = n & 1;
-                for (int j = w; j < 4; ++j) drain_block(j, true, bn);    // tile n, columns [0, a]
+                for (int j = w; j < 4; ++j) drain_block(j, true, bn, inv_c);    // tile n, columns [0, a]
                 mbar_arrive(bar(B_STAGE_FULL + bn));          // tile n's bias is complete
-                if (more) store_p(pv);                         // the MMA has read this window
                 if (more) {
+                    store_p(pv);                               // the MMA has read this window
                     // tile n + 1 shares its buffer with tile n - 1, whose reads must be done
                     if (n >= 1 && !(ok = wwait(bar(B_STAGE_EMPTY + (bn ^ 1)), ((n - 1) >> 1) & 1))) break;
-                    for (int j = 0; j <= w; ++j) drain_block(j, false, bn ^ 1);  // tile n + 1, columns (a, 128)
+                    for (int j = 0; j <= w; ++j) drain_block(j, false, bn ^ 1, inv_c);  // tile n + 1, columns (a, 128)
                 }
                 tc::fence_before();
                 mbar_arrive(bar(B_R_EMPTY));
@@ -511,7 +608,8 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             if (w == 0) {
                 tc::commit(bar(B_BDRAIN));
                 __syncwarp();
-                (void)wwait(bar(B_BDRAIN), 0);
+                (void)mbar_drain(bar(B_BDRAIN), 0, p.dev_status, A.wait_ns);
+                __syncwarp();
             }
         }
     } else {
@@ -528,7 +626,8 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         const int row = row0 + a;                             // row within the sequence
         const int i_pos = p_lo + a;
         const int cb = 64 * hw;                               // first key column of this thread
-        __half *stage = reinterpret_cast<__half *>(smem + kOffStage) + a * kStageStride;
+        const unsigned short *stage = reinterpret_cast<const unsigned short *>(smem + kOffStage) + a * kStageStride;
+        const float *sigma_s = reinterpret_cast<const float *>(smem + kOffNorm) + 12;
         float *xchg = reinterpret_cast<float *>(smem + kOffXchg);   // [2 tiles][2 halves][128 rows]
         // the two threads of each row meet on an mbarrier (a bounded wait, unlike bar.sync)
         int pair_phase = 0;
@@ -538,7 +637,8 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         };
         bool ok = true;
 
-        float m_run = -INFINITY, l_run = 0.f;
+        float m_run = -INFINITY, l_run = 0.f;   // l_run: sum of the fp32 P (for the LSE)
+        float lc_run = 0.f;                      // bf16 rounding of each tile's largest P (normaliser)
         // P V of tile m signals PV_DONE[m & 1], phase m >> 1.  The MMA warp issues Q K^T of
         // tile m + 2 after P V of tile m, so once this thread has seen S of tile m + 2 the
         // phase before tile m's (tile m - 2) is complete: a parity wait is then unambiguous
@@ -558,17 +658,21 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             if (n < n_band) {
                 const int bn = n & 1;
                 if (!(ok = wwait(bar(B_STAGE_FULL + bn), (n >> 1) & 1))) break;
-                const __half *bias_row = stage + bn * kStageBuf;
+                const unsigned short *bias_row = stage + bn * kStageBuf;
+                // columns b <= a hold chunk n's values, b > a chunk n - 1's
+                const float sg_n = sigma_s[(n + 1) & 3], sg_p = sigma_s[n & 3];
+                const int split = a - cb;                         // bb <= split: chunk n
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) {
                     const uint4 u = *reinterpret_cast<const uint4 *>(bias_row + cb + 8 * c8);
-                    const __half2 *hp = reinterpret_cast<const __half2 *>(&u);
+                    const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float2 f = fadd2(make_float2(s[8 * c8 + 2 * e], s[8 * c8 + 2 * e + 1]),
-                                               __half22float2(hp[e]));
-                        s[8 * c8 + 2 * e] = f.x;
-                        s[8 * c8 + 2 * e + 1] = f.y;
+                        const int bb = 8 * c8 + 2 * e;
+                        const float2 sg = make_float2(bb <= split ? sg_n : sg_p, bb + 1 <= split ? sg_n : sg_p);
+                        const float2 f = ffma2(fix16_decode2(wd[e]), sg, make_float2(s[bb], s[bb + 1]));
+                        s[bb] = f.x;
+                        s[bb + 1] = f.y;
                     }
                 }
                 mbar_arrive(bar(B_STAGE_EMPTY + bn));
@@ -603,6 +707,7 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             xc[hw * 128 + a] = mx;
             if (!(ok = pair_sync())) break;                       // also: both halves hold S
             mx = fmaxf(mx, xc[(1 - hw) * 128 + a]);
+            const float mx_raw = mx;                             // the row's largest logit of the tile (S units)
             mx = mx == -INFINITY ? -INFINITY : mx * c_qk;        // log2 units
             // lazy rescale: keep the running maximum unless it is exceeded by more than 8
             const bool need = mx > m_run + 8.f;
@@ -625,10 +730,16 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
                     tc::wait_st();
                 }
                 l_run *= corr;
+                lc_run *= corr;
                 m_run = m_new;
             }
             const float ref = m_run == -INFINITY ? 0.f : m_run;
             const float2 cq = make_float2(c_qk, c_qk), nref = make_float2(-ref, -ref);
+            if (hw == 0 && mx_raw != -INFINITY) {
+                // the tile's largest P of this row, computed as its element is, and its bf16 rounding
+                const float pm = fast_exp2(fmaf(mx_raw, c_qk, -ref));
+                lc_run += bf16_lo(pack_bf16(pm, 0.f)) - pm;
+            }
             float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                             make_float2(0.f, 0.f)};
             uint32_t pk[32];
@@ -646,17 +757,21 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             l_run += l2.x + l2.y;
             tc::wait_st();
             tc::fence_before();
-            mbar_arrive(bar(B_P_FULL + (n & 1)));
+            if (!(A.withhold && n == 0)) mbar_arrive(bar(B_P_FULL + (n & 1)));
         }
         // epilogue: the row sum of both halves, then O / l for this thread's 64 columns
+        // the column-half 0 thread of a row alone holds the correction (lc_run is 0 in the other)
+        // and alone writes the LSE: it publishes l + lc, the other thread l
         float *xl = xchg + 512;
-        xl[hw * 128 + a] = l_run;
+        xl[hw * 128 + a] = l_run + lc_run;
         if (ok) ok = pair_sync();
-        const float l_tot = l_run + xl[(1 - hw) * 128 + a];
+        const float l_other = xl[(1 - hw) * 128 + a];
+        const float l_tot = l_run + l_other;                  // the fp32 sum (read by half 0 only)
+        const float l_norm = l_run + lc_run + l_other;        // normaliser of P V's bf16 P
         if (ok) ok = wait_pv(N - 1);
         if (ok) {
             tc::fence_after();
-            const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+            const float inv = l_norm > 0.f ? 1.f / l_norm : 0.f;
             const bool valid = row < q_len;
             const size_t qrow = (size_t)(start + row) * p.Hq + h;
             uint32_t o[32];
@@ -716,6 +831,8 @@ cudaError_t launch_prefill_tc(const inkattn_attn_params &p, const AttnScalars &s
     TcArgs a;
     a.p = p;
     a.scale = s.scale;
+    a.wait_ns = kernel_debug().wait_ns;
+    a.withhold = kernel_debug().withhold;
     a.n_qtiles_max = (p.max_seqlen_q + kRows - 1) / kRows;
     a.kv_rows = (long long)p.num_blocks * p.Hkv * kBlock;
     dim3 grid(p.Hq, a.n_qtiles_max, p.B);

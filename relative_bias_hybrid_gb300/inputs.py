@@ -18,11 +18,11 @@ Workloads (all head_dim 128, paged KV block 64):
            prefix uniform in [0, 4096], window 4096, rel_extent=512.
 
 Value distributions: q, k, v, r and cached K/V ~ N(0, 1) rounded to bf16;
-P ~ N(0, 0.02^2) fp32; ShortConv weights ~ N(0, 0.5^2) fp32; RMSNorm gains
-1 + N(0, 0.1^2) fp32; eps 1e-6.  Carried conv-state rows ~ N(0, 1) bf16 where
-the sequence has that many earlier tokens, zero otherwise.  The block table
-is a seeded permutation of all allocated blocks; every cache slot starts with
-random bf16 values so that stray writes are detectable.
+P ~ N(0, 0.02^2) fp32 (its standard deviation is the workload field p_std);
+ShortConv weights ~ N(0, 0.5^2) fp32; RMSNorm gains 1 + N(0, 0.1^2) fp32; eps 1e-6.
+Carried conv-state rows ~ N(0, 1) bf16 where the sequence has that many earlier
+tokens, zero otherwise.  The block table is a seeded permutation of all allocated
+blocks; every cache slot starts with random bf16 values so that stray writes are detectable.
 """
 from __future__ import annotations
 
@@ -52,6 +52,7 @@ class Workload:
     random_block_table: bool = True
     eps: float = 1e-6
     spare_blocks: int = 0
+    p_std: float = 0.02           # standard deviation of the relative projection P
 
     @property
     def B(self) -> int:
@@ -145,7 +146,7 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu") -> Dict[str, torch.Ten
     out["k"] = _normal((N, C), 1.0, device, seed, "k", bf)
     out["v"] = _normal((N, C), 1.0, device, seed, "v", bf)
     out["r"] = _normal((N, w.Hq, w.d_r), 1.0, device, seed, "r", bf)
-    out["P"] = _normal((w.Hq, max(w.rel_extent, 1), w.d_r), 0.02, device, seed, "P", torch.float32)
+    out["P"] = _normal((w.Hq, max(w.rel_extent, 1), w.d_r), w.p_std, device, seed, "P", torch.float32)
     out["conv_w_k"] = _normal((C, 4), 0.5, device, seed, "conv_w_k", torch.float32)
     out["conv_w_v"] = _normal((C, 4), 0.5, device, seed, "conv_w_v", torch.float32)
     out["q_norm_w"] = 1.0 + _normal((d,), 0.1, device, seed, "q_norm_w", torch.float32)

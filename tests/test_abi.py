@@ -139,3 +139,53 @@ def test_split_heuristic_and_workspace_size(ia):
     assert ia.inkattn_decode_workspace_bytes(p, 5) == expect
     assert ia.inkattn_decode_workspace_bytes(p, 1) == 0
     assert ia.inkattn_decode_num_splits(_attn(ia, max_seqlen_q=17), 152) == 0
+
+
+def test_attention_rejects_memory_it_cannot_confirm_is_on_this_gpu(ia):
+    """q, k_cache and v_cache are read through TMA tensor maps (multicast inside a CTA pair
+    in the prefill): each must be device memory of the current device.  A host buffer is
+    rejected with INVALID_ARG before any launch (on a machine without a GPU every pointer's
+    location is unconfirmed, so the same status comes back)."""
+    import numpy as np
+    host = np.zeros(1 << 16, dtype=np.uint8)
+    addr = (host.ctypes.data + 255) & ~255
+    for field in ("q", "k_cache", "v_cache"):
+        p = _attn(ia, **{field: addr})
+        assert ia.inkattn_prefill(p, raise_on_error=False, stream=0) == ia.INKATTN_ERR_INVALID_ARG
+        assert ia.inkattn_decode(p, 1, None, raise_on_error=False, stream=0) == ia.INKATTN_ERR_INVALID_ARG
+        assert ia.inkattn_decode_noalloc(p, 1, raise_on_error=False, stream=0) == ia.INKATTN_ERR_INVALID_ARG
+
+
+def test_noalloc_scratch_address_is_cached_per_context(tmp_path):
+    """The cache behind inkattn_decode_noalloc's scratch address, compiled alone with a fake
+    lookup: each context ID gets its own lookup and address, a repeated ID is served from the
+    cache, and a context created after a reset (a new ID) looks up again."""
+    hdr = os.path.join(ROOT, "relative_bias_hybrid_gb300", "csrc", "context_cache.h")
+    src = tmp_path / "ctx_cache_check.cpp"
+    src.write_text(f'''
+#include "{hdr}"
+#include <cstdio>
+static int calls = 0;
+static unsigned long long current = 0;
+static bool lookup(void **v) {{ ++calls; *v = reinterpret_cast<void *>(0x1000 * (current + 1)); return true; }}
+int main() {{
+    inkattn::ContextCache<2> cache;
+    void *a = nullptr, *b = nullptr, *c = nullptr, *d = nullptr, *e = nullptr;
+    current = 7;  if (!cache.get(7, lookup, &a)) return 1;
+    current = 9;  if (!cache.get(9, lookup, &b)) return 2;
+    current = 7;  if (!cache.get(7, lookup, &c)) return 3;
+    if (a == b || a != c || calls != 2) return 4;          // own address per context, then cached
+    current = 11; if (!cache.get(11, lookup, &d)) return 5;  // cache full: looked up, not cached
+    current = 11; if (!cache.get(11, lookup, &e)) return 6;
+    if (d != e || calls != 4) return 7;
+    auto fail = [](void **) {{ return false; }};
+    void *f = nullptr;
+    if (cache.get(13, fail, &f)) return 8;                   // a failed lookup is reported
+    std::printf("ok\\n");
+    return 0;
+}}
+''')
+    exe = tmp_path / "ctx_cache_check"
+    subprocess.run(["g++", "-std=c++17", "-pthread", str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0 and out.stdout.strip() == "ok", (out.returncode, out.stdout, out.stderr)

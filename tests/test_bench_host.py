@@ -1,13 +1,6 @@
 """Host-side logic of bench.py: the algorithmic work counts (closed forms for the
-workloads) and the replica aggregation over ranks under torch.distributed (gloo,
-world size 2, on CPU)."""
-import os
-import socket
-
+workloads), and the one-GPU rule (a multi-GPU request is refused before any GPU work)."""
 import pytest
-import torch
-import torch.distributed as dist
-import torch.multiprocessing as mp
 
 import bench
 from relative_bias_hybrid_gb300 import inputs as gen
@@ -24,6 +17,9 @@ def test_sliding_window_pair_count_closed_form():
 def test_full_layer_pair_count_closed_form():
     w = gen.workload("full")
     assert bench.visible_pairs(w) == 32768 * 32769 // 2 == 536_887_296
+    # biased pairs: sum_i min(i + 1, 1024) = 1024*1025/2 + (32768 - 1024) * 1024
+    assert bench.biased_pairs(w) == 1024 * 1025 // 2 + (32768 - 1024) * 1024
+    assert bench.attention_flops(w) == pytest.approx(1.7593e13 + 1.353e11, rel=1e-3)
 
 
 def test_decode_bytes_and_prologue_bytes():
@@ -34,31 +30,20 @@ def test_decode_bytes_and_prologue_bytes():
     assert bench.prologue_bytes(s) == 40_964 * 8192 + 2 * 2 * 3 * 1024 * 2
 
 
-def _free_port():
-    with socket.socket() as s:
-        s.bind(("127.0.0.1", 0))
-        return s.getsockname()[1]
+def test_ragged_workload_is_seeded_and_in_range():
+    a, b = gen.workload("ragged"), gen.workload("ragged")
+    assert a.q_lens == b.q_lens and a.prefix_lens == b.prefix_lens and a.B == 16
+    assert all(1024 <= n <= 16384 for n in a.q_lens) and all(0 <= p <= 4096 for p in a.prefix_lens)
 
 
-def _worker(rank, port, q):
-    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE="2")
-    dist.init_process_group("gloo", rank=rank, world_size=2)
-    ms, units = bench.aggregate_over_ranks(10.0 + rank * 5.0, 100.0 * (rank + 1), 2)
-    q.put((rank, ms, units))
-    dist.destroy_process_group()
+@pytest.mark.parametrize("argv,env", [(["--gpus", "2"], {}), (["--gpus", "8"], {}),
+                                      ([], {"WORLD_SIZE": "2", "RANK": "0"})])
+def test_more_than_one_gpu_is_refused_before_any_gpu_work(monkeypatch, argv, env):
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
 
+    def no_gpu(*a, **k):
+        raise AssertionError("the GPU arm ran")
 
-def test_replica_aggregation_gloo_world_2():
-    ctx = mp.get_context("spawn")
-    q = ctx.Queue()
-    port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, port, q)) for r in range(2)]
-    for p in procs:
-        p.start()
-    for p in procs:
-        p.join(timeout=120)
-        assert p.exitcode == 0
-    res = sorted(q.get(timeout=10) for _ in range(2))
-    for _, ms, units in res:
-        assert ms == 15.0          # max over ranks
-        assert units == 300.0      # total over ranks
+    monkeypatch.setattr(bench, "run_gpu", no_gpu)
+    assert bench.main(argv) == 2

@@ -1,10 +1,11 @@
 """inkattn_decode_noalloc: decode for callers that cannot allocate device memory where
-they decode (host functions enqueued on a stream, plugin hosts that own all device
-memory, serving loops that must not allocate on the hot path).
+they decode (plugin hosts that own all device memory and hand over only inputs and
+outputs, serving loops that must not allocate on the hot path).
 
-It must give the same result as inkattn_decode + inkattn_combine with a workspace the
-caller allocated, on two calls in a row (the static buffer keeps the previous call's
-contents).  This file is collected last on purpose."""
+With the same split count it runs the same kernels as inkattn_decode + inkattn_combine
+with a workspace the caller allocated, so its output and LSE must be bit-identical to
+theirs, on two calls in a row (the static buffer keeps the previous call's contents).
+This file is collected last on purpose."""
 import ctypes
 
 import pytest
@@ -25,18 +26,15 @@ def env():
     return gen, ia, AttentionStep
 
 
-@pytest.mark.parametrize("splits", [5, 0])
-def test_noalloc_decode_matches_workspace_decode(env, splits):
+def _noalloc_matches_workspace_decode(env, w, splits, expect_splits, seed):
     gen, ia, AttentionStep = env
-    w = gen.custom("noalloc", Hq=64, Hkv=8, q_lens=[9, 9, 5], prefix_lens=[3000, 700, 6000],
-                   rel_extent=1024, log_scale_base=8192.0)
-    x = gen.make_inputs(w, seed=21, device="cuda")
-    ref = AttentionStep(w, x, mode="decode", num_splits=splits)
+    x = gen.make_inputs(w, seed=seed, device="cuda")
+    ref = AttentionStep(w, x, mode="decode", num_splits=expect_splits, out_dtype=torch.float32)
     ref.run_prologue()                        # fills the cache for the new tokens once
     ref.run_attention()                       # existing entry points, torch-allocated workspace
     torch.cuda.synchronize()
     assert ref.device_status() == 0
-    if splits:
+    if expect_splits > 1:
         assert ref.workspace is not None      # the split partials do go through scratch memory
     out2 = torch.empty_like(ref.out)
     lse2 = torch.empty_like(ref.lse)
@@ -53,9 +51,40 @@ def test_noalloc_decode_matches_workspace_decode(env, splits):
         assert rc == ia.INKATTN_OK, ia.status_string(rc)
         torch.cuda.synchronize()
         assert ref.device_status() == 0
-        assert torch.isfinite(out2.float()).all()
-        assert (out2.float() - ref.out.float()).abs().max().item() <= 1e-2
-        assert (lse2 - ref.lse).abs().max().item() <= 2e-3
+        assert torch.equal(out2.view(torch.int32), ref.out.view(torch.int32))
+        assert torch.equal(lse2.view(torch.int32), ref.lse.view(torch.int32))
+
+
+@pytest.mark.parametrize("splits", [5, 0])
+def test_noalloc_decode_matches_workspace_decode(env, splits):
+    gen, ia, AttentionStep = env
+    w = gen.custom("noalloc", Hq=64, Hkv=8, q_lens=[9, 9, 5], prefix_lens=[3000, 700, 6000],
+                   rel_extent=1024, log_scale_base=8192.0)
+    expect = splits
+    if splits == 0:
+        x = gen.make_inputs(w, seed=21, device="cuda")
+        probe = AttentionStep(w, x, mode="decode")
+        expect = probe.num_splits
+        assert expect > 1
+        assert ia.inkattn_decode_workspace_bytes(probe.attn, expect) <= ia.DECODE_NOALLOC_MAX_BYTES
+    _noalloc_matches_workspace_decode(env, w, splits, expect, seed=21)
+
+
+def test_noalloc_lowers_the_heuristic_split_count_to_fit(env):
+    """39 sequences x 9 queries over 16384 keys: the heuristic picks more splits than the
+    static buffer holds, and the call takes the largest count below it that fits."""
+    gen, ia, AttentionStep = env
+    w = gen.custom("noalloc-big", Hq=64, Hkv=8, q_lens=[9] * 39, prefix_lens=[16384 - 9] * 39,
+                   rel_extent=1024, log_scale_base=8192.0)
+    x = gen.make_inputs(w, seed=23, device="cuda")
+    probe = AttentionStep(w, x, mode="decode")
+    S = probe.num_splits
+    assert ia.inkattn_decode_workspace_bytes(probe.attn, S) > ia.DECODE_NOALLOC_MAX_BYTES
+    while S > 1 and ia.inkattn_decode_workspace_bytes(probe.attn, S) > ia.DECODE_NOALLOC_MAX_BYTES:
+        S -= 1
+    assert S > 1
+    del probe, x
+    _noalloc_matches_workspace_decode(env, w, 0, S, seed=23)
 
 
 def test_noalloc_rejects_partials_beyond_its_buffer(env):
