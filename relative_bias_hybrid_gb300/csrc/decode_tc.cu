@@ -27,8 +27,9 @@
 // R[t][x] = r_t . P_h[:, dlo + x] over the tile's 128 + ql distances with mma.sync (one warp
 // per head; fp16 operands, fp32 accumulation), then each thread adds its row's 64 entries.
 // fp16 keeps 11 significant bits of P (bf16 would keep 8) and represents the bf16 r exactly;
-// r and each round of P are first scaled by powers of two that keep them inside fp16's
-// range (exact, undone on the fp32 results).  The table holds 16-bit fixed point with one
+// r is first scaled, per token, by a power of two that keeps it inside fp16's range (exact,
+// undone on the fp32 results).  P must lie inside fp16's range (|P| < 65504); a table entry
+// that comes out infinite or undefined is flagged as INKATTN_ERR_DEVICE_BOUNDS.  The table holds 16-bit fixed point with one
 // step per (head, token) row and round of 72 distances, sigma = (largest |entry| of that
 // part of the row) / 32000; the staged bias is within sigma / 2 of the fp32 value.
 // Normalisation: O accumulates P V with P rounded to bf16, and each tile's largest P (its
@@ -392,8 +393,7 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
 #pragma unroll
                     for (int rd = 0; rd < 2; ++rd) {
                         float res[kGrp][4];
-                        float2 pl[kGrp][2], ph[kGrp][2];
-                        float pmx = 0.f;
+                        uint32_t pb[kGrp][2][2];
 #pragma unroll
                         for (int u = 0; u < kGrp; ++u) {
                             const int dl = dlo + (rd * kGrp + u) * 8 + gq;
@@ -401,29 +401,28 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
 #pragma unroll
                             for (int kk = 0; kk < 2; ++kk) {
                                 const int e0 = kk * 16 + 2 * tq;
-                                pl[u][kk] = dv ? __ldg(reinterpret_cast<const float2 *>(Ph + (size_t)dl * 32 + e0))
-                                               : make_float2(0.f, 0.f);
-                                ph[u][kk] = dv ? __ldg(reinterpret_cast<const float2 *>(Ph + (size_t)dl * 32 + e0 + 8))
-                                               : make_float2(0.f, 0.f);
-                                pmx = fmaxf(pmx, fmaxf(fmaxf(fabsf(pl[u][kk].x), fabsf(pl[u][kk].y)),
-                                                       fmaxf(fabsf(ph[u][kk].x), fabsf(ph[u][kk].y))));
+                                const float2 lo = dv ? __ldg(reinterpret_cast<const float2 *>(Ph + (size_t)dl * 32 + e0))
+                                                     : make_float2(0.f, 0.f);
+                                const float2 hi = dv ? __ldg(reinterpret_cast<const float2 *>(Ph + (size_t)dl * 32 + e0 + 8))
+                                                     : make_float2(0.f, 0.f);
+                                pb[u][kk][0] = pack_f16(lo.x, lo.y);
+                                pb[u][kk][1] = pack_f16(hi.x, hi.y);
                             }
                         }
-                        // one prescale for the round's P (magnitudes order like their bit patterns)
-                        pmx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(pmx)));
-                        const float psc = fp16_prescale(pmx), pusc = 1.f / psc;
+                        bool finite = true;
 #pragma unroll
                         for (int u = 0; u < kGrp; ++u) {
                             float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                            for (int kk = 0; kk < 2; ++kk)
-                                mma_16816_f16(acc, rf[kk], pack_f16(pl[u][kk].x * psc, pl[u][kk].y * psc),
-                                              pack_f16(ph[u][kk].x * psc, ph[u][kk].y * psc));
-                            res[u][0] = acc[0] * (pusc * rusc[0]);
-                            res[u][1] = acc[1] * (pusc * rusc[0]);
-                            res[u][2] = acc[2] * (pusc * rusc[1]);
-                            res[u][3] = acc[3] * (pusc * rusc[1]);
+                            for (int kk = 0; kk < 2; ++kk) mma_16816_f16(acc, rf[kk], pb[u][kk][0], pb[u][kk][1]);
+                            res[u][0] = acc[0] * rusc[0];
+                            res[u][1] = acc[1] * rusc[0];
+                            res[u][2] = acc[2] * rusc[1];
+                            res[u][3] = acc[3] * rusc[1];
+                            finite = finite && isfinite(acc[0] + acc[1] + acc[2] + acc[3]);
                         }
+                        // a P beyond fp16's range (|P| >= 65520) leaves an infinite or undefined entry
+                        if (!finite) set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
                         // each token row's largest |entry| in this round (its four lanes hold all
                         // of its columns here)
                         float mx[2] = {0.f, 0.f};

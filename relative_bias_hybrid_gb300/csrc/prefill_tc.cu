@@ -24,7 +24,7 @@
 // commits, loop) is on the critical path of the tile pipeline, while the softmax warps
 // beside it on each SM sub-partition always have independent work.
 // Registers are moved between warpgroups at the start (setmaxnreg): the softmax threads,
-// which keep 64 logits and their P live, get 176 each; the bias warps 96; TMA and MMA 64.
+// which keep 64 logits and their P live, get 176 each; the bias warps 104; TMA and MMA 56.
 // TMEM (512 columns): O [0,128) | S0 [128,256) | S1 [256,384) | R [384,512).  P (bf16)
 // overwrites the first 64 columns of its S buffer.  S is double-buffered so Q K^T of the
 // next tile runs while the softmax works on this one.
@@ -237,10 +237,10 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
 
     // Registers: the kernel is launched with 128 a thread (64 K in all).  Each warpgroup sets
     // its own budget first thing in its branch: the softmax threads keep 64 logits and their
-    // P live (176), the bias warps a 32-column TMEM load and a P row in flight (96), TMA and
-    // MMA little (64).
+    // P live (176), the bias warps a 32-column TMEM load and a P window in flight (104), TMA and
+    // MMA little (56).
     if (warp < kWarpBias) {
-      tc::reg_dealloc<64>();
+      tc::reg_dealloc<56>();
       if (warp == kWarpProducer) {
         // ================================ producer ================================
         bool ok = true;
@@ -399,7 +399,7 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
       }
     } else if (warp < kWarpSoftmax) {
         // ============================== relative bias ==============================
-        tc::reg_dealloc<96>();
+        tc::reg_dealloc<104>();
         // R is computed transposed, R^T[x][a] = P_h[:, D + 1 + x] . r_a (M = 128 distances,
         // N = 128 rows), so this thread (TMEM lane x) holds position x of the chunk for every
         // row a, in column a.  Its value for row a goes to column a - x of tile n's bias row
@@ -817,7 +817,7 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
 
 cudaError_t launch_prefill_tc(const inkattn_attn_params &p, const AttnScalars &s, const CUtensorMap &qmap,
                               const CUtensorMap &kmap, const CUtensorMap &vmap, cudaStream_t stream) {
-    // the warpgroups' register budgets (64 + 96 + 2 x 176 per thread of a warpgroup) add
+    // the warpgroups' register budgets (56 + 104 + 2 x 176 per thread of a warpgroup) add
     // up to the 64 K registers that 512 threads at 128 each are launched with
     // (checked once per process; the static's initialisation is thread-safe)
     static const cudaError_t regs_check = [] {
