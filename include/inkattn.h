@@ -145,8 +145,13 @@ INKATTN_API inkattn_status inkattn_prologue(const inkattn_prologue_params *p, vo
  * memory and another GPU's memory are rejected with INKATTN_ERR_INVALID_ARG.  The prefill
  * kernel multicasts each K/V tile to the two CTAs of a head pair inside one cluster: the
  * tensor maps cover this GPU's memory alone.
- * The bias enters the logits with 11 significant bits (it is staged in fp16, in units of
- * softmax_scale * q.k); |bias| must stay below 65504 * softmax_scale.
+ * The bias enters the logits as 16-bit fixed point in units of softmax_scale * q.k, so the
+ * absolute error of a bias value is at most half a step.  Prefill takes one step per chunk
+ * of 128 distances, max_a |r_a| * max_delta |P_h[delta]| / 32000 over the chunk's rows and
+ * distances (by Cauchy-Schwarz no value of the chunk exceeds 32000 steps); decode takes one
+ * per query row and table round, the largest magnitude in it / 32000.  The
+ * decode tables are computed with fp16 operands: P's entries must lie inside fp16's range
+ * (|P| < 65504), else the call reports INKATTN_ERR_DEVICE_BOUNDS.
  * ------------------------------------------------------------------------------ */
 typedef struct inkattn_attn_params {
     size_t struct_size;        /* = sizeof(inkattn_attn_params)                          */
