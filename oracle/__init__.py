@@ -62,6 +62,8 @@ def _load():
             lib.oracle_attention.argtypes = (
                 [I, P, P, I, I, I, I, I, I, D, D, P, P, P, P, P, P, I, I, I, P, I, P, P, I])
             lib.oracle_attention.restype = I
+            lib.oracle_output_conv.argtypes = [I, P, I, P, P, P, I, P, P, P, D, P, P, P]
+            lib.oracle_output_conv.restype = I
             _lib = lib
     return _lib
 
@@ -210,3 +212,36 @@ def attention_for_inputs(x, workload, q_bits, k_cache_bits, v_cache_bits, rows=N
                      P=_bits(x["P"]), k_cache=k_cache_bits, v_cache=v_cache_bits,
                      block_table=_bits(x["block_table"]), block_size=workload.block_size,
                      rows=rows, n_threads=n_threads)
+
+
+def output_conv(*, cu_seqlens_q, D, y, conv_w, state_slot, conv_state, residual, norm_w, eps,
+                want_conv=False):
+    """Run the attention-output ShortConv + residual add + RMSNorm oracle.
+
+    Inputs are numpy arrays (bf16 as uint16 bits): y, residual [N][D]; conv_w [D][4];
+    norm_w [D]; conv_state [slots][3][D] (copied, updated and returned).  Returns a dict
+    with h (the new residual stream), out (its RMSNorm), conv_state and, when want_conv,
+    conv (the rounded conv outputs).
+    """
+    lib = _load()
+    cu = _c(cu_seqlens_q, np.int32)
+    B = cu.shape[0] - 1
+    N = int(cu[-1])
+    y = _c(y, np.uint16)
+    w = _c(conv_w, np.float32)
+    ss = _c(state_slot, np.int32)
+    st = np.array(conv_state, dtype=np.uint16, copy=True, order="C")
+    res = _c(residual, np.uint16)
+    g = _c(norm_w, np.float32)
+    h = np.zeros((N, D), dtype=np.uint16)
+    out = np.zeros((N, D), dtype=np.uint16)
+    conv = np.zeros((N, D), dtype=np.uint16) if want_conv else None
+    rc = lib.oracle_output_conv(B, _ptr(cu), int(D), _ptr(y), _ptr(w), _ptr(ss), st.shape[0],
+                                _ptr(st), _ptr(res), _ptr(g), float(eps), _ptr(h), _ptr(out),
+                                _ptr(conv))
+    if rc != 0:
+        raise ValueError(f"oracle_output_conv failed with code {rc}")
+    d = dict(h=h, out=out, conv_state=st)
+    if want_conv:
+        d["conv"] = conv
+    return d

@@ -37,6 +37,16 @@
  *      o = softmax(s) . V, lse = log sum_j exp(s_j).
  *      lambda = max(1, ln T / ln base) on full layers that enable it (T = the
  *      sequence's key length), else 1; it scales the whole logit.
+ *   6. Attention-output ShortConv on the residual stream [SG §ShortConv：4カ所に現れる
+ *      短距離因果畳み込み (the third of the four positions: after the attention output);
+ *      SG §ShortConv 最適化 (it sits on the residual stream, and in decode RMSNorm and the
+ *      residual add are folded into the same kernel); VV §TP sharding nhận biết sconv
+ *      (the unfused order: o_proj output -> sconv -> residual connection -> RMSNorm)]:
+ *      per hidden channel c of the o_proj output y, the same W = 4 causal conv with its
+ *      own carried state as in step 1, rounded to bf16; then
+ *      h = bf16(residual + conv) (the new residual stream, the sum rounded once), and
+ *      out = bf16(h / sqrt(mean_c(h^2) + eps) * g) over the D hidden channels of the
+ *      token, from the bf16 h.
  */
 #include <math.h>
 #include <stdint.h>
@@ -305,4 +315,73 @@ int oracle_attention(int B, const int32_t *cu_seqlens_q, const int32_t *seqlen_k
     }
     free(seq_of);
     return status;
+}
+
+/*
+ * The attention-output ShortConv with the residual add and the RMSNorm: step 6 above.
+ *
+ * Layouts (row-major, bf16 as raw uint16 bit patterns):
+ *   y, residual, h_out, out [N][D]; conv_w [D][4] (w[c][3] weighs the current token);
+ *   norm_w [D]; conv_state [num_state_slots][3][D] (in/out, oldest row first).
+ * Optional output (NULL to skip): conv_bf16 [N][D] = the rounded conv outputs.
+ * h_out may be the residual array itself (each element is read before it is written).
+ * Returns ORACLE_ERR_INDEX (and writes nothing) when a state slot is out of range.
+ */
+int oracle_output_conv(int B, const int32_t *cu_seqlens_q, int D,
+                       const uint16_t *y, const float *conv_w,
+                       const int32_t *state_slot, int num_state_slots, uint16_t *conv_state,
+                       const uint16_t *residual, const float *norm_w, double eps,
+                       uint16_t *h_out, uint16_t *out, uint16_t *conv_bf16)
+{
+    if (B < 0 || D <= 0) return ORACLE_ERR_ARG;
+    const int N = cu_seqlens_q[B];
+    for (int b = 0; b < B; ++b) {
+        if (cu_seqlens_q[b] > cu_seqlens_q[b + 1] || cu_seqlens_q[b] < 0) return ORACLE_ERR_ARG;
+        if (state_slot[b] < 0 || state_slot[b] >= num_state_slots) return ORACLE_ERR_INDEX;
+    }
+    uint16_t *cv = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(N > 0 ? N : 1) * D);
+    uint16_t *xs = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(3 + (N > 0 ? N : 1)));
+    if (!cv || !xs) { free(cv); free(xs); return ORACLE_ERR_NOMEM; }
+
+    /* The conv and the state carry, one sequence and one channel at a time (as step 1). */
+    for (int b = 0; b < B; ++b) {
+        const int start = cu_seqlens_q[b];
+        const int n = cu_seqlens_q[b + 1] - start;
+        const size_t slot = (size_t)state_slot[b];
+        for (int c = 0; c < D; ++c) {
+            for (int r = 0; r < 3; ++r) xs[r] = conv_state[(slot * 3 + r) * D + c];
+            for (int t = 0; t < n; ++t) xs[3 + t] = y[(size_t)(start + t) * D + c];
+            for (int t = 0; t < n; ++t) {
+                double acc = 0.0;
+                for (int tap = 0; tap < 4; ++tap)
+                    acc += (double)conv_w[(size_t)c * 4 + tap] * bf16_bits_to_f64(xs[t + tap]);
+                cv[(size_t)(start + t) * D + c] = oracle_f64_to_bf16(acc);
+            }
+            for (int r = 0; r < 3; ++r) conv_state[(slot * 3 + r) * D + c] = xs[n + r];
+        }
+    }
+    if (conv_bf16) memcpy(conv_bf16, cv, sizeof(uint16_t) * (size_t)N * D);
+
+    /* The residual add, then the RMSNorm of each token's new residual row. */
+    for (int t = 0; t < N; ++t) {
+        double ss = 0.0;
+        for (int c = 0; c < D; ++c) {
+            const size_t i = (size_t)t * D + c;
+            /* the fp64 sum of two bf16 values is exact when their exponents differ by at
+             * most 44; beyond that the smaller is far below half a bf16 ulp of the larger,
+             * which is then the correctly rounded sum either way */
+            const uint16_t h = oracle_f64_to_bf16(bf16_bits_to_f64(residual[i]) + bf16_bits_to_f64(cv[i]));
+            h_out[i] = h;
+            const double a = bf16_bits_to_f64(h);
+            ss += a * a;
+        }
+        const double inv = 1.0 / sqrt(ss / D + eps);
+        for (int c = 0; c < D; ++c) {
+            const size_t i = (size_t)t * D + c;
+            out[i] = oracle_f64_to_bf16(bf16_bits_to_f64(h_out[i]) * inv * (double)norm_w[c]);
+        }
+    }
+    free(cv);
+    free(xs);
+    return ORACLE_OK;
 }
