@@ -44,7 +44,10 @@ KERNEL_SOURCES = {
                      "relative_bias_hybrid_gb300/csrc/common.cuh"],
     "k_decode_tc": ["relative_bias_hybrid_gb300/csrc/decode_tc.cu", "relative_bias_hybrid_gb300/csrc/tcgen05.cuh",
                     "relative_bias_hybrid_gb300/csrc/common.cuh"],
-    "k_prologue": ["relative_bias_hybrid_gb300/csrc/prologue.cu", "relative_bias_hybrid_gb300/csrc/common.cuh"],
+    "k_prologue": ["relative_bias_hybrid_gb300/csrc/prologue.cu", "relative_bias_hybrid_gb300/csrc/conv4.cuh",
+                   "relative_bias_hybrid_gb300/csrc/common.cuh"],
+    "k_output_conv": ["relative_bias_hybrid_gb300/csrc/output_conv.cu", "relative_bias_hybrid_gb300/csrc/conv4.cuh",
+                      "relative_bias_hybrid_gb300/csrc/common.cuh"],
 }
 
 
@@ -80,6 +83,12 @@ def prologue_bytes(w) -> float:
     """q in/out, k and v in, normed K and V out, slot mapping, conv state read + write."""
     per_tok = 2 * (w.Hq * w.head_dim * 2) + 2 * (w.Hkv * w.head_dim * 2) * 2 + 4
     return float(per_tok * w.N_tok + w.B * 2 * 2 * 3 * w.Hkv * w.head_dim * 2)
+
+
+def output_conv_bytes(w, D: int) -> float:
+    """y and the residual in, h and out written (bf16 rows of D), conv state read + write,
+    taps and gains once."""
+    return float(4 * 2 * D * w.N_tok + w.B * 2 * 3 * D * 2 + D * (4 * 4 + 4))
 
 
 def decode_bytes(w) -> float:
@@ -355,28 +364,31 @@ def run_reference(args, world, rank):
 # ---------------------------------------------------------------- GPU arm
 
 def timed_steps(step, steps, warmup, flush, stream):
-    """Runs warmup + steps passes; each timed pass is bracketed by CUDA events on the
-    launching stream, with an L2 flush (a 256 MiB write) between passes, outside the
-    events.  Returns per-step ms lists: whole step, attention call(s), prologue."""
-    with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            flush.zero_()
-            step.run(stream)
-    torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-            torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    with torch.cuda.stream(stream):
-        for e0, e1, e2 in evs:
-            flush.zero_()
-            e0.record(stream)
-            step.run_prologue(stream)
-            e1.record(stream)
-            step.run_attention(stream)
-            e2.record(stream)
-    torch.cuda.synchronize()
-    tot = [e0.elapsed_time(e2) for e0, _, e2 in evs]
-    att = [e1.elapsed_time(e2) for _, e1, e2 in evs]
-    pro = [t - a for t, a in zip(tot, att)]
+    """Three timed loops of warmup + steps passes, each pass bracketed by CUDA events on the
+    launching stream with an L2 flush (a 256 MiB write) before it, outside the events: the
+    whole step (prologue then attention, nothing recorded between them, so the attention
+    kernel's launch may overlap the prologue's tail), the attention call(s) alone and the
+    prologue alone.  Returns the per-pass ms lists of the three."""
+    def loop(body):
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                flush.zero_()
+                body()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        with torch.cuda.stream(stream):
+            for e0, e1 in evs:
+                flush.zero_()
+                e0.record(stream)
+                body()
+                e1.record(stream)
+        torch.cuda.synchronize()
+        return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+    tot = loop(lambda: step.run(stream))
+    att = loop(lambda: step.run_attention(stream))
+    pro = loop(lambda: step.run_prologue(stream))
     return tot, att, pro
 
 
@@ -437,6 +449,43 @@ def e2e_steps(steps_pair, x_host, steps, warmup, stream):
 DECODE_ORACLE_SEQS = 16
 
 
+def time_output_conv(w, args, dev, stream, flush, peaks, name):
+    """The attention-output ShortConv + residual + RMSNorm over the workload's new tokens
+    at hidden width Hq * 128, timed alone: warm-up calls, then args.steps calls each
+    bracketed by CUDA events on the launching stream, with the L2 flush between them
+    (outside the events).  Returns its roofline entry and the launches timed."""
+    from relative_bias_hybrid_gb300 import inputs as gen
+    from relative_bias_hybrid_gb300.step import OutputConvStep
+    D = w.Hq * w.head_dim
+    x = gen.make_output_conv_inputs(w, seed=0, D=D, device=dev)
+    oc = OutputConvStep(w, x)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            oc.run(stream)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record(stream)
+            oc.run(stream)
+            e1.record(stream)
+    torch.cuda.synchronize()
+    if oc.device_status() != 0:
+        raise RuntimeError(f"{name}: output conv device status {oc.device_status()}")
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / len(evs)
+    nbytes = output_conv_bytes(w, D)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "kernel": "k_output_conv", "achieved": gbs, "peak": peaks["hbm"],
+            "unit": "GB/s", "frac": gbs / peaks["hbm"], "traffic": ncu_traffic("k_output_conv", name),
+            "algorithmic_bytes_per_launch": nbytes, "ms": ms, "hidden": D,
+            "note": "timed alone, outside the step (its input stands in for the o_proj output)"}
+    del x, oc
+    return roof, args.steps
+
+
 def measure(name, args, peaks, dev, stream, flush):
     """Device-timed steps, then end-to-end steps, of one workload.  Returns its report
     (without cpu_baseline), the launches inside its timed regions and the host copy the
@@ -462,7 +511,11 @@ def measure(name, args, peaks, dev, stream, flush):
     e2e_ms, h2d, d2h = e2e_steps((step, step2), x_host, args.steps, args.warmup, stream)
     if step.device_status() | step2.device_status():
         raise RuntimeError(f"{name}: device status set during the end-to-end steps")
-    launches = args.steps * 2 * step.launches_per_run()
+    # timed: the step loop, the attention loop, the prologue loop, the end-to-end loop
+    n_att = step.launches_per_run() - 1
+    launches = args.steps * (2 * step.launches_per_run() + n_att + 1)
+    oc_roof, oc_launches = time_output_conv(w, args, dev, stream, flush, peaks, name)
+    launches += oc_launches
 
     pro_bytes = prologue_bytes(w)
     prologue = {"bound": "hbm", "kernel": "k_prologue", "achieved": pro_bytes / (pro_ms * 1e-3) / 1e9,
@@ -478,7 +531,7 @@ def measure(name, args, peaks, dev, stream, flush):
                 "algorithmic_flop_per_launch": fl, "ms": att_ms}
         rep = {"workload": w.describe() + "; step = inkattn_prologue + inkattn_prefill",
                "value": fl / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
-               "roofline": roof, "rooflines": {"k_prologue": prologue},
+               "roofline": roof, "rooflines": {"k_prologue": prologue, "k_output_conv": oc_roof},
                "e2e": {"value": fl / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}}
         host = HostCopy(w, x, step.q_out)
@@ -491,7 +544,7 @@ def measure(name, args, peaks, dev, stream, flush):
                 "algorithmic_bytes_per_launch": nbytes, "ms": att_ms, "num_splits": step.num_splits}
         rep = {"workload": w.describe() + "; step = inkattn_prologue + inkattn_decode (+ inkattn_combine)",
                "value": nbytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
-               "roofline": roof, "rooflines": {"k_prologue": prologue},
+               "roofline": roof, "rooflines": {"k_prologue": prologue, "k_output_conv": oc_roof},
                "e2e": {"value": nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}}
         host = HostCopy(w, x, step.q_out, seqs=list(range(DECODE_ORACLE_SEQS)))

@@ -18,6 +18,12 @@
  *   - Every call is asynchronous on the caller's CUDA stream (passed as void*, a
  *     cudaStream_t; NULL = the legacy default stream), keeps no state between calls
  *     and is safe to call from several host threads.
+ *   - Kernels are chained by programmatic dependent launch: each may become resident on
+ *     the GPU while the kernel before it on the stream finishes, and reads no global
+ *     memory before that kernel has completed, so stream order holds as for any launch.
+ *     inkattn_prologue and inkattn_output_conv let the next kernel be scheduled once all
+ *     their CTAs have started; the attention kernels do not.  Every call can be captured
+ *     into a CUDA graph.
  *   - Host-side validation runs before any launch; on failure the call returns
  *     INKATTN_ERR_INVALID_ARG or INKATTN_ERR_UNSUPPORTED and launches nothing.
  *   - Index arrays are read only on the device.  Kernels bounds-check every index
@@ -253,6 +259,50 @@ INKATTN_API inkattn_status inkattn_combine(const inkattn_attn_params *p, int num
 
 INKATTN_API inkattn_status inkattn_decode_noalloc(const inkattn_attn_params *p, int num_splits,
                                                   void *stream);
+
+/* ------------------------------------------------------------------------------
+ * Attention-output ShortConv with the residual add and the RMSNorm, one kernel
+ * [SG §ShortConv：4カ所に現れる短距離因果畳み込み (the third ShortConv position, after the
+ * attention output); SG §ShortConv 最適化：融合、グラフキャプチャ、シャーディング (it sits on the
+ * residual stream; in decode the residual add and the RMSNorm fold into the same
+ * kernel); VV §TP sharding nhận biết sconv (order: o_proj output -> sconv -> residual
+ * connection -> RMSNorm)].  On one GPU there is no all-reduce in front of it: the input is
+ * the o_proj output itself.
+ *
+ * For each sequence b and hidden channel c, with xs = the 3 carried rows (oldest first)
+ * followed by the new rows of y:
+ *   conv[t][c] = bf16( sum_{k=0..3} conv_w[c][k] * xs[t+k][c] )   (correctly rounded)
+ *   h[t][c]    = bf16( residual[t][c] + conv[t][c] )               (correctly rounded)
+ *   out[t][c]  = bf16( h[t][c] / sqrt(mean_c'(h[t][c']^2) + eps) * norm_w[c] )
+ * the mean over all D channels of the token.  The state slot then holds the last 3 rows
+ * of xs.  conv and h are bit-exact; out is within 1 bf16 ulp of the fp64 value (its sum
+ * of squares is taken in fp32).  An empty sequence keeps its state.
+ * ------------------------------------------------------------------------------ */
+typedef struct inkattn_output_conv_params {
+    size_t struct_size;        /* = sizeof(inkattn_output_conv_params)                   */
+    int32_t B;                 /* sequences, 1 .. 65535                                  */
+    int32_t N_tok;             /* new tokens = cu_seqlens_q[B], >= 0                     */
+    int32_t max_seqlen_q;      /* >= every q_len[b]; sizes the grid                      */
+    int32_t D;                 /* hidden width: a multiple of 8, 8 .. 32768              */
+    int32_t num_state_slots;   /* conv-state capacity in slots (bounds check)            */
+    float eps;                 /* RMSNorm epsilon, >= 0                                  */
+    const inkattn_bf16 *y;     /* [N_tok][D], the o_proj output                          */
+    const float *conv_w;       /* [D][4], w[c][3] weighs the current token               */
+    const float *norm_w;       /* [D]                                                    */
+    const int32_t *cu_seqlens_q;   /* [B+1], non-decreasing, cu[0] = 0                   */
+    const int32_t *state_slot;     /* [B], distinct values in [0, num_state_slots)       */
+    inkattn_bf16 *conv_state;      /* [num_state_slots][3][D], read then overwritten     */
+    const inkattn_bf16 *residual;  /* [N_tok][D], the residual stream before the add     */
+    inkattn_bf16 *h_out;           /* [N_tok][D], the new residual stream; may equal residual */
+    inkattn_bf16 *out;             /* [N_tok][D], its RMSNorm                            */
+    int32_t *dev_status;           /* nullable, see the conventions above                */
+} inkattn_output_conv_params;
+
+/* Runs the attention-output conv.  y, conv_w, norm_w, conv_state, residual, h_out and out
+ * must be 16-byte aligned.  out and h_out may not overlap y, and out may not overlap
+ * residual or h_out (INKATTN_ERR_INVALID_ARG); h_out == residual (in place) is allowed,
+ * a partial overlap of the two is not.  conv_state must not overlap the other arrays. */
+INKATTN_API inkattn_status inkattn_output_conv(const inkattn_output_conv_params *p, void *stream);
 
 #ifdef __cplusplus
 }

@@ -88,6 +88,33 @@ inkattn_status validate_prologue(const inkattn_prologue_params *p) {
     return INKATTN_OK;
 }
 
+inkattn_status validate_output_conv(const inkattn_output_conv_params *p) {
+    if (!p || p->struct_size != sizeof(inkattn_output_conv_params)) return INKATTN_ERR_INVALID_ARG;
+    if (p->B < 1 || p->B > 65535 || p->N_tok < 0 || p->max_seqlen_q < 0 || p->num_state_slots < 1 ||
+        !(p->eps >= 0.f))
+        return INKATTN_ERR_INVALID_ARG;
+    if (p->D < 8 || p->D > 32768 || p->D % 8 != 0) return INKATTN_ERR_INVALID_ARG;
+    if (p->N_tok > 0 && p->max_seqlen_q < 1) return INKATTN_ERR_INVALID_ARG;
+    const void *ptrs16[] = {p->y, p->conv_w, p->norm_w, p->conv_state, p->residual, p->h_out, p->out};
+    for (const void *ptr : ptrs16)
+        if (!ptr || !aligned(ptr, 16)) return INKATTN_ERR_INVALID_ARG;
+    const void *ptrs4[] = {p->cu_seqlens_q, p->state_slot};
+    for (const void *ptr : ptrs4)
+        if (!ptr || !aligned(ptr, 4)) return INKATTN_ERR_INVALID_ARG;
+    if (p->dev_status && !aligned(p->dev_status, 4)) return INKATTN_ERR_INVALID_ARG;
+    // h_out may be the residual array itself, but no other output may overlap an input
+    const size_t row = (size_t)p->N_tok * p->D * 2;
+    auto overlap = [](const void *a, size_t na, const void *b, size_t nb) {
+        const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+        return na && nb && x < y + nb && y < x + na;
+    };
+    if (overlap(p->out, row, p->y, row) || overlap(p->out, row, p->residual, row) ||
+        overlap(p->out, row, p->h_out, row) || overlap(p->h_out, row, p->y, row) ||
+        (p->h_out != p->residual && overlap(p->h_out, row, p->residual, row)))
+        return INKATTN_ERR_INVALID_ARG;
+    return INKATTN_OK;
+}
+
 inkattn_status validate_attn(const inkattn_attn_params *p) {
     if (!p || p->struct_size != sizeof(inkattn_attn_params)) return INKATTN_ERR_INVALID_ARG;
     if (p->B < 1 || p->B > 65535 || p->N_tok < 0 || p->max_seqlen_q < 0 || p->max_seqlen_k < 0 ||
@@ -311,6 +338,14 @@ inkattn_status inkattn_prologue(const inkattn_prologue_params *p, void *stream) 
     if ((st = check_device(nullptr)) != INKATTN_OK) return st;
     if (p->N_tok == 0) return INKATTN_OK;
     return launch_status(launch_prologue(*p, static_cast<cudaStream_t>(stream)));
+}
+
+inkattn_status inkattn_output_conv(const inkattn_output_conv_params *p, void *stream) {
+    inkattn_status st = validate_output_conv(p);
+    if (st != INKATTN_OK) return st;
+    if ((st = check_device(nullptr)) != INKATTN_OK) return st;
+    if (p->N_tok == 0) return INKATTN_OK;
+    return launch_status(launch_output_conv(*p, static_cast<cudaStream_t>(stream)));
 }
 
 inkattn_status inkattn_prefill(const inkattn_attn_params *p, void *stream) {

@@ -32,6 +32,18 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched so that it may
+// start while the kernel before it on the stream is still running; grid_dep_wait() returns
+// once that kernel has completed and its writes are visible (at once when there is none),
+// and each kernel calls it before its first read of global memory.  grid_dep_launch() lets
+// the next kernel on the stream be scheduled; the short HBM-bound kernels (prologue,
+// attention-output conv) call it right after their wait, the attention kernels not at all
+// (their successor launches when they exit), so a successor never takes SM room an
+// attention CTA still needs.  Since a kernel triggers only after its own wait, a kernel
+// that starts early still cannot overtake any work before its predecessor.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

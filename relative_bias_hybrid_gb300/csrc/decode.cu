@@ -13,6 +13,7 @@ namespace inkattn {
 __global__ void __launch_bounds__(256)
 k_combine(const inkattn_attn_params p, int S, const float *__restrict__ ws_o,
           const float *__restrict__ ws_lse) {
+    grid_dep_wait();                                   // the partials of the decode before it
     const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= (long long)p.N_tok * p.Hq) return;
@@ -51,8 +52,7 @@ cudaError_t launch_combine(const inkattn_attn_params &p, int num_splits, const f
     const long long rows = (long long)p.N_tok * p.Hq;
     if (rows == 0) return cudaSuccess;
     const unsigned blocks = (unsigned)((rows + 7) / 8);
-    k_combine<<<blocks, 256, 0, stream>>>(p, num_splits, ws_o, ws_lse);
-    return cudaGetLastError();
+    return launch_dependent(k_combine, dim3(blocks), dim3(256), 0, stream, 1, p, num_splits, ws_o, ws_lse);
 }
 
 }  // namespace inkattn

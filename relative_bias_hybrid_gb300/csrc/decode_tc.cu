@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
             const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
     extern __shared__ __align__(1024) unsigned char smem[];
+    grid_dep_wait();                                   // q and the cache: written by the prologue
     const inkattn_attn_params &p = A.p;
     const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -640,8 +641,7 @@ cudaError_t launch_decode_tc(const inkattn_attn_params &p, const AttnScalars &s,
     cudaError_t err = cudaFuncSetAttribute(k_decode_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (err != cudaSuccess) return err;
     dim3 grid(num_splits, p.Hkv, p.B);
-    k_decode_tc<<<grid, kThreads, kSmem, stream>>>(a, qmap, kmap, vmap);
-    return cudaGetLastError();
+    return launch_dependent(k_decode_tc, grid, dim3(kThreads), kSmem, stream, 1, a, qmap, kmap, vmap);
 }
 
 }  // namespace inkattn

@@ -34,6 +34,33 @@ inkattn_status validate_decode_call(const inkattn_attn_params *p, int *sms);
 int pick_splits(const inkattn_attn_params &p, int num_sms);
 size_t decode_workspace_bytes(const inkattn_attn_params &p, int S);   // 0 when S <= 1
 
+// Launches `kernel` as a programmatic dependent of the work before it on `stream` (see
+// grid_dep_wait in common.cuh), optionally as clusters of cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, int cluster_x, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = (unsigned)n;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Resolved per-call scalars of an attention call (host-computed).
 struct AttnScalars {
     float scale;          // softmax scale (1/sqrt(128) by default)
@@ -41,6 +68,7 @@ struct AttnScalars {
 };
 
 cudaError_t launch_prologue(const inkattn_prologue_params &p, cudaStream_t stream);
+cudaError_t launch_output_conv(const inkattn_output_conv_params &p, cudaStream_t stream);
 
 // Decode: S = num_splits (>= 1).  ws_o / ws_lse are unused when S == 1.
 constexpr int kDecodeMaxRows = 128;     // max_seqlen_q * group

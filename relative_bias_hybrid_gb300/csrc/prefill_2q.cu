@@ -73,6 +73,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 k_prefill_2q(const Tc2Args A, const __grid_constant__ CUtensorMap qmap,
              const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
     extern __shared__ __align__(1024) unsigned char smem[];
+    grid_dep_wait();                                   // q and the cache: written by the prologue
     const inkattn_attn_params &p = A.p;
     const int h = blockIdx.x, b = blockIdx.z;
     const int pr = A.n_pairs_max - 1 - (int)blockIdx.y;     // longest pairs first
@@ -480,8 +481,7 @@ cudaError_t launch_prefill_2q(const inkattn_attn_params &p, const AttnScalars &s
     cudaError_t err = cudaFuncSetAttribute(k_prefill_2q, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (err != cudaSuccess) return err;
     dim3 grid(p.Hq, a.n_pairs_max, p.B);
-    k_prefill_2q<<<grid, kThreads, kSmem, stream>>>(a, qmap, kmap, vmap);
-    return cudaGetLastError();
+    return launch_dependent(k_prefill_2q, grid, dim3(kThreads), kSmem, stream, 1, a, qmap, kmap, vmap);
 }
 
 }  // namespace inkattn

@@ -146,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
              const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
     extern __shared__ __align__(1024) unsigned char smem[];
+    grid_dep_wait();                                   // q and the cache: written by the prologue
     const inkattn_attn_params &p = A.p;
     const int h = blockIdx.x, b = blockIdx.z;
     const int qt = A.n_qtiles_max - 1 - (int)blockIdx.y;     // longest tiles first
@@ -841,24 +842,11 @@ cudaError_t launch_prefill_tc(const inkattn_attn_params &p, const AttnScalars &s
     if (!pair) {
         cudaError_t err = cudaFuncSetAttribute(k_prefill_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
         if (err != cudaSuccess) return err;
-        k_prefill_tc<1><<<grid, kThreads, kSmem, stream>>>(a, qmap, kmap, vmap);
-        return cudaGetLastError();
+        return launch_dependent(k_prefill_tc<1>, grid, dim3(kThreads), kSmem, stream, 1, a, qmap, kmap, vmap);
     }
     cudaError_t err = cudaFuncSetAttribute(k_prefill_tc<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (err != cudaSuccess) return err;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_prefill_tc<2>, a, qmap, kmap, vmap);
+    return launch_dependent(k_prefill_tc<2>, grid, dim3(kThreads), kSmem, stream, 2, a, qmap, kmap, vmap);
 }
 
 }  // namespace inkattn

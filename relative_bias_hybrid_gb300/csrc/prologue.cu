@@ -26,6 +26,7 @@
 // same CTA, after a block barrier, writes the new state for its own 128 channels.  No other
 // CTA touches those channels of that state slot.
 #include "common.cuh"
+#include "conv4.cuh"
 #include "internal.h"
 
 namespace inkattn {
@@ -37,100 +38,6 @@ constexpr int kPrologueThreads = 256;
 static_assert(kPrologueThreads == 256, "the row mapping assumes 16 half-warps per CTA");
 constexpr int kQInFlight = 8;      // query rows a half-warp loads before it computes
 
-__device__ __forceinline__ void unpack8(const uint4 &u, float (&x)[8]) {
-    x[0] = bf16_lo(u.x); x[1] = bf16_hi(u.x);
-    x[2] = bf16_lo(u.y); x[3] = bf16_hi(u.y);
-    x[4] = bf16_lo(u.z); x[5] = bf16_hi(u.z);
-    x[6] = bf16_lo(u.w); x[7] = bf16_hi(u.w);
-}
-
-__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
-    uint4 u;
-    u.x = pack_bf16(x[0], x[1]); u.y = pack_bf16(x[2], x[3]);
-    u.z = pack_bf16(x[4], x[5]); u.w = pack_bf16(x[6], x[7]);
-    return u;
-}
-
-// Exact-sum helpers for the conv: a*b = p + e exactly (fma), a + b = s + e exactly.
-__device__ __forceinline__ void two_prod(float a, float b, float &p, float &e) {
-    p = a * b;
-    e = fmaf(a, b, -p);
-}
-__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
-    s = a + b;
-    const float bb = s - a;
-    e = (a - (s - bb)) + (b - bb);
-}
-
-// bf16 of the value hi + lo (|lo| <= half an fp32 ulp of hi), rounded to nearest even:
-// rounding hi alone is right unless hi sits exactly on a bf16 tie, where lo decides.
-__device__ __forceinline__ float round_pair_bf16(float hi, float lo) {
-    const uint32_t u = __float_as_uint(hi);
-    if ((u & 0xFFFFu) == 0x8000u && lo != 0.f) {
-        const bool away = (lo > 0.f) == (hi > 0.f);
-        return __uint_as_float(((u >> 16) + (away ? 1u : 0u)) << 16);
-    }
-    return __bfloat162float(__float2bfloat16_rn(hi));
-}
-
-// Correctly rounded bf16 of sum_{k=0..3} w[k]*x[k]: the products are split exactly and
-// the running sum is carried as an unevaluated pair, so hi + lo equals the exact sum up
-// to ~2^-47 of the largest term (fp32 accumulation alone can lose every bit of a
-// strongly cancelling sum).
-__device__ __forceinline__ float conv4_bf16(const float (&w)[4], const float (&x)[4]) {
-    float s, c;
-    two_prod(w[0], x[0], s, c);
-#pragma unroll
-    for (int k = 1; k < 4; ++k) {
-        float p, pe, t, te;
-        two_prod(w[k], x[k], p, pe);
-        two_sum(s, p, t, te);
-        s = t;
-        c += te + pe;
-    }
-    float hi, lo;
-    two_sum(s, c, hi, lo);
-    return round_pair_bf16(hi, lo);
-}
-
-// The same correctly rounded value, cheaply in almost every case: an fp32 multiply-add
-// chain s is within 4u * sum|w_k x_k| of the exact sum (u = 2^-24), so when s is farther
-// than 8u * sum|w_k x_k| from the nearest bf16 rounding boundary (the midpoint above or
-// below it, or a quarter bf16 ulp when a power of two is near) its rounding is the exact
-// sum's; otherwise the error-free path decides.
-__device__ __forceinline__ float conv4_bf16_fast(const float (&w)[4], const float (&x)[4]) {
-    const float s = fmaf(w[3], x[3], fmaf(w[2], x[2], fmaf(w[1], x[1], w[0] * x[0])));
-    const float a = fmaf(fabsf(w[3]), fabsf(x[3]),
-                         fmaf(fabsf(w[2]), fabsf(x[2]), fmaf(fabsf(w[1]), fabsf(x[1]), fabsf(w[0] * x[0]))));
-    const float mid = __uint_as_float((__float_as_uint(s) & 0xFFFF0000u) | 0x8000u);
-    if (fabsf(s - mid) * 2097152.f > a && fabsf(s) * 2048.f > a)        // 2^21, 2^11
-        return __bfloat162float(__float2bfloat16_rn(s));
-    return conv4_bf16(w, x);
-}
-
-// conv4_bf16_fast on two channels at once: the multiply-add chains and the sums of
-// magnitudes run on paired fp32 instructions.
-__device__ __forceinline__ void conv4_bf16_fast2(const float (&wa)[4], const float (&xa)[4],
-                                                 const float (&wb)[4], const float (&xb)[4],
-                                                 float &ya, float &yb) {
-    float2 s = fmul2(make_float2(wa[0], wb[0]), make_float2(xa[0], xb[0]));
-    // the sums of magnitudes in scalar form: the absolute values then ride on the
-    // multiply-adds' operands instead of taking instructions of their own
-    float2 a = make_float2(fabsf(s.x), fabsf(s.y));
-#pragma unroll
-    for (int k = 1; k < 4; ++k) {
-        s = ffma2(make_float2(wa[k], wb[k]), make_float2(xa[k], xb[k]), s);
-        a.x = fmaf(fabsf(wa[k]), fabsf(xa[k]), a.x);
-        a.y = fmaf(fabsf(wb[k]), fabsf(xb[k]), a.y);
-    }
-    const float ma = __uint_as_float((__float_as_uint(s.x) & 0xFFFF0000u) | 0x8000u);
-    const float mb = __uint_as_float((__float_as_uint(s.y) & 0xFFFF0000u) | 0x8000u);
-    ya = (fabsf(s.x - ma) * 2097152.f > a.x && fabsf(s.x) * 2048.f > a.x)
-        ? __bfloat162float(__float2bfloat16_rn(s.x)) : conv4_bf16(wa, xa);
-    yb = (fabsf(s.y - mb) * 2097152.f > a.y && fabsf(s.y) * 2048.f > a.y)
-        ? __bfloat162float(__float2bfloat16_rn(s.y)) : conv4_bf16(wb, xb);
-}
-
 __global__ void __launch_bounds__(kPrologueThreads, 4)
 k_prologue(const inkattn_prologue_params p, const int kv_tiles) {
     __shared__ __align__(16) float s_wk[kHeadDim * 4];
@@ -138,6 +45,8 @@ k_prologue(const inkattn_prologue_params p, const int kv_tiles) {
     __shared__ float s_gk[kHeadDim];
     // this head's K and V input rows [t0 - 3, t0 + nt) of [3 carried rows ; new rows]
     __shared__ uint4 s_x[2][kKvTokens + 3][16];
+    grid_dep_wait();                                   // inputs written by the work before
+    grid_dep_launch();                                 // the attention may be scheduled
 
     // Groups of kv_tiles + 1 neighbouring CTAs along x: the first kv_tiles stream the query
     // rows of one 16-token tile each (RMSNorm only); the last takes the K and V rows of the
@@ -338,8 +247,7 @@ cudaError_t launch_prologue(const inkattn_prologue_params &p, cudaStream_t strea
     const int kv_tiles = ((long long)tiles * p.B >= 2048) ? 4 : 2;
     const int groups = (tiles + kv_tiles - 1) / kv_tiles;
     dim3 grid(groups * (kv_tiles + 1), p.B, p.Hkv);
-    k_prologue<<<grid, kPrologueThreads, 0, stream>>>(p, kv_tiles);
-    return cudaGetLastError();
+    return launch_dependent(k_prologue, grid, dim3(kPrologueThreads), 0, stream, 1, p, kv_tiles);
 }
 
 }  // namespace inkattn

@@ -61,6 +61,18 @@ class AttnParams(ctypes.Structure):
     ]
 
 
+class OutputConvParams(ctypes.Structure):
+    """inkattn_output_conv_params."""
+    _fields_ = [
+        ("struct_size", ctypes.c_size_t),
+        ("B", _c_i32), ("N_tok", _c_i32), ("max_seqlen_q", _c_i32), ("D", _c_i32),
+        ("num_state_slots", _c_i32), ("eps", ctypes.c_float),
+        ("y", _c_ptr), ("conv_w", _c_ptr), ("norm_w", _c_ptr), ("cu_seqlens_q", _c_ptr),
+        ("state_slot", _c_ptr), ("conv_state", _c_ptr), ("residual", _c_ptr), ("h_out", _c_ptr),
+        ("out", _c_ptr), ("dev_status", _c_ptr),
+    ]
+
+
 class InkattnError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -100,6 +112,8 @@ def lib():
             L.inkattn_combine.restype = ctypes.c_int
             L.inkattn_decode_noalloc.argtypes = [P(AttnParams), ctypes.c_int, _c_ptr]
             L.inkattn_decode_noalloc.restype = ctypes.c_int
+            L.inkattn_output_conv.argtypes = [P(OutputConvParams), _c_ptr]
+            L.inkattn_output_conv.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -171,6 +185,11 @@ def inkattn_decode_noalloc(p: AttnParams, num_splits: int, stream=None, raise_on
     memory where they decode."""
     return _check(lib().inkattn_decode_noalloc(ctypes.byref(p), int(num_splits), _stream(stream)),
                   "inkattn_decode_noalloc", raise_on_error)
+
+
+def inkattn_output_conv(p: OutputConvParams, stream=None, raise_on_error=True) -> int:
+    return _check(lib().inkattn_output_conv(ctypes.byref(p), _stream(stream)), "inkattn_output_conv",
+                  raise_on_error)
 
 
 # ------------------------------------------------------------------ marshalling helpers
@@ -253,5 +272,31 @@ def attn_params(*, q, k_cache, v_cache, cu_seqlens_q, seqlen_k, block_table, out
         raise TypeError(f"out: expected bfloat16 or float32, got {out.dtype}")
     p.out = _ptr(out, None, "out")
     p.lse = _ptr(lse, f32, "lse")
+    p.dev_status = _ptr(dev_status, i32, "dev_status")
+    return p
+
+
+def output_conv_params(*, y, conv_w, norm_w, cu_seqlens_q, state_slot, conv_state, residual, h_out,
+                       out, max_seqlen_q: int, eps: float = 1e-6, dev_status=None) -> OutputConvParams:
+    """Fill an inkattn_output_conv_params from torch tensors (see include/inkattn.h)."""
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    N, D = y.shape
+    p = OutputConvParams()
+    p.struct_size = ctypes.sizeof(OutputConvParams)
+    p.B = cu_seqlens_q.numel() - 1
+    p.N_tok = N
+    p.max_seqlen_q = int(max_seqlen_q)
+    p.D = D
+    p.num_state_slots = conv_state.shape[0]
+    p.eps = float(eps)
+    p.y = _ptr(y, bf, "y")
+    p.conv_w = _ptr(conv_w, f32, "conv_w")
+    p.norm_w = _ptr(norm_w, f32, "norm_w")
+    p.cu_seqlens_q = _ptr(cu_seqlens_q, i32, "cu_seqlens_q")
+    p.state_slot = _ptr(state_slot, i32, "state_slot")
+    p.conv_state = _ptr(conv_state, bf, "conv_state")
+    p.residual = _ptr(residual, bf, "residual")
+    p.h_out = _ptr(h_out, bf, "h_out")
+    p.out = _ptr(out, bf, "out")
     p.dev_status = _ptr(dev_status, i32, "dev_status")
     return p

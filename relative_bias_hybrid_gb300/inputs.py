@@ -112,7 +112,8 @@ def custom(name: str, *, Hq: int, Hkv: int, q_lens, prefix_lens=None, **kw) -> W
 
 _TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "r": 4, "P": 5, "conv_w_k": 6, "conv_w_v": 7,
                "q_norm_w": 8, "k_norm_w": 9, "conv_state_k": 10, "conv_state_v": 11,
-               "k_cache": 12, "v_cache": 13, "perm": 14}
+               "k_cache": 12, "v_cache": 13, "perm": 14, "y": 15, "residual": 16,
+               "oc_conv_w": 17, "oc_norm_w": 18, "oc_conv_state": 19}
 
 
 def _gen(device, seed: int, tensor: str) -> torch.Generator:
@@ -192,6 +193,37 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu") -> Dict[str, torch.Ten
     shape = (nb, w.Hkv, w.block_size, d)
     out["k_cache"] = _normal(shape, 1.0, device, seed, "k_cache", bf)
     out["v_cache"] = _normal(shape, 1.0, device, seed, "v_cache", bf)
+    return out
+
+
+def make_output_conv_inputs(w: Workload, seed: int = 0, device="cpu", D: int = 0) -> Dict[str, torch.Tensor]:
+    """Inputs of the attention-output ShortConv + residual + RMSNorm over the workload's
+    new tokens, hidden width D (default Hq * head_dim, the attention output's width).
+
+    Keys: y [N,D] bf16 (stands in for the o_proj output) and residual [N,D] bf16, both
+    ~ N(0, 1); conv_w [D,4] fp32 ~ N(0, 0.5^2); norm_w [D] fp32 1 + N(0, 0.1^2);
+    conv_state [B,3,D] bf16 ~ N(0, 1) where the sequence has earlier tokens, else zero;
+    state_slot [B]; cu_seqlens_q [B+1].
+    """
+    device = torch.device(device)
+    D = D or w.Hq * w.head_dim
+    N, B = w.N_tok, w.B
+    bf = torch.bfloat16
+    out: Dict[str, torch.Tensor] = {}
+    out["y"] = _normal((N, D), 1.0, device, seed, "y", bf)
+    out["residual"] = _normal((N, D), 1.0, device, seed, "residual", bf)
+    out["conv_w"] = _normal((D, 4), 0.5, device, seed, "oc_conv_w", torch.float32)
+    out["norm_w"] = 1.0 + _normal((D,), 0.1, device, seed, "oc_norm_w", torch.float32)
+    st = _normal((B, 3, D), 1.0, device, seed, "oc_conv_state", bf)
+    for b, p in enumerate(w.prefix_lens):
+        missing = max(0, 3 - p)
+        if missing:
+            st[b, :missing] = 0
+    out["conv_state"] = st
+    out["state_slot"] = torch.arange(B, dtype=torch.int32, device=device)
+    cu = np.zeros(B + 1, dtype=np.int64)
+    cu[1:] = np.cumsum(w.q_lens)
+    out["cu_seqlens_q"] = torch.tensor(cu, dtype=torch.int32, device=device)
     return out
 
 

@@ -17,7 +17,7 @@ import dataclasses
 import torch
 
 from . import inputs as gen
-from .step import AttentionStep
+from .step import AttentionStep, OutputConvStep
 
 
 def main(argv=None):
@@ -27,6 +27,8 @@ def main(argv=None):
     ap.add_argument("--seqs", type=int, default=0, help="keep only the first N sequences")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--splits", type=int, default=0, help="decode splits (0 = the library's heuristic)")
+    ap.add_argument("--output-conv", action="store_true",
+                    help="also run the attention-output conv (hidden width Hq * 128) after each pass")
     args = ap.parse_args(argv)
 
     w = gen.workload(args.workload)
@@ -37,20 +39,25 @@ def main(argv=None):
     x = gen.make_inputs(w, seed=args.seed, device=dev)
     step = AttentionStep(w, x, mode="decode" if args.workload == "decode" else "prefill",
                          num_splits=args.splits)
+    oc = OutputConvStep(w, gen.make_output_conv_inputs(w, seed=args.seed, device=dev)) if args.output_conv else None
     stream = torch.cuda.Stream(device=dev)
     print(w.describe(), f"num_splits={step.num_splits}" if step.mode == "decode" else "")
     with torch.cuda.stream(stream):
         for it in range(args.iters):
-            e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
             e[0].record(stream)
             step.run_prologue(stream)
             e[1].record(stream)
             step.run_attention(stream)
             e[2].record(stream)
+            if oc is not None:
+                oc.run(stream)
+            e[3].record(stream)
             stream.synchronize()
             print(f"pass {it}: prologue {e[0].elapsed_time(e[1]):.4f} ms, "
-                  f"attention {e[1].elapsed_time(e[2]):.4f} ms")
-    status = step.device_status()
+                  f"attention {e[1].elapsed_time(e[2]):.4f} ms"
+                  + (f", output conv {e[2].elapsed_time(e[3]):.4f} ms" if oc is not None else ""))
+    status = step.device_status() | (oc.device_status() if oc is not None else 0)
     print(f"device status {status}")
     if status != 0:
         raise SystemExit(1)

@@ -82,3 +82,31 @@ class AttentionStep:
 
     def device_status(self) -> int:
         return int(self.status.item())
+
+
+class OutputConvStep:
+    """Buffers + call of the attention-output ShortConv with the residual add and the
+    RMSNorm (inkattn_output_conv) over a workload's new tokens.
+
+    `inputs` comes from inputs.make_output_conv_inputs; y stands in for the o_proj
+    output.  The conv state in `inputs` is updated in place by every run; h (the new
+    residual stream) and out (its RMSNorm) are buffers of this object.
+    """
+
+    def __init__(self, w: Workload, inputs: Dict[str, torch.Tensor]):
+        self.w, self.x = w, inputs
+        dev = inputs["y"].device
+        self.h = torch.empty_like(inputs["y"])
+        self.out = torch.empty_like(inputs["y"])
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.p = ia.output_conv_params(
+            y=inputs["y"], conv_w=inputs["conv_w"], norm_w=inputs["norm_w"],
+            cu_seqlens_q=inputs["cu_seqlens_q"], state_slot=inputs["state_slot"],
+            conv_state=inputs["conv_state"], residual=inputs["residual"], h_out=self.h, out=self.out,
+            max_seqlen_q=max(w.q_lens) if w.q_lens else 0, eps=w.eps, dev_status=self.status)
+
+    def run(self, stream=None):
+        ia.inkattn_output_conv(self.p, stream)
+
+    def device_status(self) -> int:
+        return int(self.status.item())

@@ -30,7 +30,8 @@ def test_header_declares_the_entry_points():
     names = set(_declared_functions())
     assert {"inkattn_prologue", "inkattn_prefill", "inkattn_decode", "inkattn_combine",
             "inkattn_decode_num_splits", "inkattn_decode_workspace_bytes",
-            "inkattn_status_string", "inkattn_abi_version"} <= names
+            "inkattn_status_string", "inkattn_abi_version", "inkattn_decode_noalloc",
+            "inkattn_output_conv"} <= names
 
 
 def test_library_exports_every_declared_symbol(ia):
@@ -45,7 +46,8 @@ def test_library_exports_every_declared_symbol(ia):
 
 
 def test_ctypes_structs_match_c_layout(ia, tmp_path):
-    structs = {"inkattn_prologue_params": ia.PrologueParams, "inkattn_attn_params": ia.AttnParams}
+    structs = {"inkattn_prologue_params": ia.PrologueParams, "inkattn_attn_params": ia.AttnParams,
+               "inkattn_output_conv_params": ia.OutputConvParams}
     lines = ["#include <stdio.h>", "#include <stddef.h>", f'#include "{HEADER}"', "int main(void){"]
     for cname, py in structs.items():
         lines.append(f'printf("{cname} sizeof %zu\\n", sizeof({cname}));')
@@ -189,3 +191,45 @@ int main() {{
     subprocess.run(["g++", "-std=c++17", "-pthread", str(src), "-o", str(exe)], check=True)
     out = subprocess.run([str(exe)], capture_output=True, text=True)
     assert out.returncode == 0 and out.stdout.strip() == "ok", (out.returncode, out.stdout, out.stderr)
+
+
+def _oc(ia, **kw):
+    p = ia.OutputConvParams()
+    p.struct_size = ctypes.sizeof(ia.OutputConvParams)
+    p.B, p.N_tok, p.max_seqlen_q, p.D, p.num_state_slots = 2, 32, 16, 8192, 2
+    p.eps = 1e-6
+    big = 32 * 8192 * 2     # bytes of one [N_tok][D] bf16 array
+    base = 1 << 30          # fake, never dereferenced: every array gets its own range
+    for i, f in enumerate(("y", "conv_w", "norm_w", "cu_seqlens_q", "state_slot", "conv_state",
+                           "residual", "h_out", "out")):
+        setattr(p, f, base + i * (big + 4096))
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_output_conv_host_validation(ia):
+    """Validation of inkattn_output_conv runs before it looks for a device: every case
+    here is rejected with INVALID_ARG; a valid struct gets past it (and, without a GPU,
+    stops at the device check)."""
+    L = ia.lib()
+    bad = ia.INKATTN_ERR_INVALID_ARG
+    call = lambda p: ia.inkattn_output_conv(p, stream=0, raise_on_error=False)
+    assert L.inkattn_output_conv(None, None) == bad
+    assert call(_oc(ia, struct_size=8)) == bad
+    assert call(_oc(ia, D=8190)) == bad            # not a multiple of 8
+    assert call(_oc(ia, D=0)) == bad
+    assert call(_oc(ia, D=32776)) == bad           # above 32768
+    assert call(_oc(ia, B=0)) == bad
+    assert call(_oc(ia, eps=-1.0)) == bad
+    assert call(_oc(ia, max_seqlen_q=0)) == bad    # tokens but no rows
+    assert call(_oc(ia, y=None)) == bad
+    assert call(_oc(ia, out=(1 << 30) + 8)) == bad # not 16-byte aligned
+    p = _oc(ia)
+    assert call(_oc(ia, out=p.y)) == bad           # out overlaps y
+    assert call(_oc(ia, h_out=p.y + 64)) == bad    # h_out overlaps y
+    assert call(_oc(ia, out=p.residual)) == bad    # out overlaps the residual
+    assert call(_oc(ia, h_out=p.residual + 16)) == bad   # partial overlap of h_out and residual
+    # in place (h_out == residual) passes validation
+    assert call(_oc(ia, h_out=p.residual)) != bad
+    assert call(_oc(ia)) != bad
