@@ -64,6 +64,12 @@ def _load():
             lib.oracle_attention.restype = I
             lib.oracle_output_conv.argtypes = [I, P, I, P, P, P, I, P, P, P, D, P, P, P]
             lib.oracle_output_conv.restype = I
+            lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_to_f64.restype = D
+            lib.oracle_f64_to_e4m3.argtypes = [D]
+            lib.oracle_f64_to_e4m3.restype = ctypes.c_uint8
+            lib.oracle_quantize_rows_e4m3.argtypes = [P, I, I, P, P]
+            lib.oracle_quantize_rows_e4m3.restype = I
             _lib = lib
     return _lib
 
@@ -245,3 +251,35 @@ def output_conv(*, cu_seqlens_q, D, y, conv_w, state_slot, conv_state, residual,
     if want_conv:
         d["conv"] = conv
     return d
+
+
+def e4m3_to_f64(code: int) -> float:
+    """Value of one E4M3 code (OCP FP8 E4M3FN)."""
+    return float(_load().oracle_e4m3_to_f64(int(code) & 0xFF))
+
+
+def f64_to_e4m3(x: float) -> int:
+    """Nearest E4M3 code to x, ties to even, saturating at 448."""
+    return int(_load().oracle_f64_to_e4m3(float(x)))
+
+
+def quantize_rows_e4m3(x_bits):
+    """Quantise rows of bf16 values (uint16 bits, shape [..., width]) to E4M3 codes with
+    one power-of-two scale per row.  Returns (codes uint8 same shape, scales float32
+    shape [...])."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    width = x.shape[-1]
+    rows = int(np.prod(x.shape[:-1])) if x.ndim > 1 else 1
+    codes = np.zeros(x.shape, dtype=np.uint8)
+    scales = np.zeros(x.shape[:-1], dtype=np.float32)
+    rc = _load().oracle_quantize_rows_e4m3(_ptr(x), rows, width, _ptr(codes), _ptr(scales))
+    if rc != 0:
+        raise ValueError(f"oracle_quantize_rows_e4m3 failed with code {rc}")
+    return codes, scales
+
+
+def dequantize_e4m3(codes, scales) -> np.ndarray:
+    """code * scale for every element (scales broadcast over the last axis), as float64.
+    For the power-of-two scales of quantize_rows_e4m3 the result is exact."""
+    lut = np.array([e4m3_to_f64(c) for c in range(256)], dtype=np.float64)
+    return lut[np.asarray(codes, dtype=np.uint8)] * np.asarray(scales, dtype=np.float64)[..., None]

@@ -47,6 +47,13 @@
  *      h = bf16(residual + conv) (the new residual stream, the sum rounded once), and
  *      out = bf16(h / sqrt(mean_c(h^2) + eps) * g) over the D hidden channels of the
  *      token, from the bf16 h.
+ *   7. FP8 KV cache [SG §Relative Attention と FA4 経路 (the FA4 path runs in MXFP8);
+ *      VJ §フューチャーロードマップ and VV (FP8 for global attention, to relieve compute and
+ *      the KV cache)]: a cache row (one token, one KV head, 128 values, after step 3's
+ *      rounding to bf16) is stored as E4M3 codes with one power-of-two scale 2^k, k the
+ *      smallest integer >= -24 with 448 * 2^k >= max|x| (k = 0 for an all-zero row); each
+ *      code is x / 2^k rounded to the nearest E4M3 value, ties to even.  Reading the row
+ *      back gives code * 2^k exactly; attention (step 5) runs on those values.
  */
 #include <math.h>
 #include <stdint.h>
@@ -383,5 +390,62 @@ int oracle_output_conv(int B, const int32_t *cu_seqlens_q, int D,
     }
     free(cv);
     free(xs);
+    return ORACLE_OK;
+}
+
+/*
+ * E4M3 (OCP FP8, "E4M3FN"): 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits;
+ * subnormals; no infinities; the largest finite magnitude is 448 (S.1111.110) and
+ * S.1111.111 is NaN.
+ */
+double oracle_e4m3_to_f64(uint8_t c) {
+    const int sgn = (c >> 7) & 1, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double v = e == 0 ? ldexp((double)m, -9)                 /* m/8 * 2^(1-7) */
+                            : ldexp(8.0 + (double)m, e - 10);     /* (1 + m/8) * 2^(e-7) */
+    return sgn ? -v : v;
+}
+
+/* The nearest E4M3 value to x, ties to the even code; magnitudes past 448 saturate to 448. */
+uint8_t oracle_f64_to_e4m3(double x) {
+    if (isnan(x)) return 0x7F;
+    const uint8_t sgn = signbit(x) ? 0x80 : 0x00;
+    double a = fabs(x);
+    if (a >= 448.0) return (uint8_t)(sgn | 0x7E);
+    /* candidates are the 127 finite non-negative codes, in increasing order of value */
+    int best = 0;
+    double best_d = a;                           /* distance to code 0 */
+    for (int c = 1; c <= 0x7E; ++c) {
+        const double d = fabs(oracle_e4m3_to_f64((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0 && (best & 1) == 1)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return (uint8_t)(sgn | (uint8_t)best);
+}
+
+/*
+ * Step 7: quantise `rows` rows of `width` bf16 values (x, row-major) to E4M3 codes with
+ * one power-of-two scale per row (scales receive 2^k as fp32).
+ */
+int oracle_quantize_rows_e4m3(const uint16_t *x, int rows, int width, uint8_t *codes, float *scales) {
+    if (rows < 0 || width <= 0) return ORACLE_ERR_ARG;
+    for (int r = 0; r < rows; ++r) {
+        const uint16_t *xr = x + (size_t)r * width;
+        double amax = 0.0;
+        for (int i = 0; i < width; ++i) {
+            const double a = fabs(bf16_bits_to_f64(xr[i]));
+            if (a > amax) amax = a;
+        }
+        int k = 0;
+        if (amax > 0.0) {
+            k = -24;
+            while (ldexp(448.0, k) < amax) ++k;
+        }
+        scales[r] = (float)ldexp(1.0, k);
+        for (int i = 0; i < width; ++i)
+            codes[(size_t)r * width + i] = oracle_f64_to_e4m3(ldexp(bf16_bits_to_f64(xr[i]), -k));
+    }
     return ORACLE_OK;
 }
