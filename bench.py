@@ -91,13 +91,15 @@ def output_conv_bytes(w, D: int) -> float:
     return float(4 * 2 * D * w.N_tok + w.B * 2 * 3 * D * 2 + D * (4 * 4 + 4))
 
 
-def decode_bytes(w) -> float:
-    """Every visible K and V row once per (sequence, KV head), plus q, out, r, P, table."""
+def decode_bytes(w, kv_dtype: str = "bf16") -> float:
+    """Every visible K and V row once per (sequence, KV head), plus q, out, r, P, table.
+    An E4M3 row is 128 one-byte codes and a 4-byte scale."""
+    row = w.head_dim * 2 if kv_dtype == "bf16" else w.head_dim + 4
     kv = 0
     for n, pre in zip(w.q_lens, w.prefix_lens):
         T = n + pre
         first = 0 if w.window == 0 else max(0, pre - w.window + 1)
-        kv += (T - first) * w.Hkv * w.head_dim * 2 * 2
+        kv += (T - first) * w.Hkv * row * 2
     q = w.N_tok * w.Hq * w.head_dim * 2
     r = w.N_tok * w.Hq * w.d_r * 2
     P = w.Hq * w.d_r * w.rel_extent * 4
@@ -243,6 +245,7 @@ class HostCopy:
         from relative_bias_hybrid_gb300 import inputs as gen
         self.w = w
         self.B_full = w.B
+        self.e4m3 = False
         if seqs is None:
             self.x = {k: x[k].cpu() for k in ("cu_seqlens_q", "seqlen_k", "r", "P", "block_table")}
             self.q = gen.bits(q_out)
@@ -259,8 +262,14 @@ class HostCopy:
             table[i, :n] = np.arange(len(blocks), len(blocks) + n)
             blocks.extend(bt[b, :n].tolist())
         idx = torch.as_tensor(np.asarray(blocks, np.int64), device=x["k_cache"].device)
-        self.kc = gen.bits(x["k_cache"].index_select(0, idx))
-        self.vc = gen.bits(x["v_cache"].index_select(0, idx))
+        self.e4m3 = x["k_cache"].dtype == torch.uint8
+        if self.e4m3:
+            # codes and row scales; the oracle leg dequantises them
+            self.kc = (x["k_cache"].index_select(0, idx).cpu().numpy(), x["k_scale"].index_select(0, idx).cpu().numpy())
+            self.vc = (x["v_cache"].index_select(0, idx).cpu().numpy(), x["v_scale"].index_select(0, idx).cpu().numpy())
+        else:
+            self.kc = gen.bits(x["k_cache"].index_select(0, idx))
+            self.vc = gen.bits(x["v_cache"].index_select(0, idx))
         rows = np.concatenate([np.arange(cu[b], cu[b + 1]) for b in seqs]).astype(np.int64)
         ridx = torch.as_tensor(rows, device=q_out.device)
         self.q = gen.bits(q_out.index_select(0, ridx))
@@ -308,6 +317,15 @@ def cpu_baseline_decode(h, target_s):
     import dataclasses
     import oracle
     oracle.build()
+    if h.e4m3:
+        # the cache the decode reads: code * scale, exact in bf16
+        from relative_bias_hybrid_gb300 import inputs as gen
+        h.kc, h.vc = (gen.bits(torch.from_numpy(oracle.dequantize_e4m3(c, sc)).to(torch.bfloat16))
+                      for c, sc in (h.kc, h.vc))
+        h.e4m3 = False
+        kv = "e4m3"
+    else:
+        kv = "bf16"
     cores = host_cores()
     cu = h.x["cu_seqlens_q"].numpy()
     n_seq = 1
@@ -318,7 +336,7 @@ def cpu_baseline_decode(h, target_s):
             break
         n_seq = int(min(h.w.B, max(n_seq + 1, n_seq * target_s / max(dt, 1e-3))))
     sub = dataclasses.replace(h.w, q_lens=h.w.q_lens[:n_seq], prefix_lens=h.w.prefix_lens[:n_seq])
-    nbytes = decode_bytes(sub)
+    nbytes = decode_bytes(sub, kv)
     return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"{n_seq} of {h.B_full} sequences (all {cu[n_seq]} query rows, all {h.w.Hq} heads), "
                       f"{nbytes:.3g} algorithmic bytes in {dt:.1f} s"}
@@ -492,9 +510,10 @@ def measure(name, args, peaks, dev, stream, flush):
     oracle sample needs."""
     from relative_bias_hybrid_gb300 import inputs as gen
     from relative_bias_hybrid_gb300.step import AttentionStep
-    w = gen.workload(name)
-    mode = "decode" if name == "decode" else "prefill"
-    x = gen.make_inputs(w, seed=0, device=dev)
+    kv = "e4m3" if name.endswith("_e4m3") else "bf16"
+    w = gen.workload(name.replace("_e4m3", ""))
+    mode = "decode" if name.startswith("decode") else "prefill"
+    x = gen.make_inputs(w, seed=0, device=dev, kv_dtype=kv)
     step = AttentionStep(w, x, mode=mode)
     tot, att, pro = timed_steps(step, args.steps, args.warmup, flush, stream)
     if step.device_status() != 0:
@@ -514,8 +533,10 @@ def measure(name, args, peaks, dev, stream, flush):
     # timed: the step loop, the attention loop, the prologue loop, the end-to-end loop
     n_att = step.launches_per_run() - 1
     launches = args.steps * (2 * step.launches_per_run() + n_att + 1)
-    oc_roof, oc_launches = time_output_conv(w, args, dev, stream, flush, peaks, name)
-    launches += oc_launches
+    oc_roof = None
+    if kv == "bf16":            # (the output conv does not depend on the cache type)
+        oc_roof, oc_launches = time_output_conv(w, args, dev, stream, flush, peaks, name)
+        launches += oc_launches
 
     pro_bytes = prologue_bytes(w)
     prologue = {"bound": "hbm", "kernel": "k_prologue", "achieved": pro_bytes / (pro_ms * 1e-3) / 1e9,
@@ -531,27 +552,28 @@ def measure(name, args, peaks, dev, stream, flush):
                 "algorithmic_flop_per_launch": fl, "ms": att_ms}
         rep = {"workload": w.describe() + "; step = inkattn_prologue + inkattn_prefill",
                "value": fl / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
-               "roofline": roof, "rooflines": {"k_prologue": prologue, "k_output_conv": oc_roof},
+               "roofline": roof, "rooflines": {"k_prologue": prologue, **({"k_output_conv": oc_roof} if oc_roof else {})},
                "e2e": {"value": fl / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}}
         host = HostCopy(w, x, step.q_out)
     else:
-        nbytes = decode_bytes(w)
+        nbytes = decode_bytes(w, kv)
         gbs = nbytes / (att_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "kernel": "k_decode_tc" + ("+k_combine" if step.num_splits > 1 else ""),
                 "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"],
                 "peak_src": peaks["src"] + " (copy bandwidth)", "traffic": ncu_traffic("k_decode_tc", name),
                 "algorithmic_bytes_per_launch": nbytes, "ms": att_ms, "num_splits": step.num_splits}
-        rep = {"workload": w.describe() + "; step = inkattn_prologue + inkattn_decode (+ inkattn_combine)",
+        rep = {"workload": w.describe() + (", E4M3 KV cache with a power-of-two scale per row" if kv == "e4m3" else "")
+                           + "; step = inkattn_prologue + inkattn_decode (+ inkattn_combine)",
                "value": nbytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
-               "roofline": roof, "rooflines": {"k_prologue": prologue, "k_output_conv": oc_roof},
+               "roofline": roof, "rooflines": {"k_prologue": prologue, **({"k_output_conv": oc_roof} if oc_roof else {})},
                "e2e": {"value": nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}}
         host = HostCopy(w, x, step.q_out, seqs=list(range(DECODE_ORACLE_SEQS)))
     return rep, launches, host
 
 
-WORKLOADS = ("full", "swa", "ragged", "decode")
+WORKLOADS = ("full", "swa", "ragged", "decode", "decode_e4m3")
 
 
 def run_gpu(args):

@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define INKATTN_ABI_VERSION 1
+#define INKATTN_ABI_VERSION 2
 
 /* The library is built with hidden visibility; only these entry points are exported. */
 #if defined(__GNUC__)
@@ -63,6 +63,25 @@ typedef uint16_t inkattn_bf16;
 /* Element type of the attention output. */
 #define INKATTN_DTYPE_BF16 0
 #define INKATTN_DTYPE_F32 1
+
+/* Element type of the paged KV cache (kv_dtype).
+ * INKATTN_KV_BF16: k_cache and v_cache hold bf16 values.
+ * INKATTN_KV_E4M3: they hold OCP FP8 E4M3 codes (1 byte per value, same
+ *   [num_blocks][Hkv][64][128] layout), and k_scale / v_scale hold one fp32 scale per
+ *   row ([num_blocks][Hkv][64]): the row's values are code * scale.  The prologue writes
+ *   scale = 2^k, k the smallest integer >= -24 with 448 * 2^k >= the row's largest
+ *   magnitude (1 for an all-zero row), and each code as the nearest E4M3 value to
+ *   x / 2^k (ties to even), where x is the bf16 value the bf16 cache would hold; the
+ *   dequantised value is exact.  [SG §Relative Attention と FA4 経路: MXFP8 on the FA4
+ *   path; VJ §フューチャーロードマップ and VV: FP8 for the global-attention layers.]
+ *   The decode reads such a cache; prefill over it returns INKATTN_ERR_UNSUPPORTED.
+ *   The decode expands each row to f16 (code * scale, exact for the prologue's scales
+ *   down to 2^-15; below, values under 2^-24 flush) and requires every scale to lie in
+ *   [2^-24, 2^7], which the prologue's scales do for rows whose magnitudes stay below
+ *   57344; a scale outside that range is flagged as INKATTN_ERR_DEVICE_BOUNDS and its
+ *   row read as zeros. */
+#define INKATTN_KV_BF16 0
+#define INKATTN_KV_E4M3 1
 
 typedef enum inkattn_status {
     INKATTN_OK = 0,
@@ -96,7 +115,9 @@ INKATTN_API int inkattn_abi_version(void);
  *   kn    = kc / sqrt(mean(kc^2) + eps) * k_norm_w
  * [SG §Inkling のモデルアーキテクチャ: ShortConv on K and V before the Q/K normalisation].
  * Then, with slot = slot_mapping[t]: k_cache[slot/64][hk][slot%64][:] = kn,
- * v_cache[...] = vc.  V is not normalised and Q is not convolved.
+ * v_cache[...] = vc (with kv_dtype = INKATTN_KV_E4M3: their E4M3 codes, and the row
+ * scales to k_scale / v_scale[slot/64][hk][slot%64]).  V is not normalised and Q is not
+ * convolved.
  * ------------------------------------------------------------------------------ */
 typedef struct inkattn_prologue_params {
     size_t struct_size;        /* = sizeof(inkattn_prologue_params)                      */
@@ -122,8 +143,11 @@ typedef struct inkattn_prologue_params {
     inkattn_bf16 *conv_state_k;    /* [num_state_slots][3][C], read then overwritten     */
     inkattn_bf16 *conv_state_v;    /* [num_state_slots][3][C]                            */
     inkattn_bf16 *q_out;           /* [N_tok][Hq][128]                                   */
-    inkattn_bf16 *k_cache;         /* [num_blocks][Hkv][64][128]                         */
-    inkattn_bf16 *v_cache;         /* [num_blocks][Hkv][64][128]                         */
+    void *k_cache;                 /* [num_blocks][Hkv][64][128], bf16 or E4M3 (kv_dtype) */
+    void *v_cache;                 /* [num_blocks][Hkv][64][128]                         */
+    int32_t kv_dtype;              /* INKATTN_KV_BF16 (0) or INKATTN_KV_E4M3 (1)          */
+    float *k_scale;                /* E4M3 only: [num_blocks][Hkv][64] row scales, 16-byte */
+    float *v_scale;                /* aligned; written for the mapped slots (else NULL)   */
     int32_t *dev_status;           /* nullable, see the conventions above                */
 } inkattn_prologue_params;
 
@@ -181,8 +205,11 @@ typedef struct inkattn_attn_params {
     const float *P;            /* [Hq][rel_extent][d_r]: per query head, per distance,   */
                                /* the d_r projection weights; 16-byte aligned (nullable  */
                                /* iff rel_extent == 0)                                   */
-    const inkattn_bf16 *k_cache;   /* [num_blocks][Hkv][64][128]                         */
-    const inkattn_bf16 *v_cache;   /* [num_blocks][Hkv][64][128]                         */
+    const void *k_cache;           /* [num_blocks][Hkv][64][128], bf16 or E4M3 (kv_dtype) */
+    const void *v_cache;           /* [num_blocks][Hkv][64][128]                         */
+    int32_t kv_dtype;              /* INKATTN_KV_BF16 (0) or INKATTN_KV_E4M3 (1)          */
+    const float *k_scale;          /* E4M3 only: [num_blocks][Hkv][64] row scales, 16-byte */
+    const float *v_scale;          /* aligned (else NULL)                                */
     const int32_t *cu_seqlens_q;   /* [B+1]                                              */
     const int32_t *seqlen_k;       /* [B], q_len[b] <= seqlen_k[b] <= max_seqlen_k       */
     const int32_t *block_table;    /* [B][max_blocks_per_seq]                            */

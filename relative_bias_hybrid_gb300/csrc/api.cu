@@ -85,6 +85,10 @@ inkattn_status validate_prologue(const inkattn_prologue_params *p) {
     for (const void *ptr : ptrs4)
         if (!ptr || !aligned(ptr, 4)) return INKATTN_ERR_INVALID_ARG;
     if (p->dev_status && !aligned(p->dev_status, 4)) return INKATTN_ERR_INVALID_ARG;
+    if (p->kv_dtype != INKATTN_KV_BF16 && p->kv_dtype != INKATTN_KV_E4M3) return INKATTN_ERR_INVALID_ARG;
+    if (p->kv_dtype == INKATTN_KV_E4M3 &&
+        (!p->k_scale || !p->v_scale || !aligned(p->k_scale, 16) || !aligned(p->v_scale, 16)))
+        return INKATTN_ERR_INVALID_ARG;
     return INKATTN_OK;
 }
 
@@ -137,6 +141,10 @@ inkattn_status validate_attn(const inkattn_attn_params *p) {
         if (!ptr || !aligned(ptr, 4)) return INKATTN_ERR_INVALID_ARG;
     if (p->lse && !aligned(p->lse, 4)) return INKATTN_ERR_INVALID_ARG;
     if (p->dev_status && !aligned(p->dev_status, 4)) return INKATTN_ERR_INVALID_ARG;
+    if (p->kv_dtype != INKATTN_KV_BF16 && p->kv_dtype != INKATTN_KV_E4M3) return INKATTN_ERR_INVALID_ARG;
+    if (p->kv_dtype == INKATTN_KV_E4M3 &&
+        (!p->k_scale || !p->v_scale || !aligned(p->k_scale, 16) || !aligned(p->v_scale, 16)))
+        return INKATTN_ERR_INVALID_ARG;
     if (p->rel_extent > 0) {
         if (p->d_r != 32) return INKATTN_ERR_UNSUPPORTED;
         if (!p->r || !p->P || !aligned(p->r, 16) || !aligned(p->P, 16)) return INKATTN_ERR_INVALID_ARG;
@@ -155,7 +163,10 @@ inkattn_status validate_locations(const inkattn_attn_params *p) {
         (void)cudaGetLastError();
         return INKATTN_ERR_INVALID_ARG;
     }
-    const void *ptrs[] = {p->q, p->k_cache, p->v_cache};
+    const bool f8 = p->kv_dtype == INKATTN_KV_E4M3;
+    const void *q = p->q;
+    const void *ptrs[] = {q, p->k_cache, p->v_cache, f8 ? static_cast<const void *>(p->k_scale) : q,
+                          f8 ? static_cast<const void *>(p->v_scale) : q};
     for (const void *ptr : ptrs) {
         cudaPointerAttributes a;
         if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
@@ -288,6 +299,18 @@ bool make_cache_map(CUtensorMap *map, const void *base, long long rows) {
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_cache_map_e4m3(CUtensorMap *map, const void *base, long long rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)kHeadDim};
+    cuuint32_t box[2] = {(cuuint32_t)kHeadDim, (cuuint32_t)kBlock};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_q_map(CUtensorMap *map, const void *base, int n_tok, int hq, int box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
     if (!enc) return false;
@@ -351,6 +374,7 @@ inkattn_status inkattn_output_conv(const inkattn_output_conv_params *p, void *st
 inkattn_status inkattn_prefill(const inkattn_attn_params *p, void *stream) {
     inkattn_status st = validate_attn(p);
     if (st != INKATTN_OK) return st;
+    if (p->kv_dtype != INKATTN_KV_BF16) return INKATTN_ERR_UNSUPPORTED;
     if ((st = validate_locations(p)) != INKATTN_OK) return st;
     if ((st = check_device(nullptr)) != INKATTN_OK) return st;
     if (p->N_tok == 0) return INKATTN_OK;
@@ -396,7 +420,8 @@ inkattn_status inkattn_decode(const inkattn_attn_params *p, int num_splits, void
     if (p->N_tok == 0) return INKATTN_OK;
     CUtensorMap qmap, kmap, vmap;
     const long long rows = (long long)p->num_blocks * p->Hkv * kBlock;
-    if (!make_cache_map(&kmap, p->k_cache, rows) || !make_cache_map(&vmap, p->v_cache, rows) ||
+    auto cache_map = p->kv_dtype == INKATTN_KV_E4M3 ? make_cache_map_e4m3 : make_cache_map;
+    if (!cache_map(&kmap, p->k_cache, rows) || !cache_map(&vmap, p->v_cache, rows) ||
         !make_q_group_map(&qmap, p->q, p->N_tok, p->Hq, p->Hq / p->Hkv, p->max_seqlen_q))
         return INKATTN_ERR_CUDA;
     return launch_status(launch_decode_tc(*p, scalars(*p), S, ws_o, ws_lse, qmap, kmap, vmap,

@@ -136,6 +136,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, int c
         : "memory");
 }
 
+// 1D bulk copy global -> shared: both addresses 16-byte aligned, bytes a multiple of 16;
+// completes on the mbarrier's transaction count
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, int c0, int c1, int c2,
                                             uint32_t bar) {
     asm volatile(

@@ -40,6 +40,7 @@
 // rescaled only when the running maximum grows by more than 8).  The epilogue writes O / l
 // and the natural-log LSE: straight to `out` with one split, else to the split workspace.
 #include "common.cuh"
+#include "fp8.cuh"
 #include "internal.h"
 #include "tcgen05.cuh"
 
@@ -49,35 +50,52 @@ namespace {
 
 constexpr int kRows = 128;                 // MMA M: (token, query head) rows, padded
 constexpr int kKeys = 128;                 // keys per tile (two cache blocks)
-constexpr int kSlots = 4;                  // K/V ring slots
-constexpr int kSlotBytes = 32768;          // one K or V tile: [d half][128 keys][128 B]
-constexpr int kThreads = 320;              // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
+constexpr int kSlotBytes = 32768;          // one MMA operand tile: [d half][128 keys][128 B]
 constexpr int kTabW = 144;                 // distances per table row: 128 keys + up to 16 tokens
 constexpr int kTabRows = kDecodeMaxRows;   // g * ql <= 128
+constexpr int kF8TileBytes = kKeys * kHeadDim;           // one E4M3 tile: [128 keys][128 B]
+constexpr int kF8SlotBytes = kF8TileBytes + kKeys * 4;   // + its 128 row scales
 
-constexpr int kOffQ = 0;
-constexpr int kOffKV = 32768;
-constexpr int kOffTab = kOffKV + kSlots * kSlotBytes;              // 16-bit fixed point [g][ql][kTabW]
-constexpr int kOffXchg = kOffTab + kTabRows * kTabW * 2;           // row maxima / sums
-constexpr int kOffTsig = kOffXchg + 3 * 2 * kRows * 4;             // fp32 steps [g][ql][2 rounds]
-constexpr int kOffBar = kOffTsig + kTabRows * 2 * 4;
-
-// mbarrier indices, laid out from the slot count
-enum Bar {
-    B_Q = 0,
-    B_KV_FULL = 1,
-    B_KV_EMPTY = B_KV_FULL + kSlots,
-    B_S_FULL = B_KV_EMPTY + kSlots,
-    B_P_FULL = B_S_FULL + 2,
-    B_PV_DONE = B_P_FULL + 2,
-    B_TAB_FULL = B_PV_DONE + 2,
-    B_TAB_FREE = B_TAB_FULL + 1,
-    B_DRAIN = B_TAB_FREE + 1,
-    B_PAIR = B_DRAIN + 1,
-    B_COUNT = B_PAIR + 4
+// Two variants.  kF8 = false (bf16 cache): TMA loads K/V tiles straight into the MMAs'
+// 4-slot ring.  kF8 = true (E4M3 cache): TMA loads E4M3 tiles and their row scales into a
+// 3-slot ring, and four converter warps (4-7) expand each tile (code * scale, exactly) to
+// f16 in a 3-slot MMA ring; warps 2-3 convert Q to f16 in place, and P is packed as f16, so
+// the MMAs run kind::f16 on f16 operands.  Warps: 0 TMA, 1 MMA, [2, 8) converters (E4M3
+// only), then 8 softmax warps.
+template <bool kF8>
+struct Dec {
+    static constexpr int kThreads = kF8 ? 512 : 320;
+    static constexpr int kWarpSm = kF8 ? 8 : 2;              // first softmax warp
+    static constexpr int kConvThreads = kF8 ? 128 : 0;       // tile converters (warps 4-7)
+    static constexpr int kSlots = kF8 ? 3 : 4;               // MMA operand ring
+    static constexpr int kF8Slots = kF8 ? 3 : 0;             // E4M3 ring
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffKV = 32768;
+    static constexpr int kOffF8 = kOffKV + kSlots * kSlotBytes;
+    static constexpr int kOffTab = kOffF8 + kF8Slots * kF8SlotBytes;   // 16-bit fixed point [g][ql][kTabW]
+    static constexpr int kOffXchg = kOffTab + kTabRows * kTabW * 2;     // row maxima / sums
+    static constexpr int kOffTsig = kOffXchg + 3 * 2 * kRows * 4;       // fp32 steps [g][ql][2 rounds]
+    static constexpr int kOffBar = kOffTsig + kTabRows * 2 * 4;
+    // mbarrier indices, laid out from the slot counts
+    static constexpr int B_Q = 0;
+    static constexpr int B_KV_FULL = 1;
+    static constexpr int B_KV_EMPTY = B_KV_FULL + kSlots;
+    static constexpr int B_S_FULL = B_KV_EMPTY + kSlots;
+    static constexpr int B_P_FULL = B_S_FULL + 2;
+    static constexpr int B_PV_DONE = B_P_FULL + 2;
+    static constexpr int B_TAB_FULL = B_PV_DONE + 2;
+    static constexpr int B_TAB_FREE = B_TAB_FULL + 1;
+    static constexpr int B_DRAIN = B_TAB_FREE + 1;
+    static constexpr int B_PAIR = B_DRAIN + 1;
+    static constexpr int B_QF = B_PAIR + 4;                  // E4M3: Q converted to f16
+    static constexpr int B_F8_FULL = B_QF + 1;
+    static constexpr int B_F8_EMPTY = B_F8_FULL + kF8Slots;
+    static constexpr int B_COUNT = B_F8_EMPTY + kF8Slots;
+    static constexpr int kSmem = kOffBar + B_COUNT * 8 + 16;
+    static_assert(kSmem <= 232448, "shared memory budget");
+    static_assert(kOffKV % 1024 == 0 && kOffF8 % 1024 == 0 && kF8SlotBytes % 128 == 0, "alignment of the rings");
+    static_assert(kThreads == 32 * (kWarpSm + 8), "eight softmax warps last");
 };
-constexpr int kSmem = kOffBar + B_COUNT * 8 + 16;
-static_assert(kSmem <= 232448, "shared memory budget");
 
 constexpr uint32_t kTmemO = 0, kTmemS0 = 128;
 
@@ -95,11 +113,13 @@ struct DecTcArgs {
 
 }  // namespace
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kF8>
+__global__ void __launch_bounds__(Dec<kF8>::kThreads, 1)
 k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
             const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
     extern __shared__ __align__(1024) unsigned char smem[];
     grid_dep_wait();                                   // q and the cache: written by the prologue
+    using C = Dec<kF8>;
     const inkattn_attn_params &p = A.p;
     const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -131,7 +151,7 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
 
     if (N == 0) {
         // an empty split: its partial result is empty (O = 0, LSE = -inf)
-        for (int idx = threadIdx.x; idx < n_rows * (kHeadDim / 4); idx += kThreads) {
+        for (int idx = threadIdx.x; idx < n_rows * (kHeadDim / 4); idx += C::kThreads) {
             const int row = idx / (kHeadDim / 4), c4 = idx - row * (kHeadDim / 4);
             const int t = g_shift >= 0 ? row >> g_shift : row / g, hh = row - t * g;
             const size_t qrow = (size_t)(start + t) * p.Hq + hk * g + hh;
@@ -147,29 +167,36 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
         if (threadIdx.x == 0) set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
         return;
     }
-    auto bar = [&](int i) { return s_base + kOffBar + 8u * (uint32_t)i; };
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffBar + B_COUNT * 8);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffBar + B_COUNT * 8 + 4);
+    auto bar = [&](int i) { return s_base + C::kOffBar + 8u * (uint32_t)i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffBar + C::B_COUNT * 8);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffBar + C::B_COUNT * 8 + 4);
     auto wwait = [&](uint32_t addr, uint32_t parity) -> bool {
         const bool r = mbar_wait(addr, parity, p.dev_status, abort_flag, A.wait_ns);
         return __all_sync(0xffffffffu, r);
     };
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(B_Q), 1);
-        for (int s = 0; s < kSlots; ++s) {
-            mbar_init(bar(B_KV_FULL + s), 1);
-            mbar_init(bar(B_KV_EMPTY + s), 1);
+        mbar_init(bar(C::B_Q), 1);
+        for (int s = 0; s < C::kSlots; ++s) {
+            mbar_init(bar(C::B_KV_FULL + s), kF8 ? C::kConvThreads : 1);   // tile converters, or the TMA
+            mbar_init(bar(C::B_KV_EMPTY + s), 1);
+        }
+        if constexpr (kF8) {
+            mbar_init(bar(C::B_QF), 64);                                  // the two Q converter warps
+            for (int s = 0; s < C::kF8Slots; ++s) {
+                mbar_init(bar(C::B_F8_FULL + s), 1);
+                mbar_init(bar(C::B_F8_EMPTY + s), C::kConvThreads);
+            }
         }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(B_S_FULL + s), 1);
-            mbar_init(bar(B_P_FULL + s), 256);
-            mbar_init(bar(B_PV_DONE + s), 1);
+            mbar_init(bar(C::B_S_FULL + s), 1);
+            mbar_init(bar(C::B_P_FULL + s), 256);
+            mbar_init(bar(C::B_PV_DONE + s), 1);
         }
-        mbar_init(bar(B_TAB_FULL), 256);
-        mbar_init(bar(B_TAB_FREE), 256);
-        mbar_init(bar(B_DRAIN), 1);
-        for (int q = 0; q < 4; ++q) mbar_init(bar(B_PAIR + q), 64);
+        mbar_init(bar(C::B_TAB_FULL), 256);
+        mbar_init(bar(C::B_TAB_FREE), 256);
+        mbar_init(bar(C::B_DRAIN), 1);
+        for (int q = 0; q < 4; ++q) mbar_init(bar(C::B_PAIR + q), 64);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -186,21 +213,28 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
     const float c_qk = lam * A.scale * kLog2e;       // S (with the bias folded in) -> log2 logit
     const float inv_scale = 1.f / A.scale;           // bias in S units
 
+    // E4M3 variant (512 threads, 128 registers each at launch): the warpgroups of the TMA,
+    // MMA and converter warps give registers to the two softmax warpgroups (80 + 176).
     if (warp == 0) {
         // ================================ producer ================================
+        if constexpr (kF8) tc::reg_dealloc<80>();
         bool ok = true;
         if (lane == 0) {
             tma_prefetch_desc(&qmap);
             tma_prefetch_desc(&kmap);
             tma_prefetch_desc(&vmap);
             const uint32_t qbytes = (uint32_t)(2 * 64 * 2 * g * A.ql);
-            mbar_arrive_expect_tx(bar(B_Q), qbytes);
-            tma_load_3d(s_base + kOffQ, &qmap, 0, hk * g, start, bar(B_Q));
-            tma_load_3d(s_base + kOffQ + 16384, &qmap, 64, hk * g, start, bar(B_Q));
+            mbar_arrive_expect_tx(bar(C::B_Q), qbytes);
+            tma_load_3d(s_base + C::kOffQ, &qmap, 0, hk * g, start, bar(C::B_Q));
+            tma_load_3d(s_base + C::kOffQ + 16384, &qmap, 64, hk * g, start, bar(C::B_Q));
         }
+        // the ring the TMA fills: the MMAs' own (bf16 cache) or the E4M3 one
+        constexpr int kRing = kF8 ? C::kF8Slots : C::kSlots;
+        constexpr int kRingFull = kF8 ? C::B_F8_FULL : C::B_KV_FULL;
+        constexpr int kRingEmpty = kF8 ? C::B_F8_EMPTY : C::B_KV_EMPTY;
         int kv_loads = 0;
         auto load_kv = [&](int n, int isv) -> bool {
-            const int L = kv_loads++, slot = L % kSlots;
+            const int L = kv_loads++, slot = L % kRing;
             // the tile's block-table entries are read before the wait for the slot, so that
             // their round trip to memory overlaps it instead of delaying the copy
             int blk[2];                                      // -2: past this split's range
@@ -211,24 +245,54 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
                           : lb < p.max_blocks_per_seq ? __ldg(p.block_table + (size_t)b * p.max_blocks_per_seq + lb)
                           : -1;
             }
-            if (L >= kSlots && !wwait(bar(B_KV_EMPTY + slot), ((L / kSlots) - 1) & 1)) {
+            if (L >= kRing && !wwait(bar(kRingEmpty + slot), ((L / kRing) - 1) & 1)) {
                 --kv_loads;                                  // not issued
                 return false;
             }
-            if (lane == 0) {
-                const uint32_t dst = s_base + kOffKV + slot * kSlotBytes;
-                const uint32_t fb = bar(B_KV_FULL + slot);
-                mbar_arrive_expect_tx(fb, kSlotBytes);
-                const void *map = isv ? static_cast<const void *>(&vmap) : static_cast<const void *>(&kmap);
+            const void *map = isv ? static_cast<const void *>(&vmap) : static_cast<const void *>(&kmap);
+            long long row[2];
+            bool have[2];
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    long long row = A.kv_rows;                   // past the tensor: TMA fills zeros
-                    if (blk[half] != -2) {
-                        if (blk[half] >= 0 && blk[half] < p.num_blocks) row = ((long long)blk[half] * p.Hkv + hk) * kBlock;
-                        else set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
+            for (int half = 0; half < 2; ++half) {
+                row[half] = A.kv_rows;                       // past the tensor: TMA fills zeros
+                have[half] = blk[half] >= 0 && blk[half] < p.num_blocks;
+                if (have[half]) row[half] = ((long long)blk[half] * p.Hkv + hk) * kBlock;
+            }
+            if constexpr (!kF8) {
+                if (lane == 0) {
+                    const uint32_t dst = s_base + C::kOffKV + slot * kSlotBytes;
+                    const uint32_t fb = bar(C::B_KV_FULL + slot);
+                    mbar_arrive_expect_tx(fb, kSlotBytes);
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        if (blk[half] != -2 && !have[half]) set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
+                        tma_load_2d(dst + half * 8192, map, 0, (int)row[half], fb);
+                        tma_load_2d(dst + 16384 + half * 8192, map, 64, (int)row[half], fb);
                     }
-                    tma_load_2d(dst + half * 8192, map, 0, (int)row, fb);
-                    tma_load_2d(dst + 16384 + half * 8192, map, 64, (int)row, fb);
+                }
+            } else {
+                // codes [128 keys][128 B], then the 128 row scales; a half without a loaded
+                // block reads as zero codes (TMA fill) with zero scales (written here)
+                unsigned char *slot_p = smem + C::kOffF8 + slot * kF8SlotBytes;
+                float *sc = reinterpret_cast<float *>(slot_p + kF8TileBytes);
+#pragma unroll
+                for (int half = 0; half < 2; ++half)
+                    if (!have[half]) {
+                        sc[half * 64 + lane] = 0.f;
+                        sc[half * 64 + 32 + lane] = 0.f;
+                    }
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t dst = smem_u32(slot_p);
+                    const uint32_t fb = bar(C::B_F8_FULL + slot);
+                    mbar_arrive_expect_tx(fb, kF8TileBytes + 256u * (uint32_t)(have[0] + have[1]));
+                    const float *scales = isv ? p.v_scale : p.k_scale;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        if (blk[half] != -2 && !have[half]) set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
+                        tma_load_2d(dst + half * 8192, map, 0, (int)row[half], fb);
+                        if (have[half]) bulk_load(dst + kF8TileBytes + half * 256, scales + row[half], 256u, fb);
+                    }
                 }
             }
             __syncwarp();
@@ -242,33 +306,35 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
         }
         if (ok) ok = load_kv(N - 1, 1);
         // nothing may still be landing in shared memory when the CTA tears down, also when a
-        // role gave up: the copies issued and not yet consumed are the last kSlots
+        // role gave up: the copies issued and not yet consumed are the last kRing
         if (lane == 0) {
-            mbar_drain(bar(B_Q), 0, p.dev_status, A.wait_ns);
-            for (int L = max(0, kv_loads - kSlots); L < kv_loads; ++L)
-                mbar_drain(bar(B_KV_FULL + L % kSlots), (L / kSlots) & 1, p.dev_status, A.wait_ns);
+            mbar_drain(bar(C::B_Q), 0, p.dev_status, A.wait_ns);
+            for (int L = max(0, kv_loads - kRing); L < kv_loads; ++L)
+                mbar_drain(bar(kRingFull + L % kRing), (L / kRing) & 1, p.dev_status, A.wait_ns);
         }
     } else if (warp == 1) {
         // ================================ MMA issuer ================================
-        const uint32_t id_qk = tc::idesc(128, 128, tc::kFmtBF16, 0, 0);
-        const uint32_t id_pv = tc::idesc(128, 128, tc::kFmtBF16, 0, 1);
+        if constexpr (kF8) tc::reg_dealloc<80>();
+        constexpr uint32_t kFmt = kF8 ? tc::kFmtF16 : tc::kFmtBF16;   // both operands alike
+        const uint32_t id_qk = tc::idesc(128, 128, kFmt, 0, 0);
+        const uint32_t id_pv = tc::idesc(128, 128, kFmt, 0, 1);
         // the whole warp runs this loop with the same values in every lane (the MMAs and
         // commits are warp-collective); per-slot descriptors differ only in the start address
         // field, which stays below its 14 bits (shared memory < 256 KB)
-        const uint64_t dq = tc::sdesc_sw128(s_base + kOffQ, 16, 1024);
-        const uint64_t dk0 = tc::sdesc_sw128(s_base + kOffKV, 16, 1024);
-        const uint64_t dv0 = tc::sdesc_sw128(s_base + kOffKV, 16384, 1024);
+        const uint64_t dq = tc::sdesc_sw128(s_base + C::kOffQ, 16, 1024);
+        const uint64_t dk0 = tc::sdesc_sw128(s_base + C::kOffKV, 16, 1024);
+        const uint64_t dv0 = tc::sdesc_sw128(s_base + C::kOffKV, 16384, 1024);
         auto slot_off = [](int slot) { return (uint64_t)(slot * (kSlotBytes >> 4)); };
-        bool ok = wwait(bar(B_Q), 0);
+        bool ok = wwait(bar(kF8 ? C::B_QF : C::B_Q), 0);      // (E4M3: Q once converted to f16)
         int kv_used = 0;
         auto next_tile = [&](int &slot, bool &last) -> bool {
             const int L = kv_used++;
-            slot = L % kSlots;
-            last = L + kSlots >= 2 * N;
-            return wwait(bar(B_KV_FULL + slot), (L / kSlots) & 1);
+            slot = L % C::kSlots;
+            last = L + C::kSlots >= 2 * N;
+            return wwait(bar(C::B_KV_FULL + slot), (L / C::kSlots) & 1);
         };
         auto issue_pv = [&](int m) -> bool {
-            if (!wwait(bar(B_P_FULL + (m & 1)), (m >> 1) & 1)) return false;
+            if (!wwait(bar(C::B_P_FULL + (m & 1)), (m >> 1) & 1)) return false;
             int slot;
             bool last;
             if (!next_tile(slot, last)) return false;
@@ -278,7 +344,7 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
             const int nvalid = max(0, min(kKeys, T - j0));
             const int nload = min(kKeys, (my_hi - my_lo - 2 * m) * kBlock);
             if (nvalid < nload) {
-                unsigned char *vp = smem + kOffKV + slot * kSlotBytes;
+                unsigned char *vp = smem + C::kOffKV + slot * kSlotBytes;
                 const int rows = nload - nvalid;
                 for (int idx = lane; idx < rows * 16; idx += 32) {
                     const int key = nvalid + idx / 16, dh = (idx >> 3) & 1, ch = idx & 7;
@@ -290,8 +356,8 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
             }
             tc::fence_after();
             tc::mma_bf16_ts_k128_commit<false>(tmem + kTmemO, tmem + kTmemS0 + (uint32_t)(m & 1) * 128,
-                                               dv0 + slot_off(slot), id_pv, m > 0 ? 1u : 0u, bar(B_PV_DONE + (m & 1)),
-                                               bar(B_KV_EMPTY + slot), last ? 0u : 1u);
+                                               dv0 + slot_off(slot), id_pv, m > 0 ? 1u : 0u, bar(C::B_PV_DONE + (m & 1)),
+                                               bar(C::B_KV_EMPTY + slot), last ? 0u : 1u);
             __syncwarp();
             return true;
         };
@@ -302,36 +368,99 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
             if (!ok) break;
             tc::fence_after();
             tc::mma_bf16_ss_k128_commit<false>(tmem + kTmemS0 + (uint32_t)(n & 1) * 128, dq, dk0 + slot_off(slot),
-                                               id_qk, 0u, bar(B_S_FULL + (n & 1)), bar(B_KV_EMPTY + slot),
+                                               id_qk, 0u, bar(C::B_S_FULL + (n & 1)), bar(C::B_KV_EMPTY + slot),
                                                last ? 0u : 1u);
             __syncwarp();
             if (n >= 1) ok = issue_pv(n - 1);
         }
         if (ok) ok = issue_pv(N - 1);
         // every MMA of this CTA has completed before TMEM is released (also after a role gave up)
-        tc::commit(bar(B_DRAIN));
+        tc::commit(bar(C::B_DRAIN));
         __syncwarp();
-        (void)mbar_drain(bar(B_DRAIN), 0, p.dev_status, A.wait_ns);
+        (void)mbar_drain(bar(C::B_DRAIN), 0, p.dev_status, A.wait_ns);
         __syncwarp();
+    } else if (kF8 && warp < C::kWarpSm) {
+        // ================================ converters (E4M3 cache) ================================
+        if constexpr (kF8) tc::reg_dealloc<80>();
+        // warps 2-3 convert Q, warps 4-7 (one warpgroup) the K/V tiles
+        bool ok = true;
+        if (warp < 4) {
+            // Q in place, bf16 -> f16 (exact for the normal range; values below 2^-14 round)
+            const int qt = threadIdx.x - 64;                  // 0 .. 63
+            ok = wwait(bar(C::B_Q), 0);
+            if (ok) {
+                uint4 *qw = reinterpret_cast<uint4 *>(smem + C::kOffQ);
+                for (int i = qt; i < 32768 / 16; i += 64) {
+                    const uint4 w = qw[i];
+                    qw[i] = make_uint4(pack_f16(bf16_lo(w.x), bf16_hi(w.x)), pack_f16(bf16_lo(w.y), bf16_hi(w.y)),
+                                       pack_f16(bf16_lo(w.z), bf16_hi(w.z)), pack_f16(bf16_lo(w.w), bf16_hi(w.w)));
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(bar(C::B_QF));
+            }
+        } else {
+            // thread ct owns dims [16 j16, 16 j16 + 16) of keys key0 + 16 i, i = 0..7: its E4M3
+            // source and f16 destination addresses are a fixed base plus i * 2048 (the f16
+            // tile: [d half][128 keys][128 B], 128-byte swizzle by key & 7 = key0 & 7)
+            const int ct = threadIdx.x - 128;                 // 0 .. 127
+            const int j16 = ct & 7, key0 = ct >> 3;
+            const int sw = key0 & 7;
+            const int src_off = key0 * 128 + j16 * 16;
+            const int dst_off0 = (j16 >> 2) * 16384 + key0 * 128 + ((((j16 & 3) * 2) ^ sw) << 4);
+            const int dst_off1 = (j16 >> 2) * 16384 + key0 * 128 + ((((j16 & 3) * 2 + 1) ^ sw) << 4);
+            // tiles in the MMA warp's order (K_0, then K_n, V_{n-1} for n >= 1, then V_{N-1})
+            for (int L = 0; L < 2 * N && ok; ++L) {
+                const int n = L == 0 ? 0 : L == 2 * N - 1 ? N - 1 : (L & 1) ? (L + 1) >> 1 : (L >> 1) - 1;
+                const int s8 = L % C::kF8Slots, s16 = L % C::kSlots;
+                if (!(ok = wwait(bar(C::B_F8_FULL + s8), (L / C::kF8Slots) & 1))) break;
+                if (L >= C::kSlots && !(ok = wwait(bar(C::B_KV_EMPTY + s16), ((L / C::kSlots) - 1) & 1))) break;
+                const unsigned char *src = smem + C::kOffF8 + s8 * kF8SlotBytes;
+                const float *sc = reinterpret_cast<const float *>(src + kF8TileBytes);
+                unsigned char *dst = smem + C::kOffKV + s16 * kSlotBytes;
+                const int key_end = min(T, kr_hi) - (kr_lo + n * kKeys);   // keys of the tile that exist
+                bool bad = false;
+#pragma unroll 4
+                for (int i = 0; i < 8; ++i) {
+                    const int key = key0 + 16 * i;
+                    const uint4 w = *reinterpret_cast<const uint4 *>(src + src_off + i * 2048);
+                    float sv = key < key_end ? sc[key] : 0.f;
+                    const bool good = sv == 0.f || (sv >= 0x1p-24f && sv <= 128.f);   // (false for NaN)
+                    bad |= !good;
+                    const __half2 s2 = __float2half2_rn(good ? sv : 0.f);
+                    *reinterpret_cast<uint4 *>(dst + dst_off0 + i * 2048) =
+                        make_uint4(e4m3x2_to_f16x2_scaled(w.x, s2), e4m3x2_to_f16x2_scaled(w.x >> 16, s2),
+                                   e4m3x2_to_f16x2_scaled(w.y, s2), e4m3x2_to_f16x2_scaled(w.y >> 16, s2));
+                    *reinterpret_cast<uint4 *>(dst + dst_off1 + i * 2048) =
+                        make_uint4(e4m3x2_to_f16x2_scaled(w.z, s2), e4m3x2_to_f16x2_scaled(w.z >> 16, s2),
+                                   e4m3x2_to_f16x2_scaled(w.w, s2), e4m3x2_to_f16x2_scaled(w.w >> 16, s2));
+                }
+                if (bad && j16 == 0) set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
+                fence_proxy_async_smem();
+                mbar_arrive(bar(C::B_F8_EMPTY + s8));
+                mbar_arrive(bar(C::B_KV_FULL + s16));
+            }
+        }
     } else {
         // ================================ softmax ================================
+        if constexpr (kF8) tc::reg_alloc<176>();
         const int quad = warp & 3;
-        const int hw = (warp - 2) >> 2;                       // column half
-        const int sw = warp - 2;                              // softmax warp index 0..7
+        const int sw = warp - C::kWarpSm;                     // softmax warp index 0..7
+        const int hw = sw >> 2;                               // column half
         const int a = quad * 32 + lane;                       // MMA row = TMEM lane
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         const bool valid_row = a < n_rows;
+        const bool quad_live = quad * 32 < n_rows;            // uniform over the warp (and its pair)
         const int t = valid_row ? (g_shift >= 0 ? a >> g_shift : a / g) : 0;
         const int hh = a - t * g;
         const int i_pos = pos0 + t;
         const int cb = 64 * hw;
-        unsigned short *tab = reinterpret_cast<unsigned short *>(smem + kOffTab);
-        float *tsig = reinterpret_cast<float *>(smem + kOffTsig);
-        float *xchg = reinterpret_cast<float *>(smem + kOffXchg);
+        unsigned short *tab = reinterpret_cast<unsigned short *>(smem + C::kOffTab);
+        float *tsig = reinterpret_cast<float *>(smem + C::kOffTsig);
+        float *xchg = reinterpret_cast<float *>(smem + C::kOffXchg);
         int pair_phase = 0;
         auto pair_sync = [&]() -> bool {
-            mbar_arrive(bar(B_PAIR + quad));
-            return wwait(bar(B_PAIR + quad), (pair_phase++) & 1);
+            mbar_arrive(bar(C::B_PAIR + quad));
+            return wwait(bar(C::B_PAIR + quad), (pair_phase++) & 1);
         };
         const bool has_bias = p.rel_extent > 0;
         const int gq = lane >> 2, tq = lane & 3;              // mma.sync fragment coordinates
@@ -340,14 +469,14 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
 
         float m_run = -INFINITY, l_run = 0.f;   // l_run: sum of the fp32 P (for the LSE)
         float lc_run = 0.f;                      // bf16 rounding of each tile's largest P (normaliser)
-        auto wait_pv = [&](int m) -> bool { return wwait(bar(B_PV_DONE + (m & 1)), (m >> 1) & 1); };
+        auto wait_pv = [&](int m) -> bool { return wwait(bar(C::B_PV_DONE + (m & 1)), (m >> 1) & 1); };
         for (int n = 0; n < N; ++n) {
             const int j0 = kr_lo + n * kKeys;
             const bool band = has_bias && (pos0 - (j0 + kKeys - 1) < p.rel_extent);
             const int dlo = pos0 - j0 - (kKeys - 1);          // distance at table column 0
             if (band) {
                 // ---- relative rows of this tile, one query head per warp, into the table
-                if (band_round > 0 && !(ok = wwait(bar(B_TAB_FREE), (band_round - 1) & 1))) break;
+                if (band_round > 0 && !(ok = wwait(bar(C::B_TAB_FREE), (band_round - 1) & 1))) break;
                 for (int hq = sw; hq < g; hq += 8) {
                     const int h = hk * g + hq;
                     const float *Ph = p.P + (size_t)h * p.rel_extent * 32;
@@ -458,11 +587,22 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
                         }
                     }
                 }
-                mbar_arrive(bar(B_TAB_FULL));
-                if (!(ok = wwait(bar(B_TAB_FULL), band_round & 1))) break;
+                mbar_arrive(bar(C::B_TAB_FULL));
+                if (!(ok = wwait(bar(C::B_TAB_FULL), band_round & 1))) break;
             }
 
-            if (!(ok = wwait(bar(B_S_FULL + (n & 1)), (n >> 1) & 1))) break;
+            if (!(ok = wwait(bar(C::B_S_FULL + (n & 1)), (n >> 1) & 1))) break;
+            if (!quad_live) {
+                // every row of this warp's lane quarter is padding: its P rows feed only O rows
+                // that are never written, so the warp only keeps the barrier counts
+                if (band) {
+                    mbar_arrive(bar(C::B_TAB_FREE));
+                    ++band_round;
+                }
+                tc::fence_before();
+                if (!(A.withhold && n == 0)) mbar_arrive(bar(C::B_P_FULL + (n & 1)));
+                continue;
+            }
             tc::fence_after();
             const uint32_t sbuf = tmem + kTmemS0 + (uint32_t)(n & 1) * 128 + lane_off;
             float s[64];
@@ -484,7 +624,7 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
                         s[bb] = fmaf(q, c0 - bb < 72 ? sg0 : sg1, s[bb]);   // columns [0, 72): first round
                     }
                 }
-                mbar_arrive(bar(B_TAB_FREE));
+                mbar_arrive(bar(C::B_TAB_FREE));
                 ++band_round;
             }
             // mask: key j visible iff it is in this split's range, j <= i and (SWA) i - j < window
@@ -545,7 +685,8 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
             if (hw == 0 && mx_raw != -INFINITY) {
                 // the tile's largest P of this row, computed as its element is, and its bf16 rounding
                 const float pm = fast_exp2(fmaf(mx_raw, c_qk, -ref));
-                lc_run += bf16_lo(pack_bf16(pm, 0.f)) - pm;
+                if constexpr (kF8) lc_run += __half2float(__float2half_rn(pm)) - pm;
+                else lc_run += bf16_lo(pack_bf16(pm, 0.f)) - pm;
             }
             float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                             make_float2(0.f, 0.f)};
@@ -555,14 +696,14 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
                 const float2 x = ffma2(make_float2(s[2 * e], s[2 * e + 1]), cq, nref);
                 const float2 y = make_float2(fast_exp2(x.x), fast_exp2(x.y));
                 l4[e & 3] = fadd2(l4[e & 3], y);
-                pk[e] = pack_bf16(y.x, y.y);
+                pk[e] = kF8 ? pack_f16(y.x, y.y) : pack_bf16(y.x, y.y);
             }
             tc::st32(sbuf + 32 * hw, pk);
             const float2 l2 = fadd2(fadd2(l4[0], l4[1]), fadd2(l4[2], l4[3]));
             l_run += l2.x + l2.y;
             tc::wait_st();
             tc::fence_before();
-            if (!(A.withhold && n == 0)) mbar_arrive(bar(B_P_FULL + (n & 1)));
+            if (!(A.withhold && n == 0)) mbar_arrive(bar(C::B_P_FULL + (n & 1)));
         }
         // epilogue: the row sum of both halves, then O / l for this thread's 64 columns
         // the column-half 0 thread of a row alone holds the correction (lc_run is 0 in the other)
@@ -625,6 +766,25 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
     }
 }
 
+template <bool kF8>
+cudaError_t launch_decode_variant(const DecTcArgs &a, dim3 grid, const CUtensorMap &qmap, const CUtensorMap &kmap,
+                                  const CUtensorMap &vmap, cudaStream_t stream) {
+    using C = Dec<kF8>;
+    if constexpr (kF8) {
+        // the register split (2 warpgroups at 80 + 2 at 176 = 512 x 128) needs exactly 128
+        // registers a thread at launch: with fewer, setmaxnreg.inc could never be satisfied
+        static const cudaError_t regs_check = [] {
+            cudaFuncAttributes fa;
+            if (cudaFuncGetAttributes(&fa, k_decode_tc<true>) != cudaSuccess) return cudaErrorInvalidDeviceFunction;
+            return fa.numRegs == 128 ? cudaSuccess : cudaErrorInvalidConfiguration;
+        }();
+        if (regs_check != cudaSuccess) return regs_check;
+    }
+    cudaError_t err = cudaFuncSetAttribute(k_decode_tc<kF8>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (err != cudaSuccess) return err;
+    return launch_dependent(k_decode_tc<kF8>, grid, dim3(C::kThreads), C::kSmem, stream, 1, a, qmap, kmap, vmap);
+}
+
 cudaError_t launch_decode_tc(const inkattn_attn_params &p, const AttnScalars &s, int num_splits,
                              float *ws_o, float *ws_lse, const CUtensorMap &qmap, const CUtensorMap &kmap,
                              const CUtensorMap &vmap, cudaStream_t stream) {
@@ -638,10 +798,9 @@ cudaError_t launch_decode_tc(const inkattn_attn_params &p, const AttnScalars &s,
     a.kv_rows = (long long)p.num_blocks * p.Hkv * kBlock;
     a.wait_ns = kernel_debug().wait_ns;
     a.withhold = kernel_debug().withhold;
-    cudaError_t err = cudaFuncSetAttribute(k_decode_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (err != cudaSuccess) return err;
     dim3 grid(num_splits, p.Hkv, p.B);
-    return launch_dependent(k_decode_tc, grid, dim3(kThreads), kSmem, stream, 1, a, qmap, kmap, vmap);
+    return p.kv_dtype == INKATTN_KV_E4M3 ? launch_decode_variant<true>(a, grid, qmap, kmap, vmap, stream)
+                                         : launch_decode_variant<false>(a, grid, qmap, kmap, vmap, stream);
 }
 
 }  // namespace inkattn

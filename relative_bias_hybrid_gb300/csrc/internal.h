@@ -93,6 +93,9 @@ cudaError_t launch_prefill_2q(const inkattn_attn_params &p, const AttnScalars &s
 // TMA descriptor for a paged cache viewed as [num_blocks*Hkv*64 rows][128] bf16,
 // box 64 rows x 64 columns, 128-byte swizzle.  Returns false on failure.
 bool make_cache_map(CUtensorMap *map, const void *base, long long rows);
+// The same rows as E4M3 codes: [num_blocks*Hkv*64 rows][128] bytes, box 64 rows x 128 bytes,
+// no swizzle (the decode's converter warps read it row by row).
+bool make_cache_map_e4m3(CUtensorMap *map, const void *base, long long rows);
 // TMA descriptor for q viewed as [N_tok][Hq][128] bf16, box {64, 1, box_rows}, 128-byte swizzle.
 bool make_q_map(CUtensorMap *map, const void *base, int n_tok, int hq, int box_rows);
 // Q as [N_tok][Hq][128] with a box of {64 dims, `group` heads, `tokens` tokens}: the rows of

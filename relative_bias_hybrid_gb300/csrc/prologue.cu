@@ -27,6 +27,7 @@
 // CTA touches those channels of that state slot.
 #include "common.cuh"
 #include "conv4.cuh"
+#include "fp8.cuh"
 #include "internal.h"
 
 namespace inkattn {
@@ -173,6 +174,7 @@ k_prologue(const inkattn_prologue_params p, const int kv_tiles) {
     // conv (rounded to bf16), K RMSNorm, cache write.  Half-warps 0-7 take the K stream and
     // 8-15 the V stream.
     const long long slot_limit = (long long)p.num_blocks * kBlock;
+    const bool f8 = p.kv_dtype == INKATTN_KV_E4M3;
     const int stream = half >> 3;
     const float *wsm = stream == 0 ? s_wk : s_wv;
 #pragma unroll 1
@@ -201,21 +203,48 @@ k_prologue(const inkattn_prologue_params p, const int kv_tiles) {
         ss += __shfl_xor_sync(0xffffffffu, ss, 4);
         ss += __shfl_xor_sync(0xffffffffu, ss, 2);
         ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        // the row this stream stores: the normalised K or the conv'd V, rounded to bf16
+        uint4 row;
+        if (stream == 0) {
+            const float inv = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = x[e] * inv * s_gk[e * 16 + lane16];
+            row = pack8(y);
+        } else {
+            row = pack8(x);
+        }
+        // E4M3 cache: one power-of-two scale per row (the half-warp's 128 values)
+        uint2 codes = make_uint2(0, 0);
+        float row_scale = 1.f;
+        if (f8) {
+            float r8[8];
+            unpack8(row, r8);
+            float am = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) am = fmaxf(am, fabsf(r8[e]));
+            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 8));
+            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
+            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+            am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+            const int k = e4m3_row_exponent(am);
+            row_scale = pow2f(k);
+            codes = e4m3_encode8(r8, pow2f(-k));
+        }
         const int sm = __shfl_sync(0xffffffffu, sm_mine, ((half & 1) << 4) + u);
         if (!valid) continue;
         if (sm < 0 || (long long)sm >= slot_limit) {
             if (lane16 == 0) set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
             continue;
         }
-        const size_t dst = (((size_t)(sm / kBlock) * p.Hkv + hk) * kBlock + (sm % kBlock)) * kHeadDim + c0;
-        if (stream == 0) {
-            const float inv = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
-            float y[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) y[e] = x[e] * inv * s_gk[e * 16 + lane16];
-            *reinterpret_cast<uint4 *>(p.k_cache + dst) = pack8(y);
+        const size_t drow = ((size_t)(sm / kBlock) * p.Hkv + hk) * kBlock + (sm % kBlock);
+        const size_t dst = drow * kHeadDim + c0;
+        void *cache = stream == 0 ? p.k_cache : p.v_cache;
+        if (!f8) {
+            *reinterpret_cast<uint4 *>(static_cast<inkattn_bf16 *>(cache) + dst) = row;
         } else {
-            *reinterpret_cast<uint4 *>(p.v_cache + dst) = pack8(x);
+            *reinterpret_cast<uint2 *>(static_cast<unsigned char *>(cache) + dst) = codes;
+            if (lane16 == 0) (stream == 0 ? p.k_scale : p.v_scale)[drow] = row_scale;
         }
     }
 

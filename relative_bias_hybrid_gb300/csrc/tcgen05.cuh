@@ -66,6 +66,7 @@ __host__ __device__ constexpr uint32_t idesc(int M, int N, uint32_t ab_format, i
            ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 constexpr uint32_t kFmtBF16 = 1;
+constexpr uint32_t kFmtF16 = 0;
 
 // ---------------------------------------------------------------- MMA + commit
 // Warp-collective: all 32 lanes of a converged warp make the call with the same operands,

@@ -26,6 +26,8 @@ INKATTN_ERR_DEVICE_TIMEOUT = 4
 INKATTN_ERR_DEVICE_BOUNDS = 5
 INKATTN_DTYPE_BF16 = 0
 INKATTN_DTYPE_F32 = 1
+INKATTN_KV_BF16 = 0
+INKATTN_KV_E4M3 = 1
 
 _c_i32 = ctypes.c_int32
 _c_ptr = ctypes.c_void_p
@@ -42,7 +44,8 @@ class PrologueParams(ctypes.Structure):
         ("conv_w_k", _c_ptr), ("conv_w_v", _c_ptr), ("q_norm_w", _c_ptr), ("k_norm_w", _c_ptr),
         ("cu_seqlens_q", _c_ptr), ("state_slot", _c_ptr), ("slot_mapping", _c_ptr),
         ("conv_state_k", _c_ptr), ("conv_state_v", _c_ptr), ("q_out", _c_ptr),
-        ("k_cache", _c_ptr), ("v_cache", _c_ptr), ("dev_status", _c_ptr),
+        ("k_cache", _c_ptr), ("v_cache", _c_ptr), ("kv_dtype", _c_i32), ("k_scale", _c_ptr),
+        ("v_scale", _c_ptr), ("dev_status", _c_ptr),
     ]
 
 
@@ -56,7 +59,7 @@ class AttnParams(ctypes.Structure):
         ("rel_extent", _c_i32), ("window", _c_i32), ("out_dtype", _c_i32),
         ("softmax_scale", ctypes.c_float), ("log_scale_base", ctypes.c_float),
         ("q", _c_ptr), ("r", _c_ptr), ("P", _c_ptr), ("k_cache", _c_ptr), ("v_cache", _c_ptr),
-        ("cu_seqlens_q", _c_ptr), ("seqlen_k", _c_ptr), ("block_table", _c_ptr),
+        ("kv_dtype", _c_i32), ("k_scale", _c_ptr), ("v_scale", _c_ptr), ("cu_seqlens_q", _c_ptr), ("seqlen_k", _c_ptr), ("block_table", _c_ptr),
         ("out", _c_ptr), ("lse", _c_ptr), ("dev_status", _c_ptr),
     ]
 
@@ -204,9 +207,19 @@ def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor") -> Optional[int]:
     return t.data_ptr()
 
 
+def _kv_dtype(cache):
+    """kv_dtype of a cache tensor: bf16 values, or E4M3 codes held as uint8."""
+    if cache.dtype == torch.bfloat16:
+        return INKATTN_KV_BF16, torch.bfloat16
+    if cache.dtype == torch.uint8:
+        return INKATTN_KV_E4M3, torch.uint8
+    raise TypeError(f"KV cache: expected bfloat16 or uint8 (E4M3 codes), got {cache.dtype}")
+
+
 def prologue_params(*, q, k, v, conv_w_k, conv_w_v, q_norm_w, k_norm_w, cu_seqlens_q, state_slot,
                     slot_mapping, conv_state_k, conv_state_v, q_out, k_cache, v_cache,
-                    max_seqlen_q: int, eps: float = 1e-6, dev_status=None) -> PrologueParams:
+                    max_seqlen_q: int, eps: float = 1e-6, dev_status=None, k_scale=None,
+                    v_scale=None) -> PrologueParams:
     """Fill an inkattn_prologue_params from torch tensors (see include/inkattn.h)."""
     bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
     N, Hq, d = q.shape
@@ -230,7 +243,10 @@ def prologue_params(*, q, k, v, conv_w_k, conv_w_v, q_norm_w, k_norm_w, cu_seqle
     p.conv_state_k = _ptr(conv_state_k, bf, "conv_state_k")
     p.conv_state_v = _ptr(conv_state_v, bf, "conv_state_v")
     p.q_out = _ptr(q_out, bf, "q_out")
-    p.k_cache = _ptr(k_cache, bf, "k_cache"); p.v_cache = _ptr(v_cache, bf, "v_cache")
+    p.kv_dtype, cache_dt = _kv_dtype(k_cache)
+    p.k_cache = _ptr(k_cache, cache_dt, "k_cache"); p.v_cache = _ptr(v_cache, cache_dt, "v_cache")
+    if p.kv_dtype == INKATTN_KV_E4M3:
+        p.k_scale = _ptr(k_scale, f32, "k_scale"); p.v_scale = _ptr(v_scale, f32, "v_scale")
     p.dev_status = _ptr(dev_status, i32, "dev_status")
     return p
 
@@ -238,7 +254,7 @@ def prologue_params(*, q, k, v, conv_w_k, conv_w_v, q_norm_w, k_norm_w, cu_seqle
 def attn_params(*, q, k_cache, v_cache, cu_seqlens_q, seqlen_k, block_table, out, max_seqlen_q: int,
                 max_seqlen_k: int, r=None, P=None, rel_extent: int = 0, window: int = 0,
                 softmax_scale: float = 0.0, log_scale_base: float = 0.0, lse=None,
-                dev_status=None) -> AttnParams:
+                dev_status=None, k_scale=None, v_scale=None) -> AttnParams:
     """Fill an inkattn_attn_params from torch tensors (see include/inkattn.h)."""
     bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
     N, Hq, d = q.shape
@@ -260,7 +276,10 @@ def attn_params(*, q, k_cache, v_cache, cu_seqlens_q, seqlen_k, block_table, out
     p.q = _ptr(q, bf, "q")
     p.r = _ptr(r, bf, "r") if rel_extent > 0 else None
     p.P = _ptr(P, f32, "P") if rel_extent > 0 else None
-    p.k_cache = _ptr(k_cache, bf, "k_cache"); p.v_cache = _ptr(v_cache, bf, "v_cache")
+    p.kv_dtype, cache_dt = _kv_dtype(k_cache)
+    p.k_cache = _ptr(k_cache, cache_dt, "k_cache"); p.v_cache = _ptr(v_cache, cache_dt, "v_cache")
+    if p.kv_dtype == INKATTN_KV_E4M3:
+        p.k_scale = _ptr(k_scale, f32, "k_scale"); p.v_scale = _ptr(v_scale, f32, "v_scale")
     p.cu_seqlens_q = _ptr(cu_seqlens_q, i32, "cu_seqlens_q")
     p.seqlen_k = _ptr(seqlen_k, i32, "seqlen_k")
     p.block_table = _ptr(block_table, i32, "block_table")

@@ -113,7 +113,8 @@ def custom(name: str, *, Hq: int, Hkv: int, q_lens, prefix_lens=None, **kw) -> W
 _TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "r": 4, "P": 5, "conv_w_k": 6, "conv_w_v": 7,
                "q_norm_w": 8, "k_norm_w": 9, "conv_state_k": 10, "conv_state_v": 11,
                "k_cache": 12, "v_cache": 13, "perm": 14, "y": 15, "residual": 16,
-               "oc_conv_w": 17, "oc_norm_w": 18, "oc_conv_state": 19}
+               "oc_conv_w": 17, "oc_norm_w": 18, "oc_conv_state": 19, "k_cache_e4m3": 20,
+               "v_cache_e4m3": 21}
 
 
 def _gen(device, seed: int, tensor: str) -> torch.Generator:
@@ -130,14 +131,15 @@ def _normal(shape, std, device, seed, tensor, dtype):
     return x.to(dtype)
 
 
-def make_inputs(w: Workload, seed: int = 0, device="cpu") -> Dict[str, torch.Tensor]:
+def make_inputs(w: Workload, seed: int = 0, device="cpu", kv_dtype: str = "bf16") -> Dict[str, torch.Tensor]:
     """All inputs of one prologue + attention pass, as torch tensors on `device`.
 
     Keys: q, k, v [N,Hq,d]/[N,C]/[N,C] bf16; r [N,Hq,d_r] bf16; P [Hq,rel_extent,d_r]
     fp32; conv_w_k, conv_w_v [C,4] fp32; q_norm_w, k_norm_w [d] fp32;
     conv_state_k, conv_state_v [B,3,C] bf16; state_slot [B]; cu_seqlens_q [B+1];
     seqlen_k [B]; block_table [B,max_blocks] (-1 past each sequence's blocks);
-    slot_mapping [N]; k_cache, v_cache [num_blocks,Hkv,64,d] bf16.
+    slot_mapping [N]; k_cache, v_cache [num_blocks,Hkv,64,d] bf16, or with kv_dtype "e4m3"
+    uint8 E4M3 codes plus k_scale, v_scale [num_blocks,Hkv,64] fp32.
     """
     device = torch.device(device)
     d, C, N, B = w.head_dim, w.Hkv * w.head_dim, w.N_tok, w.B
@@ -191,8 +193,18 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu") -> Dict[str, torch.Ten
             t += 1
     out["slot_mapping"] = torch.tensor(slots, dtype=torch.int32, device=device)
     shape = (nb, w.Hkv, w.block_size, d)
-    out["k_cache"] = _normal(shape, 1.0, device, seed, "k_cache", bf)
-    out["v_cache"] = _normal(shape, 1.0, device, seed, "v_cache", bf)
+    if kv_dtype == "bf16":
+        out["k_cache"] = _normal(shape, 1.0, device, seed, "k_cache", bf)
+        out["v_cache"] = _normal(shape, 1.0, device, seed, "v_cache", bf)
+    elif kv_dtype == "e4m3":
+        # E4M3 codes (held as uint8) of N(0, 1) draws times 128, and row scales 2^-7: the
+        # cached rows read back as values of about unit size
+        for name in ("k", "v"):
+            x = _normal(shape, 128.0, device, seed, f"{name}_cache_e4m3", torch.float32)
+            out[f"{name}_cache"] = x.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+            out[f"{name}_scale"] = torch.full(shape[:3], 2.0 ** -7, dtype=torch.float32, device=device)
+    else:
+        raise ValueError(kv_dtype)
     return out
 
 

@@ -27,6 +27,7 @@ def main(argv=None):
     ap.add_argument("--seqs", type=int, default=0, help="keep only the first N sequences")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--splits", type=int, default=0, help="decode splits (0 = the library's heuristic)")
+    ap.add_argument("--kv", choices=["bf16", "e4m3"], default="bf16", help="KV-cache element type")
     ap.add_argument("--output-conv", action="store_true",
                     help="also run the attention-output conv (hidden width Hq * 128) after each pass")
     args = ap.parse_args(argv)
@@ -36,7 +37,7 @@ def main(argv=None):
         w = dataclasses.replace(w, name=f"{w.name}[:{args.seqs}]", q_lens=w.q_lens[:args.seqs],
                                 prefix_lens=w.prefix_lens[:args.seqs])
     dev = torch.device("cuda", torch.cuda.current_device())
-    x = gen.make_inputs(w, seed=args.seed, device=dev)
+    x = gen.make_inputs(w, seed=args.seed, device=dev, kv_dtype=args.kv)
     step = AttentionStep(w, x, mode="decode" if args.workload == "decode" else "prefill",
                          num_splits=args.splits)
     oc = OutputConvStep(w, gen.make_output_conv_inputs(w, seed=args.seed, device=dev)) if args.output_conv else None

@@ -41,13 +41,15 @@ class AttentionStep:
             cu_seqlens_q=inputs["cu_seqlens_q"], state_slot=inputs["state_slot"],
             slot_mapping=inputs["slot_mapping"], conv_state_k=inputs["conv_state_k"],
             conv_state_v=inputs["conv_state_v"], q_out=self.q_out, k_cache=inputs["k_cache"],
-            v_cache=inputs["v_cache"], max_seqlen_q=max_q, eps=w.eps, dev_status=self.status)
+            v_cache=inputs["v_cache"], max_seqlen_q=max_q, eps=w.eps, dev_status=self.status,
+            k_scale=inputs.get("k_scale"), v_scale=inputs.get("v_scale"))
         self.attn = ia.attn_params(
             q=self.q_out, k_cache=inputs["k_cache"], v_cache=inputs["v_cache"],
             cu_seqlens_q=inputs["cu_seqlens_q"], seqlen_k=inputs["seqlen_k"],
             block_table=inputs["block_table"], out=self.out, max_seqlen_q=max_q, max_seqlen_k=max_k,
             r=inputs["r"], P=inputs["P"], rel_extent=w.rel_extent, window=w.window,
-            log_scale_base=w.log_scale_base, lse=self.lse, dev_status=self.status)
+            log_scale_base=w.log_scale_base, lse=self.lse, dev_status=self.status,
+            k_scale=inputs.get("k_scale"), v_scale=inputs.get("v_scale"))
         self.num_splits = 0
         self.workspace: Optional[torch.Tensor] = None
         if mode == "decode":

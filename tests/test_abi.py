@@ -73,7 +73,7 @@ def test_status_strings(ia):
     assert "invalid" in ia.status_string(1)
     assert "timed out" in ia.status_string(4)
     assert "bounds" in ia.status_string(5)
-    assert ia.abi_version() == 1
+    assert ia.abi_version() == 2
 
 
 def _attn(ia, **kw):
@@ -112,6 +112,13 @@ def test_host_validation_rejects_before_any_launch(ia):
         ia.INKATTN_ERR_UNSUPPORTED
     assert ia.inkattn_prefill(_attn(ia, max_blocks_per_seq=10), raise_on_error=False, stream=0) == \
         ia.INKATTN_ERR_INVALID_ARG      # table too short for max_seqlen_k
+    # an E4M3 cache needs its row scales; the prefill does not read one
+    assert ia.inkattn_prefill(_attn(ia, kv_dtype=1), raise_on_error=False, stream=0) == \
+        ia.INKATTN_ERR_INVALID_ARG
+    assert ia.inkattn_prefill(_attn(ia, kv_dtype=1, k_scale=1 << 20, v_scale=1 << 20), raise_on_error=False,
+                              stream=0) == ia.INKATTN_ERR_UNSUPPORTED
+    assert ia.inkattn_prefill(_attn(ia, kv_dtype=2), raise_on_error=False, stream=0) == \
+        ia.INKATTN_ERR_INVALID_ARG
     # decode-only shape limits
     assert ia.inkattn_decode(_attn(ia, max_seqlen_q=17), 4, None, raise_on_error=False, stream=0) == \
         ia.INKATTN_ERR_UNSUPPORTED
