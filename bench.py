@@ -600,7 +600,7 @@ def run_gpu(args):
         per = args.cpu_seconds / len(names)
         for name in names:
             h = hosts.pop(name)
-            reps[name]["cpu_baseline"] = (cpu_baseline_decode(h, per) if name == "decode"
+            reps[name]["cpu_baseline"] = (cpu_baseline_decode(h, per) if name.startswith("decode")
                                           else cpu_baseline_prefill(h, per))
     head_name = names[0]
     head = reps.pop(head_name)
