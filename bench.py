@@ -43,9 +43,9 @@ KERNEL_SOURCES = {
     "k_prefill_tc": ["relative_bias_hybrid_gb300/csrc/prefill_tc.cu", "relative_bias_hybrid_gb300/csrc/tcgen05.cuh",
                      "relative_bias_hybrid_gb300/csrc/common.cuh"],
     "k_decode_tc": ["relative_bias_hybrid_gb300/csrc/decode_tc.cu", "relative_bias_hybrid_gb300/csrc/tcgen05.cuh",
-                    "relative_bias_hybrid_gb300/csrc/common.cuh"],
+                    "relative_bias_hybrid_gb300/csrc/fp8.cuh", "relative_bias_hybrid_gb300/csrc/common.cuh"],
     "k_prologue": ["relative_bias_hybrid_gb300/csrc/prologue.cu", "relative_bias_hybrid_gb300/csrc/conv4.cuh",
-                   "relative_bias_hybrid_gb300/csrc/common.cuh"],
+                   "relative_bias_hybrid_gb300/csrc/fp8.cuh", "relative_bias_hybrid_gb300/csrc/common.cuh"],
     "k_output_conv": ["relative_bias_hybrid_gb300/csrc/output_conv.cu", "relative_bias_hybrid_gb300/csrc/conv4.cuh",
                       "relative_bias_hybrid_gb300/csrc/common.cuh"],
 }
