@@ -96,12 +96,22 @@ __device__ __forceinline__ void conv4_bf16_fast2(const float (&wa)[4], const flo
         a.x = fmaf(fabsf(wa[k]), fabsf(xa[k]), a.x);
         a.y = fmaf(fabsf(wb[k]), fabsf(xb[k]), a.y);
     }
-    const float ma = __uint_as_float((__float_as_uint(s.x) & 0xFFFF0000u) | 0x8000u);
-    const float mb = __uint_as_float((__float_as_uint(s.y) & 0xFFFF0000u) | 0x8000u);
-    ya = (fabsf(s.x - ma) * 2097152.f > a.x && fabsf(s.x) * 2048.f > a.x)
-        ? __bfloat162float(__float2bfloat16_rn(s.x)) : conv4_bf16(wa, xa);
-    yb = (fabsf(s.y - mb) * 2097152.f > a.y && fabsf(s.y) * 2048.f > a.y)
-        ? __bfloat162float(__float2bfloat16_rn(s.y)) : conv4_bf16(wb, xb);
+    // The exact sums lie within 2^-21 of the sums of magnitudes of s (the chain's error is
+    // at most 4u of it, u = 2^-24; the margin also covers the rounding of the magnitudes'
+    // own sum).  Rounding to nearest is monotonic, so when both ends of that interval
+    // (computed rounding outwards) round to the same bf16, so does the exact sum: one
+    // packed compare decides both channels.  Magnitudes below 2^-100 (where products can
+    // lose bits to underflow) and anything non-finite take the error-free path.
+    const float ea = a.x * 0x1p-21f, eb = a.y * 0x1p-21f;
+    const uint32_t lo = pack_bf16(__fsub_rd(s.x, ea), __fsub_rd(s.y, eb));
+    const uint32_t hi = pack_bf16(__fadd_ru(s.x, ea), __fadd_ru(s.y, eb));
+    if (lo == hi && fminf(a.x, a.y) > 0x1p-100f) {
+        ya = bf16_lo(lo);
+        yb = bf16_hi(lo);
+    } else {
+        ya = conv4_bf16(wa, xa);
+        yb = conv4_bf16(wb, xb);
+    }
 }
 
 }  // namespace inkattn

@@ -152,3 +152,38 @@ def test_output_conv_ragged_batch_sampled(env):
     gen = env[0]
     w = gen.workload("ragged")
     _check(env, w, *_run(env, w), seqs=[0, 5, 11, 15])
+
+
+def test_conv_rounding_hard_cases(env):
+    """Conv sums whose fp32 evaluation lands on or next to a bf16 rounding boundary, or
+    cancels: the kernel's fast path must hand each of them to its error-free evaluation
+    and store the correctly rounded value (h bit-exact with a zero residual).  Per channel,
+    taps w and carried rows x (oldest first), with y = 0 for the one new token:
+      1 + 2^-8 + 2^-30 (just above a tie: rounds up), 1 + 2^-8 - 2^-30 (just below: down),
+      1 + 2^-8 (an exact tie: even, 1), (1 + 2^-23) * 1.5 - 1.5 (cancellation, 1.5 * 2^-23),
+      a sum whose terms cancel to 2^-40, and their negatives."""
+    gen, ia, _ = env
+    cases = [
+        ([1.0, 2.0 ** -8, 2.0 ** -30, 0.0], [1.0, 1.0, 1.0]),
+        ([1.0, 2.0 ** -8, -(2.0 ** -30), 0.0], [1.0, 1.0, 1.0]),
+        ([1.0, 2.0 ** -8, 0.0, 0.0], [1.0, 1.0, 1.0]),
+        ([1.0 + 2.0 ** -23, -1.0, 0.0, 0.0], [1.5, 1.5, 0.0]),
+        ([3.0, -1.0, 2.0 ** -40, 0.0], [1.0, 3.0, 1.0]),
+        ([0.1, 0.2, 0.3, 0.0], [-3.0, 1.5, 0.5]),
+    ]
+    cases += [([-w for w in ws], xs) for ws, xs in cases]
+    D = 8 * ((len(cases) + 7) // 8)
+    w = gen.custom("oc_hard", Hq=1, Hkv=1, q_lens=[1], prefix_lens=[3])
+    x_cpu = gen.make_output_conv_inputs(w, seed=1, D=D, device="cpu")
+    conv_w = torch.zeros(D, 4)
+    state = torch.zeros(1, 3, D)
+    for c, (ws, xs) in enumerate(cases):
+        conv_w[c] = torch.tensor(ws, dtype=torch.float64).float()
+        state[0, :, c] = torch.tensor(xs)
+    x_cpu["conv_w"] = conv_w
+    x_cpu["conv_state"] = state.to(torch.bfloat16)
+    assert torch.equal(x_cpu["conv_state"].float(), state)         # the rows are bf16 values
+    x_cpu["y"] = torch.zeros_like(x_cpu["y"])
+    x_cpu["residual"] = torch.zeros_like(x_cpu["residual"])
+    x_cpu, x, h, out, status = _run(env, w, x_cpu=x_cpu)
+    _check(env, w, x_cpu, x, h, out, status)
