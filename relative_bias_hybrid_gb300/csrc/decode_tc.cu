@@ -58,15 +58,15 @@ constexpr int kF8SlotBytes = kF8TileBytes + kKeys * 4;   // + its 128 row scales
 
 // Two variants.  kF8 = false (bf16 cache): TMA loads K/V tiles straight into the MMAs'
 // 4-slot ring.  kF8 = true (E4M3 cache): TMA loads E4M3 tiles and their row scales into a
-// 3-slot ring, and four converter warps (4-7) expand each tile (code * scale, exactly) to
-// f16 in a 3-slot MMA ring; warps 2-3 convert Q to f16 in place, and P is packed as f16, so
-// the MMAs run kind::f16 on f16 operands.  Warps: 0 TMA, 1 MMA, [2, 8) converters (E4M3
+// 3-slot ring, and six converter warps (2-7) convert Q to f16 in place, then expand each
+// tile (code * scale, exactly) to f16 in a 3-slot MMA ring; P is packed as f16, so the MMAs
+// run kind::f16 on f16 operands.  Warps: 0 TMA, 1 MMA, [2, 8) converters (E4M3
 // only), then 8 softmax warps.
 template <bool kF8>
 struct Dec {
     static constexpr int kThreads = kF8 ? 512 : 320;
     static constexpr int kWarpSm = kF8 ? 8 : 2;              // first softmax warp
-    static constexpr int kConvThreads = kF8 ? 128 : 0;       // tile converters (warps 4-7)
+    static constexpr int kConvThreads = kF8 ? 192 : 0;       // converter warps 2-7
     static constexpr int kSlots = kF8 ? 3 : 4;               // MMA operand ring
     static constexpr int kF8Slots = kF8 ? 3 : 0;             // E4M3 ring
     static constexpr int kOffQ = 0;
@@ -182,7 +182,7 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
             mbar_init(bar(C::B_KV_EMPTY + s), 1);
         }
         if constexpr (kF8) {
-            mbar_init(bar(C::B_QF), 64);                                  // the two Q converter warps
+            mbar_init(bar(C::B_QF), 192);
             for (int s = 0; s < C::kF8Slots; ++s) {
                 mbar_init(bar(C::B_F8_FULL + s), 1);
                 mbar_init(bar(C::B_F8_EMPTY + s), C::kConvThreads);
@@ -382,63 +382,48 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
     } else if (kF8 && warp < C::kWarpSm) {
         // ================================ converters (E4M3 cache) ================================
         if constexpr (kF8) tc::reg_dealloc<80>();
-        // warps 2-3 convert Q, warps 4-7 (one warpgroup) the K/V tiles
-        bool ok = true;
-        if (warp < 4) {
-            // Q in place, bf16 -> f16 (exact for the normal range; values below 2^-14 round)
-            const int qt = threadIdx.x - 64;                  // 0 .. 63
-            ok = wwait(bar(C::B_Q), 0);
-            if (ok) {
-                uint4 *qw = reinterpret_cast<uint4 *>(smem + C::kOffQ);
-                for (int i = qt; i < 32768 / 16; i += 64) {
-                    const uint4 w = qw[i];
-                    qw[i] = make_uint4(pack_f16(bf16_lo(w.x), bf16_hi(w.x)), pack_f16(bf16_lo(w.y), bf16_hi(w.y)),
-                                       pack_f16(bf16_lo(w.z), bf16_hi(w.z)), pack_f16(bf16_lo(w.w), bf16_hi(w.w)));
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(bar(C::B_QF));
+        // warps 2-7 convert Q, then the K/V tiles
+        const int ct = threadIdx.x - 64;                      // 0 .. 191
+        bool ok = wwait(bar(C::B_Q), 0);
+        if (ok) {
+            uint4 *qw = reinterpret_cast<uint4 *>(smem + C::kOffQ);
+            for (int i = ct; i < 32768 / 16; i += 192) {
+                const uint4 w = qw[i];
+                qw[i] = make_uint4(pack_f16(bf16_lo(w.x), bf16_hi(w.x)), pack_f16(bf16_lo(w.y), bf16_hi(w.y)),
+                                   pack_f16(bf16_lo(w.z), bf16_hi(w.z)), pack_f16(bf16_lo(w.w), bf16_hi(w.w)));
             }
-        } else {
-            // thread ct owns dims [16 j16, 16 j16 + 16) of keys key0 + 16 i, i = 0..7: its E4M3
-            // source and f16 destination addresses are a fixed base plus i * 2048 (the f16
-            // tile: [d half][128 keys][128 B], 128-byte swizzle by key & 7 = key0 & 7)
-            const int ct = threadIdx.x - 128;                 // 0 .. 127
-            const int j16 = ct & 7, key0 = ct >> 3;
-            const int sw = key0 & 7;
-            const int src_off = key0 * 128 + j16 * 16;
-            const int dst_off0 = (j16 >> 2) * 16384 + key0 * 128 + ((((j16 & 3) * 2) ^ sw) << 4);
-            const int dst_off1 = (j16 >> 2) * 16384 + key0 * 128 + ((((j16 & 3) * 2 + 1) ^ sw) << 4);
-            // tiles in the MMA warp's order (K_0, then K_n, V_{n-1} for n >= 1, then V_{N-1})
-            for (int L = 0; L < 2 * N && ok; ++L) {
-                const int n = L == 0 ? 0 : L == 2 * N - 1 ? N - 1 : (L & 1) ? (L + 1) >> 1 : (L >> 1) - 1;
-                const int s8 = L % C::kF8Slots, s16 = L % C::kSlots;
-                if (!(ok = wwait(bar(C::B_F8_FULL + s8), (L / C::kF8Slots) & 1))) break;
-                if (L >= C::kSlots && !(ok = wwait(bar(C::B_KV_EMPTY + s16), ((L / C::kSlots) - 1) & 1))) break;
-                const unsigned char *src = smem + C::kOffF8 + s8 * kF8SlotBytes;
-                const float *sc = reinterpret_cast<const float *>(src + kF8TileBytes);
-                unsigned char *dst = smem + C::kOffKV + s16 * kSlotBytes;
-                const int key_end = min(T, kr_hi) - (kr_lo + n * kKeys);   // keys of the tile that exist
-                bool bad = false;
-#pragma unroll 4
-                for (int i = 0; i < 8; ++i) {
-                    const int key = key0 + 16 * i;
-                    const uint4 w = *reinterpret_cast<const uint4 *>(src + src_off + i * 2048);
-                    float sv = key < key_end ? sc[key] : 0.f;
-                    const bool good = sv == 0.f || (sv >= 0x1p-24f && sv <= 128.f);   // (false for NaN)
-                    bad |= !good;
-                    const __half2 s2 = __float2half2_rn(good ? sv : 0.f);
-                    *reinterpret_cast<uint4 *>(dst + dst_off0 + i * 2048) =
-                        make_uint4(e4m3x2_to_f16x2_scaled(w.x, s2), e4m3x2_to_f16x2_scaled(w.x >> 16, s2),
-                                   e4m3x2_to_f16x2_scaled(w.y, s2), e4m3x2_to_f16x2_scaled(w.y >> 16, s2));
-                    *reinterpret_cast<uint4 *>(dst + dst_off1 + i * 2048) =
-                        make_uint4(e4m3x2_to_f16x2_scaled(w.z, s2), e4m3x2_to_f16x2_scaled(w.z >> 16, s2),
-                                   e4m3x2_to_f16x2_scaled(w.w, s2), e4m3x2_to_f16x2_scaled(w.w >> 16, s2));
-                }
-                if (bad && j16 == 0) set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
-                fence_proxy_async_smem();
-                mbar_arrive(bar(C::B_F8_EMPTY + s8));
-                mbar_arrive(bar(C::B_KV_FULL + s16));
+            fence_proxy_async_smem();
+            mbar_arrive(bar(C::B_QF));
+        }
+        for (int L = 0; L < 2 * N && ok; ++L) {
+            const int n = L == 0 ? 0 : L == 2 * N - 1 ? N - 1 : (L & 1) ? (L + 1) >> 1 : (L >> 1) - 1;
+            const int s8 = L % C::kF8Slots, s16 = L % C::kSlots;
+            if (!(ok = wwait(bar(C::B_F8_FULL + s8), (L / C::kF8Slots) & 1))) break;
+            if (L >= C::kSlots && !(ok = wwait(bar(C::B_KV_EMPTY + s16), ((L / C::kSlots) - 1) & 1))) break;
+            const unsigned char *src = smem + C::kOffF8 + s8 * kF8SlotBytes;
+            const float *sc = reinterpret_cast<const float *>(src + kF8TileBytes);
+            unsigned char *dst = smem + C::kOffKV + s16 * kSlotBytes;
+            const int key_end = min(T, kr_hi) - (kr_lo + n * kKeys);
+            bool bad = false;
+            for (int it = ct; it < kKeys * 8; it += 192) {
+                const int key = it >> 3, j16 = it & 7, sw = key & 7;
+                const uint4 w = *reinterpret_cast<const uint4 *>(src + key * 128 + j16 * 16);
+                float sv = key < key_end ? sc[key] : 0.f;
+                const bool good = sv == 0.f || (sv >= 0x1p-24f && sv <= 128.f);
+                bad |= !good;
+                const __half2 s2 = __float2half2_rn(good ? sv : 0.f);
+                const int base = (j16 >> 2) * 16384 + key * 128;
+                *reinterpret_cast<uint4 *>(dst + base + ((((j16 & 3) * 2) ^ sw) << 4)) =
+                    make_uint4(e4m3x2_to_f16x2_scaled(w.x, s2), e4m3x2_to_f16x2_scaled(w.x >> 16, s2),
+                               e4m3x2_to_f16x2_scaled(w.y, s2), e4m3x2_to_f16x2_scaled(w.y >> 16, s2));
+                *reinterpret_cast<uint4 *>(dst + base + ((((j16 & 3) * 2 + 1) ^ sw) << 4)) =
+                    make_uint4(e4m3x2_to_f16x2_scaled(w.z, s2), e4m3x2_to_f16x2_scaled(w.z >> 16, s2),
+                               e4m3x2_to_f16x2_scaled(w.w, s2), e4m3x2_to_f16x2_scaled(w.w >> 16, s2));
             }
+            if (bad) set_status(p.dev_status, INKATTN_ERR_DEVICE_BOUNDS);
+            fence_proxy_async_smem();
+            mbar_arrive(bar(C::B_F8_EMPTY + s8));
+            mbar_arrive(bar(C::B_KV_FULL + s16));
         }
     } else {
         // ================================ softmax ================================
