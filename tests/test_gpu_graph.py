@@ -20,31 +20,35 @@ def env():
     return gen, AttentionStep
 
 
-@pytest.mark.parametrize("mode,splits", [("prefill", 0), ("prefill_nobias", 0), ("decode", 1), ("decode", 3)])
+@pytest.mark.parametrize("mode,splits", [("prefill", 0), ("prefill_nobias", 0), ("decode", 1), ("decode", 3),
+                                         ("decode_e4m3", 3)])
 def test_step_replays_from_a_cuda_graph(env, mode, splits):
     gen, AttentionStep = env
+    kv = "e4m3" if mode.endswith("e4m3") else "bf16"
+    mode = mode.replace("_e4m3", "")
     if mode == "decode":
         w = gen.custom("graph-dec", Hq=16, Hkv=2, q_lens=[9, 4], prefix_lens=[900, 2000], rel_extent=200,
                        log_scale_base=256.0)
     else:
         w = gen.custom("graph-pre", Hq=8, Hkv=2, q_lens=[300, 140], prefix_lens=[20, 0], window=200,
                        rel_extent=0 if mode == "prefill_nobias" else 150)
-    x = gen.make_inputs(w, seed=21, device="cuda")
-    saved = {k: x[k].clone() for k in _STATE}
+    x = gen.make_inputs(w, seed=21, device="cuda", kv_dtype=kv)
+    state = _STATE + (("k_scale", "v_scale") if kv == "e4m3" else ())
+    saved = {k: x[k].clone() for k in state}
     step = AttentionStep(w, x, mode="decode" if mode == "decode" else "prefill", num_splits=splits)
 
     step.run()
     torch.cuda.synchronize()
-    direct = {"out": step.out.clone(), "lse": step.lse.clone(), **{k: x[k].clone() for k in _STATE}}
+    direct = {"out": step.out.clone(), "lse": step.lse.clone(), **{k: x[k].clone() for k in state}}
     assert int(step.status.item()) == 0
 
-    for k in _STATE:
+    for k in state:
         x[k].copy_(saved[k])
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         step.run()
     # capturing records the work without running it; start the replay from the same state
-    for k in _STATE:
+    for k in state:
         x[k].copy_(saved[k])
     step.out.zero_()
     step.lse.zero_()
@@ -54,5 +58,5 @@ def test_step_replays_from_a_cuda_graph(env, mode, splits):
     assert int(step.status.item()) == 0
     assert torch.equal(step.out, direct["out"])
     assert torch.equal(step.lse, direct["lse"])
-    for k in _STATE:
+    for k in state:
         assert torch.equal(x[k], direct[k]), k

@@ -4,7 +4,9 @@ the attention kernels' softmax withholds its first arrival on the barrier that t
 waits on before P V.  That wait runs out after 2 ms; the kernel must record
 INKATTN_ERR_DEVICE_TIMEOUT in dev_status, drain the copies and MMAs it issued, release TMEM
 and return, leaving the CUDA context usable.  Covered: the relative-bias prefill with CTA
-pairs (K/V multicast) and without, the prefill without bias, and the decode."""
+pairs (K/V multicast) and without, the prefill without bias, and the decode over a bf16
+and over an E4M3 cache (the latter with its converter warps between the copies and the
+MMAs)."""
 import json
 import os
 import subprocess
@@ -28,10 +30,11 @@ cases = {
     "prefill_unpaired": (gen.custom("t2", Hq=6, Hkv=2, q_lens=[300], prefix_lens=[0], rel_extent=100), "prefill"),
     "prefill_no_bias": (gen.custom("t3", Hq=8, Hkv=2, q_lens=[600], prefix_lens=[0], rel_extent=0), "prefill"),
     "decode": (gen.custom("t4", Hq=16, Hkv=2, q_lens=[9, 4], prefix_lens=[2000, 700], rel_extent=200), "decode"),
+    "decode_e4m3": (gen.custom("t5", Hq=16, Hkv=2, q_lens=[9, 4], prefix_lens=[2000, 700], rel_extent=200), "decode"),
 }
 res = {}
 for name, (w, mode) in cases.items():
-    x = gen.make_inputs(w, seed=3, device="cuda")
+    x = gen.make_inputs(w, seed=3, device="cuda", kv_dtype="e4m3" if name.endswith("e4m3") else "bf16")
     st = AttentionStep(w, x, mode=mode, num_splits=1 if mode == "decode" else 0)
     st.run_prologue()                 # no bounded waits in the prologue
     torch.cuda.synchronize()
