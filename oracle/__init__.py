@@ -70,6 +70,8 @@ def _load():
             lib.oracle_f64_to_e4m3.restype = ctypes.c_uint8
             lib.oracle_quantize_rows_e4m3.argtypes = [P, I, I, P, P]
             lib.oracle_quantize_rows_e4m3.restype = I
+            lib.oracle_round_bf16_array.argtypes = [P, ctypes.c_longlong, P]
+            lib.oracle_round_bf16_array.restype = None
             _lib = lib
     return _lib
 
@@ -283,3 +285,37 @@ def dequantize_e4m3(codes, scales) -> np.ndarray:
     For the power-of-two scales of quantize_rows_e4m3 the result is exact."""
     lut = np.array([e4m3_to_f64(c) for c in range(256)], dtype=np.float64)
     return lut[np.asarray(codes, dtype=np.uint8)] * np.asarray(scales, dtype=np.float64)[..., None]
+
+
+def round_bf16(x) -> np.ndarray:
+    """float64 array -> bf16 bit patterns, each value rounded once (ties to even)."""
+    a = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.zeros(a.shape, dtype=np.uint16)
+    _load().oracle_round_bf16_array(_ptr(a), a.size, _ptr(out))
+    return out
+
+
+def qkvr_projection(x, w, *, Hq, Hkv, d, d_r):
+    """Step 8 of oracle.c: y = x . w^T in float64 (numpy's matrix product), each value
+    rounded once to bf16, split into q [N][Hq][d], k [N][Hkv*d], v [N][Hkv*d] and
+    r [N][Hq][d_r] (bf16 bit patterns).  x: [N][d_model] bits, w: [Hq*d + 2*Hkv*d + Hq*d_r]
+    [d_model] bits."""
+    xf = bf16_bits_to_f64(np.asarray(x, dtype=np.uint16))
+    wf = bf16_bits_to_f64(np.asarray(w, dtype=np.uint16))
+    y = round_bf16(xf @ wf.T)
+    N = y.shape[0]
+    c = np.cumsum([0, Hq * d, Hkv * d, Hkv * d, Hq * d_r])
+    assert y.shape[1] == c[-1]
+    return (y[:, c[0]:c[1]].reshape(N, Hq, d), y[:, c[1]:c[2]], y[:, c[2]:c[3]],
+            y[:, c[3]:c[4]].reshape(N, Hq, d_r))
+
+
+def qkvr_prologue(*, x, w, d_r, **prologue_args):
+    """Steps 8 then 1-4: the projections of the hidden states x, then the prologue on the
+    projected q, k, v.  prologue_args are those of prologue() except q, k and v.  Returns
+    prologue()'s dict plus r (bf16 bits) and q_proj, k_proj, v_proj (the projections)."""
+    q, k, v, r = qkvr_projection(x, w, Hq=prologue_args["Hq"], Hkv=prologue_args["Hkv"],
+                                 d=prologue_args["d"], d_r=d_r)
+    out = prologue(q=q, k=k, v=v, **prologue_args)
+    out.update(r=r, q_proj=q, k_proj=k, v_proj=v)
+    return out

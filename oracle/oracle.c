@@ -54,6 +54,13 @@
  *      smallest integer >= -24 with 448 * 2^k >= max|x| (k = 0 for an all-zero row); each
  *      code is x / 2^k rounded to the nearest E4M3 value, ties to even.  Reading the row
  *      back gives code * 2^k exactly; attention (step 5) runs on those values.
+ *   8. The qkvr projections in front of the prologue [VJ §TML Inkling モデルアーキテクチャ and
+ *      VV §"MoE" (the q, k, v and r linears are BF16 layers); SG §ShortConv：4カ所に現れる
+ *      短距離因果畳み込み (the K and V ShortConvs follow the K and V projections)]: from the
+ *      hidden states x [N][d_model] and one weight matrix w [Hq*d + 2*Hkv*d + Hq*d_r][d_model]
+ *      (a row per output feature), y = x . w^T, each value rounded once to bf16; its columns
+ *      are q, k, v and r in that order, and q, k, v then go through steps 1-4.  (The matrix
+ *      product itself is library arithmetic on the Python side; this file only rounds.)
  */
 #include <math.h>
 #include <stdint.h>
@@ -448,4 +455,9 @@ int oracle_quantize_rows_e4m3(const uint16_t *x, int rows, int width, uint8_t *c
             codes[(size_t)r * width + i] = oracle_f64_to_e4m3(ldexp(bf16_bits_to_f64(xr[i]), -k));
     }
     return ORACLE_OK;
+}
+
+/* Round n doubles to bf16 bit patterns (ties to even), as oracle_f64_to_bf16 does one. */
+void oracle_round_bf16_array(const double *x, long long n, uint16_t *out) {
+    for (long long i = 0; i < n; ++i) out[i] = oracle_f64_to_bf16(x[i]);
 }
