@@ -21,8 +21,8 @@
  *   - Kernels are chained by programmatic dependent launch: each may become resident on
  *     the GPU while the kernel before it on the stream finishes, and reads no global
  *     memory before that kernel has completed, so stream order holds as for any launch.
- *     inkattn_prologue and inkattn_output_conv let the next kernel be scheduled once all
- *     their CTAs have started; the attention kernels do not.  Every call can be captured
+ *     inkattn_prologue, inkattn_output_conv and inkattn_qkvr_prologue let the next kernel
+ *     be scheduled once all their CTAs have started; the attention kernels do not.  Every call can be captured
  *     into a CUDA graph.
  *   - Host-side validation runs before any launch; on failure the call returns
  *     INKATTN_ERR_INVALID_ARG or INKATTN_ERR_UNSUPPORTED and launches nothing.
@@ -330,6 +330,79 @@ typedef struct inkattn_output_conv_params {
  * residual or h_out (INKATTN_ERR_INVALID_ARG); h_out == residual (in place) is allowed,
  * a partial overlap of the two is not.  conv_state must not overlap the other arrays. */
 INKATTN_API inkattn_status inkattn_output_conv(const inkattn_output_conv_params *p, void *stream);
+
+/* ------------------------------------------------------------------------------
+ * The qkvr projections with the attention prologue fused into their epilogue: one pass
+ * from the hidden states to what inkattn_prologue writes, plus r
+ * [VJ §TML Inkling モデルアーキテクチャ and VV, the MoE item of the architecture list: the
+ * q, k, v and r projections ("qkvr linears") are one bf16 linear layer in front of the
+ * attention; SG §ShortConv 最適化：融合、グラフキャプチャ、シャーディング: the prologue's work
+ * fused so that nothing intermediate is written back].
+ *
+ * With F = Hq*128 + 2*Hkv*128 + Hq*d_r output features and the rows of w ordered
+ * [q heads | k | v | r heads] (nn.Linear layout, [F][d_model]):
+ *   y[t][o] = bf16( sum_k x[t][k] * w[o][k] )       (fp32 accumulation on the tensor cores)
+ *   q = y[:, 0:Hq*128] as [N_tok][Hq][128],  k = the next Hkv*128 features,
+ *   v = the next Hkv*128,  r = the last Hq*d_r as [N_tok][Hq][d_r] (written to r_out).
+ * Then everything inkattn_prologue does, on q, k and v, with two differences: the conv
+ * state is read from conv_state_*_in and the new state written to conv_state_*_out, and
+ * a sequence with no new tokens copies its state from in to out.  The projections are
+ * rounded once from the fp32 sum; against the exactly rounded sum that can differ by one
+ * bf16 ulp where the sum lies within the fp32 accumulation error of a rounding midpoint.
+ *
+ * Work is cut into tiles of INKATTN_QKVR_TILE_TOKENS (125) new tokens of one sequence plus
+ * the 3 before them (the conv's history, recomputed rather than exchanged), so a tile
+ * never waits on another.  The new conv state is written by the tile holding a sequence's
+ * last tokens while the sequence's first tile reads the old one; in and out may therefore
+ * be the same array only when max_seqlen_q <= INKATTN_QKVR_TILE_TOKENS (every sequence in
+ * one tile), else INKATTN_ERR_INVALID_ARG.
+ * ------------------------------------------------------------------------------ */
+#define INKATTN_QKVR_TILE_TOKENS 125
+#define INKATTN_QKVR_MAX_SEQS 1024
+
+typedef struct inkattn_qkvr_params {
+    size_t struct_size;        /* = sizeof(inkattn_qkvr_params)                          */
+    int32_t B;                 /* sequences, 1 .. INKATTN_QKVR_MAX_SEQS                  */
+    int32_t N_tok;             /* new tokens = cu_seqlens_q[B], >= 0                     */
+    int32_t max_seqlen_q;      /* >= every q_len[b]                                      */
+    int32_t Hq, Hkv;           /* query / KV heads, Hq % Hkv == 0                        */
+    int32_t head_dim;          /* 128                                                    */
+    int32_t d_r;               /* relative features per query head; Hq*d_r % 8 == 0      */
+    int32_t d_model;           /* hidden width: a multiple of 8, >= 8                    */
+    int32_t block_size;        /* paged-cache block, 64                                  */
+    int32_t num_blocks;        /* cache capacity in blocks (bounds check)                */
+    int32_t num_state_slots;   /* conv-state capacity in slots (bounds check)            */
+    float eps;                 /* RMSNorm epsilon, >= 0                                  */
+    const inkattn_bf16 *x;     /* [N_tok][d_model] hidden states; device memory of this GPU */
+    const inkattn_bf16 *w;     /* [F][d_model]; device memory of this GPU                */
+    const float *conv_w_k;     /* [C][4], C = Hkv*128; w[c][3] weighs the current token  */
+    const float *conv_w_v;     /* [C][4]                                                 */
+    const float *q_norm_w;     /* [128]                                                  */
+    const float *k_norm_w;     /* [128]                                                  */
+    const int32_t *cu_seqlens_q;   /* [B+1], non-decreasing, cu[0] = 0                   */
+    const int32_t *state_slot;     /* [B], distinct values in [0, num_state_slots)       */
+    const int32_t *slot_mapping;   /* [N_tok], distinct values in [0, num_blocks*64)     */
+    const inkattn_bf16 *conv_state_k_in;  /* [num_state_slots][3][C]                     */
+    const inkattn_bf16 *conv_state_v_in;  /* [num_state_slots][3][C]                     */
+    inkattn_bf16 *conv_state_k_out;       /* [num_state_slots][3][C], rows of the        */
+    inkattn_bf16 *conv_state_v_out;       /* sequences' slots written                    */
+    inkattn_bf16 *q_out;           /* [N_tok][Hq][128], normalised                       */
+    inkattn_bf16 *r_out;           /* [N_tok][Hq][d_r]                                   */
+    inkattn_bf16 *y_out;           /* nullable: [N_tok][F], every projection as rounded  */
+    void *k_cache;                 /* as in inkattn_prologue_params                      */
+    void *v_cache;
+    int32_t kv_dtype;              /* INKATTN_KV_BF16 or INKATTN_KV_E4M3                  */
+    float *k_scale;                /* E4M3 only (else NULL), as in inkattn_prologue_params */
+    float *v_scale;
+    int32_t *dev_status;           /* nullable, see the conventions above                */
+} inkattn_qkvr_params;
+
+/* Runs the fused projections and prologue.  x and w are read by TMA (device memory of the
+ * current device, 16-byte aligned; anything else is INKATTN_ERR_INVALID_ARG); q_out,
+ * r_out, y_out, the caches and the states must be 16-byte aligned.  With y_out non-NULL the
+ * projections (before conv and norm) are written there too, at the cost of their bytes.  No output may overlap an
+ * input except conv_state_*_out == conv_state_*_in under the rule above. */
+INKATTN_API inkattn_status inkattn_qkvr_prologue(const inkattn_qkvr_params *p, void *stream);
 
 #ifdef __cplusplus
 }

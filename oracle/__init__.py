@@ -210,6 +210,19 @@ def prologue_for_inputs(x, workload):
                     v_cache=_bits(x["v_cache"]))
 
 
+def qkvr_prologue_for_inputs(x, workload):
+    """qkvr_prologue on a dict of workload tensors (any device, as produced by
+    relative_bias_hybrid_gb300.inputs.make_qkvr_inputs).  Returns numpy arrays."""
+    return qkvr_prologue(x=_bits(x["x"]), w=_bits(x["w_qkvr"]), d_r=workload.d_r,
+                         cu_seqlens_q=_bits(x["cu_seqlens_q"]), Hq=workload.Hq, Hkv=workload.Hkv,
+                         d=workload.head_dim, conv_w_k=_bits(x["conv_w_k"]), conv_w_v=_bits(x["conv_w_v"]),
+                         q_norm_w=_bits(x["q_norm_w"]), k_norm_w=_bits(x["k_norm_w"]), eps=workload.eps,
+                         state_slot=_bits(x["state_slot"]), conv_state_k=_bits(x["conv_state_k"]),
+                         conv_state_v=_bits(x["conv_state_v"]), slot_mapping=_bits(x["slot_mapping"]),
+                         block_size=workload.block_size, k_cache=_bits(x["k_cache"]),
+                         v_cache=_bits(x["v_cache"]))
+
+
 def attention_for_inputs(x, workload, q_bits, k_cache_bits, v_cache_bits, rows=None, n_threads=0):
     """The attention oracle for a workload, on the given normalised queries and caches
     (bf16 bit arrays) and the workload's r, P, lengths and block table."""

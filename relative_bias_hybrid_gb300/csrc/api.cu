@@ -2,7 +2,7 @@
 // descriptor setup, the decode split heuristic, and the launches.
 //
 // Nothing here computes on the host: every step of the path runs in the kernels of
-// prologue.cu, prefill_tc.cu and decode.cu.
+// prologue.cu, qkvr.cu, output_conv.cu, prefill_tc.cu and decode.cu.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -116,6 +116,84 @@ inkattn_status validate_output_conv(const inkattn_output_conv_params *p) {
         overlap(p->out, row, p->h_out, row) || overlap(p->h_out, row, p->y, row) ||
         (p->h_out != p->residual && overlap(p->h_out, row, p->residual, row)))
         return INKATTN_ERR_INVALID_ARG;
+    return INKATTN_OK;
+}
+
+inkattn_status validate_qkvr(const inkattn_qkvr_params *p) {
+    if (!p || p->struct_size != sizeof(inkattn_qkvr_params)) return INKATTN_ERR_INVALID_ARG;
+    if (p->B < 1 || p->B > INKATTN_QKVR_MAX_SEQS || p->N_tok < 0 || p->max_seqlen_q < 0 || p->Hq < 1 ||
+        p->Hkv < 1 || p->Hq % p->Hkv != 0 || p->Hq > 1024 || p->num_blocks < 1 || p->num_state_slots < 1 ||
+        !(p->eps >= 0.f))
+        return INKATTN_ERR_INVALID_ARG;
+    if (p->N_tok > 0 && p->max_seqlen_q < 1) return INKATTN_ERR_INVALID_ARG;
+    if (p->d_r < 1 || p->d_r > 1024 || ((long long)p->Hq * p->d_r) % 8 != 0) return INKATTN_ERR_INVALID_ARG;
+    if (p->d_model < 8 || p->d_model % 8 != 0 || p->d_model > (1 << 20)) return INKATTN_ERR_INVALID_ARG;
+    if ((long long)p->num_blocks * 64 > INT_MAX) return INKATTN_ERR_INVALID_ARG;
+    if (p->head_dim != kHeadDim || p->block_size != kBlock) return INKATTN_ERR_UNSUPPORTED;
+    const void *ptrs16[] = {p->x, p->w, p->conv_state_k_in, p->conv_state_v_in, p->conv_state_k_out,
+                            p->conv_state_v_out, p->q_out, p->r_out, p->k_cache, p->v_cache};
+    for (const void *ptr : ptrs16)
+        if (!ptr || !aligned(ptr, 16)) return INKATTN_ERR_INVALID_ARG;
+    const void *ptrs4[] = {p->conv_w_k, p->conv_w_v, p->q_norm_w, p->k_norm_w, p->cu_seqlens_q,
+                           p->state_slot, p->slot_mapping};
+    for (const void *ptr : ptrs4)
+        if (!ptr || !aligned(ptr, 4)) return INKATTN_ERR_INVALID_ARG;
+    if (p->dev_status && !aligned(p->dev_status, 4)) return INKATTN_ERR_INVALID_ARG;
+    if (p->y_out && !aligned(p->y_out, 16)) return INKATTN_ERR_INVALID_ARG;
+    if (p->kv_dtype != INKATTN_KV_BF16 && p->kv_dtype != INKATTN_KV_E4M3) return INKATTN_ERR_INVALID_ARG;
+    if (p->kv_dtype == INKATTN_KV_E4M3 &&
+        (!p->k_scale || !p->v_scale || !aligned(p->k_scale, 16) || !aligned(p->v_scale, 16)))
+        return INKATTN_ERR_INVALID_ARG;
+    // the new state is written while a sequence's first tile still reads the old one,
+    // unless every sequence fits one tile
+    if ((p->conv_state_k_out == p->conv_state_k_in || p->conv_state_v_out == p->conv_state_v_in) &&
+        p->max_seqlen_q > INKATTN_QKVR_TILE_TOKENS)
+        return INKATTN_ERR_INVALID_ARG;
+    // no output overlaps an input or another output (in == out for the states excepted)
+    const size_t F = (size_t)(p->Hq + 2 * p->Hkv) * kHeadDim + (size_t)p->Hq * p->d_r;
+    const size_t st = (size_t)p->num_state_slots * 3 * p->Hkv * kHeadDim * 2;
+    const size_t cache = (size_t)p->num_blocks * p->Hkv * 64 * kHeadDim * (p->kv_dtype == INKATTN_KV_E4M3 ? 1 : 2);
+    struct Range { const void *a; size_t n; };
+    const Range ins[] = {{p->x, (size_t)p->N_tok * p->d_model * 2}, {p->w, F * p->d_model * 2},
+                         {p->conv_state_k_in, st}, {p->conv_state_v_in, st}};
+    const Range outs[] = {{p->q_out, (size_t)p->N_tok * p->Hq * kHeadDim * 2},
+                          {p->r_out, (size_t)p->N_tok * p->Hq * p->d_r * 2},
+                          {p->k_cache, cache}, {p->v_cache, cache},
+                          {p->conv_state_k_out, st}, {p->conv_state_v_out, st},
+                          {p->y_out, p->y_out ? (size_t)p->N_tok * F * 2 : 0}};
+    auto overlap = [](const Range &x, const Range &y) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(x.a), b = reinterpret_cast<uintptr_t>(y.a);
+        return x.n && y.n && a < b + y.n && b < a + x.n;
+    };
+    constexpr int kOuts = sizeof(outs) / sizeof(outs[0]);
+    for (int o = 0; o < kOuts; ++o) {
+        for (int i = 0; i < 4; ++i) {
+            const bool same_state = (o == 4 && i == 2 && outs[o].a == ins[i].a) ||
+                                    (o == 5 && i == 3 && outs[o].a == ins[i].a);
+            if (!same_state && overlap(outs[o], ins[i])) return INKATTN_ERR_INVALID_ARG;
+        }
+        for (int o2 = o + 1; o2 < kOuts; ++o2)
+            if (overlap(outs[o], outs[o2])) return INKATTN_ERR_INVALID_ARG;
+    }
+    return INKATTN_OK;
+}
+
+// x and w are read by TMA: device memory of the current device (as for validate_locations)
+inkattn_status validate_qkvr_locations(const inkattn_qkvr_params *p) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return INKATTN_ERR_INVALID_ARG;
+    }
+    const void *ptrs[] = {p->x, p->w};
+    for (const void *ptr : ptrs) {
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return INKATTN_ERR_INVALID_ARG;
+        }
+        if (a.type != cudaMemoryTypeDevice || a.device != dev) return INKATTN_ERR_INVALID_ARG;
+    }
     return INKATTN_OK;
 }
 
@@ -311,6 +389,23 @@ bool make_cache_map_e4m3(CUtensorMap *map, const void *base, long long rows) {
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_qkvr_maps(const inkattn_qkvr_params &p, CUtensorMap *xmap, CUtensorMap *wmap) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+    if (!enc) return false;
+    const long long F = (long long)(p.Hq + 2 * p.Hkv) * kHeadDim + (long long)p.Hq * p.d_r;
+    cuuint64_t strides[1] = {(cuuint64_t)p.d_model * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t estr[2] = {1, 1};
+    cuuint64_t xdims[2] = {(cuuint64_t)p.d_model, (cuuint64_t)(p.N_tok > 0 ? p.N_tok : 1)};
+    cuuint64_t wdims[2] = {(cuuint64_t)p.d_model, (cuuint64_t)F};
+    return enc(xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<inkattn_bf16 *>(p.x), xdims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
+           enc(wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<inkattn_bf16 *>(p.w), wdims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_q_map(CUtensorMap *map, const void *base, int n_tok, int hq, int box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
     if (!enc) return false;
@@ -369,6 +464,20 @@ inkattn_status inkattn_output_conv(const inkattn_output_conv_params *p, void *st
     if ((st = check_device(nullptr)) != INKATTN_OK) return st;
     if (p->N_tok == 0) return INKATTN_OK;
     return launch_status(launch_output_conv(*p, static_cast<cudaStream_t>(stream)));
+}
+
+inkattn_status inkattn_qkvr_prologue(const inkattn_qkvr_params *p, void *stream) {
+    inkattn_status st = validate_qkvr(p);
+    if (st != INKATTN_OK) return st;
+    int sms = 0;
+    if ((st = check_device(&sms)) != INKATTN_OK) return st;
+    if ((st = validate_qkvr_locations(p)) != INKATTN_OK) return st;
+    // no tokens and the states in place: nothing to do
+    if (p->N_tok == 0 && p->conv_state_k_out == p->conv_state_k_in && p->conv_state_v_out == p->conv_state_v_in)
+        return INKATTN_OK;
+    CUtensorMap xmap, wmap;
+    if (!make_qkvr_maps(*p, &xmap, &wmap)) return INKATTN_ERR_CUDA;
+    return launch_status(launch_qkvr(*p, xmap, wmap, sms, static_cast<cudaStream_t>(stream)));
 }
 
 inkattn_status inkattn_prefill(const inkattn_attn_params *p, void *stream) {

@@ -69,6 +69,12 @@ struct AttnScalars {
 
 cudaError_t launch_prologue(const inkattn_prologue_params &p, cudaStream_t stream);
 cudaError_t launch_output_conv(const inkattn_output_conv_params &p, cudaStream_t stream);
+// qkvr projections with the prologue in their epilogue; xmap / wmap from make_qkvr_maps
+cudaError_t launch_qkvr(const inkattn_qkvr_params &p, const CUtensorMap &xmap, const CUtensorMap &wmap,
+                        int num_sms, cudaStream_t stream);
+// TMA descriptors of x as [max(N_tok, 1)][d_model] and w as [F][d_model] bf16, box 64
+// columns x 128 rows, 128-byte swizzle.  Returns false on failure.
+bool make_qkvr_maps(const inkattn_qkvr_params &p, CUtensorMap *xmap, CUtensorMap *wmap);
 
 // Decode: S = num_splits (>= 1).  ws_o / ws_lse are unused when S == 1.
 constexpr int kDecodeMaxRows = 128;     // max_seqlen_q * group

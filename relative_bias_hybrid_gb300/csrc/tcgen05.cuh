@@ -192,6 +192,33 @@ __device__ __forceinline__ void mma_bf16_ts_k128_commit(uint32_t d, uint32_t a_t
     }
 }
 
+// One K = 64 stage of a GEMM tile: four K = 16 MMAs over 128-byte-swizzled K-major A and B
+// tiles (the k steps advance the start addresses by 32 bytes, 2 in descriptor units), then,
+// when `rel` is nonzero, a commit of them to the mbarrier at `rel_bar`'s offset in every CTA
+// of the cluster named in `mask`, and, when `done` is nonzero, a second commit to the local
+// `done_bar`.  acc0 = 0 makes the first MMA overwrite D.  Warp-collective like mma_bf16_ss.
+__device__ __forceinline__ void mma_bf16_ss_k64_commit_mc(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
+                                                          uint32_t acc0, uint32_t rel_bar, uint32_t rel,
+                                                          uint16_t mask, uint32_t done_bar, uint32_t done) {
+    asm volatile("{\n\t.reg .pred e, p0, pt, pr, pd;\n\t.reg .b64 a1, b1;\n\t"
+                 "setp.ne.b32 p0, %4, 0;\n\tsetp.eq.u32 pt, 0, 0;\n\t"
+                 "setp.ne.b32 pr, %6, 0;\n\tsetp.ne.b32 pd, %9, 0;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\tand.pred pr, pr, e;\n\tand.pred pd, pd, e;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n\t"
+                 "add.s64 a1, %1, 2;\n\tadd.s64 b1, %2, 2;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t"
+                 "add.s64 a1, %1, 4;\n\tadd.s64 b1, %2, 4;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t"
+                 "add.s64 a1, %1, 6;\n\tadd.s64 b1, %2, 6;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t"
+                 "@pr tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+                 " [%5], %7;\n\t"
+                 "@pd tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%8];\n\t}"
+                 :: "r"(d), "l"(a), "l"(b), "r"(id), "r"(acc0), "r"(rel_bar), "r"(rel), "h"(mask),
+                    "r"(done_bar), "r"(done)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- TMEM <-> registers
 // 32x32b shape: thread i of the warp reads/writes TMEM lane (quarter base + i), 32
 // consecutive 32-bit columns starting at the address's column.

@@ -76,6 +76,24 @@ class OutputConvParams(ctypes.Structure):
     ]
 
 
+class QkvrParams(ctypes.Structure):
+    """inkattn_qkvr_params."""
+    _fields_ = [
+        ("struct_size", ctypes.c_size_t),
+        ("B", _c_i32), ("N_tok", _c_i32), ("max_seqlen_q", _c_i32), ("Hq", _c_i32), ("Hkv", _c_i32),
+        ("head_dim", _c_i32), ("d_r", _c_i32), ("d_model", _c_i32), ("block_size", _c_i32),
+        ("num_blocks", _c_i32), ("num_state_slots", _c_i32), ("eps", ctypes.c_float),
+        ("x", _c_ptr), ("w", _c_ptr),
+        ("conv_w_k", _c_ptr), ("conv_w_v", _c_ptr), ("q_norm_w", _c_ptr), ("k_norm_w", _c_ptr),
+        ("cu_seqlens_q", _c_ptr), ("state_slot", _c_ptr), ("slot_mapping", _c_ptr),
+        ("conv_state_k_in", _c_ptr), ("conv_state_v_in", _c_ptr),
+        ("conv_state_k_out", _c_ptr), ("conv_state_v_out", _c_ptr),
+        ("q_out", _c_ptr), ("r_out", _c_ptr), ("y_out", _c_ptr),
+        ("k_cache", _c_ptr), ("v_cache", _c_ptr), ("kv_dtype", _c_i32), ("k_scale", _c_ptr),
+        ("v_scale", _c_ptr), ("dev_status", _c_ptr),
+    ]
+
+
 class InkattnError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -117,6 +135,8 @@ def lib():
             L.inkattn_decode_noalloc.restype = ctypes.c_int
             L.inkattn_output_conv.argtypes = [P(OutputConvParams), _c_ptr]
             L.inkattn_output_conv.restype = ctypes.c_int
+            L.inkattn_qkvr_prologue.argtypes = [P(QkvrParams), _c_ptr]
+            L.inkattn_qkvr_prologue.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -196,6 +216,11 @@ def inkattn_output_conv(p: OutputConvParams, stream=None, raise_on_error=True) -
 
 
 # ------------------------------------------------------------------ marshalling helpers
+
+def inkattn_qkvr_prologue(p: QkvrParams, stream=None, raise_on_error=True) -> int:
+    return _check(lib().inkattn_qkvr_prologue(ctypes.byref(p), _stream(stream)), "inkattn_qkvr_prologue",
+                  raise_on_error)
+
 
 def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor") -> Optional[int]:
     if t is None:
@@ -317,5 +342,45 @@ def output_conv_params(*, y, conv_w, norm_w, cu_seqlens_q, state_slot, conv_stat
     p.residual = _ptr(residual, bf, "residual")
     p.h_out = _ptr(h_out, bf, "h_out")
     p.out = _ptr(out, bf, "out")
+    p.dev_status = _ptr(dev_status, i32, "dev_status")
+    return p
+
+
+def qkvr_params(*, x, w, conv_w_k, conv_w_v, q_norm_w, k_norm_w, cu_seqlens_q, state_slot, slot_mapping,
+                conv_state_k_in, conv_state_v_in, conv_state_k_out, conv_state_v_out, q_out, r_out,
+                k_cache, v_cache, max_seqlen_q: int, eps: float = 1e-6, dev_status=None, k_scale=None,
+                v_scale=None, y_out=None) -> QkvrParams:
+    """Fill an inkattn_qkvr_params from torch tensors (see include/inkattn.h): x [N][d_model],
+    w [F][d_model], q_out [N][Hq][128], r_out [N][Hq][d_r], y_out None or [N][F]."""
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    N, Hq, d = q_out.shape
+    p = QkvrParams()
+    p.struct_size = ctypes.sizeof(QkvrParams)
+    p.B = cu_seqlens_q.numel() - 1
+    p.N_tok = N
+    p.max_seqlen_q = int(max_seqlen_q)
+    p.Hq, p.Hkv, p.head_dim = Hq, k_cache.shape[1], d
+    p.d_r = r_out.shape[2]
+    p.d_model = x.shape[1]
+    p.block_size = k_cache.shape[2]
+    p.num_blocks = k_cache.shape[0]
+    p.num_state_slots = conv_state_k_in.shape[0]
+    p.eps = float(eps)
+    p.x = _ptr(x, bf, "x"); p.w = _ptr(w, bf, "w")
+    p.conv_w_k = _ptr(conv_w_k, f32, "conv_w_k"); p.conv_w_v = _ptr(conv_w_v, f32, "conv_w_v")
+    p.q_norm_w = _ptr(q_norm_w, f32, "q_norm_w"); p.k_norm_w = _ptr(k_norm_w, f32, "k_norm_w")
+    p.cu_seqlens_q = _ptr(cu_seqlens_q, i32, "cu_seqlens_q")
+    p.state_slot = _ptr(state_slot, i32, "state_slot")
+    p.slot_mapping = _ptr(slot_mapping, i32, "slot_mapping")
+    p.conv_state_k_in = _ptr(conv_state_k_in, bf, "conv_state_k_in")
+    p.conv_state_v_in = _ptr(conv_state_v_in, bf, "conv_state_v_in")
+    p.conv_state_k_out = _ptr(conv_state_k_out, bf, "conv_state_k_out")
+    p.conv_state_v_out = _ptr(conv_state_v_out, bf, "conv_state_v_out")
+    p.q_out = _ptr(q_out, bf, "q_out"); p.r_out = _ptr(r_out, bf, "r_out")
+    p.y_out = _ptr(y_out, bf, "y_out")
+    p.kv_dtype, cache_dt = _kv_dtype(k_cache)
+    p.k_cache = _ptr(k_cache, cache_dt, "k_cache"); p.v_cache = _ptr(v_cache, cache_dt, "v_cache")
+    if p.kv_dtype == INKATTN_KV_E4M3:
+        p.k_scale = _ptr(k_scale, f32, "k_scale"); p.v_scale = _ptr(v_scale, f32, "v_scale")
     p.dev_status = _ptr(dev_status, i32, "dev_status")
     return p

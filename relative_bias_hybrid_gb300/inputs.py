@@ -114,7 +114,7 @@ _TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "r": 4, "P": 5, "conv_w_k": 6, "conv_w_v"
                "q_norm_w": 8, "k_norm_w": 9, "conv_state_k": 10, "conv_state_v": 11,
                "k_cache": 12, "v_cache": 13, "perm": 14, "y": 15, "residual": 16,
                "oc_conv_w": 17, "oc_norm_w": 18, "oc_conv_state": 19, "k_cache_e4m3": 20,
-               "v_cache_e4m3": 21}
+               "v_cache_e4m3": 21, "x": 22, "w_qkvr": 23}
 
 
 def _gen(device, seed: int, tensor: str) -> torch.Generator:
@@ -205,6 +205,40 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu", kv_dtype: str = "bf16"
             out[f"{name}_scale"] = torch.full(shape[:3], 2.0 ** -7, dtype=torch.float32, device=device)
     else:
         raise ValueError(kv_dtype)
+    return out
+
+
+def qkvr_features(w: Workload) -> int:
+    """Output features of the qkvr projections: Hq*d + 2*Hkv*d + Hq*d_r."""
+    return (w.Hq + 2 * w.Hkv) * w.head_dim + w.Hq * w.d_r
+
+
+def make_qkvr_inputs(w: Workload, d_model: int, seed: int = 0, device="cpu", kv_dtype: str = "bf16",
+                     grid: bool = False) -> Dict[str, torch.Tensor]:
+    """Inputs of the qkvr projections with the prologue fused in: make_inputs' tensors with
+    q, k, v and r replaced by the hidden states x [N, d_model] bf16 and the projection
+    weight w_qkvr [F, d_model] bf16 (nn.Linear layout, rows [q heads | k | v | r heads],
+    F = qkvr_features(w)); P, seqlen_k and block_table are kept for the attention after it.
+
+    Default: x ~ N(0, 1) and w_qkvr ~ N(0, 1/d_model), so each projection is about N(0, 1).
+    grid=True: x = i/8 and w_qkvr = j/64 with integers i, j uniform in [-8, 8]: every product
+    is a multiple of 2^-9 and every partial sum of a row is at most d_model/8 in magnitude,
+    so for d_model < 2^18 each sum is exact in fp32 whatever the order of accumulation.
+    """
+    device = torch.device(device)
+    out = make_inputs(w, seed=seed, device=device, kv_dtype=kv_dtype)
+    for k in ("q", "k", "v", "r"):
+        del out[k]
+    N, F = w.N_tok, qkvr_features(w)
+    bf = torch.bfloat16
+    if grid:
+        gx, gw = _gen(device, seed, "x"), _gen(device, seed, "w_qkvr")
+        out["x"] = (torch.randint(-8, 9, (N, d_model), generator=gx, device=device).to(torch.float32) / 8).to(bf)
+        out["w_qkvr"] = (torch.randint(-8, 9, (F, d_model), generator=gw, device=device).to(torch.float32)
+                         / 64).to(bf)
+    else:
+        out["x"] = _normal((N, d_model), 1.0, device, seed, "x", bf)
+        out["w_qkvr"] = _normal((F, d_model), d_model ** -0.5, device, seed, "w_qkvr", bf)
     return out
 
 

@@ -112,3 +112,46 @@ class OutputConvStep:
 
     def device_status(self) -> int:
         return int(self.status.item())
+
+
+class QkvrStep:
+    """Buffers + call of the qkvr projections with the prologue fused in
+    (inkattn_qkvr_prologue) over a workload's new tokens.
+
+    `inputs` comes from inputs.make_qkvr_inputs.  The conv state is read from
+    inputs["conv_state_k"/"conv_state_v"] and the new state written to this object's
+    state_k / state_v (in place when `in_place`, allowed when every sequence fits one
+    tile); q_out, r_out and, with want_y, y_out (the projections) are buffers of this object;
+    the caches in `inputs` receive the new rows.
+    """
+
+    def __init__(self, w: Workload, inputs: Dict[str, torch.Tensor], in_place: bool = False,
+                 want_y: bool = False):
+        self.w, self.x = w, inputs
+        dev = inputs["x"].device
+        N = w.N_tok
+        self.q_out = torch.empty((N, w.Hq, w.head_dim), dtype=torch.bfloat16, device=dev)
+        self.r_out = torch.empty((N, w.Hq, w.d_r), dtype=torch.bfloat16, device=dev)
+        self.y_out = (torch.empty((N, inputs["w_qkvr"].shape[0]), dtype=torch.bfloat16, device=dev)
+                      if want_y else None)
+        if in_place:
+            self.state_k, self.state_v = inputs["conv_state_k"], inputs["conv_state_v"]
+        else:
+            self.state_k = torch.empty_like(inputs["conv_state_k"])
+            self.state_v = torch.empty_like(inputs["conv_state_v"])
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.p = ia.qkvr_params(
+            x=inputs["x"], w=inputs["w_qkvr"], conv_w_k=inputs["conv_w_k"], conv_w_v=inputs["conv_w_v"],
+            q_norm_w=inputs["q_norm_w"], k_norm_w=inputs["k_norm_w"], cu_seqlens_q=inputs["cu_seqlens_q"],
+            state_slot=inputs["state_slot"], slot_mapping=inputs["slot_mapping"],
+            conv_state_k_in=inputs["conv_state_k"], conv_state_v_in=inputs["conv_state_v"],
+            conv_state_k_out=self.state_k, conv_state_v_out=self.state_v, q_out=self.q_out,
+            r_out=self.r_out, k_cache=inputs["k_cache"], v_cache=inputs["v_cache"],
+            max_seqlen_q=max(w.q_lens) if w.q_lens else 0, eps=w.eps, dev_status=self.status,
+            k_scale=inputs.get("k_scale"), v_scale=inputs.get("v_scale"), y_out=self.y_out)
+
+    def run(self, stream=None):
+        ia.inkattn_qkvr_prologue(self.p, stream)
+
+    def device_status(self) -> int:
+        return int(self.status.item())

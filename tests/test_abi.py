@@ -31,7 +31,7 @@ def test_header_declares_the_entry_points():
     assert {"inkattn_prologue", "inkattn_prefill", "inkattn_decode", "inkattn_combine",
             "inkattn_decode_num_splits", "inkattn_decode_workspace_bytes",
             "inkattn_status_string", "inkattn_abi_version", "inkattn_decode_noalloc",
-            "inkattn_output_conv"} <= names
+            "inkattn_output_conv", "inkattn_qkvr_prologue"} <= names
 
 
 def test_library_exports_every_declared_symbol(ia):
@@ -47,7 +47,7 @@ def test_library_exports_every_declared_symbol(ia):
 
 def test_ctypes_structs_match_c_layout(ia, tmp_path):
     structs = {"inkattn_prologue_params": ia.PrologueParams, "inkattn_attn_params": ia.AttnParams,
-               "inkattn_output_conv_params": ia.OutputConvParams}
+               "inkattn_output_conv_params": ia.OutputConvParams, "inkattn_qkvr_params": ia.QkvrParams}
     lines = ["#include <stdio.h>", "#include <stddef.h>", f'#include "{HEADER}"', "int main(void){"]
     for cname, py in structs.items():
         lines.append(f'printf("{cname} sizeof %zu\\n", sizeof({cname}));')
@@ -240,3 +240,54 @@ def test_output_conv_host_validation(ia):
     # in place (h_out == residual) passes validation
     assert call(_oc(ia, h_out=p.residual)) != bad
     assert call(_oc(ia)) != bad
+
+
+def _qk(ia, **kw):
+    p = ia.QkvrParams()
+    p.struct_size = ctypes.sizeof(ia.QkvrParams)
+    p.B, p.N_tok, p.max_seqlen_q = 2, 300, 200
+    p.Hq, p.Hkv, p.head_dim, p.d_r, p.d_model = 16, 2, 128, 32, 1024
+    p.block_size, p.num_blocks, p.num_state_slots = 64, 16, 2
+    p.eps = 1e-6
+    span = 16 << 20         # bytes reserved per array, more than any of them needs
+    base = 1 << 32          # fake, never dereferenced: every array gets its own range
+    for i, f in enumerate(("x", "w", "conv_w_k", "conv_w_v", "q_norm_w", "k_norm_w", "cu_seqlens_q",
+                           "state_slot", "slot_mapping", "conv_state_k_in", "conv_state_v_in",
+                           "conv_state_k_out", "conv_state_v_out", "q_out", "r_out", "k_cache", "v_cache")):
+        setattr(p, f, base + i * span)
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_qkvr_host_validation(ia):
+    """Validation of inkattn_qkvr_prologue runs before it looks for a device: every case
+    here is rejected with INVALID_ARG (or UNSUPPORTED); a valid struct gets past it (and,
+    without a GPU, stops at the device check)."""
+    L = ia.lib()
+    bad = ia.INKATTN_ERR_INVALID_ARG
+    call = lambda p: ia.inkattn_qkvr_prologue(p, stream=0, raise_on_error=False)
+    assert L.inkattn_qkvr_prologue(None, None) == bad
+    assert call(_qk(ia, struct_size=8)) == bad
+    assert call(_qk(ia, B=0)) == bad
+    assert call(_qk(ia, B=1025)) == bad                 # above INKATTN_QKVR_MAX_SEQS
+    assert call(_qk(ia, d_model=1020)) == bad           # not a multiple of 8
+    assert call(_qk(ia, Hq=15)) == bad                  # Hq % Hkv
+    assert call(_qk(ia, Hq=1, Hkv=1, d_r=4)) == bad     # Hq * d_r not a multiple of 8
+    assert call(_qk(ia, head_dim=64)) == ia.INKATTN_ERR_UNSUPPORTED
+    assert call(_qk(ia, x=None)) == bad
+    assert call(_qk(ia, y_out=(1 << 40) + 8)) == bad    # not 16-byte aligned
+    assert call(_qk(ia, kv_dtype=1)) == bad             # E4M3 without row scales
+    p = _qk(ia)
+    # the new state may replace the old in place only when every sequence fits one tile
+    assert call(_qk(ia, conv_state_k_out=p.conv_state_k_in)) == bad
+    assert call(_qk(ia, conv_state_v_out=p.conv_state_v_in, max_seqlen_q=126)) == bad
+    assert call(_qk(ia, conv_state_k_out=p.conv_state_k_in, conv_state_v_out=p.conv_state_v_in,
+                    max_seqlen_q=125)) != bad
+    # outputs overlapping an input or each other
+    assert call(_qk(ia, q_out=p.x + 1024)) == bad
+    assert call(_qk(ia, r_out=p.q_out + 4096)) == bad
+    assert call(_qk(ia, conv_state_k_out=p.conv_state_v_in)) == bad
+    assert call(_qk(ia, y_out=p.k_cache)) == bad
+    assert call(_qk(ia, y_out=(1 << 40))) != bad
+    assert call(_qk(ia)) != bad
