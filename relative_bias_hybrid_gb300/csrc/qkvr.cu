@@ -18,17 +18,25 @@
 // tile the carried conv state takes their place).  Recomputing those 3 rows (2.4% of the
 // MMAs) makes every tile independent: no tile waits for another's projections.  A work item
 // is a pair of M tiles (consecutive in the list of all sequences' tiles) times a block of
-// 256 output features; the pair's two CTAs form a cluster, each loads its own 128 x 64 A
-// box and one 128-row half of the 256 x 64 weight box, multicast to both, so each weight
-// byte crosses from L2 once per pair.  Items go round-robin over a persistent grid of
-// clusters, in groups of 8 feature blocks with the M pairs fastest inside a group, so that
-// the weight blocks of a group stay in L2 while the tiles stream past them.
+// 256 output features, computed by the two CTAs of a cluster as one M = 256, N = 256 tile of
+// pair MMAs (tcgen05 cta_group::2): each CTA holds its own 128 rows of x and one 128-row
+// half of the weight block, and the even CTA issues MMAs that read both CTAs' shared
+// memory and write each CTA's 128 rows of D to that CTA's TMEM.  Per SM and MMA step the
+// tensor core thus reads 8 KB of operands from shared memory instead of the 12 KB of an
+// M = 128, N = 256 MMA, and TMA writes 32 KB per stage instead of 48: shared-memory
+// bandwidth, which bounds the single-CTA form near two thirds of the tensor rate, stays
+// within reach.  Items go round-robin over a persistent grid of clusters, in groups of 8
+// feature blocks with the M pairs fastest inside a group, so that the weight blocks of a
+// group stay in L2 while the tiles stream past them.
 //
 // One CTA per SM, 10 warps:
-//   warp 0      producer: TMA of the A and weight boxes into a 3-stage ring (48 KB a stage)
-//   warp 1      MMA issuer (whole warp, one elected lane): M = 128, N = 256, K = 16 steps
-//               into one of two TMEM accumulators (2 x 256 columns), so the epilogue of
-//               one item overlaps the MMAs of the next
+//   warp 0      producer: TMA of the CTA's A and weight boxes into a 4-stage ring (32 KB a
+//               stage)
+//   warp 1      even CTA: MMA issuer (whole warp, one elected lane), M = 256, N = 256,
+//               K = 16 steps into one of two TMEM accumulators (2 x 256 columns), so the
+//               epilogue of one item overlaps the MMAs of the next (idle in the odd CTA)
+// Both CTAs' copies of a stage complete on the even CTA's barrier for it, which the MMA
+// warp waits on; the pair MMAs' commits release the stage in both CTAs.
 //   warps 2-5   epilogue of the item's first 128 features, warps 6-9 of the second: each
 //               128-feature block is one q head, one k or v head, or 128 features of r.
 // Epilogue of a block: each thread moves its TMEM lane (one tile row) to bf16 in a shared
@@ -55,10 +63,10 @@ constexpr int kTileTok = kRowsM - kHalo;          // new tokens per M tile
 static_assert(kTileTok == INKATTN_QKVR_TILE_TOKENS, "the tile size the header publishes");
 constexpr int kCols = 256;                        // MMA N: output features of an item
 constexpr int kKStep = 64;                        // K per ring stage (one 128-byte row)
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kABytes = kRowsM * 128;             // 16 KB
 constexpr int kBHalfBytes = 128 * 128;            // 16 KB, one CTA's half of the weight box
-constexpr int kStageBytes = kABytes + 2 * kBHalfBytes;
+constexpr int kStageBytes = kABytes + kBHalfBytes;
 constexpr int kThreads = 320;
 constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpEpi = 2;
 constexpr int kRowStride = 272;                   // staging row: 256 bytes + 16
@@ -125,24 +133,29 @@ k_qkvr(const QkvrArgs A, const __grid_constant__ CUtensorMap xmap, const __grid_
         const bool r = mbar_wait(addr, parity, p.dev_status, abort_flag, A.wait_ns);
         return __all_sync(0xffffffffu, r);
     };
+    // for phases completed from the other CTA (its commits, its remote arrivals)
+    auto cwait = [&](uint32_t addr, uint32_t parity) -> bool {
+        const bool r = mbar_wait_cluster(addr, parity, p.dev_status, abort_flag, A.wait_ns);
+        return __all_sync(0xffffffffu, r);
+    };
     const int C = p.Hkv * kHeadDim;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar(B_FULL + s), 1);
-            mbar_init(bar(B_EMPTY + s), 2);                  // released by both CTAs' MMAs
+            mbar_init(bar(B_FULL + s), 1);                   // (the even CTA's counts both CTAs' copies)
+            mbar_init(bar(B_EMPTY + s), 1);                  // released by the pair's MMAs
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(B_ACC_FULL + s), 1);
-            mbar_init(bar(B_ACC_EMPTY + s), 8);              // one arrival per epilogue warp
+            mbar_init(bar(B_ACC_EMPTY + s), 16);             // every epilogue warp of both CTAs
         }
         mbar_init(bar(B_DRAIN), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == kWarpMma) {
-        tc::tmem_alloc(smem_u32(tmem_slot), 512);
-        tc::tmem_relinquish();
+    if (warp == kWarpMma) {                            // with the peer CTA's MMA warp
+        tc::tmem_alloc_pair(smem_u32(tmem_slot), 512);
+        tc::tmem_relinquish_pair();
     }
     if (warp == kWarpEpi) {
         // tile prefix over the sequences: s_tiles[b] = M tiles of sequences 0 .. b-1
@@ -234,32 +247,41 @@ k_qkvr(const QkvrArgs A, const __grid_constant__ CUtensorMap xmap, const __grid_
                 const int b = seq_of(mt);
                 row0 = p.cu_seqlens_q[b] + (mt - s_tiles[b]) * kTileTok - kHalo;
             }
-            const int wrow = cb * kCols + (int)crank * 128;
+            const int wrow = cb * kCols + (int)crank * 128;   // this CTA's half of the block
             for (int k = 0; k < nk; ++k, ++L) {
                 const int s = L % kStages;
-                if (L >= kStages && !wwait(bar(B_EMPTY + s), ((L / kStages) - 1) & 1)) {
+                if (L >= kStages && !cwait(bar(B_EMPTY + s), ((L / kStages) - 1) & 1)) {
                     ok = false;
                     break;
                 }
                 if (lane == 0) {
                     const uint32_t dst = s_base + kOffRing + (uint32_t)(s * kStageBytes);
-                    const uint32_t fb = bar(B_FULL + s);
-                    mbar_arrive_expect_tx(fb, kStageBytes);   // A, and both weight halves
-                    tma_load_2d(dst, &xmap, k * kKStep, row0, fb);
-                    tma_load_2d_mc(dst + kABytes + crank * kBHalfBytes, &wmap, k * kKStep, wrow, fb, 3);
+                    if (crank == 0) {
+                        const uint32_t fb = bar(B_FULL + s);
+                        mbar_arrive_expect_tx(fb, 2 * kStageBytes);   // this CTA's copies and the peer's
+                        tma_load_2d(dst, &xmap, k * kKStep, row0, fb);
+                        tma_load_2d(dst + kABytes, &wmap, k * kKStep, wrow, fb);
+                    } else {
+                        const uint32_t fb = mapa_shared(bar(B_FULL + s), 0);
+                        tma_load_2d_pair(dst, &xmap, k * kKStep, row0, fb);
+                        tma_load_2d_pair(dst + kABytes, &wmap, k * kKStep, wrow, fb);
+                    }
                 }
                 __syncwarp();
             }
         }
-        // nothing may still be landing in shared memory when the CTA tears down: the last
-        // kStages loads issued are waited for (earlier ones were consumed before their slot
-        // was reloaded)
-        if (lane == 0)
+        // nothing may still be landing in shared memory when the pair tears down: the even
+        // CTA waits for the last kStages stages of both CTAs (earlier ones were consumed
+        // before their slot was reloaded), and the odd CTA leaves only after it (the
+        // cluster barrier at the end)
+        if (lane == 0 && crank == 0)
             for (int l = max(0, L - kStages); l < L; ++l)
                 mbar_drain(bar(B_FULL + l % kStages), (l / kStages) & 1, p.dev_status, A.wait_ns);
+    } else if (warp == kWarpMma && crank != 0) {
+        // the odd CTA issues no MMAs
     } else if (warp == kWarpMma) {
-        // ================================ MMA issuer ================================
-        const uint32_t id = tc::idesc(kRowsM, kCols, tc::kFmtBF16, 0, 0);
+        // ================================ even CTA: MMA issuer ================================
+        const uint32_t id = tc::idesc(2 * kRowsM, kCols, tc::kFmtBF16, 0, 0);
         const uint64_t da0 = tc::sdesc_sw128(s_base + kOffRing, 16, 1024);
         const uint64_t db0 = tc::sdesc_sw128(s_base + kOffRing + kABytes, 16, 1024);
         // loads of this cluster in all; the last kStages are not released, so that no
@@ -271,27 +293,29 @@ k_qkvr(const QkvrArgs A, const __grid_constant__ CUtensorMap xmap, const __grid_
         int i = 0;
         for (int w = cid; w < n_items && ok; w += nclusters, ++i) {
             const int buf = i & 1;
-            if (i >= 2 && !wwait(bar(B_ACC_EMPTY + buf), ((i >> 1) - 1) & 1)) {
+            // both CTAs' epilogues are done with this accumulator
+            if (i >= 2 && !cwait(bar(B_ACC_EMPTY + buf), ((i >> 1) - 1) & 1)) {
                 ok = false;
                 break;
             }
             tc::fence_after();
             for (int k = 0; k < nk; ++k, ++L) {
                 const int s = (int)(L % kStages);
-                if (!wwait(bar(B_FULL + s), (uint32_t)((L / kStages) & 1))) {
+                const uint32_t par = (uint32_t)((L / kStages) & 1);
+                if (!cwait(bar(B_FULL + s), par)) {
                     ok = false;
                     break;
                 }
                 tc::fence_after();
                 const uint64_t off = (uint64_t)(s * (kStageBytes >> 4));
-                tc::mma_bf16_ss_k64_commit_mc(tmem + (uint32_t)(buf * kCols), da0 + off, db0 + off, id,
-                                              k > 0 ? 1u : 0u, bar(B_EMPTY + s), L + kStages < total ? 1u : 0u,
-                                              3, bar(B_ACC_FULL + buf), k == nk - 1 ? 1u : 0u);
+                tc::mma_pair_bf16_ss_k64_commit(tmem + (uint32_t)(buf * kCols), da0 + off, db0 + off, id,
+                                                k > 0 ? 1u : 0u, bar(B_EMPTY + s), L + kStages < total ? 1u : 0u,
+                                                bar(B_ACC_FULL + buf), k == nk - 1 ? 1u : 0u);
                 __syncwarp();
             }
         }
-        // every MMA of this CTA has completed before TMEM is released
-        tc::commit(bar(B_DRAIN));
+        // every MMA of the pair has completed before TMEM is released
+        tc::commit_pair(bar(B_DRAIN));
         __syncwarp();
         (void)mbar_drain(bar(B_DRAIN), 0, p.dev_status, A.wait_ns);
         __syncwarp();
@@ -338,8 +362,8 @@ k_qkvr(const QkvrArgs A, const __grid_constant__ CUtensorMap xmap, const __grid_
 
             // the accumulator is ready, and (the same barrier) the group is done with the
             // staging rows of the previous item
-            bool ok = mbar_wait(bar(B_ACC_FULL + buf), (uint32_t)((i >> 1) & 1), p.dev_status, abort_flag,
-                                A.wait_ns);
+            bool ok = mbar_wait_cluster(bar(B_ACC_FULL + buf), (uint32_t)((i >> 1) & 1), p.dev_status,
+                                        abort_flag, A.wait_ns);
             if (!group_all(gid, ok)) break;
             tc::fence_after();
 
@@ -369,7 +393,7 @@ k_qkvr(const QkvrArgs A, const __grid_constant__ CUtensorMap xmap, const __grid_
             }
             tc::fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_ACC_EMPTY + buf));
+            if (lane == 0) mbar_remote_arrive(bar(B_ACC_EMPTY + buf), 0);   // the even CTA's MMA warp waits
             if (!live) continue;                              // uniform over the group
             group_sync(gid);                                  // the staging rows are complete
 
@@ -487,9 +511,9 @@ k_qkvr(const QkvrArgs A, const __grid_constant__ CUtensorMap xmap, const __grid_
 
     tc::fence_before();
     __syncthreads();
-    if (warp == kWarpMma) {
+    if (warp == kWarpMma) {                            // with the peer CTA's MMA warp
         tc::fence_after();
-        tc::tmem_dealloc(tmem, 512);
+        tc::tmem_dealloc_pair(tmem, 512);
     }
     cluster_sync();                  // a CTA leaves only when its peer no longer writes into it
 }
