@@ -9,7 +9,10 @@ value = its algorithmic attention TFLOP/s per step.  The same JSON line carries 
 sliding-window layer, the ragged mixed-prefill batch and the MTP-verify decode under
 "workloads", each with its kernel rooflines, the end-to-end number through the C ABI
 with host buffers, and the fp64 oracle timed on a bounded sample on the host cores;
-plus the SM clocks sampled during the timed regions.
+plus the SM clocks sampled during the timed regions.  Beside the step, each prefill
+workload also times two kernels alone: the attention-output ShortConv (k_output_conv) and
+the qkvr projections with the prologue fused in (k_qkvr, from hidden states of width
+8192), each with its own roofline entry.
 
   python bench.py [--steps K] [--warmup W] [--impl reference] [--only NAME ...]
 
@@ -48,7 +51,12 @@ KERNEL_SOURCES = {
                    "relative_bias_hybrid_gb300/csrc/fp8.cuh", "relative_bias_hybrid_gb300/csrc/common.cuh"],
     "k_output_conv": ["relative_bias_hybrid_gb300/csrc/output_conv.cu", "relative_bias_hybrid_gb300/csrc/conv4.cuh",
                       "relative_bias_hybrid_gb300/csrc/common.cuh"],
+    "k_qkvr": ["relative_bias_hybrid_gb300/csrc/qkvr.cu", "relative_bias_hybrid_gb300/csrc/tcgen05.cuh",
+               "relative_bias_hybrid_gb300/csrc/cta_pair.cuh",
+               "relative_bias_hybrid_gb300/csrc/conv4.cuh", "relative_bias_hybrid_gb300/csrc/fp8.cuh",
+               "relative_bias_hybrid_gb300/csrc/common.cuh"],
 }
+QKVR_D_MODEL = 8192     # hidden width of the qkvr projections' input (Hq * 128)
 
 
 # ---------------------------------------------------------------- algorithmic work
@@ -89,6 +97,14 @@ def output_conv_bytes(w, D: int) -> float:
     """y and the residual in, h and out written (bf16 rows of D), conv state read + write,
     taps and gains once."""
     return float(4 * 2 * D * w.N_tok + w.B * 2 * 3 * D * 2 + D * (4 * 4 + 4))
+
+
+def qkvr_flops(w, d_model: int) -> float:
+    """The projections y = x . w^T of the new tokens: 2 FLOP per multiply-add, F = Hq*d +
+    2*Hkv*d + Hq*d_r outputs of length d_model each.  The 3 rows per 125-token tile that
+    the kernel recomputes for the conv, and the prologue's arithmetic, are not counted."""
+    F = (w.Hq + 2 * w.Hkv) * w.head_dim + w.Hq * w.d_r
+    return 2.0 * w.N_tok * F * d_model
 
 
 def decode_bytes(w, kv_dtype: str = "bf16") -> float:
@@ -504,6 +520,43 @@ def time_output_conv(w, args, dev, stream, flush, peaks, name):
     return roof, args.steps
 
 
+def time_qkvr(w, args, dev, stream, flush, peaks, name):
+    """The qkvr projections of the workload's new tokens (hidden width QKVR_D_MODEL) with the
+    prologue fused in, timed alone like the output conv.  Returns its roofline entry and the
+    launches timed."""
+    from relative_bias_hybrid_gb300 import inputs as gen
+    from relative_bias_hybrid_gb300.step import QkvrStep
+    x = gen.make_qkvr_inputs(w, QKVR_D_MODEL, seed=0, device=dev)
+    qk = QkvrStep(w, x)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            qk.run(stream)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record(stream)
+            qk.run(stream)
+            e1.record(stream)
+    torch.cuda.synchronize()
+    if qk.device_status() != 0:
+        raise RuntimeError(f"{name}: qkvr device status {qk.device_status()}")
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / len(evs)
+    fl = qkvr_flops(w, QKVR_D_MODEL)
+    tf = fl / (ms * 1e-3) / 1e12
+    roof = {"bound": "tensor", "kernel": "k_qkvr", "achieved": tf, "peak": peaks["bf16"], "unit": "TFLOP/s",
+            "frac": tf / peaks["bf16"], "peak_src": peaks["src"] + " (burst bf16)",
+            "frac_of_sustained": tf / peaks["bf16_sustained"], "traffic": ncu_traffic("k_qkvr", name),
+            "algorithmic_flop_per_launch": fl, "ms": ms, "d_model": QKVR_D_MODEL,
+            "note": "timed alone, outside the step: the qkvr projections with the prologue fused in, "
+                    "from synthetic hidden states"}
+    del x, qk
+    return roof, args.steps
+
+
 def measure(name, args, peaks, dev, stream, flush):
     """Device-timed steps, then end-to-end steps, of one workload.  Returns its report
     (without cpu_baseline), the launches inside its timed regions and the host copy the
@@ -533,10 +586,14 @@ def measure(name, args, peaks, dev, stream, flush):
     # timed: the step loop, the attention loop, the prologue loop, the end-to-end loop
     n_att = step.launches_per_run() - 1
     launches = args.steps * (2 * step.launches_per_run() + n_att + 1)
-    oc_roof = None
+    oc_roof = qk_roof = None
     if kv == "bf16":            # (the output conv does not depend on the cache type)
         oc_roof, oc_launches = time_output_conv(w, args, dev, stream, flush, peaks, name)
         launches += oc_launches
+    if mode == "prefill":       # (the qkvr kernel's 125-token tiles are made for prefill)
+        qk_roof, qk_launches = time_qkvr(w, args, dev, stream, flush, peaks, name)
+        launches += qk_launches
+    extra = {**({"k_output_conv": oc_roof} if oc_roof else {}), **({"k_qkvr": qk_roof} if qk_roof else {})}
 
     pro_bytes = prologue_bytes(w)
     prologue = {"bound": "hbm", "kernel": "k_prologue", "achieved": pro_bytes / (pro_ms * 1e-3) / 1e9,
@@ -552,7 +609,7 @@ def measure(name, args, peaks, dev, stream, flush):
                 "algorithmic_flop_per_launch": fl, "ms": att_ms}
         rep = {"workload": w.describe() + "; step = inkattn_prologue + inkattn_prefill",
                "value": fl / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
-               "roofline": roof, "rooflines": {"k_prologue": prologue, **({"k_output_conv": oc_roof} if oc_roof else {})},
+               "roofline": roof, "rooflines": {"k_prologue": prologue, **extra},
                "e2e": {"value": fl / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}}
         host = HostCopy(w, x, step.q_out)
@@ -566,7 +623,7 @@ def measure(name, args, peaks, dev, stream, flush):
         rep = {"workload": w.describe() + (", E4M3 KV cache with a power-of-two scale per row" if kv == "e4m3" else "")
                            + "; step = inkattn_prologue + inkattn_decode (+ inkattn_combine)",
                "value": nbytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
-               "roofline": roof, "rooflines": {"k_prologue": prologue, **({"k_output_conv": oc_roof} if oc_roof else {})},
+               "roofline": roof, "rooflines": {"k_prologue": prologue, **extra},
                "e2e": {"value": nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}}
         host = HostCopy(w, x, step.q_out, seqs=list(range(DECODE_ORACLE_SEQS)))

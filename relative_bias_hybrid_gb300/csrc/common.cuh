@@ -111,46 +111,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t
     }
 }
 
-// Non-blocking test of a phase that other CTAs of the cluster complete (arrivals made with
-// release at cluster scope, mbar_remote_arrive): cluster-scope acquire.
-__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-    return ok != 0;
-}
-
-// mbar_wait for a phase completed from another CTA of the cluster (a remote arrival, or a
-// tensor-core commit issued there).  It polls, with a short back-off: a thread suspended in
-// try_wait is not woken promptly by such an arrival.
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int32_t *status,
-                                                  volatile int *abort, uint64_t limit_ns) {
-    if (mbar_test_wait_cluster(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (uint32_t n = 1;; ++n) {
-        if (mbar_test_wait_cluster(bar, parity)) return true;
-        __nanosleep(32);
-        if ((n & 255u) == 0u) {
-            if (abort && *abort) return false;
-            if (globaltimer() - t0 > limit_ns) {
-                set_status(status, INKATTN_ERR_DEVICE_TIMEOUT);
-                if (abort) *abort = 1;
-                return false;
-            }
-        }
-    }
-}
-
-// One arrival, with release at cluster scope, on the mbarrier at `bar`'s offset in the
-// shared memory of CTA `cta_rank` of the cluster.
-__device__ __forceinline__ void mbar_remote_arrive(uint32_t bar, uint32_t cta_rank) {
-    asm volatile("{\n\t.reg .b32 ra;\n\tmapa.shared::cluster.u32 ra, %0, %1;\n\t"
-                 "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [ra];\n\t}"
-                 :: "r"(bar), "r"(cta_rank) : "memory");
-}
-
 // Teardown wait for asynchronous work this CTA has already issued (TMA copies landing in
 // its shared memory, tensor-core operations on its TMEM): unlike mbar_wait it does not
 // stop when another role gives up, since the CTA may release neither while that work is in
@@ -192,25 +152,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, int c
         " [%0], [%1, {%2, %3, %4}], [%5];"
         :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
-}
-
-// As tma_load_2d, for a CTA pair: the box lands in this CTA's shared memory and its bytes
-// complete on the mbarrier `bar_pair` of the even CTA of the pair (a shared::cluster
-// address, from mapa), which counts the copies of both CTAs.
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *map, int c0, int c1,
-                                                 uint32_t bar_pair) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];"
-        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_pair)
-        : "memory");
-}
-
-// The shared::cluster address of the object at `addr`'s offset in CTA `cta_rank`.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t cta_rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(cta_rank));
-    return r;
 }
 
 // As tma_load_2d, multicast: the box lands at the same shared-memory offset in every CTA

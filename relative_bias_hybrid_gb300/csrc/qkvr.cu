@@ -30,8 +30,8 @@
 // group stay in L2 while the tiles stream past them.
 //
 // One CTA per SM, 10 warps:
-//   warp 0      producer: TMA of the CTA's A and weight boxes into a 4-stage ring (32 KB a
-//               stage)
+//   warp 0      producer: TMA of the CTA's A and weight boxes into a 5-stage ring (32 KB a
+//               stage; 4 stages ran 12% slower, 3 stages 30%)
 //   warp 1      even CTA: MMA issuer (whole warp, one elected lane), M = 256, N = 256,
 //               K = 16 steps into one of two TMEM accumulators (2 x 256 columns), so the
 //               epilogue of one item overlaps the MMAs of the next (idle in the odd CTA)
@@ -41,7 +41,8 @@
 //               128-feature block is one q head, one k or v head, or 128 features of r.
 // Epilogue of a block: each thread moves its TMEM lane (one tile row) to bf16 in a shared
 // staging buffer (rows of 272 bytes: row-wise 16-byte and column-wise 2-byte accesses
-// are both free of bank conflicts) and releases the accumulator; a k/v block then runs the
+// are both free of bank conflicts; one buffer, which the two groups use in turn, so that
+// the ring can hold 5 stages) and releases the accumulator; a k/v block then runs the
 // conv down each channel in place (thread = channel, oldest row first, a 3-value window in
 // registers); finally each half-warp takes whole rows (16 lanes x 8 values): RMSNorm for q
 // and k, the cache write for k and v, plain stores for q and r.  Rows 0-2 of a sequence's
@@ -52,6 +53,7 @@
 #include "fp8.cuh"
 #include "internal.h"
 #include "tcgen05.cuh"
+#include "cta_pair.cuh"
 
 namespace inkattn {
 
@@ -63,7 +65,7 @@ constexpr int kTileTok = kRowsM - kHalo;          // new tokens per M tile
 static_assert(kTileTok == INKATTN_QKVR_TILE_TOKENS, "the tile size the header publishes");
 constexpr int kCols = 256;                        // MMA N: output features of an item
 constexpr int kKStep = 64;                        // K per ring stage (one 128-byte row)
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kABytes = kRowsM * 128;             // 16 KB
 constexpr int kBHalfBytes = 128 * 128;            // 16 KB, one CTA's half of the weight box
 constexpr int kStageBytes = kABytes + kBHalfBytes;
@@ -76,7 +78,7 @@ constexpr int kMaxSeqs = INKATTN_QKVR_MAX_SEQS;
 
 constexpr int kOffRing = 0;
 constexpr int kOffStaging = kOffRing + kStages * kStageBytes;
-constexpr int kOffTiles = kOffStaging + 2 * kStagingBytes;        // int tile prefix [B + 1]
+constexpr int kOffTiles = kOffStaging + kStagingBytes;            // int tile prefix [B + 1]
 constexpr int kOffBar = kOffTiles + ((kMaxSeqs + 1) * 4 + 7) / 8 * 8;
 enum Bar {
     B_FULL = 0,
@@ -97,15 +99,22 @@ struct QkvrArgs {
     uint64_t wait_ns;        // limit of every bounded wait
 };
 
-// bar.sync over the 128 threads of one epilogue group, reducing a predicate with AND
-__device__ __forceinline__ bool group_all(int id, bool v) {
+// Named barriers of the epilogue warps: 1 and 2 for one group of 128 threads each, 3 and 4
+// for both groups (256 threads).
+constexpr int kBarBoth = 3, kBarHandoff = 4;
+// bar.sync over n threads, reducing a predicate with AND
+__device__ __forceinline__ bool named_all(int id, int n, bool v) {
     int r;
-    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.and.pred q, %2, 128, p;\n\t"
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.and.pred q, %2, %3, p;\n\t"
                  "selp.s32 %0, 1, 0, q;\n\t}"
-                 : "=r"(r) : "r"((int)v), "r"(id) : "memory");
+                 : "=r"(r) : "r"((int)v), "r"(id), "r"(n) : "memory");
     return r != 0;
 }
-__device__ __forceinline__ void group_sync(int id) { asm volatile("bar.sync %0, 128;" :: "r"(id) : "memory"); }
+__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ void named_arrive(int id, int n) {
+    asm volatile("bar.arrive %0, %1;" :: "r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void group_sync(int id) { named_sync(id, 128); }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
 
@@ -326,7 +335,7 @@ k_qkvr(const QkvrArgs A, const __grid_constant__ CUtensorMap xmap, const __grid_
         const int quarter = warp & 3;                         // TMEM lanes this warp may access
         const int row = quarter * 32 + lane;                  // this thread's tile row
         const int gid = 1 + e;                                // named barrier of the group
-        unsigned char *stg = smem + kOffStaging + e * kStagingBytes;
+        unsigned char *stg = smem + kOffStaging;              // one buffer, the groups take turns
         const int hw = gt >> 4, l16 = gt & 15, c0 = l16 * 8;  // row phase: half-warp hw, 8 values
         const int Qw = p.Hq * kHeadDim, F_kv = Qw + 2 * C, Rw = p.Hq * p.d_r;
         float gq[8], gk[8];
@@ -360,12 +369,20 @@ k_qkvr(const QkvrArgs A, const __grid_constant__ CUtensorMap xmap, const __grid_
             const inkattn_bf16 *st_in = type == 1 ? p.conv_state_k_in : p.conv_state_v_in;
             inkattn_bf16 *st_out = type == 1 ? p.conv_state_k_out : p.conv_state_v_out;
 
-            // the accumulator is ready, and (the same barrier) the group is done with the
-            // staging rows of the previous item
+            // the accumulator is ready; both groups decide together whether to go on (a
+            // named barrier must never wait for a group that has left), and the same barrier
+            // finds the second group done with the staging rows of the previous item
             bool ok = mbar_wait_cluster(bar(B_ACC_FULL + buf), (uint32_t)((i >> 1) & 1), p.dev_status,
                                         abort_flag, A.wait_ns);
-            if (!group_all(gid, ok)) break;
+            if (!named_all(kBarBoth, 256, ok)) break;
             tc::fence_after();
+            if (e == 1) named_sync(kBarHandoff, 256);         // the first group is done with them
+            if (!live) {
+                __syncwarp();
+                if (lane == 0) mbar_remote_arrive(bar(B_ACC_EMPTY + buf), 0);
+                if (e == 0) named_arrive(kBarHandoff, 256);
+                continue;
+            }
 
             // ---- TMEM lane `row` -> bf16 staging row (or the carried state, rows 0-2 of a
             // sequence's first tile)
@@ -394,7 +411,6 @@ k_qkvr(const QkvrArgs A, const __grid_constant__ CUtensorMap xmap, const __grid_
             tc::fence_before();
             __syncwarp();
             if (lane == 0) mbar_remote_arrive(bar(B_ACC_EMPTY + buf), 0);   // the even CTA's MMA warp waits
-            if (!live) continue;                              // uniform over the group
             group_sync(gid);                                  // the staging rows are complete
 
             if (p.y_out != nullptr) {                         // the projections themselves
@@ -506,6 +522,7 @@ k_qkvr(const QkvrArgs A, const __grid_constant__ CUtensorMap xmap, const __grid_
                     if (l16 == 0) (type == 1 ? p.k_scale : p.v_scale)[drow] = row_scale;
                 }
             }
+            if (e == 0) named_arrive(kBarHandoff, 256);       // the staging rows go to the second group
         }
     }
 

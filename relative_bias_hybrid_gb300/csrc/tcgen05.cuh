@@ -192,61 +192,6 @@ __device__ __forceinline__ void mma_bf16_ts_k128_commit(uint32_t d, uint32_t a_t
     }
 }
 
-// ---------------------------------------------------------------- CTA pairs (cta_group::2)
-// A kernel uses either these forms or the cta_group::1 ones above, never both.  The pair is
-// the two CTAs of a cluster of two; the MMA is issued from the even one and reads its A rows
-// and B columns from the shared memory of both (the same offsets in each), writing the D
-// rows of each CTA to that CTA's TMEM.
-
-// TMEM allocation for the pair: one warp of each of the two CTAs executes it.
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
-                 :: "r"(dst_smem), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish_pair() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
-}
-
-// One K = 64 stage of a pair GEMM tile (M = 256 over the two CTAs): four K = 16 MMAs over
-// 128-byte-swizzled K-major A and B tiles (the k steps advance the start addresses by 32
-// bytes, 2 in descriptor units), then, when `rel` is nonzero, a commit of them to the
-// mbarrier at `rel_bar`'s offset in both CTAs, and, when `done` is nonzero, a second such
-// commit to `done_bar`.  acc0 = 0 makes the first MMA overwrite D.  Warp-collective like
-// mma_bf16_ss (one elected lane issues).
-__device__ __forceinline__ void mma_pair_bf16_ss_k64_commit(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
-                                                            uint32_t acc0, uint32_t rel_bar, uint32_t rel,
-                                                            uint32_t done_bar, uint32_t done) {
-    asm volatile("{\n\t.reg .pred e, p0, pt, pr, pd;\n\t.reg .b64 a1, b1;\n\t.reg .b16 m;\n\t"
-                 "mov.b16 m, 3;\n\t"
-                 "setp.ne.b32 p0, %4, 0;\n\tsetp.eq.u32 pt, 0, 0;\n\t"
-                 "setp.ne.b32 pr, %6, 0;\n\tsetp.ne.b32 pd, %8, 0;\n\t"
-                 "elect.sync _|e, 0xffffffff;\n\tand.pred pr, pr, e;\n\tand.pred pd, pd, e;\n\t"
-                 "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p0;\n\t"
-                 "add.s64 a1, %1, 2;\n\tadd.s64 b1, %2, 2;\n\t"
-                 "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a1, b1, %3, pt;\n\t"
-                 "add.s64 a1, %1, 4;\n\tadd.s64 b1, %2, 4;\n\t"
-                 "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a1, b1, %3, pt;\n\t"
-                 "add.s64 a1, %1, 6;\n\tadd.s64 b1, %2, 6;\n\t"
-                 "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a1, b1, %3, pt;\n\t"
-                 "@pr tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-                 " [%5], m;\n\t"
-                 "@pd tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-                 " [%7], m;\n\t}"
-                 :: "r"(d), "l"(a), "l"(b), "r"(id), "r"(acc0), "r"(rel_bar), "r"(rel), "r"(done_bar),
-                    "r"(done)
-                 : "memory");
-}
-// Arrives once on the local mbarrier when every pair MMA issued so far by the elected lane
-// has completed.  Warp-collective.
-__device__ __forceinline__ void commit_pair(uint32_t bar) {
-    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-                 "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
-                 :: "r"(bar) : "memory");
-}
-
 // ---------------------------------------------------------------- TMEM <-> registers
 // 32x32b shape: thread i of the warp reads/writes TMEM lane (quarter base + i), 32
 // consecutive 32-bit columns starting at the address's column.

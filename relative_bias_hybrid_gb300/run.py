@@ -5,9 +5,10 @@ per-pass device time of each call.  Meant as the target of a profiler command, e
         python -m relative_bias_hybrid_gb300.run swa --iters 3
 
 Every pass is the whole path (prologue, then prefill or decode + combine) on seeded
-synthetic inputs already resident on the device.  ``--seqs N`` keeps only the first N
-sequences of a batched workload (a smaller case of the same kernel, for captures that
-must hold less memory).
+synthetic inputs already resident on the device, optionally with the qkvr projections
+(their own inputs and outputs) before it and the attention-output conv after it.
+``--seqs N`` keeps only the first N sequences of a batched workload (a smaller case of the
+same kernel, for captures that must hold less memory).
 """
 from __future__ import annotations
 
@@ -17,7 +18,7 @@ import dataclasses
 import torch
 
 from . import inputs as gen
-from .step import AttentionStep, OutputConvStep
+from .step import AttentionStep, OutputConvStep, QkvrStep
 
 
 def main(argv=None):
@@ -30,6 +31,9 @@ def main(argv=None):
     ap.add_argument("--kv", choices=["bf16", "e4m3"], default="bf16", help="KV-cache element type")
     ap.add_argument("--output-conv", action="store_true",
                     help="also run the attention-output conv (hidden width Hq * 128) after each pass")
+    ap.add_argument("--qkvr", action="store_true",
+                    help="also run the qkvr projections with the prologue fused in (hidden width "
+                         "Hq * 128) before each pass")
     args = ap.parse_args(argv)
 
     w = gen.workload(args.workload)
@@ -41,11 +45,16 @@ def main(argv=None):
     step = AttentionStep(w, x, mode="decode" if args.workload == "decode" else "prefill",
                          num_splits=args.splits)
     oc = OutputConvStep(w, gen.make_output_conv_inputs(w, seed=args.seed, device=dev)) if args.output_conv else None
+    qk = (QkvrStep(w, gen.make_qkvr_inputs(w, w.Hq * w.head_dim, seed=args.seed, device=dev, kv_dtype=args.kv))
+          if args.qkvr else None)
     stream = torch.cuda.Stream(device=dev)
     print(w.describe(), f"num_splits={step.num_splits}" if step.mode == "decode" else "")
     with torch.cuda.stream(stream):
         for it in range(args.iters):
-            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            e[4].record(stream)
+            if qk is not None:
+                qk.run(stream)
             e[0].record(stream)
             step.run_prologue(stream)
             e[1].record(stream)
@@ -55,10 +64,12 @@ def main(argv=None):
                 oc.run(stream)
             e[3].record(stream)
             stream.synchronize()
-            print(f"pass {it}: prologue {e[0].elapsed_time(e[1]):.4f} ms, "
+            print(f"pass {it}: " + (f"qkvr {e[4].elapsed_time(e[0]):.4f} ms, " if qk is not None else "")
+                  + f"prologue {e[0].elapsed_time(e[1]):.4f} ms, "
                   f"attention {e[1].elapsed_time(e[2]):.4f} ms"
                   + (f", output conv {e[2].elapsed_time(e[3]):.4f} ms" if oc is not None else ""))
-    status = step.device_status() | (oc.device_status() if oc is not None else 0)
+    status = (step.device_status() | (oc.device_status() if oc is not None else 0)
+              | (qk.device_status() if qk is not None else 0))
     print(f"device status {status}")
     if status != 0:
         raise SystemExit(1)
