@@ -73,7 +73,7 @@ inkattn_status validate_prologue(const inkattn_prologue_params *p) {
         p->Hq % p->Hkv != 0 || p->num_blocks < 1 || p->num_state_slots < 1 || !(p->eps >= 0.f))
         return INKATTN_ERR_INVALID_ARG;
     if (p->N_tok > 0 && p->max_seqlen_q < 1) return INKATTN_ERR_INVALID_ARG;
-    if (p->B > 65535 || p->Hkv > 65535) return INKATTN_ERR_INVALID_ARG;
+    if (p->B > 65535 || p->Hq > 65535) return INKATTN_ERR_INVALID_ARG;   // (query rows of a tile: 32-bit offsets)
     if ((long long)p->num_blocks * 64 > INT_MAX) return INKATTN_ERR_INVALID_ARG;
     if (p->head_dim != kHeadDim || p->block_size != kBlock) return INKATTN_ERR_UNSUPPORTED;
     const void *ptrs16[] = {p->q, p->k, p->v, p->conv_state_k, p->conv_state_v, p->q_out,

@@ -80,6 +80,10 @@ k_prologue(const inkattn_prologue_params p, const int kv_tiles) {
     if (!role_kv) {
         // ======================= query rows: RMSNorm, kQInFlight rows per lane in flight
         const int q_rows = nt * g;
+        // the tile's query rows from one base: 32-bit offsets within the tile
+        const size_t q_base = (size_t)(start + t0) * p.Hq * kHeadDim;
+        const inkattn_bf16 *qb = p.q + q_base;
+        inkattn_bf16 *ob = p.q_out + q_base;
         const int g_shift = (g & (g - 1)) == 0 ? __ffs(g) - 1 : -1;
         auto div_g = [&](int row) { return g_shift >= 0 ? row >> g_shift : row / g; };
         float2 gq[4];
@@ -98,7 +102,7 @@ k_prologue(const inkattn_prologue_params p, const int kv_tiles) {
                 if (row < q_rows) {
                     const int tt = div_g(row), h = hk * g + (row - tt * g);
                     qraw[j] = __ldg(reinterpret_cast<const uint4 *>(
-                        p.q + ((size_t)(start + t0 + tt) * p.Hq + h) * kHeadDim + c0));
+                        qb + (uint32_t)((tt * p.Hq + h) * kHeadDim + c0)));
                 }
             }
 #pragma unroll
@@ -124,7 +128,7 @@ k_prologue(const inkattn_prologue_params p, const int kv_tiles) {
                     y[2 * e] = v.x;
                     y[2 * e + 1] = v.y;
                 }
-                *reinterpret_cast<uint4 *>(p.q_out + ((size_t)(start + t0 + tt) * p.Hq + h) * kHeadDim + c0) =
+                *reinterpret_cast<uint4 *>(ob + (uint32_t)((tt * p.Hq + h) * kHeadDim + c0)) =
                     pack8(y);
             }
         }
