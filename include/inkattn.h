@@ -36,8 +36,9 @@
  *   - Bounded device waits give up after 1 s.  For tests of that failure path only, two
  *     environment variables are read once per process: INKATTN_TEST_WAIT_LIMIT_US
  *     (100 .. 10000000: a shorter limit) and INKATTN_TEST_WITHHOLD_ARRIVAL=1 (the
- *     attention kernels' softmax withholds its first arrival before P V, so that the MMA
- *     warp's wait runs out).  Leave both unset in normal use.
+ *     attention kernels' softmax withholds its first arrival before P V, and the qkvr
+ *     kernel one release of an accumulator, so that the MMA warp's wait runs out).  Leave
+ *     both unset in normal use.
  */
 #ifndef INKATTN_H
 #define INKATTN_H

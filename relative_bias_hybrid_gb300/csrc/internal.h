@@ -19,8 +19,9 @@ constexpr int kBlock = 64;          // paged-cache block (tokens)
 // gives up after 1 s and nothing is withheld.  A test of the failure path sets the
 // environment variables INKATTN_TEST_WAIT_LIMIT_US (a shorter limit, 100 us .. 10 s) and
 // INKATTN_TEST_WITHHOLD_ARRIVAL=1 (the attention kernels' softmax withholds its first
-// arrival on the barrier the MMA warp waits on before P V, so that wait runs out and the
-// kernel winds down through its error path).
+// arrival on the barrier the MMA warp waits on before P V, and the qkvr kernel's odd CTAs
+// their first accumulator release, so that wait runs out and the kernel winds down through
+// its error path).
 struct KernelDebug {
     uint64_t wait_ns;
     int withhold;

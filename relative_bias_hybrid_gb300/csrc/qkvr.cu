@@ -97,6 +97,8 @@ struct QkvrArgs {
     inkattn_qkvr_params p;
     int n_cblocks;           // feature blocks: ceil(F / 256)
     uint64_t wait_ns;        // limit of every bounded wait
+    int withhold;            // failure-path test: one epilogue warp of each odd CTA withholds
+                             // its first accumulator release, so the MMA warp's wait runs out
 };
 
 // Named barriers of the epilogue warps: 1 and 2 for one group of 128 threads each, 3 and 4
@@ -377,9 +379,10 @@ k_qkvr(const QkvrArgs A, const __grid_constant__ CUtensorMap xmap, const __grid_
             if (!named_all(kBarBoth, 256, ok)) break;
             tc::fence_after();
             if (e == 1) named_sync(kBarHandoff, 256);         // the first group is done with them
+            const bool release = !(A.withhold && i == 0 && crank == 1 && warp == kWarpEpi);
             if (!live) {
                 __syncwarp();
-                if (lane == 0) mbar_remote_arrive(bar(B_ACC_EMPTY + buf), 0);
+                if (lane == 0 && release) mbar_remote_arrive(bar(B_ACC_EMPTY + buf), 0);
                 if (e == 0) named_arrive(kBarHandoff, 256);
                 continue;
             }
@@ -410,7 +413,7 @@ k_qkvr(const QkvrArgs A, const __grid_constant__ CUtensorMap xmap, const __grid_
             }
             tc::fence_before();
             __syncwarp();
-            if (lane == 0) mbar_remote_arrive(bar(B_ACC_EMPTY + buf), 0);   // the even CTA's MMA warp waits
+            if (lane == 0 && release) mbar_remote_arrive(bar(B_ACC_EMPTY + buf), 0);   // the even CTA's MMA warp waits
             group_sync(gid);                                  // the staging rows are complete
 
             if (p.y_out != nullptr) {                         // the projections themselves
@@ -542,6 +545,7 @@ cudaError_t launch_qkvr(const inkattn_qkvr_params &p, const CUtensorMap &xmap, c
     const long long F = (long long)(p.Hq + 2 * p.Hkv) * kHeadDim + (long long)p.Hq * p.d_r;
     a.n_cblocks = (int)((F + kCols - 1) / kCols);
     a.wait_ns = kernel_debug().wait_ns;
+    a.withhold = kernel_debug().withhold;
     cudaError_t err = cudaFuncSetAttribute(k_qkvr, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (err != cudaSuccess) return err;
     // a persistent grid: as many clusters as are resident at once (one CTA per SM), and no

@@ -6,7 +6,10 @@ INKATTN_ERR_DEVICE_TIMEOUT in dev_status, drain the copies and MMAs it issued, r
 and return, leaving the CUDA context usable.  Covered: the relative-bias prefill with CTA
 pairs (K/V multicast) and without, the prefill without bias, and the decode over a bf16
 and over an E4M3 cache (the latter with its converter warps between the copies and the
-MMAs)."""
+MMAs); and the qkvr projections (CTA pairs), where one epilogue warp of each odd CTA
+withholds its first accumulator release, so the even CTA's MMA warp gives up, and both
+CTAs of every pair wind down (the pair's copies and commits drained, TMEM released by
+both)."""
 import json
 import os
 import subprocess
@@ -43,6 +46,15 @@ for name, (w, mode) in cases.items():
     st.run_attention()
     torch.cuda.synchronize()
     res[name] = {"status": st.device_status(), "seconds": time.time() - t0}
+from relative_bias_hybrid_gb300.step import QkvrStep
+# enough items that every cluster of the persistent grid takes at least three
+wq = gen.custom("t6", Hq=16, Hkv=2, q_lens=[12000, 300], prefix_lens=[0, 5], rel_extent=16)
+xq = gen.make_qkvr_inputs(wq, 128, seed=3, device="cuda", grid=True)
+sq = QkvrStep(wq, xq)
+t0 = time.time()
+sq.run()
+torch.cuda.synchronize()
+res["qkvr"] = {"status": sq.device_status(), "seconds": time.time() - t0}
 res["context_usable"] = torch.arange(1000, device="cuda", dtype=torch.float32).sum().item() == 499500.0
 print("RESULT " + json.dumps(res))
 """
