@@ -1,6 +1,7 @@
 """The C-ABI calls issue only stream-ordered work, so a whole step (prologue, then prefill,
-or decode and combine) can be captured into a CUDA graph and replayed: the replay must
-write exactly what the same calls wrote when issued directly (same inputs, same state)."""
+or decode and combine), and the qkvr projections with the prologue fused in, can be captured
+into a CUDA graph and replayed: the replay must write exactly what the same calls wrote
+when issued directly (same inputs, same state)."""
 import pytest
 import torch
 
@@ -59,4 +60,34 @@ def test_step_replays_from_a_cuda_graph(env, mode, splits):
     assert torch.equal(step.out, direct["out"])
     assert torch.equal(step.lse, direct["lse"])
     for k in state:
+        assert torch.equal(x[k], direct[k]), k
+
+
+def test_qkvr_replays_from_a_cuda_graph(env):
+    """The qkvr projections with the prologue fused in (persistent CTA-pair kernel),
+    captured and replayed: q, r, the cache rows and the new conv state as issued directly."""
+    gen, _ = env
+    from relative_bias_hybrid_gb300.step import QkvrStep
+    w = gen.custom("graph-qkvr", Hq=16, Hkv=2, q_lens=[300, 9, 140], prefix_lens=[0, 40, 2], rel_extent=16)
+    x = gen.make_qkvr_inputs(w, 256, seed=22, device="cuda")
+    saved = {k: x[k].clone() for k in ("k_cache", "v_cache")}
+    step = QkvrStep(w, x)
+    step.run()
+    torch.cuda.synchronize()
+    assert step.device_status() == 0
+    direct = {"q": step.q_out.clone(), "r": step.r_out.clone(), "sk": step.state_k.clone(),
+              "sv": step.state_v.clone(), **{k: x[k].clone() for k in saved}}
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step.run()
+    for k in saved:
+        x[k].copy_(saved[k])
+    for t in (step.q_out, step.r_out, step.state_k, step.state_v):
+        t.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert step.device_status() == 0
+    assert torch.equal(step.q_out, direct["q"]) and torch.equal(step.r_out, direct["r"])
+    assert torch.equal(step.state_k, direct["sk"]) and torch.equal(step.state_v, direct["sv"])
+    for k in saved:
         assert torch.equal(x[k], direct[k]), k

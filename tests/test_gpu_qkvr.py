@@ -186,35 +186,49 @@ def test_bad_slot_is_flagged_and_the_rest_written(env):
     assert np.array_equal(gen.bits(step.state_k), ref["conv_state_k"])
 
 
-def _window_reference(oracle, gen, w, x_cpu, xb, wb, t_lo, t_hi):
-    """Oracle outputs for tokens [t_lo, t_hi) of the single sequence of a full-size
-    workload: the projections of x rows [t_lo - 3, t_hi), the first three standing in for
-    the conv state when t_lo >= 3 (else the carried state), then the prologue."""
-    Qw, C, d = w.Hq * w.head_dim, w.Hkv * w.head_dim, w.head_dim
+def _window_reference(oracle, gen, w, x_cpu, xb, wb, b, t_lo, t_hi):
+    """Oracle outputs for tokens [t_lo, t_hi) of sequence b of a full-size workload: the
+    projections of its x rows [t_lo - 3, t_hi), the first three standing in for the conv
+    state when t_lo >= 3 (else the sequence's carried state), then the prologue."""
+    d = w.head_dim
+    s0 = int(x_cpu["cu_seqlens_q"][b])
     a = max(0, t_lo - 3)
-    q, k, v, r = oracle.qkvr_projection(xb[a:t_hi], wb, Hq=w.Hq, Hkv=w.Hkv, d=d, d_r=w.d_r)
+    q, k, v, r = oracle.qkvr_projection(xb[s0 + a:s0 + t_hi], wb, Hq=w.Hq, Hkv=w.Hkv, d=d, d_r=w.d_r)
     h = t_lo - a
-    st_k, st_v = gen.bits(x_cpu["conv_state_k"]).copy(), gen.bits(x_cpu["conv_state_v"]).copy()
+    slot = int(x_cpu["state_slot"][b])
+    st_k = gen.bits(x_cpu["conv_state_k"])[slot:slot + 1].copy()
+    st_v = gen.bits(x_cpu["conv_state_v"])[slot:slot + 1].copy()
     if t_lo >= 3:
         st_k[0], st_v[0] = k[:3], v[:3]
     n = t_hi - t_lo
-    sm = x_cpu["slot_mapping"].numpy()[t_lo:t_hi]
+    sm = x_cpu["slot_mapping"].numpy()[s0 + t_lo:s0 + t_hi]
     ref = oracle.prologue(cu_seqlens_q=np.array([0, n], np.int32), Hq=w.Hq, Hkv=w.Hkv, d=d, q=q[h:], k=k[h:],
                           v=v[h:], conv_w_k=x_cpu["conv_w_k"].numpy(), conv_w_v=x_cpu["conv_w_v"].numpy(),
                           q_norm_w=x_cpu["q_norm_w"].numpy(), k_norm_w=x_cpu["k_norm_w"].numpy(), eps=w.eps,
-                          state_slot=np.array([0], np.int32), conv_state_k=st_k[:1], conv_state_v=st_v[:1],
+                          state_slot=np.array([0], np.int32), conv_state_k=st_k, conv_state_v=st_v,
                           slot_mapping=sm, block_size=w.block_size,
                           k_cache=np.zeros((w.num_blocks, w.Hkv, w.block_size, d), np.uint16),
                           v_cache=np.zeros((w.num_blocks, w.Hkv, w.block_size, d), np.uint16))
-    return ref, r[h:], sm
+    return ref, r[h:], sm, slot
 
 
-@pytest.mark.parametrize("name", ["swa"])
+def _windows(w):
+    """(sequence, first token, end) windows: a sequence's start (the carried state), the
+    edges of its 125-token tiles, its middle and its end (the new state)."""
+    out = []
+    for b in ([0] if w.B == 1 else [0, w.B // 2, w.B - 1]):
+        n = w.q_lens[b]
+        out += [(b, lo, hi) for lo, hi in ((0, 6), (122, 130), (247, 253), (n // 2, n // 2 + 3), (n - 5, n))
+                if 0 <= lo < hi <= n]
+    return out
+
+
+@pytest.mark.parametrize("name", ["swa", "full", "ragged"])
 def test_full_size_layer_grid_sampled(env, name):
-    """One SWA prefill layer at full size (8192 tokens, d_model 8192, F 12288) in the
-    launch configuration the bench times; token windows at the start, across tile
-    boundaries, in the middle and at the end are checked against the oracle, and the new
-    state against the projections of the last three tokens."""
+    """The prefill workloads at full size (d_model 8192, F 12288) in the launch configuration
+    the bench times: token windows at a sequence's start, across tile edges, in the middle
+    and at the end are checked against the oracle, and the new state against the
+    projections of the last three tokens."""
     gen, _, oracle, _ = env
     w = gen.workload(name)
     x_cpu, x, step = _run(env, w, 8192, seed=7, want_y=False)
@@ -222,17 +236,19 @@ def test_full_size_layer_grid_sampled(env, name):
     xb, wb = gen.bits(x_cpu["x"]), gen.bits(x_cpu["w_qkvr"])
     kg, vg = gen.bits(x["k_cache"]), gen.bits(x["v_cache"])
     q_out, r_out = gen.bits(step.q_out), gen.bits(step.r_out)
-    N = w.N_tok
-    for t_lo, t_hi in ((0, 6), (122, 130), (247, 253), (4001, 4004), (N - 5, N)):
-        ref, r_ref, sm = _window_reference(oracle, gen, w, x_cpu, xb, wb, t_lo, t_hi)
-        assert bf16_ulp_diff(q_out[t_lo:t_hi], ref["q_out"]).max() <= 1.0, (t_lo, t_hi)
-        assert np.array_equal(r_out[t_lo:t_hi], r_ref), (t_lo, t_hi)
+    state_k, state_v = gen.bits(step.state_k), gen.bits(step.state_v)
+    for b, t_lo, t_hi in _windows(w):
+        s0 = int(x_cpu["cu_seqlens_q"][b])
+        ref, r_ref, sm, slot = _window_reference(oracle, gen, w, x_cpu, xb, wb, b, t_lo, t_hi)
+        where = (name, b, t_lo, t_hi)
+        assert bf16_ulp_diff(q_out[s0 + t_lo:s0 + t_hi], ref["q_out"]).max() <= 1.0, where
+        assert np.array_equal(r_out[s0 + t_lo:s0 + t_hi], r_ref), where
         blk, off = sm // 64, sm % 64
-        assert bf16_ulp_diff(kg[blk, :, off, :], ref["k_cache"][blk, :, off, :]).max() <= 1.0, (t_lo, t_hi)
-        assert np.array_equal(vg[blk, :, off, :], ref["v_cache"][blk, :, off, :]), (t_lo, t_hi)
-        if t_hi == N:
-            assert np.array_equal(gen.bits(step.state_k)[0], ref["conv_state_k"][0])
-            assert np.array_equal(gen.bits(step.state_v)[0], ref["conv_state_v"][0])
+        assert bf16_ulp_diff(kg[blk, :, off, :], ref["k_cache"][blk, :, off, :]).max() <= 1.0, where
+        assert np.array_equal(vg[blk, :, off, :], ref["v_cache"][blk, :, off, :]), where
+        if t_hi == w.q_lens[b]:
+            assert np.array_equal(state_k[slot], ref["conv_state_k"][0]), where
+            assert np.array_equal(state_v[slot], ref["conv_state_v"][0]), where
 
 
 def test_full_size_gaussian_projections_sampled(env):
