@@ -35,10 +35,11 @@
 //   warp 1      even CTA: MMA issuer (whole warp, one elected lane), M = 256, N = 256,
 //               K = 16 steps into one of two TMEM accumulators (2 x 256 columns), so the
 //               epilogue of one item overlaps the MMAs of the next (idle in the odd CTA)
-// Both CTAs' copies of a stage complete on the even CTA's barrier for it, which the MMA
-// warp waits on; the pair MMAs' commits release the stage in both CTAs.
 //   warps 2-5   epilogue of the item's first 128 features, warps 6-9 of the second: each
 //               128-feature block is one q head, one k or v head, or 128 features of r.
+// Both CTAs' copies of a stage complete on the even CTA's barrier for it, which the MMA
+// warp waits on; the pair MMAs' commits release the stage in both CTAs.  Waits for phases
+// completed from the other CTA poll (a suspended waiter is not woken promptly by them).
 // Epilogue of a block: each thread moves its TMEM lane (one tile row) to bf16 in a shared
 // staging buffer (rows of 272 bytes: row-wise 16-byte and column-wise 2-byte accesses
 // are both free of bank conflicts; one buffer, which the two groups use in turn, so that
