@@ -86,8 +86,7 @@ struct Dec {
     static constexpr int B_TAB_FULL = B_PV_DONE + 2;
     static constexpr int B_TAB_FREE = B_TAB_FULL + 1;
     static constexpr int B_DRAIN = B_TAB_FREE + 1;
-    static constexpr int B_PAIR = B_DRAIN + 1;
-    static constexpr int B_QF = B_PAIR + 4;                  // E4M3: Q converted to f16
+    static constexpr int B_QF = B_DRAIN + 1;                 // E4M3: Q converted to f16
     static constexpr int B_F8_FULL = B_QF + 1;
     static constexpr int B_F8_EMPTY = B_F8_FULL + kF8Slots;
     static constexpr int B_COUNT = B_F8_EMPTY + kF8Slots;
@@ -98,6 +97,7 @@ struct Dec {
 };
 
 constexpr uint32_t kTmemO = 0, kTmemS0 = 128;
+constexpr int kBarPair = 8;                // named barriers 8-11: the softmax row pairs, per lane quarter
 
 struct DecTcArgs {
     inkattn_attn_params p;
@@ -196,7 +196,6 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
         mbar_init(bar(C::B_TAB_FULL), 256);
         mbar_init(bar(C::B_TAB_FREE), 256);
         mbar_init(bar(C::B_DRAIN), 1);
-        for (int q = 0; q < 4; ++q) mbar_init(bar(C::B_PAIR + q), 64);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -442,11 +441,12 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
         unsigned short *tab = reinterpret_cast<unsigned short *>(smem + C::kOffTab);
         float *tsig = reinterpret_cast<float *>(smem + C::kOffTsig);
         float *xchg = reinterpret_cast<float *>(smem + C::kOffXchg);
-        int pair_phase = 0;
-        auto pair_sync = [&]() -> bool {
-            mbar_arrive(bar(C::B_PAIR + quad));
-            return wwait(bar(C::B_PAIR + quad), (pair_phase++) & 1);
-        };
+        // The two threads of a row meet on a named barrier of the row's lane quarter (64
+        // threads, one warp of each column half), as in the prefill kernel: every thread
+        // makes exactly N + 1 meetings (warps whose rows are all padding skip their tiles'
+        // meetings and make them up at the end, as a thread that left the loop early does).
+        auto pair_meet = [&]() { asm volatile("bar.sync %0, 64;" :: "r"(kBarPair + quad) : "memory"); };
+        int met = 0;
         const bool has_bias = p.rel_extent > 0;
         const int gq = lane >> 2, tq = lane & 3;              // mma.sync fragment coordinates
         int band_round = 0;
@@ -639,7 +639,8 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
             float mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
             float *xc = xchg + (n & 1) * 256;
             xc[hw * 128 + a] = mx;
-            if (!(ok = pair_sync())) break;
+            pair_meet();
+            ++met;
             mx = fmaxf(mx, xc[(1 - hw) * 128 + a]);
             const float mx_raw = mx;                             // the row's largest logit of the tile (S units)
             mx = mx == -INFINITY ? -INFINITY : mx * c_qk;        // log2 units
@@ -693,9 +694,10 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
         // epilogue: the row sum of both halves, then O / l for this thread's 64 columns
         // the column-half 0 thread of a row alone holds the correction (lc_run is 0 in the other)
         // and alone writes the LSE: it publishes l + lc, the other thread l
+        for (; met < N; ++met) pair_meet();
         float *xl = xchg + 512;
         xl[hw * 128 + a] = l_run + lc_run;
-        if (ok) ok = pair_sync();
+        pair_meet();
         const float l_other = xl[(1 - hw) * 128 + a];
         const float l_tot = l_run + l_other;                  // the fp32 sum (read by half 0 only)
         const float l_norm = l_run + lc_run + l_other;        // normaliser of P V's bf16 P

@@ -111,8 +111,7 @@ enum Bar {
     B_R_EMPTY = B_R_FULL + 1,
     B_PW_READY = B_R_EMPTY + 1,
     B_DRAIN = B_PW_READY + 1,
-    B_PAIR = B_DRAIN + 1,
-    B_STAGE_FULL = B_PAIR + 4,
+    B_STAGE_FULL = B_DRAIN + 1,
     B_STAGE_EMPTY = B_STAGE_FULL + 2,
     B_BDRAIN = B_STAGE_EMPTY + 2,
     B_NORM = B_BDRAIN + 1,
@@ -123,6 +122,7 @@ static_assert(kSmem <= 232448, "dynamic shared memory above the 227 KB a CTA may
 static_assert(kOffBar % 8 == 0 && kOffKV % 1024 == 0 && kOffStage % 16 == 0, "alignment of the regions");
 
 constexpr uint32_t kTmemO = 0, kTmemS0 = 128, kTmemR = 384;
+constexpr int kBarPair = 8;                // named barriers 8-11: the softmax row pairs, per lane quarter
 
 struct TcArgs {
     inkattn_attn_params p;
@@ -218,7 +218,6 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         mbar_init(bar(B_DRAIN), 1);
         mbar_init(bar(B_BDRAIN), 1);
         mbar_init(bar(B_NORM), 128);
-        for (int q = 0; q < 4; ++q) mbar_init(bar(B_PAIR + q), 64);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -630,12 +629,14 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         const unsigned short *stage = reinterpret_cast<const unsigned short *>(smem + kOffStage) + a * kStageStride;
         const float *sigma_s = reinterpret_cast<const float *>(smem + kOffNorm) + 12;
         float *xchg = reinterpret_cast<float *>(smem + kOffXchg);   // [2 tiles][2 halves][128 rows]
-        // the two threads of each row meet on an mbarrier (a bounded wait, unlike bar.sync)
-        int pair_phase = 0;
-        auto pair_sync = [&]() -> bool {
-            mbar_arrive(bar(B_PAIR + quad));
-            return wwait(bar(B_PAIR + quad), (pair_phase++) & 1);
-        };
+        // The two threads of each row meet on a named barrier of the row's lane quarter (one
+        // warp of each column half, 64 threads): a hardware barrier, quicker than an mbarrier
+        // round trip on this path, but with no time limit.  So every thread meets its partner
+        // exactly N + 1 times, once per key tile and once at the end: a thread that leaves
+        // the tile loop early (a wait that ran out) still makes the meetings it skipped, and
+        // its partner, whose next wait then gives up too (the abort flag), does the same.
+        auto pair_meet = [&]() { asm volatile("bar.sync %0, 64;" :: "r"(kBarPair + quad) : "memory"); };
+        int met = 0;                             // meetings made in the tile loop
         bool ok = true;
 
         float m_run = -INFINITY, l_run = 0.f;   // l_run: sum of the fp32 P (for the LSE)
@@ -706,7 +707,8 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
             float mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
             float *xc = xchg + (n & 1) * 256;
             xc[hw * 128 + a] = mx;
-            if (!(ok = pair_sync())) break;                       // also: both halves hold S
+            pair_meet();                                          // also: both halves hold S
+            ++met;
             mx = fmaxf(mx, xc[(1 - hw) * 128 + a]);
             const float mx_raw = mx;                             // the row's largest logit of the tile (S units)
             mx = mx == -INFINITY ? -INFINITY : mx * c_qk;        // log2 units
@@ -764,8 +766,9 @@ k_prefill_tc(const TcArgs A, const __grid_constant__ CUtensorMap qmap,
         // the column-half 0 thread of a row alone holds the correction (lc_run is 0 in the other)
         // and alone writes the LSE: it publishes l + lc, the other thread l
         float *xl = xchg + 512;
+        for (; met < N; ++met) pair_meet();
         xl[hw * 128 + a] = l_run + lc_run;
-        if (ok) ok = pair_sync();
+        pair_meet();
         const float l_other = xl[(1 - hw) * 128 + a];
         const float l_tot = l_run + l_other;                  // the fp32 sum (read by half 0 only)
         const float l_norm = l_run + lc_run + l_other;        // normaliser of P V's bf16 P
