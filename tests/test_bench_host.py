@@ -47,3 +47,34 @@ def test_more_than_one_gpu_is_refused_before_any_gpu_work(monkeypatch, argv, env
 
     monkeypatch.setattr(bench, "run_gpu", no_gpu)
     assert bench.main(argv) == 2
+
+
+def test_qkvr_flop_count_and_grid_inputs_are_exact_in_fp32():
+    """The bench's qkvr FLOP count, and the claim the GPU parity tests rest on: with the
+    integer-grid inputs every projection sum is exact in fp32 whatever the order of the
+    additions (checked on sampled rows of the full-width weight against float64, summing in
+    the natural order, in reverse and pairwise)."""
+    import numpy as np
+    import torch
+    import bench
+    from relative_bias_hybrid_gb300 import inputs as gen
+    w = gen.workload("swa")
+    assert bench.qkvr_flops(w, 8192) == 2.0 * 8192 * 12288 * 8192
+    small = gen.custom("g", Hq=16, Hkv=2, q_lens=[5], prefix_lens=[0], rel_extent=16)
+    x = gen.make_qkvr_inputs(small, 8192, seed=3, grid=True)
+    xf = x["x"].to(torch.float64).numpy()
+    wf = x["w_qkvr"].to(torch.float64).numpy()[::97]
+    exact = xf @ wf.T
+    prod = (xf[:, None, :] * wf[None, :, :]).astype(np.float32)       # exact in fp32 (multiples of 2^-9)
+    assert np.array_equal(prod.astype(np.float64), xf[:, None, :] * wf[None, :, :])
+    fwd = np.zeros(exact.shape, np.float32)
+    for k in range(prod.shape[2]):
+        fwd += prod[:, :, k]
+    rev = np.zeros(exact.shape, np.float32)
+    for k in reversed(range(prod.shape[2])):
+        rev += prod[:, :, k]
+    pair = prod
+    while pair.shape[2] > 1:
+        pair = pair[:, :, 0::2] + pair[:, :, 1::2]
+    for got in (fwd, rev, pair[:, :, 0]):
+        assert np.array_equal(got.astype(np.float64), exact)
