@@ -6,8 +6,8 @@ inkattn_prologue then inkattn_prefill (prefill layers), or inkattn_prologue then
 inkattn_decode + inkattn_combine (decode).  The headline is the full-attention prefill
 layer (B=1, T=32768, Hq=64, Hkv=8, rel_extent=1024, logits scaled by ln T / ln 8192):
 value = its algorithmic attention TFLOP/s per step.  The same JSON line carries the
-sliding-window layer, the ragged mixed-prefill batch and the MTP-verify decode under
-"workloads", each with its kernel rooflines, the end-to-end number through the C ABI
+sliding-window layer, the ragged mixed-prefill batch, the full layer over an E4M3 cache
+and the MTP-verify decode (bf16 and E4M3 caches) under "workloads", each with its kernel rooflines, the end-to-end number through the C ABI
 with host buffers, and the fp64 oracle timed on a bounded sample on the host cores;
 plus the SM clocks sampled during the timed regions.  Beside the step, each prefill
 workload also times two kernels alone: the attention-output ShortConv (k_output_conv) and
@@ -261,11 +261,16 @@ class HostCopy:
         from relative_bias_hybrid_gb300 import inputs as gen
         self.w = w
         self.B_full = w.B
-        self.e4m3 = False
+        self.e4m3 = x["k_cache"].dtype == torch.uint8
         if seqs is None:
             self.x = {k: x[k].cpu() for k in ("cu_seqlens_q", "seqlen_k", "r", "P", "block_table")}
             self.q = gen.bits(q_out)
-            self.kc, self.vc = gen.bits(x["k_cache"]), gen.bits(x["v_cache"])
+            if self.e4m3:
+                # codes and row scales; the oracle leg dequantises them
+                self.kc = (x["k_cache"].cpu().numpy(), x["k_scale"].cpu().numpy())
+                self.vc = (x["v_cache"].cpu().numpy(), x["v_scale"].cpu().numpy())
+            else:
+                self.kc, self.vc = gen.bits(x["k_cache"]), gen.bits(x["v_cache"])
             return
         # decode: a few whole sequences, their cache blocks gathered and renumbered
         import dataclasses
@@ -278,7 +283,6 @@ class HostCopy:
             table[i, :n] = np.arange(len(blocks), len(blocks) + n)
             blocks.extend(bt[b, :n].tolist())
         idx = torch.as_tensor(np.asarray(blocks, np.int64), device=x["k_cache"].device)
-        self.e4m3 = x["k_cache"].dtype == torch.uint8
         if self.e4m3:
             # codes and row scales; the oracle leg dequantises them
             self.kc = (x["k_cache"].index_select(0, idx).cpu().numpy(), x["k_scale"].index_select(0, idx).cpu().numpy())
@@ -299,6 +303,16 @@ class HostCopy:
                   "block_table": torch.from_numpy(table)}
 
 
+def _dequantise_host_cache(h):
+    """An E4M3 host copy's cache as the kernels read it: code * scale, exact in bf16."""
+    if h.e4m3:
+        import oracle
+        from relative_bias_hybrid_gb300 import inputs as gen
+        h.kc, h.vc = (gen.bits(torch.from_numpy(oracle.dequantize_e4m3(c, sc)).to(torch.bfloat16))
+                      for c, sc in (h.kc, h.vc))
+        h.e4m3 = False
+
+
 def _oracle_time(h, rows, n_threads):
     import oracle
     t0 = time.perf_counter()
@@ -311,6 +325,7 @@ def cpu_baseline_prefill(h, target_s, seed=0):
     all host cores; scaled to TFLOP/s by the sample's algorithmic FLOP."""
     import oracle
     oracle.build()
+    _dequantise_host_cache(h)
     w = h.w
     cu = h.x["cu_seqlens_q"].numpy()
     rng = np.random.default_rng(seed)
@@ -333,15 +348,8 @@ def cpu_baseline_decode(h, target_s):
     import dataclasses
     import oracle
     oracle.build()
-    if h.e4m3:
-        # the cache the decode reads: code * scale, exact in bf16
-        from relative_bias_hybrid_gb300 import inputs as gen
-        h.kc, h.vc = (gen.bits(torch.from_numpy(oracle.dequantize_e4m3(c, sc)).to(torch.bfloat16))
-                      for c, sc in (h.kc, h.vc))
-        h.e4m3 = False
-        kv = "e4m3"
-    else:
-        kv = "bf16"
+    kv = "e4m3" if h.e4m3 else "bf16"
+    _dequantise_host_cache(h)
     cores = host_cores()
     cu = h.x["cu_seqlens_q"].numpy()
     n_seq = 1
@@ -590,7 +598,7 @@ def measure(name, args, peaks, dev, stream, flush):
     if kv == "bf16":            # (the output conv does not depend on the cache type)
         oc_roof, oc_launches = time_output_conv(w, args, dev, stream, flush, peaks, name)
         launches += oc_launches
-    if mode == "prefill":       # (the qkvr kernel's 125-token tiles are made for prefill)
+    if mode == "prefill" and kv == "bf16":   # (the qkvr kernel's tiles are made for prefill)
         qk_roof, qk_launches = time_qkvr(w, args, dev, stream, flush, peaks, name)
         launches += qk_launches
     extra = {**({"k_output_conv": oc_roof} if oc_roof else {}), **({"k_qkvr": qk_roof} if qk_roof else {})}
@@ -603,11 +611,15 @@ def measure(name, args, peaks, dev, stream, flush):
     if mode == "prefill":
         fl = attention_flops(w)
         tf = fl / (att_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "kernel": "k_prefill_tc", "achieved": tf, "peak": peaks["bf16"],
+        roof = {"bound": "tensor", "kernel": "k_prefill_tc" if kv == "bf16" else "k_dequant_e4m3+k_prefill_tc",
+                "achieved": tf, "peak": peaks["bf16"],
                 "unit": "TFLOP/s", "frac": tf / peaks["bf16"], "peak_src": peaks["src"] + " (burst bf16)",
                 "frac_of_sustained": tf / peaks["bf16_sustained"], "traffic": ncu_traffic("k_prefill_tc", name),
                 "algorithmic_flop_per_launch": fl, "ms": att_ms}
-        rep = {"workload": w.describe() + "; step = inkattn_prologue + inkattn_prefill",
+        rep = {"workload": w.describe() + ("; step = inkattn_prologue + inkattn_prefill" if kv == "bf16" else
+                                           ", E4M3 KV cache with a power-of-two scale per row; step = "
+                                           "inkattn_prologue + inkattn_prefill_e4m3 (the blocks read expanded "
+                                           "to bf16, then the bf16 prefill)"),
                "value": fl / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
                "roofline": roof, "rooflines": {"k_prologue": prologue, **extra},
                "e2e": {"value": fl / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
@@ -630,7 +642,7 @@ def measure(name, args, peaks, dev, stream, flush):
     return rep, launches, host
 
 
-WORKLOADS = ("full", "swa", "ragged", "decode", "decode_e4m3")
+WORKLOADS = ("full", "swa", "ragged", "full_e4m3", "decode", "decode_e4m3")
 
 
 def run_gpu(args):

@@ -75,7 +75,8 @@ typedef uint16_t inkattn_bf16;
  *   x / 2^k (ties to even), where x is the bf16 value the bf16 cache would hold; the
  *   dequantised value is exact.  [SG §Relative Attention と FA4 経路: MXFP8 on the FA4
  *   path; VJ §フューチャーロードマップ and VV: FP8 for the global-attention layers.]
- *   The decode reads such a cache; prefill over it returns INKATTN_ERR_UNSUPPORTED.
+ *   The decode reads such a cache, and inkattn_prefill_e4m3 (inkattn_prefill returns
+ *   INKATTN_ERR_UNSUPPORTED for it).
  *   The decode expands each row to f16 (code * scale, exact for the prologue's scales
  *   down to 2^-15; below, values under 2^-24 flush) and requires every scale to lie in
  *   [2^-24, 2^7], which the prologue's scales do for rows whose magnitudes stay below
@@ -220,8 +221,24 @@ typedef struct inkattn_attn_params {
     int32_t *dev_status;           /* nullable                                           */
 } inkattn_attn_params;
 
-/* Prefill (any q_len): writes out (and lse). */
+/* Prefill (any q_len) over a bf16 cache: writes out (and lse).  An E4M3 cache returns
+ * INKATTN_ERR_UNSUPPORTED here; it takes inkattn_prefill_e4m3. */
 INKATTN_API inkattn_status inkattn_prefill(const inkattn_attn_params *p, void *stream);
+
+/* Prefill over an E4M3 cache (kv_dtype = INKATTN_KV_E4M3) [SG §Relative Attention と FA4
+ * 経路; VJ §フューチャーロードマップ: FP8 for the global-attention layers].  The blocks the
+ * batch reads, block_table[b][0 .. ceil(seqlen_k[b]/64)), are first expanded, code * scale
+ * (exact in bf16), into a bf16 copy in the workspace with a block table of its own; then the
+ * bf16 prefill runs on the copy, so the result is the bf16 prefill's over the dequantised
+ * cache.  A row inside a sequence whose scale lies outside [2^-24, 2^7] (or a block id out
+ * of range) is flagged INKATTN_ERR_DEVICE_BOUNDS and read as zeros, as in the decode.
+ * workspace: device memory of the current device, 256-byte aligned, at least
+ * inkattn_prefill_workspace_bytes(p) bytes (B * max_blocks_per_seq blocks of bf16 K and V
+ * plus their table), else INKATTN_ERR_INVALID_ARG; a bf16 cache is INKATTN_ERR_INVALID_ARG
+ * (it takes inkattn_prefill).  Two launches, chained like the others. */
+INKATTN_API size_t inkattn_prefill_workspace_bytes(const inkattn_attn_params *p);   /* 0 if invalid or bf16 */
+INKATTN_API inkattn_status inkattn_prefill_e4m3(const inkattn_attn_params *p, void *workspace,
+                                                size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------------
  * Split-KV decode [VJ §低レイテンシコレクティブとカーネル "FA4 Kernel"; VV §FA4 với

@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libinkattn.so")
 SOURCES = ["api.cu", "prologue.cu", "decode.cu", "decode_tc.cu", "prefill_tc.cu", "prefill_2q.cu", "decode_noalloc.cu",
-           "output_conv.cu", "qkvr.cu"]
+           "output_conv.cu", "qkvr.cu", "dequant.cu"]
 HEADERS = ["common.cuh", "internal.h", "tcgen05.cuh", "context_cache.h", "conv4.cuh", "fp8.cuh", "cta_pair.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

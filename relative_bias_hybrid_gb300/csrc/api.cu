@@ -480,21 +480,84 @@ inkattn_status inkattn_qkvr_prologue(const inkattn_qkvr_params *p, void *stream)
     return launch_status(launch_qkvr(*p, xmap, wmap, sms, static_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+
+// The prefill over a bf16 cache, once the call is validated.
+inkattn_status run_prefill_bf16(const inkattn_attn_params &p, cudaStream_t stream) {
+    CUtensorMap qmap, kmap, vmap;
+    const long long rows = (long long)p.num_blocks * p.Hkv * kBlock;
+    if (!make_q_map(&qmap, p.q, p.N_tok, p.Hq, kPrefillTcRows) ||
+        !make_cache_map(&kmap, p.k_cache, rows) || !make_cache_map(&vmap, p.v_cache, rows))
+        return INKATTN_ERR_CUDA;
+    if (p.rel_extent == 0)   // no bias band: two query tiles per CTA
+        return launch_status(launch_prefill_2q(p, scalars(p), qmap, kmap, vmap, stream));
+    return launch_status(launch_prefill_tc(p, scalars(p), qmap, kmap, vmap, stream));
+}
+
+// Workspace of the prefill over an E4M3 cache: bf16 K and V copies of B * max_blocks_per_seq
+// blocks, then their block table, each piece 256-byte aligned.
+size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
+size_t prefill_copy_bytes(const inkattn_attn_params &p) {
+    return (size_t)p.B * p.max_blocks_per_seq * p.Hkv * kBlock * kHeadDim * 2;
+}
+size_t prefill_ws_bytes(const inkattn_attn_params &p) {
+    return 2 * round256(prefill_copy_bytes(p)) + round256((size_t)p.B * p.max_blocks_per_seq * 4);
+}
+
+}  // namespace
+
 inkattn_status inkattn_prefill(const inkattn_attn_params *p, void *stream) {
     inkattn_status st = validate_attn(p);
     if (st != INKATTN_OK) return st;
-    if (p->kv_dtype != INKATTN_KV_BF16) return INKATTN_ERR_UNSUPPORTED;
+    if (p->kv_dtype != INKATTN_KV_BF16) return INKATTN_ERR_UNSUPPORTED;   // (inkattn_prefill_e4m3)
     if ((st = validate_locations(p)) != INKATTN_OK) return st;
     if ((st = check_device(nullptr)) != INKATTN_OK) return st;
     if (p->N_tok == 0) return INKATTN_OK;
-    CUtensorMap qmap, kmap, vmap;
-    const long long rows = (long long)p->num_blocks * p->Hkv * kBlock;
-    if (!make_q_map(&qmap, p->q, p->N_tok, p->Hq, kPrefillTcRows) ||
-        !make_cache_map(&kmap, p->k_cache, rows) || !make_cache_map(&vmap, p->v_cache, rows))
-        return INKATTN_ERR_CUDA;
-    if (p->rel_extent == 0)   // no bias band: two query tiles per CTA
-        return launch_status(launch_prefill_2q(*p, scalars(*p), qmap, kmap, vmap, static_cast<cudaStream_t>(stream)));
-    return launch_status(launch_prefill_tc(*p, scalars(*p), qmap, kmap, vmap, static_cast<cudaStream_t>(stream)));
+    return run_prefill_bf16(*p, static_cast<cudaStream_t>(stream));
+}
+
+size_t inkattn_prefill_workspace_bytes(const inkattn_attn_params *p) {
+    if (validate_attn(p) != INKATTN_OK || p->kv_dtype != INKATTN_KV_E4M3) return 0;
+    return prefill_ws_bytes(*p);
+}
+
+inkattn_status inkattn_prefill_e4m3(const inkattn_attn_params *p, void *workspace, size_t workspace_bytes,
+                                    void *stream) {
+    inkattn_status st = validate_attn(p);
+    if (st != INKATTN_OK) return st;
+    if (p->kv_dtype != INKATTN_KV_E4M3) return INKATTN_ERR_INVALID_ARG;     // (inkattn_prefill)
+    // the copy's rows are addressed by TMA as 32-bit coordinates
+    if ((long long)p->B * p->max_blocks_per_seq * p->Hkv * kBlock >= (1ll << 31)) return INKATTN_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < prefill_ws_bytes(*p))
+        return INKATTN_ERR_INVALID_ARG;
+    if ((st = check_device(nullptr)) != INKATTN_OK) return st;
+    if ((st = validate_locations(p)) != INKATTN_OK) return st;
+    {   // the copy is read by TMA too: device memory of this GPU
+        int dev = -1;
+        cudaPointerAttributes a;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaPointerGetAttributes(&a, workspace) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return INKATTN_ERR_INVALID_ARG;
+        }
+        if (a.type != cudaMemoryTypeDevice || a.device != dev) return INKATTN_ERR_INVALID_ARG;
+    }
+    if (p->N_tok == 0) return INKATTN_OK;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    const size_t copy = round256(prefill_copy_bytes(*p));
+    inkattn_bf16 *k16 = reinterpret_cast<inkattn_bf16 *>(ws);
+    inkattn_bf16 *v16 = reinterpret_cast<inkattn_bf16 *>(ws + copy);
+    int32_t *table = reinterpret_cast<int32_t *>(ws + 2 * copy);
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((st = launch_status(launch_dequant_e4m3(*p, k16, v16, table, s))) != INKATTN_OK) return st;
+    inkattn_attn_params q = *p;
+    q.k_cache = k16;
+    q.v_cache = v16;
+    q.kv_dtype = INKATTN_KV_BF16;
+    q.k_scale = nullptr;
+    q.v_scale = nullptr;
+    q.block_table = table;
+    q.num_blocks = p->B * p->max_blocks_per_seq;
+    return run_prefill_bf16(q, s);
 }
 
 int inkattn_decode_num_splits(const inkattn_attn_params *p, int num_sms) {

@@ -70,6 +70,10 @@ struct AttnScalars {
 
 cudaError_t launch_prologue(const inkattn_prologue_params &p, cudaStream_t stream);
 cudaError_t launch_output_conv(const inkattn_output_conv_params &p, cudaStream_t stream);
+// The E4M3 cache blocks a prefill batch reads, expanded to bf16 copies (k_out, v_out:
+// [B * max_blocks_per_seq][Hkv][64][128]) with their block table (table_out: [B][max_blocks_per_seq]).
+cudaError_t launch_dequant_e4m3(const inkattn_attn_params &p, inkattn_bf16 *k_out, inkattn_bf16 *v_out,
+                                int32_t *table_out, cudaStream_t stream);
 // qkvr projections with the prologue in their epilogue; xmap / wmap from make_qkvr_maps
 cudaError_t launch_qkvr(const inkattn_qkvr_params &p, const CUtensorMap &xmap, const CUtensorMap &wmap,
                         int num_sms, cudaStream_t stream);

@@ -137,6 +137,10 @@ def lib():
             L.inkattn_output_conv.restype = ctypes.c_int
             L.inkattn_qkvr_prologue.argtypes = [P(QkvrParams), _c_ptr]
             L.inkattn_qkvr_prologue.restype = ctypes.c_int
+            L.inkattn_prefill_workspace_bytes.argtypes = [P(AttnParams)]
+            L.inkattn_prefill_workspace_bytes.restype = ctypes.c_size_t
+            L.inkattn_prefill_e4m3.argtypes = [P(AttnParams), _c_ptr, ctypes.c_size_t, _c_ptr]
+            L.inkattn_prefill_e4m3.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -173,6 +177,18 @@ def inkattn_prologue(p: PrologueParams, stream=None, raise_on_error=True) -> int
 def inkattn_prefill(p: AttnParams, stream=None, raise_on_error=True) -> int:
     return _check(lib().inkattn_prefill(ctypes.byref(p), _stream(stream)), "inkattn_prefill",
                   raise_on_error)
+
+
+def inkattn_prefill_workspace_bytes(p: AttnParams) -> int:
+    return int(lib().inkattn_prefill_workspace_bytes(ctypes.byref(p)))
+
+
+def inkattn_prefill_e4m3(p: AttnParams, workspace: Optional[torch.Tensor], stream=None,
+                         raise_on_error=True) -> int:
+    ptr = workspace.data_ptr() if workspace is not None else None
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return _check(lib().inkattn_prefill_e4m3(ctypes.byref(p), ptr, nbytes, _stream(stream)),
+                  "inkattn_prefill_e4m3", raise_on_error)
 
 
 def inkattn_decode_num_splits(p: AttnParams, num_sms: int) -> int:

@@ -16,7 +16,8 @@ from .inputs import Workload
 class AttentionStep:
     """Buffers + calls of one attention-layer pass over device-resident inputs.
 
-    mode "prefill": inkattn_prologue then inkattn_prefill.
+    mode "prefill": inkattn_prologue then inkattn_prefill (inkattn_prefill_e4m3 over an
+                    E4M3 cache, with its workspace).
     mode "decode":  inkattn_prologue then inkattn_decode (+ inkattn_combine when the
                     split count is above one).
     The conv state and the KV cache in `inputs` are updated in place by every run.
@@ -52,6 +53,10 @@ class AttentionStep:
             k_scale=inputs.get("k_scale"), v_scale=inputs.get("v_scale"))
         self.num_splits = 0
         self.workspace: Optional[torch.Tensor] = None
+        self.e4m3 = inputs["k_cache"].dtype == torch.uint8
+        if mode == "prefill" and self.e4m3:
+            nbytes = ia.inkattn_prefill_workspace_bytes(self.attn)
+            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         if mode == "decode":
             self.num_splits = num_splits if num_splits > 0 else self.heuristic_splits()
             nbytes = ia.inkattn_decode_workspace_bytes(self.attn, self.num_splits)
@@ -66,7 +71,9 @@ class AttentionStep:
         ia.inkattn_prologue(self.pro, stream)
 
     def run_attention(self, stream=None):
-        if self.mode == "prefill":
+        if self.mode == "prefill" and self.e4m3:
+            ia.inkattn_prefill_e4m3(self.attn, self.workspace, stream)
+        elif self.mode == "prefill":
             ia.inkattn_prefill(self.attn, stream)
         else:
             ia.inkattn_decode(self.attn, self.num_splits, self.workspace, stream)
@@ -78,7 +85,7 @@ class AttentionStep:
 
     def launches_per_run(self) -> int:
         n = 2
-        if self.mode == "decode" and self.num_splits > 1:
+        if (self.mode == "decode" and self.num_splits > 1) or (self.mode == "prefill" and self.e4m3):
             n += 1
         return n
 

@@ -291,3 +291,29 @@ def test_qkvr_host_validation(ia):
     assert call(_qk(ia, y_out=p.k_cache)) == bad
     assert call(_qk(ia, y_out=(1 << 40))) != bad
     assert call(_qk(ia)) != bad
+
+
+def test_prefill_over_e4m3_host_validation(ia):
+    """The E4M3 prefill's workspace size and validation, before any device work: the
+    workspace holds bf16 K and V copies of B * max_blocks_per_seq blocks and their table; a
+    bf16 cache, a missing, short or misaligned workspace are rejected; a valid call gets past
+    validation (and, without a GPU, stops at the device check)."""
+    L = ia.lib()
+    bad = ia.INKATTN_ERR_INVALID_ARG
+    e8 = dict(kv_dtype=1, k_scale=1 << 22, v_scale=1 << 22)
+    p = _attn(ia, B=2, N_tok=300, max_seqlen_q=200, max_seqlen_k=1000, num_blocks=64, max_blocks_per_seq=16, **e8)
+    copy = 2 * 16 * 8 * 64 * 128 * 2
+    want = 2 * ((copy + 255) // 256 * 256) + (2 * 16 * 4 + 255) // 256 * 256
+    assert ia.inkattn_prefill_workspace_bytes(p) == want
+    assert ia.inkattn_prefill_workspace_bytes(_attn(ia)) == 0            # a bf16 cache needs none
+    assert ia.inkattn_prefill_workspace_bytes(_attn(ia, struct_size=8, **e8)) == 0
+    call = lambda q, ws, n: L.inkattn_prefill_e4m3(ctypes.byref(q), ws, n, None)
+    ws = 1 << 30
+    assert call(_attn(ia, B=2, N_tok=300, max_seqlen_q=200, max_seqlen_k=1000, num_blocks=64,
+                      max_blocks_per_seq=16), ws, want) == bad                # bf16 cache
+    assert call(p, None, want) == bad
+    assert call(p, ws, want - 256) == bad
+    assert call(p, ws + 128, want) == bad                                     # not 256-byte aligned
+    assert call(p, ws, want) != bad
+    # inkattn_prefill itself still sends an E4M3 cache away
+    assert ia.inkattn_prefill(p, raise_on_error=False, stream=0) == ia.INKATTN_ERR_UNSUPPORTED

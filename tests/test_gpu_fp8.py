@@ -1,12 +1,14 @@
-"""GPU parity of the E4M3 (FP8) KV cache: the prologue's quantised cache write and the
-decode over such a cache.
+"""GPU parity of the E4M3 (FP8) KV cache: the prologue's quantised cache write, and the
+decode and the prefill over such a cache.
 
 Bars: the prologue's codes and row scales are bit-exact against the oracle's quantisation
 of the very bf16 rows the bf16 prologue writes (the quantisation is an integer decision
 taken in exact power-of-two arithmetic on both sides); its queries and conv state equal
 the bf16 run's.  The decode reads code * scale exactly (f16 holds every such value of the
 prologue's rows), so it is held to the bf16 path's bar against the oracle run on the
-dequantised cache: max-abs <= 1e-2, mean-abs <= 1e-3, |dLSE| <= 2e-3."""
+dequantised cache: max-abs <= 1e-2, mean-abs <= 1e-3, |dLSE| <= 2e-3.  The prefill expands
+the blocks it reads into a bf16 copy (exact) and runs the bf16 prefill on it: the copy is
+checked bit for bit, the outputs at the same bar."""
 import numpy as np
 import pytest
 import torch
@@ -206,3 +208,96 @@ def test_decode_e4m3_noalloc_is_bit_identical(env):
     torch.cuda.synchronize()
     assert step.device_status() == 0
     assert torch.equal(step.out, ref)
+
+
+# ---------------------------------------------------------------- prefill over an E4M3 cache
+
+def _prefill_e4m3(env, w, seed):
+    gen, AttentionStep, _, _ = env
+    x = gen.make_inputs(w, seed=seed, device="cuda", kv_dtype="e4m3")
+    step = AttentionStep(w, x, mode="prefill", out_dtype=torch.float32)
+    step.run()
+    torch.cuda.synchronize()
+    return x, step
+
+
+def _check_prefill_rows(env, w, x, step, rows=None, lse_tol=LSE_ABS):
+    """The prefill's rows against the oracle on the dequantised cache (after the prologue
+    wrote the new tokens' rows), at the bf16 bars."""
+    gen, _, oracle, _ = env
+    assert step.device_status() == 0
+    kc = _dequant_bits(oracle, gen, x["k_cache"].cpu().numpy(), x["k_scale"].cpu().numpy())
+    vc = _dequant_bits(oracle, gen, x["v_cache"].cpu().numpy(), x["v_scale"].cpu().numpy())
+    xs = {k: x[k].cpu() for k in ("cu_seqlens_q", "seqlen_k", "r", "P", "block_table")}
+    o_ref, lse_ref = oracle.attention_for_inputs(xs, w, gen.bits(step.q_out), kc, vc, rows=rows)
+    out, lse = step.out.float().cpu().numpy(), step.lse.cpu().numpy()
+    if rows is not None:
+        out, lse = out[rows], lse[rows]
+    _compare(out, lse, o_ref, lse_ref, w.name, lse_tol)
+
+
+@pytest.mark.parametrize("case", ["window_strong_bias", "full_lambda"])
+def test_prefill_e4m3_small(env, case):
+    """Prefill over an E4M3 cache: ragged sequences with prefixes, several band tiles, the
+    strong bias (P ~ N(0, 0.5)) with a window, and a full layer with log scaling."""
+    gen = env[0]
+    if case == "window_strong_bias":
+        w = gen.custom(case, Hq=8, Hkv=2, q_lens=[700, 130, 3], prefix_lens=[0, 200, 61], window=400,
+                       rel_extent=600, p_std=0.5)
+    else:
+        w = gen.custom(case, Hq=16, Hkv=2, q_lens=[300, 260], prefix_lens=[900, 0], rel_extent=256,
+                       log_scale_base=256.0)
+    _check_prefill_rows(env, w, *_prefill_e4m3(env, w, seed=11))
+
+
+def test_prefill_e4m3_copy_is_the_dequantised_cache(env):
+    """The workspace copy: for each block a sequence reads, code * scale bit for bit (rows past
+    the sequence's end zero), and the copy's block table (-1 past each sequence's blocks)."""
+    gen, _, oracle, _ = env
+    w = gen.custom("copy8", Hq=8, Hkv=2, q_lens=[70, 5], prefix_lens=[100, 250], rel_extent=64)
+    x, step = _prefill_e4m3(env, w, seed=12)
+    assert step.device_status() == 0
+    mb = x["block_table"].shape[1]
+    per = w.B * mb * w.Hkv * 64 * 128 * 2
+    ws = step.workspace
+    pad = (per + 255) // 256 * 256
+    k16 = gen.bits(ws[:per].view(torch.bfloat16)).reshape(w.B * mb, w.Hkv, 64, 128)
+    v16 = gen.bits(ws[pad:pad + per].view(torch.bfloat16)).reshape(w.B * mb, w.Hkv, 64, 128)
+    table = ws[2 * pad:2 * pad + w.B * mb * 4].view(torch.int32).cpu().numpy().reshape(w.B, mb)
+    bt = x["block_table"].cpu().numpy()
+    for b, T in enumerate(w.seqlen_k):
+        n = (T + 63) // 64
+        assert np.array_equal(table[b, :n], b * mb + np.arange(n))
+        assert (table[b, n:] == -1).all()
+        for j in range(n):
+            phys = int(bt[b, j])
+            rows = min(64, T - 64 * j)
+            for got, name in ((k16, "k"), (v16, "v")):
+                want = oracle.dequantize_e4m3(x[f"{name}_cache"][phys].cpu().numpy(),
+                                              x[f"{name}_scale"][phys].cpu().numpy())
+                g = got[b * mb + j]
+                assert np.array_equal(g[:, :rows].view(np.uint16), gen.bits(torch.from_numpy(want[:, :rows]).to(torch.bfloat16))), (b, j, name)
+                assert not g[:, rows:].any(), (b, j, name)
+
+
+def test_prefill_e4m3_full_layer_sampled(env):
+    """The full layer (32768 tokens, rel_extent 1024, log scaling) over an E4M3 cache, in the
+    launch configuration the bench times, on one row of every 128-row tile and the edges."""
+    gen = env[0]
+    from test_gpu_attention import _one_row_per_tile
+    w = gen.workload("full")
+    x, step = _prefill_e4m3(env, w, seed=13)
+    _check_prefill_rows(env, w, x, step, rows=_one_row_per_tile(w))
+
+
+def test_prefill_e4m3_bad_scale_is_flagged(env):
+    gen, AttentionStep, _, ia = env
+    w = gen.custom("pre8-bad", Hq=8, Hkv=2, q_lens=[100], prefix_lens=[200], rel_extent=64)
+    x = gen.make_inputs(w, seed=14, device="cuda", kv_dtype="e4m3")
+    blk = int(x["block_table"][0, 1].item())
+    x["v_scale"][blk, 0, 5] = float("inf")          # a row the prologue does not rewrite
+    step = AttentionStep(w, x, mode="prefill", out_dtype=torch.float32)
+    step.run()
+    torch.cuda.synchronize()
+    assert step.device_status() == ia.INKATTN_ERR_DEVICE_BOUNDS
+    assert torch.isfinite(step.out).all()
