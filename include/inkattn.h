@@ -26,6 +26,11 @@
  *     into a CUDA graph.
  *   - Host-side validation runs before any launch; on failure the call returns
  *     INKATTN_ERR_INVALID_ARG or INKATTN_ERR_UNSUPPORTED and launches nothing.
+ *   - Alignment: bf16 arrays (activations, caches, conv states, outputs) must be 16-byte
+ *     aligned; the fp32 conv weights and RMSNorm gains of inkattn_prologue and
+ *     inkattn_qkvr_prologue, the index arrays, lse and dev_status 4-byte aligned; further
+ *     rules are stated per entry point.  A pointer that breaks its rule is
+ *     INKATTN_ERR_INVALID_ARG.
  *   - Index arrays are read only on the device.  Kernels bounds-check every index
  *     they read (cu_seqlens_q, seqlen_k, state_slot, slot_mapping, block_table);
  *     an out-of-range value skips the access and, when dev_status is non-NULL,

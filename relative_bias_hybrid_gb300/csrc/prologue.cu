@@ -86,13 +86,11 @@ k_prologue(const inkattn_prologue_params p, const int kv_tiles) {
         inkattn_bf16 *ob = p.q_out + q_base;
         const int g_shift = (g & (g - 1)) == 0 ? __ffs(g) - 1 : -1;
         auto div_g = [&](int row) { return g_shift >= 0 ? row >> g_shift : row / g; };
+        // the gains need only 4-byte alignment: scalar loads
         float2 gq[4];
-        {
-            const float4 g0 = __ldg(reinterpret_cast<const float4 *>(p.q_norm_w + c0));
-            const float4 g1 = __ldg(reinterpret_cast<const float4 *>(p.q_norm_w + c0 + 4));
-            gq[0] = make_float2(g0.x, g0.y); gq[1] = make_float2(g0.z, g0.w);
-            gq[2] = make_float2(g1.x, g1.y); gq[3] = make_float2(g1.z, g1.w);
-        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            gq[e] = make_float2(__ldg(p.q_norm_w + c0 + 2 * e), __ldg(p.q_norm_w + c0 + 2 * e + 1));
         for (int j0 = 0; j0 * 16 < q_rows; j0 += kQInFlight) {   // uniform over the CTA
             uint4 qraw[kQInFlight];
 #pragma unroll
@@ -137,14 +135,17 @@ k_prologue(const inkattn_prologue_params p, const int kv_tiles) {
 
     // ======================= K and V rows
     // conv weights and the K gains, interleaved by lane: channel c = 8 * lane + e, tap k at
-    // [(e * 16 + lane) * 4 + k], so the 16 lanes of a half-warp read consecutive float4s
-    for (int i = tid; i < kHeadDim * 4; i += kPrologueThreads) {
-        const int c = i >> 2, k = i & 3;
-        const int j = (((c & 7) * 16 + (c >> 3)) << 2) + k;
-        s_wk[j] = p.conv_w_k[(size_t)hk * kHeadDim * 4 + i];
-        s_wv[j] = p.conv_w_v[(size_t)hk * kHeadDim * 4 + i];
+    // [(e * 16 + lane) * 4 + k], so the 16 lanes of a half-warp read consecutive float4s.
+    // Consecutive threads fill consecutive entries (no bank conflicts), each from the
+    // channel and tap that entry holds.
+    for (int j = tid; j < kHeadDim * 4; j += kPrologueThreads) {
+        const int q = j >> 2, k = j & 3;
+        const int c = ((q & 15) << 3) + (q >> 4);
+        const size_t src = ((size_t)hk * kHeadDim + c) * 4 + k;
+        s_wk[j] = p.conv_w_k[src];
+        s_wv[j] = p.conv_w_v[src];
     }
-    if (tid < kHeadDim) s_gk[(tid & 7) * 16 + (tid >> 3)] = p.k_norm_w[tid];
+    if (tid < kHeadDim) s_gk[tid] = p.k_norm_w[((tid & 15) << 3) + (tid >> 4)];
     // one 16-byte chunk of one row of both streams per step (no division by the row count)
     for (int i = tid; i < (nt + 3) * 16; i += kPrologueThreads) {
         const int r = i >> 4, chunk = i & 15;

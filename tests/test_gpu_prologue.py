@@ -59,6 +59,26 @@ def test_prologue_tiny(env):
     _check(env, w, *_run(env, w))
 
 
+def test_weights_at_4_byte_alignment(env):
+    # the fp32 conv weights and gains need only 4-byte alignment: each passed 4 bytes past a
+    # 16-byte boundary
+    gen, AttentionStep, _ = env
+    w = gen.workload("tiny")
+    x_cpu = gen.make_inputs(w, seed=3, device="cpu")
+    x = {k: v.cuda() for k, v in x_cpu.items()}
+    for name in ("conv_w_k", "conv_w_v", "q_norm_w", "k_norm_w"):
+        t = x[name]
+        buf = torch.zeros(t.numel() + 4, dtype=t.dtype, device=t.device)
+        view = buf[1:1 + t.numel()].view(t.shape)
+        view.copy_(t)
+        assert view.data_ptr() % 16 == 4
+        x[name] = view
+    step = AttentionStep(w, x, mode="prefill")
+    step.run_prologue()
+    torch.cuda.synchronize()
+    _check(env, w, x_cpu, x, step)
+
+
 def test_prologue_ragged_short_sequences(env):
     gen = env[0]
     w = gen.custom("mix", Hq=8, Hkv=2, q_lens=[1, 2, 3, 0, 17, 40, 5, 64],
