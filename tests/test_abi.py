@@ -242,6 +242,53 @@ def test_output_conv_host_validation(ia):
     assert call(_oc(ia)) != bad
 
 
+_PRO_PTRS = ("q", "k", "v", "conv_w_k", "conv_w_v", "q_norm_w", "k_norm_w", "cu_seqlens_q", "state_slot",
+             "slot_mapping", "conv_state_k", "conv_state_v", "q_out", "k_cache", "v_cache")
+
+
+def _pro(ia, **kw):
+    p = ia.PrologueParams()
+    p.struct_size = ctypes.sizeof(ia.PrologueParams)
+    p.B, p.N_tok, p.max_seqlen_q = 2, 300, 200
+    p.Hq, p.Hkv, p.head_dim, p.block_size = 16, 2, 128, 64
+    p.num_blocks, p.num_state_slots, p.eps = 16, 2, 1e-6
+    span = 16 << 20         # bytes reserved per array
+    base = 1 << 32          # fake, never dereferenced
+    for i, f in enumerate(_PRO_PTRS):
+        setattr(p, f, base + i * span)
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_prologue_host_validation(ia):
+    """Validation of inkattn_prologue before it looks for a device: the bf16 arrays must be
+    16-byte aligned, the fp32 weights and gains and the index arrays only 4-byte aligned (the
+    kernel reads the weights with scalar loads); sizes and the E4M3 scales are checked; a
+    valid struct gets past validation (and, without a GPU, stops at the device check)."""
+    bad = ia.INKATTN_ERR_INVALID_ARG
+    call = lambda p: ia.inkattn_prologue(p, stream=0, raise_on_error=False)
+    assert call(_pro(ia, struct_size=8)) == bad
+    assert call(_pro(ia, B=0)) == bad
+    assert call(_pro(ia, Hq=15)) == bad                 # Hq % Hkv
+    assert call(_pro(ia, N_tok=5, max_seqlen_q=0)) == bad
+    assert call(_pro(ia, eps=-1.0)) == bad
+    assert call(_pro(ia, eps=float("nan"))) == bad
+    assert call(_pro(ia, head_dim=64)) == ia.INKATTN_ERR_UNSUPPORTED
+    assert call(_pro(ia, block_size=32)) == ia.INKATTN_ERR_UNSUPPORTED
+    ok = _pro(ia)
+    for f in ("q", "k", "v", "conv_state_k", "conv_state_v", "q_out", "k_cache", "v_cache"):
+        assert call(_pro(ia, **{f: getattr(ok, f) + 8})) == bad, f
+        assert call(_pro(ia, **{f: None})) == bad, f
+    for f in ("conv_w_k", "conv_w_v", "q_norm_w", "k_norm_w", "cu_seqlens_q", "state_slot", "slot_mapping"):
+        assert call(_pro(ia, **{f: getattr(ok, f) + 4})) != bad, f
+        assert call(_pro(ia, **{f: getattr(ok, f) + 2})) == bad, f
+    assert call(_pro(ia, kv_dtype=1)) == bad            # E4M3 without row scales
+    assert call(_pro(ia, kv_dtype=1, k_scale=1 << 40, v_scale=(1 << 40) + 8)) == bad
+    assert call(_pro(ia, kv_dtype=1, k_scale=1 << 40, v_scale=(1 << 40) + 16)) != bad
+    assert call(ok) != bad
+
+
 def _qk(ia, **kw):
     p = ia.QkvrParams()
     p.struct_size = ctypes.sizeof(ia.QkvrParams)
