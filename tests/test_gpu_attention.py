@@ -331,6 +331,33 @@ def test_bad_block_id_is_flagged(env):
     assert step.device_status() == 5
 
 
+def test_malformed_batch_is_flagged_by_the_prefill(env):
+    # in a batch of several sequences, one whose cu_seqlens_q entries run backwards (and the
+    # next, which then has more rows than keys) is flagged and skipped; the others are still
+    # computed
+    gen, AttentionStep, oracle = env
+    w = gen.custom("badcu", Hq=8, Hkv=2, q_lens=[600, 60, 140], prefix_lens=[0, 30, 0], rel_extent=90)
+    x_cpu = gen.make_inputs(w, seed=17, device="cpu")
+    x = {k: v.cuda() for k, v in x_cpu.items()}
+    step = AttentionStep(w, x, mode="prefill")
+    step.run_prologue()
+    torch.cuda.synchronize()
+    assert step.device_status() == 0
+    x["cu_seqlens_q"][2] = 550            # sequence 1: [600, 550); sequence 2: 250 rows, 140 keys
+    step.run_attention()
+    torch.cuda.synchronize()
+    assert step.device_status() == 5
+    # sequence 0 is intact
+    rows = np.arange(0, 600, 7, dtype=np.int32)
+    x_ref = {k: x_cpu[k] for k in ("seqlen_k", "r", "P", "block_table")}
+    x_ref["cu_seqlens_q"] = x_cpu["cu_seqlens_q"]
+    o_ref, lse_ref = oracle.attention_for_inputs(x_ref, w, gen.bits(step.q_out), gen.bits(x["k_cache"]),
+                                                 gen.bits(x["v_cache"]), rows=rows)
+    idx = torch.as_tensor(rows.astype(np.int64), device="cuda")
+    _compare(step.out.index_select(0, idx).float().cpu().numpy(), step.lse.index_select(0, idx).cpu().numpy(),
+             o_ref, lse_ref, w.name)
+
+
 @pytest.mark.parametrize("mode,splits", [("prefill", 0), ("decode", 1), ("decode", 4)])
 def test_bf16_output_is_the_fp32_output_rounded_once(env, mode, splits):
     gen, AttentionStep, _ = env
