@@ -16,9 +16,9 @@ the qkvr projections with the prologue fused in (k_qkvr, from hidden states of w
 
   python bench.py [--steps K] [--warmup W] [--impl reference] [--only NAME ...]
 
-One GPU only.  The prefill kernel multicasts K/V tiles inside a CTA pair, which this
-build keeps to single-GPU runs: --gpus N > 1 (or a torch.distributed launch with more
-than one rank) is refused before any GPU is touched.  The reference arm (the CPU
+One GPU only.  The prefill kernel multicasts K/V tiles inside a CTA pair, a form the
+library confines to single-GPU runs: --gpus N > 1 (or a torch.distributed launch with
+more than one rank) is refused before any GPU is touched.  The reference arm (the CPU
 oracle) touches no GPU; under a multi-rank launch its rank 0 alone runs.
 """
 from __future__ import annotations
@@ -710,7 +710,7 @@ def main(argv=None):
         return 0
     if args.gpus != 1 or world != 1:
         sys.stderr.write("bench.py: one GPU only.  The prefill kernel multicasts K/V tiles inside a CTA pair, "
-                         "which this build keeps to single-GPU runs; --gpus must be 1 (no multi-rank launch).\n")
+                         "a form the library confines to single-GPU runs; --gpus must be 1 (no multi-rank launch).\n")
         return 2
     run_gpu(args)
     return 0
