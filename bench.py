@@ -49,6 +49,7 @@ KERNEL_SOURCES = {
                     "relative_bias_hybrid_gb300/csrc/fp8.cuh", "relative_bias_hybrid_gb300/csrc/common.cuh"],
     "k_prologue": ["relative_bias_hybrid_gb300/csrc/prologue.cu", "relative_bias_hybrid_gb300/csrc/conv4.cuh",
                    "relative_bias_hybrid_gb300/csrc/fp8.cuh", "relative_bias_hybrid_gb300/csrc/common.cuh"],
+    "k_combine": ["relative_bias_hybrid_gb300/csrc/decode.cu", "relative_bias_hybrid_gb300/csrc/common.cuh"],
     "k_output_conv": ["relative_bias_hybrid_gb300/csrc/output_conv.cu", "relative_bias_hybrid_gb300/csrc/conv4.cuh",
                       "relative_bias_hybrid_gb300/csrc/common.cuh"],
     "k_qkvr": ["relative_bias_hybrid_gb300/csrc/qkvr.cu", "relative_bias_hybrid_gb300/csrc/tcgen05.cuh",
@@ -628,9 +629,13 @@ def measure(name, args, peaks, dev, stream, flush):
     else:
         nbytes = decode_bytes(w, kv)
         gbs = nbytes / (att_ms * 1e-3) / 1e9
+        traffic = ncu_traffic("k_decode_tc", name)
+        if step.num_splits > 1 and traffic is not None:
+            comb = ncu_traffic("k_combine", name)
+            traffic = traffic + comb if comb is not None else None
         roof = {"bound": "hbm", "kernel": "k_decode_tc" + ("+k_combine" if step.num_splits > 1 else ""),
                 "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s", "frac": gbs / peaks["hbm"],
-                "peak_src": peaks["src"] + " (copy bandwidth)", "traffic": ncu_traffic("k_decode_tc", name),
+                "peak_src": peaks["src"] + " (copy bandwidth)", "traffic": traffic,
                 "algorithmic_bytes_per_launch": nbytes, "ms": att_ms, "num_splits": step.num_splits}
         rep = {"workload": w.describe() + (", E4M3 KV cache with a power-of-two scale per row" if kv == "e4m3" else "")
                            + "; step = inkattn_prologue + inkattn_decode (+ inkattn_combine)",

@@ -260,10 +260,15 @@ INKATTN_API int inkattn_decode_num_splits(const inkattn_attn_params *p, int num_
  * current device): N_tok*Hq*S*(128+1)*4 rounded up to 256, or 0 when S resolves to 1. */
 INKATTN_API size_t inkattn_decode_workspace_bytes(const inkattn_attn_params *p, int num_splits);
 
-/* Decode pass.  num_splits: 0 = heuristic, else 1..64.  With one split the result
- * goes straight to out/lse; otherwise each split's own softmax-normalised partial
- * output and its lse go to the workspace, and inkattn_combine must follow on the
- * same stream with the same num_splits.
+/* Decode pass.  num_splits: 0 = heuristic, else 1..64.  The keys a sequence attends to
+ * are divided into num_splits contiguous parts of near-equal size, except that with
+ * num_splits = 2 and rel_extent > 0 the cut is at the start of the band (the keys
+ * within rel_extent of the first query, moved down so that the part before it holds
+ * whole 128-key tiles): the
+ * streaming part and the band part then run in separate CTAs, the streaming ones
+ * scheduled first.  With one split the result goes straight to out/lse; otherwise each
+ * split's own softmax-normalised partial output and its lse go to the workspace, and
+ * inkattn_combine must follow on the same stream with the same num_splits.
  * workspace: device memory of at least inkattn_decode_workspace_bytes bytes,
  * 256-byte aligned, owned by the caller, not read by the host. */
 INKATTN_API inkattn_status inkattn_decode(const inkattn_attn_params *p, int num_splits,

@@ -286,11 +286,19 @@ int pick_splits(const inkattn_attn_params &p, int num_sms) {
     const double r = kDecodeHbmSmFrac * (double)slots;
     const long long rows_per_unit = (long long)p.max_seqlen_q * g;
     const double block_bytes = 2.0 * kBlock * kHeadDim * 2;   // K + V of one block
+    // With a relative bias, two splits cut the keys at the band's start instead of halving
+    // them (csrc/decode_tc.cu): the CTAs streaming the keys before the band come first in the
+    // grid and the short band CTAs, whose bias tables take the longest, run beside them on
+    // the SMs the last wave leaves free.  That pays when the streaming CTAs alone keep HBM
+    // busy and the band is a small part of the keys; halves are then not a choice.
+    const bool band_split = p.rel_extent > 0;
+    const long long band_blk = ((long long)p.rel_extent + p.max_seqlen_q + kBlock - 1) / kBlock + 2;
     int best = 1;
     double best_cost = 1e300;
     for (int S = 1; S <= kDecodeMaxSplits; ++S) {
         const long long per = (nblk + S - 1) / S;
         if (S > 1 && per < kDecodeMinSplitBlocks) break;
+        if (band_split && S == 2) continue;
         const long long ctas = units * S;
         const long long full = ctas / slots, rest = ctas - full * slots;
         double waves = (double)full * fmax(r, (double)slots);
@@ -305,6 +313,7 @@ int pick_splits(const inkattn_attn_params &p, int num_sms) {
             best = S;
         }
     }
+    if (band_split && best == 1 && (double)units >= r && nblk >= 4 * band_blk) return 2;
     return best;
 }
 

@@ -103,6 +103,7 @@ struct DecTcArgs {
     inkattn_attn_params p;
     float scale;            // softmax scale
     int S;                  // number of splits
+    int band_split;         // S == 2 cut at the band's start; the grid is (Hkv, B, 2)
     int ql;                 // rows of the Q box per head (max_seqlen_q)
     float *ws_o;
     float *ws_lse;
@@ -121,7 +122,11 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
     grid_dep_wait();                                   // q and the cache: written by the prologue
     using C = Dec<kF8>;
     const inkattn_attn_params &p = A.p;
-    const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+    // band split: the CTAs of split 0 (the keys before the band) come first in the grid, so
+    // that the short split-1 CTAs run on the SMs the streaming ones leave free
+    const int split = A.band_split ? (int)blockIdx.z : (int)blockIdx.x;
+    const int hk = A.band_split ? (int)blockIdx.x : (int)blockIdx.y;
+    const int b = A.band_split ? (int)blockIdx.y : (int)blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = p.Hq / p.Hkv;
 
@@ -141,9 +146,19 @@ k_decode_tc(const DecTcArgs A, const __grid_constant__ CUtensorMap qmap,
     if (p.window > 0) blk_first = max(0, pos0 - p.window + 1) / kBlock;
     const int blk_end = (T + kBlock - 1) / kBlock;    // exclusive
     const int nblk = blk_end - blk_first;
-    const int per = (nblk + A.S - 1) / A.S;
-    const int my_lo = blk_first + split * per;
-    const int my_hi = min(blk_end, my_lo + per);
+    int my_lo, my_hi;
+    if (A.band_split) {
+        // two parts: the keys before the band, in whole 128-key tiles, and the rest (the keys
+        // within rel_extent of the first query, whose tiles build bias tables)
+        const int band_key_lo = max(0, pos0 - p.rel_extent + 1);
+        const int cut = blk_first + ((max(blk_first, min(blk_end, band_key_lo / kBlock)) - blk_first) & ~1);
+        my_lo = split == 0 ? blk_first : cut;
+        my_hi = split == 0 ? cut : blk_end;
+    } else {
+        const int per = (nblk + A.S - 1) / A.S;
+        my_lo = blk_first + split * per;
+        my_hi = min(blk_end, my_lo + per);
+    }
     const int my_n = max(0, my_hi - my_lo);
     const int N = (my_n + 1) / 2;                     // 128-key tiles
     const int kr_lo = my_lo * kBlock, kr_hi = my_hi * kBlock;
@@ -779,13 +794,14 @@ cudaError_t launch_decode_tc(const inkattn_attn_params &p, const AttnScalars &s,
     a.p = p;
     a.scale = s.scale;
     a.S = num_splits;
+    a.band_split = num_splits == 2 && p.rel_extent > 0;
     a.ql = p.max_seqlen_q;
     a.ws_o = ws_o;
     a.ws_lse = ws_lse;
     a.kv_rows = (long long)p.num_blocks * p.Hkv * kBlock;
     a.wait_ns = kernel_debug().wait_ns;
     a.withhold = kernel_debug().withhold;
-    dim3 grid(num_splits, p.Hkv, p.B);
+    const dim3 grid = a.band_split ? dim3(p.Hkv, p.B, 2) : dim3(num_splits, p.Hkv, p.B);
     return p.kv_dtype == INKATTN_KV_E4M3 ? launch_decode_variant<true>(a, grid, qmap, kmap, vmap, stream)
                                          : launch_decode_variant<false>(a, grid, qmap, kmap, vmap, stream);
 }

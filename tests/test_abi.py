@@ -128,13 +128,19 @@ def test_host_validation_rejects_before_any_launch(ia):
 
 def test_split_heuristic_and_workspace_size(ia):
     p = _attn(ia)
-    # 32 sequences x 8 KV heads = 256 CTAs already keep HBM busy on 152 SMs: no split
-    assert ia.inkattn_decode_num_splits(p, 152) == 1
-    assert ia.inkattn_decode_num_splits(_attn(ia, B=16, N_tok=16 * 9), 152) == 1
+    # 32 sequences x 8 KV heads = 256 CTAs already keep HBM busy on 152 SMs: no even split;
+    # with the relative bias, two splits cut at the band (the streaming CTAs first, the band
+    # CTAs beside the last wave); without it, one split
+    assert ia.inkattn_decode_num_splits(p, 152) == 2
+    assert ia.inkattn_decode_num_splits(_attn(ia, B=16, N_tok=16 * 9), 152) == 2
+    assert ia.inkattn_decode_num_splits(_attn(ia, rel_extent=0), 152) == 1
+    assert ia.inkattn_decode_num_splits(_attn(ia, B=16, N_tok=16 * 9, rel_extent=0), 152) == 1
+    # ... and not when the band is a large part of the keys
+    assert ia.inkattn_decode_num_splits(_attn(ia, max_seqlen_k=2048, max_blocks_per_seq=32), 152) == 1
     # a few sequences: split the KV length until the GPU is full
     few = _attn(ia, B=2, N_tok=2 * 9)
     S = ia.inkattn_decode_num_splits(few, 152)
-    assert 4 <= S <= 64 and 2 * 8 * S >= 0.6 * 152   # enough CTAs to keep HBM busy
+    assert 4 <= S <= 64 and 2 * 8 * S >= 0.6 * 152   # enough CTAs to keep HBM busy (even parts)
     nblk = 32768 // 64
     assert -(-nblk // S) >= 8                      # each split streams >= 8 blocks
     # 160 units: one full wave plus 8 CTAs would idle most SMs in the second wave

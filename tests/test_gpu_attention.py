@@ -197,7 +197,7 @@ def test_prefill_strong_bias(env, case):
 
 # ---------------------------------------------------------------- decode
 
-@pytest.mark.parametrize("splits", [1, 0, 3, 7])
+@pytest.mark.parametrize("splits", [1, 0, 2, 3, 7])
 def test_decode_small(env, splits):
     gen = env[0]
     w = gen.custom("dec", Hq=16, Hkv=2, q_lens=[9, 9, 4, 1], prefix_lens=[700, 40, 1500, 3000],
@@ -223,7 +223,7 @@ def test_decode_sliding_window(env):
     _check_all_rows(env, w, *_run(env, w, mode="decode", seed=6, num_splits=4))
 
 
-@pytest.mark.parametrize("splits", [0, 1])
+@pytest.mark.parametrize("splits", [0, 1, 2])
 def test_decode_strong_bias_mtp_shape(env, splits):
     """The MTP-verify shape (9 queries, key length 32768, Hq 64, Hkv 8, rel_extent 1024,
     lambda = 15/13) on three sequences with P ~ N(0, 0.5): the bias tables decide the output.
